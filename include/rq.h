@@ -1,0 +1,226 @@
+/*
+ * rq.h -- C ABI of the GB300 (sm_103a) per-frame decode step of a Moshi-style
+ * RQ-Transformer.
+ *
+ * What one frame computes ("inferencelayer 0.2.4 -- src/moshi_lm.rs", module doc and
+ * `MoshiLm::step_ext`): for each of B independent sessions,
+ *   1. the 8 user-audio codes are written into the 17-stream, 3-slot delayed-token
+ *      ring at (offset + delay) % 3;
+ *   2. the 17 model inputs are gathered at offset % 3, INITIAL tokens (text_card for
+ *      the text stream, audio_card for audio) while offset <= delay;
+ *   3. their embeddings are summed (16 audio tables, then the text table; code -1
+ *      adds nothing, any other code adds row max(code, 0));
+ *   4. the temporal decoder runs at position `offset` (pre-norm RMSNorm, fused qkv,
+ *      interleaved-pair rotary embedding, K/V window of `context` positions, SiLU-gated
+ *      FFN), then out_norm;
+ *   5. the text head's first-wins argmax picks the text token;
+ *   6. the depformer runs its 8 codebook steps (fresh per-frame K/V, step-specific
+ *      weights, shared norms, no rotary embedding), each ending in an argmax;
+ *   7. offset advances and the 9 generated tokens are written at offset % 3;
+ *   8. once offset > 1 the delay-realigned [text, audio0..7] is read at
+ *      (offset - 1 + delay) % 3.
+ * Streams: 0 text, 1..8 generated audio codebooks, 9..16 user codebooks; delays
+ * [0 | 0,1,1,1,1,1,1,1 | 0,1,1,1,1,1,1,1]; the ring starts UNGENERATED (-2).
+ *
+ * Ownership: weights belong to the caller; they must stay valid and unchanged until
+ * rq_destroy and are never copied or freed here.  The handle owns the ring, the
+ * offsets, the K/V caches, all scratch, the captured CUDA graph and the status word.
+ *
+ * Streams: every call enqueues on the stream given to rq_create (NULL = the legacy
+ * default stream).  Calls with host outputs synchronize that stream before return.
+ *
+ * Errors: argument and token validation happens before anything is enqueued, so a
+ * validation error leaves every session unchanged.  A CUDA error or a device-side
+ * timeout poisons the handle: later calls return RQ_ERR_POISONED until
+ * rq_reset(h, -1) or rq_destroy.  rq_last_error gives a one-line reason.
+ *
+ * Thread safety: one handle must not be used from two threads at once.
+ */
+#ifndef RQ_H_
+#define RQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RQ_ABI_VERSION 1
+#define RQ_N_STREAMS 17
+#define RQ_N_Q 8 /* generated audio codebooks per frame */
+
+typedef enum {
+  RQ_OK = 0,
+  RQ_ERR_ARG = 1,         /* bad pointer, size, shape or alignment */
+  RQ_ERR_TOKEN = 2,       /* a user or forced token outside its range */
+  RQ_ERR_CUDA = 3,        /* a CUDA runtime error (handle poisoned) */
+  RQ_ERR_OOM = 4,         /* device or pinned-host allocation failed */
+  RQ_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (handle poisoned) */
+  RQ_ERR_UNSUPPORTED = 6, /* shape or dtype this build does not implement */
+  RQ_ERR_POISONED = 7     /* an earlier CUDA error or timeout; rq_reset(h, -1) */
+} rq_status;
+
+typedef enum { RQ_F32 = 0, RQ_BF16 = 1 } rq_dtype;
+
+/* Model shape.  Defaults of the Moshi-7B shape ("moshi_lm.rs", consts DIM..DHIDDEN,
+ * CARD, TEXT_CARD, RMS_EPS) in brackets. */
+typedef struct {
+  int32_t batch;      /* B independent sessions [1] */
+  int32_t dim;        /* temporal model width D [4096] = heads * head_dim */
+  int32_t layers;     /* temporal layers L [32] */
+  int32_t heads;      /* [32] */
+  int32_t head_dim;   /* [128]; must be 32, 64 or 128 */
+  int32_t hidden;     /* gated-FFN hidden F [11264] */
+  int32_t context;    /* K/V window C [3000] */
+  int32_t text_card;  /* V [32000]; text tables have V+1 rows, V = INITIAL */
+  int32_t audio_card; /* A [2048]; audio input tables have A+1 rows, A = INITIAL */
+  int32_t ddim;       /* depformer width DD [1024] = dheads * dhead_dim */
+  int32_t dlayers;    /* DL [6] */
+  int32_t dheads;     /* [16] */
+  int32_t dhead_dim;  /* [64]; must be 32, 64 or 128 */
+  int32_t dhidden;    /* DF [2816] */
+  int32_t weight_dtype; /* rq_dtype of every matrix and table [RQ_BF16] */
+  int32_t kv_dtype;     /* rq_dtype of the temporal K/V cache [RQ_BF16] */
+  float rms_eps;        /* [1e-8], inside the mean */
+  float rope_theta;     /* [10000] */
+} rq_config;
+
+/* Device pointers to the weights, row-major, matrices [out][in] ("moshi_lm.rs",
+ * structs TemporalLayer, DepLayer, MoshiLm and `load_band`).  Matrices and tables are
+ * in weight_dtype; the RMSNorm alphas are always f32.  Every pointer must be 16-byte
+ * aligned.  Stacked arrays hold one block per layer / step / table, in this order:
+ *   emb          [16][A+1][D]      audio input tables, stream 1+k uses table k
+ *   text_emb     [V+1][D]
+ *   norm1, norm2 [L][D]            f32 alphas
+ *   in_proj      [L][3D][D]        rows: q, then k, then v
+ *   out_proj     [L][D][D]
+ *   gate_in      [L][2F][D]        rows 0..F-1 the SiLU half, F..2F-1 the multiplier
+ *   gate_out     [L][D][F]
+ *   out_norm     [D]               f32
+ *   text_linear  [V][D]
+ *   dep_in       [8][DD][D]
+ *   dep_text_emb [V+1][DD]         conditions depformer step 0 on the text token
+ *   dep_emb      [7][A+1][DD]      step cb >= 1 on audio token cb-1
+ *   dnorm1, dnorm2 [DL][DD]        f32 alphas, shared by the 8 steps
+ *   d_in_proj    [DL][8][3DD][DD]
+ *   d_out_proj   [DL][8][DD][DD]
+ *   d_gate_in    [DL][8][2DF][DD]
+ *   d_gate_out   [DL][8][DD][DF]
+ *   linears      [8][A][DD]        per-codebook output heads */
+typedef struct {
+  const void *emb, *text_emb;
+  const float *norm1;
+  const void *in_proj, *out_proj;
+  const float *norm2;
+  const void *gate_in, *gate_out;
+  const float *out_norm;
+  const void *text_linear;
+  const void *dep_in, *dep_text_emb, *dep_emb;
+  const float *dnorm1, *dnorm2;
+  const void *d_in_proj, *d_out_proj, *d_gate_in, *d_gate_out;
+  const void *linears;
+} rq_weights;
+
+typedef struct rq_handle rq_handle;
+
+/* Create a decoder for cfg->batch sessions on the current CUDA device, all sessions
+ * fresh (ring UNGENERATED, offset 0, empty K/V).  `cuda_stream` is a cudaStream_t
+ * (may be NULL).  Allocates every device buffer and captures the frame as a CUDA
+ * graph.  On failure *out is NULL and nothing is leaked. */
+rq_status rq_create(const rq_config *cfg, const rq_weights *w, void *cuda_stream,
+                    rq_handle **out);
+
+/* Free every resource of the handle (after synchronizing its stream).  NULL is a
+ * no-op. */
+void rq_destroy(rq_handle *h);
+
+/* Return session `session` (or every session, -1) to the fresh state.  K/V memory is
+ * not cleared: positions past the offset are never read.  rq_reset(h, -1) also
+ * clears a poisoned handle. */
+rq_status rq_reset(rq_handle *h, int32_t session);
+
+/* One frame for every session ("moshi_lm.rs", `MoshiLm::step`).
+ *   user_tokens  host [B][8]  codes in [-1, audio_card]; -1 = no code (embeds to
+ *                zero); anything else -> RQ_ERR_TOKEN before any state changes.
+ *   out_tokens   host [B][9]  the delay-realigned [text, audio0..7] (meaningful only
+ *                where has_output is 1).
+ *   has_output   host [B]     0 until that session's offset exceeds 1, then 1.
+ * Synchronizes the stream. */
+rq_status rq_step(rq_handle *h, const int32_t *user_tokens, int32_t *out_tokens,
+                  uint8_t *has_output);
+
+/* Teacher-forced frame: computes exactly as rq_step but conditions the depformer on
+ * `forced` and writes `forced` into the ring in place of its own tokens
+ * ("moshi_lm.rs", `MoshiState::force_generated`; "rlx_lm.rs",
+ * `depformer_forced_logits_rlx`).
+ *   forced      host [B][9]  [text, audio0..7]: text in [0, text_card), audio in
+ *               [0, audio_card).
+ *   own_tokens  host [B][9]  the frame's own argmax tokens [text, audio0..7].
+ *   out_tokens, has_output   as rq_step (realigned from the forced ring). */
+rq_status rq_step_forced(rq_handle *h, const int32_t *user_tokens,
+                         const int32_t *forced, int32_t *own_tokens,
+                         int32_t *out_tokens, uint8_t *has_output);
+
+/* Enqueue one frame whose inputs and outputs stay on the device; no host
+ * synchronization and no validation of the token values (the caller guarantees
+ * [-1, audio_card]).
+ *   d_user        device [B][8]  int32
+ *   d_out_tokens  device [B][9]  int32, realigned output
+ *   d_has_output  device [B]     uint8
+ * Either output pointer may be NULL.  Errors of the frame show up at the next
+ * rq_sync. */
+rq_status rq_step_device(rq_handle *h, const int32_t *d_user, int32_t *d_out_tokens,
+                         uint8_t *d_has_output);
+
+/* Synchronize the handle's stream and read the device status word. */
+rq_status rq_sync(rq_handle *h);
+
+/* Debug / parity reads of the last frame (synchronize the stream).
+ *   text  host [B][V] text-head logits;  audio host [B][8][A] depformer logits.
+ * Either pointer may be NULL. */
+rq_status rq_get_logits(rq_handle *h, float *text, float *audio);
+
+/* The last frame's embedding sum and post-out_norm hidden ("moshi_lm.rs",
+ * `StepTrace.emb_sum`, `.transformer_out`), host [B][D] each; either may be NULL. */
+rq_status rq_get_trace(rq_handle *h, float *emb_sum, float *transformer_out);
+
+/* The ring cache (host [B][17][3]) and offsets (host [B]); either may be NULL. */
+rq_status rq_get_ring(rq_handle *h, int32_t *ring, int32_t *offsets);
+
+/* Pre-fill session `session`: temporal K/V positions 0..n_pos-1 of every layer take
+ * k, v ([L][n_pos][D] in kv_dtype, keys already rotated; host or device memory),
+ * the offset becomes n_pos and the ring is left as it is ("moshi_lm.rs",
+ * `MoshiState::advance_clock`).  0 <= n_pos <= context. */
+rq_status rq_set_kv(rq_handle *h, int32_t session, int32_t n_pos, const void *k,
+                    const void *v);
+
+/* Per-kernel timing hook: enqueue `count` launches of one operation of the frame with
+ * the frame's own buffers and launch configuration, so a caller can time that kernel
+ * alone with events on the handle's stream.  Repeating an operation repeats its side
+ * effects on activations and caches: call rq_reset(h, -1) before decoding again.
+ *   op     one of RQ_OP_*;  layer  temporal layer index.
+ * *bytes_per_launch (may be NULL) receives the weight + K/V bytes one launch must
+ * stream. */
+enum {
+  RQ_OP_QKV = 0,      /* RMSNorm + in_proj GEMV + rotary + K/V append */
+  RQ_OP_ATTN = 1,     /* split-K decode attention */
+  RQ_OP_OUT = 2,      /* out_proj GEMV + residual */
+  RQ_OP_GATE_IN = 3,  /* RMSNorm + gate_in GEMV + SiLU gate */
+  RQ_OP_GATE_OUT = 4, /* gate_out GEMV + residual */
+  RQ_OP_HEAD = 5      /* out_norm + text head GEMV + argmax */
+};
+rq_status rq_launch_op(rq_handle *h, int32_t op, int32_t layer, int32_t count,
+                       double *bytes_per_launch);
+
+/* Number of kernel launches in one frame (the captured graph's kernel nodes). */
+int32_t rq_frame_kernel_count(const rq_handle *h);
+
+const char *rq_last_error(const rq_handle *h);
+const char *rq_status_string(rq_status s);
+int32_t rq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RQ_H_ */

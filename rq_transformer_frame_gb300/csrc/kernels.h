@@ -1,0 +1,123 @@
+// kernels.h -- parameter blocks and host launchers of the decode-step kernels.
+// Shared by the kernel translation units and the C-ABI engine (rq_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rqk {
+
+// ---------------------------------------------------------------- streaming GEMV
+// y = W x for one weight matrix W [rows][K] streamed once from HBM through a
+// shared-memory ring filled by bulk copies, with a fused prologue (how x is formed)
+// and epilogue (where y goes).
+enum GemvPro : int {
+  PRO_PLAIN = 0,  // x = in[b]
+  PRO_RMS = 1,    // x = in[b] * alpha * 1/sqrt(eps + mean(in[b]^2))
+  PRO_DATTN = 2   // x = depformer attention of dq[b] over keys 0..n_keys-1
+};
+enum GemvEpi : int {
+  EPI_STORE = 0,   // out[b][r] = y
+  EPI_RESID = 1,   // out[b][r] += y
+  EPI_SWIGLU = 2,  // out[b][j] = silu(y_j) * y_{F+j}
+  EPI_QKV = 3,     // rotary on q, k; q -> out, k/v -> temporal cache slot pos % C
+  EPI_DQKV = 4,    // q -> out, k/v -> depformer per-frame cache entry
+  EPI_ARGMAX = 5,  // out[b][r] = y (logits) and first-wins argmax -> keys
+  EPI_DEPIN = 6    // out[b][r] = y + E[prev][r]
+};
+
+struct GemvPlan {
+  int n_out;       // output rows (EPI_SWIGLU: F)
+  int K;           // reduction length
+  int tile_rows;   // weight rows per pipeline stage (SWIGLU: half gate, half mult)
+  int tiles;       // number of tiles
+  int grid;        // CTAs per session
+  int n_stages;    // pipeline depth
+  int tpr;         // threads per row group (power of two, 32..256)
+  int rg;          // rows per thread per tile (1 or 2)
+  int max_tiles;   // tiles of the busiest CTA
+  int smem;        // dynamic shared memory bytes
+  double bytes;    // weight bytes one launch streams
+};
+
+struct GemvParams {
+  const void* W;
+  long long w_half;  // SWIGLU: element offset of the multiplier half
+  GemvPlan pl;
+  // prologue
+  const float* in;
+  long long in_bs;     // batch stride (elements)
+  const float* alpha;
+  float eps;
+  float* side_out;     // PRO_RMS: CTA 0 also stores x here (nullable)
+  long long side_bs;
+  const float* dq;     // PRO_DATTN: query [B][DD]
+  long long dq_bs;
+  const float* dk;     // PRO_DATTN: keys [n][DD] at dk + b*dkv_bs
+  const float* dv;
+  long long dkv_bs;
+  int n_keys, dheads, dhead_dim;
+  // epilogue
+  float* out;
+  long long out_bs;
+  void* kcache;        // EPI_QKV: cache of this layer, session stride kv_bs
+  void* vcache;
+  long long kv_bs;
+  int kv_bf16;
+  int head_dim;
+  int context;
+  float rope_theta;
+  const int* offsets;  // [B] current positions
+  float* dk_out;       // EPI_DQKV
+  float* dv_out;
+  unsigned long long* keys;  // EPI_ARGMAX / EPI_DEPIN: [B][9]
+  int key_index;
+  const void* emb;     // EPI_DEPIN: table [rows][n_out] in the weight dtype
+  const int* d_in;     // per-step input block (forced tokens / flags)
+  int batch;
+  uint32_t* status;
+};
+
+GemvPlan plan_gemv(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
+                   int num_sms);
+int gemv_chunks_per_thread(const GemvPlan& pl, int elem_bytes);
+cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
+                        cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- decode attention
+struct AttnParams {
+  const float* q;       // [B][D]
+  const void* kc;       // layer's K cache, [C][D] per session (stride kv_bs)
+  const void* vc;
+  long long kv_bs;
+  const int* offsets;   // [B]
+  float* part;          // [B][H][nsplit][hd + 2]
+  int* counters;        // [B][H], zero between uses
+  float* out;           // [B][D]
+  int D, H, hd, C, kps, nsplit;
+  int batch;
+  uint32_t* status;
+};
+cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- frame begin / end
+struct FrameParams {
+  int B, D, V, A;
+  int32_t* ring;        // [B][17][3]
+  int32_t* offsets;     // [B]
+  const int32_t* d_in;  // per-step input block
+  int32_t* d_out;       // per-step output block (int32 words)
+  uint8_t* d_has;
+  unsigned long long* keys;  // [B][9]
+  const void* emb;      // [16][A+1][D]
+  const void* text_emb; // [V+1][D]
+  float* x;             // [B][D]
+  float* emb_sum;       // [B][D]
+};
+cudaError_t launch_frame_begin(const FrameParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_frame_end(const FrameParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_reset(int32_t* ring, int32_t* offsets, int B, int session,
+                         cudaStream_t s);
+cudaError_t launch_set_offset(int32_t* offsets, int session, int value, cudaStream_t s);
+
+}  // namespace rqk
