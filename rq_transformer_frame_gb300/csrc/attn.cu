@@ -1,0 +1,161 @@
+// attn.cu -- split-K single-query decode attention over the temporal K/V window.
+//
+// "inferencelayer 0.2.4 -- src/moshi_lm.rs", `attend`: for each head,
+// s_j = (q . k_j) / sqrt(head_dim) over the cached positions j of the window,
+// p = softmax(s) with the maximum subtracted, o = sum_j p_j v_j.
+//
+// The window of session b holds positions [pos - len + 1, pos] with
+// len = min(pos + 1, C); position j lives in cache slot j % C.  Grid (split, head,
+// session): each CTA covers `kps` consecutive positions with 4 warps (one key per
+// warp per step, the head's dimensions spread over the lanes), keeps an online
+// softmax (running max m, sum l, weighted values) in registers, merges its warps in a
+// fixed order and writes a partial (m, l, acc).  The last CTA of a (session, head)
+// to finish -- found with an atomic ticket -- merges the partials in split order, so
+// the result does not depend on which CTA finished last.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rqk {
+
+template <typename KT>
+__device__ __forceinline__ float kv_load(const KT* p);
+template <>
+__device__ __forceinline__ float kv_load<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float kv_load<uint16_t>(const uint16_t* p) {
+  return __uint_as_float(((uint32_t)*p) << 16);
+}
+
+template <typename KT, int EPL>
+__global__ void __launch_bounds__(128) attn_decode_kernel(const AttnParams p) {
+  constexpr int HD = EPL * 32;
+  __shared__ float s_m[4], s_l[4];
+  __shared__ float s_acc[4][HD];
+  __shared__ int s_last;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
+  const int pos = p.offsets[b];
+  const int len = min(pos + 1, p.C);
+  const int first = pos + 1 - len;
+  const int nsplit = (len + p.kps - 1) / p.kps;
+  if (split >= nsplit) return;
+  const int j0 = first + split * p.kps;
+  const int j1 = min(j0 + p.kps, pos + 1);
+
+  float q[EPL];
+  const float* qp = p.q + (size_t)b * p.D + (size_t)h * HD + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) q[e] = qp[e];
+  const float scale = 1.0f / sqrtf((float)HD);
+  const float ninf = -__int_as_float(0x7f800000);
+  float m = ninf, l = 0.f, acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  const KT* kb = static_cast<const KT*>(p.kc) + (size_t)b * p.kv_bs + (size_t)h * HD + lane * EPL;
+  const KT* vb = static_cast<const KT*>(p.vc) + (size_t)b * p.kv_bs + (size_t)h * HD + lane * EPL;
+  for (int j = j0 + warp; j < j1; j += 4) {
+    const size_t off = (size_t)(j % p.C) * p.D;
+    float k[EPL], v[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      k[e] = kv_load<KT>(kb + off + e);
+      v[e] = kv_load<KT>(vb + off + e);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s = fmaf(q[e], k[e], s);
+    s = warp_sum(s) * scale;
+    const float mn = fmaxf(m, s);
+    const float corr = expf(m - mn);
+    const float pe = expf(s - mn);
+    l = l * corr + pe;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * corr + pe * v[e];
+    m = mn;
+  }
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = acc[e];
+  __syncthreads();
+
+  const size_t pstride = (size_t)HD + 2;
+  float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + split) * pstride;
+  if (tid < HD) {
+    float M = ninf;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w]);
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (s_l[w] > 0.f) {
+        const float c = expf(s_m[w] - M);
+        L += s_l[w] * c;
+        A += s_acc[w][tid] * c;
+      }
+    }
+    part[2 + tid] = A;
+    if (tid == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(&p.counters[b * p.H + h], 1);
+    s_last = (t == nsplit - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* pb = p.part + ((size_t)b * p.H + h) * p.nsplit * pstride;
+  if (tid < HD) {
+    float M = ninf;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(pb + s * pstride));
+    float L = 0.f, A = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float c = expf(__ldcg(pb + s * pstride) - M);
+      L += __ldcg(pb + s * pstride + 1) * c;
+      A += __ldcg(pb + s * pstride + 2 + tid) * c;
+    }
+    p.out[(size_t)b * p.D + (size_t)h * HD + tid] = A / L;
+  }
+  if (tid == 0) p.counters[b * p.H + h] = 0;
+}
+
+template <typename KT, int EPL>
+static cudaError_t launch_attn_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.nsplit, (unsigned)p.H, (unsigned)p.batch);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<KT, EPL>, p);
+}
+
+cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl) {
+  switch (p.hd) {
+    case 32:
+      return kv_bf16 ? launch_attn_t<uint16_t, 1>(p, s, pdl) : launch_attn_t<float, 1>(p, s, pdl);
+    case 64:
+      return kv_bf16 ? launch_attn_t<uint16_t, 2>(p, s, pdl) : launch_attn_t<float, 2>(p, s, pdl);
+    case 128:
+      return kv_bf16 ? launch_attn_t<uint16_t, 4>(p, s, pdl) : launch_attn_t<float, 4>(p, s, pdl);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace rqk

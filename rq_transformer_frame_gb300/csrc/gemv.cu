@@ -439,16 +439,37 @@ int gemv_chunks_per_thread(const GemvPlan& pl, int es) {
   return (CC + pl.tpr - 1) / pl.tpr;
 }
 
+constexpr int kMaxDynSmem = 200 * 1024;
+
+template <typename WT, int PRO, int EPI>
+static cudaError_t configure_t() {
+  return cudaFuncSetAttribute(gemv_kernel<WT, PRO, EPI>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+}
+
+template <typename WT>
+static cudaError_t configure_all_t() {
+  cudaError_t e = cudaSuccess, r;
+#define RQ_CFG(P, E) if ((r = configure_t<WT, P, E>()) != cudaSuccess) e = r;
+  RQ_CFG(PRO_RMS, EPI_QKV) RQ_CFG(PRO_PLAIN, EPI_RESID) RQ_CFG(PRO_RMS, EPI_SWIGLU)
+  RQ_CFG(PRO_RMS, EPI_ARGMAX) RQ_CFG(PRO_PLAIN, EPI_DEPIN) RQ_CFG(PRO_RMS, EPI_DQKV)
+  RQ_CFG(PRO_DATTN, EPI_RESID) RQ_CFG(PRO_PLAIN, EPI_ARGMAX) RQ_CFG(PRO_PLAIN, EPI_STORE)
+#undef RQ_CFG
+  return e;
+}
+
+// Raise the dynamic shared-memory limit of every instantiation once per device,
+// before any launch is captured into a graph.
+cudaError_t gemv_configure_all() {
+  cudaError_t e = configure_all_t<uint16_t>();
+  cudaError_t f = configure_all_t<float>();
+  return e != cudaSuccess ? e : f;
+}
+
 template <typename WT, int PRO, int EPI>
 static cudaError_t launch_t(const GemvParams& p, int batch, cudaStream_t s, bool pdl) {
   auto k = gemv_kernel<WT, PRO, EPI>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if (p.pl.smem > kMaxDynSmem) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.pl.grid, (unsigned)batch, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -81,6 +81,8 @@ struct GemvParams {
 GemvPlan plan_gemv(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
                    int num_sms);
 int gemv_chunks_per_thread(const GemvPlan& pl, int elem_bytes);
+cudaError_t gemv_configure_all();
+constexpr int kGemvMaxChunks = 6;  // 16-byte chunks of x per thread
 cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
                         cudaStream_t s, bool pdl);
 

@@ -1,0 +1,788 @@
+// rq_api.cu -- the C ABI (include/rq.h): handle, device state, the per-frame kernel
+// schedule captured once as a CUDA graph with programmatic-dependent-launch edges,
+// and the host-side validation and error model.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/rq.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace rqk;
+
+namespace {
+thread_local std::string g_create_err;  // why the last rq_create failed
+}  // namespace
+
+struct rq_handle {
+  rq_config cfg{};
+  rq_weights w{};
+  cudaStream_t stream = nullptr;  // caller's stream
+  cudaStream_t cap = nullptr;     // private stream used for graph capture
+  int device = 0, num_sms = 0;
+  bool wbf = false, kvbf = false;
+  int wes = 4, kves = 4;
+  IoLayout io{1};
+  // device state
+  int32_t* ring = nullptr;
+  int32_t* offsets = nullptr;
+  void* kcache = nullptr;
+  void* vcache = nullptr;
+  int32_t* d_in = nullptr;
+  uint8_t* d_outb = nullptr;
+  float *x = nullptr, *emb_sum = nullptr, *q = nullptr, *attn = nullptr, *u = nullptr;
+  float *tout = nullptr, *text_logits = nullptr, *audio_logits = nullptr;
+  unsigned long long* keys = nullptr;
+  float *dx = nullptr, *dq = nullptr, *dkv = nullptr, *du = nullptr;
+  float* part = nullptr;
+  int* counters = nullptr;
+  // pinned host staging
+  int32_t* h_in = nullptr;
+  uint8_t* h_out = nullptr;
+  // graph
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int n_kernels = 0;
+  // plans
+  GemvPlan p_qkv{}, p_out{}, p_gin{}, p_gout{}, p_head{};
+  GemvPlan p_depin{}, p_dqkv{}, p_dout{}, p_dgin{}, p_dgout{}, p_lin{};
+  int kps = 64, nsplit = 1;
+  std::vector<int> host_off;  // host mirror of the offsets (for byte accounting)
+  bool poisoned = false;
+  bool forcing_dirty = true;
+  std::string err;
+
+  int32_t* d_out_words() const { return reinterpret_cast<int32_t*>(d_outb); }
+  uint8_t* d_has() const { return d_outb + io.has_off_bytes(); }
+  uint32_t* d_status() const { return reinterpret_cast<uint32_t*>(d_outb + io.status_off_bytes()); }
+};
+
+namespace {
+
+rq_status fail(rq_handle* h, rq_status s, const std::string& msg) {
+  if (h) h->err = msg;
+  return s;
+}
+
+rq_status cuda_fail(rq_handle* h, cudaError_t e, const char* where) {
+  if (h) {
+    h->poisoned = true;
+    h->err = std::string(where) + ": " + cudaGetErrorString(e);
+  }
+  return RQ_ERR_CUDA;
+}
+
+#define RQ_CUDA(h, call)                               \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+  } while (0)
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// elements -> byte offset into a weight array
+const void* woff(const void* base, size_t elems, int es) {
+  return static_cast<const char*>(base) + elems * (size_t)es;
+}
+
+bool hd_ok(int hd) { return hd == 32 || hd == 64 || hd == 128; }
+
+rq_status validate_config(const rq_config* c, std::string* why) {
+  auto bad = [&](const char* m) { *why = m; return RQ_ERR_ARG; };
+  auto uns = [&](const char* m) { *why = m; return RQ_ERR_UNSUPPORTED; };
+  if (c->batch < 1 || c->dim < 1 || c->layers < 1 || c->heads < 1 || c->hidden < 1 ||
+      c->context < 1 || c->text_card < 1 || c->audio_card < 1 || c->ddim < 1 ||
+      c->dlayers < 1 || c->dheads < 1 || c->dhidden < 1)
+    return bad("every size must be positive");
+  if (c->heads * c->head_dim != c->dim) return bad("dim != heads * head_dim");
+  if (c->dheads * c->dhead_dim != c->ddim) return bad("ddim != dheads * dhead_dim");
+  if (!hd_ok(c->head_dim) || !hd_ok(c->dhead_dim)) return uns("head dims must be 32, 64 or 128");
+  if (c->dheads > 32) return uns("at most 32 depformer heads");
+  if ((c->weight_dtype != RQ_F32 && c->weight_dtype != RQ_BF16) ||
+      (c->kv_dtype != RQ_F32 && c->kv_dtype != RQ_BF16))
+    return bad("dtype must be RQ_F32 or RQ_BF16");
+  if (c->dim % 8 || c->hidden % 8 || c->ddim % 8 || c->dhidden % 8)
+    return uns("dim, hidden, ddim and dhidden must be multiples of 8");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
+  return RQ_OK;
+}
+
+}  // namespace
+
+namespace {
+
+GemvParams base_params(const rq_handle* h, const GemvPlan& pl, const void* W) {
+  GemvParams p{};
+  p.W = W;
+  p.pl = pl;
+  p.eps = h->cfg.rms_eps;
+  p.kv_bf16 = h->kvbf ? 1 : 0;
+  p.head_dim = h->cfg.head_dim;
+  p.context = h->cfg.context;
+  p.rope_theta = h->cfg.rope_theta;
+  p.offsets = h->offsets;
+  p.keys = h->keys;
+  p.d_in = h->d_in;
+  p.batch = h->cfg.batch;
+  p.status = h->d_status();
+  return p;
+}
+
+// ---- temporal layer l ("moshi_lm.rs", `temporal_step`)
+cudaError_t op_qkv(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
+  const rq_config& c = h->cfg;
+  const size_t D = c.dim, C = c.context, L = c.layers;
+  GemvParams p = base_params(h, h->p_qkv, woff(h->w.in_proj, (size_t)l * 3 * D * D, h->wes));
+  p.in = h->x;
+  p.in_bs = D;
+  p.alpha = h->w.norm1 + (size_t)l * D;
+  p.out = h->q;
+  p.out_bs = D;
+  p.kcache = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
+  p.vcache = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
+  p.kv_bs = (long long)(L * C * D);
+  return launch_gemv(p, PRO_RMS, EPI_QKV, h->wbf, c.batch, s, pdl);
+}
+
+cudaError_t op_attn(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
+  const rq_config& c = h->cfg;
+  const size_t D = c.dim, C = c.context, L = c.layers;
+  AttnParams a{};
+  a.q = h->q;
+  a.kc = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
+  a.vc = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
+  a.kv_bs = (long long)(L * C * D);
+  a.offsets = h->offsets;
+  a.part = h->part;
+  a.counters = h->counters;
+  a.out = h->attn;
+  a.D = c.dim;
+  a.H = c.heads;
+  a.hd = c.head_dim;
+  a.C = c.context;
+  a.kps = h->kps;
+  a.nsplit = h->nsplit;
+  a.batch = c.batch;
+  a.status = h->d_status();
+  return launch_attn(a, h->kvbf, s, pdl);
+}
+
+cudaError_t op_out(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
+  const size_t D = h->cfg.dim;
+  GemvParams p = base_params(h, h->p_out, woff(h->w.out_proj, (size_t)l * D * D, h->wes));
+  p.in = h->attn;
+  p.in_bs = D;
+  p.out = h->x;
+  p.out_bs = D;
+  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, h->cfg.batch, s, pdl);
+}
+
+cudaError_t op_gate_in(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
+  const size_t D = h->cfg.dim, F = h->cfg.hidden;
+  GemvParams p = base_params(h, h->p_gin, woff(h->w.gate_in, (size_t)l * 2 * F * D, h->wes));
+  p.w_half = (long long)(F * D);
+  p.in = h->x;
+  p.in_bs = D;
+  p.alpha = h->w.norm2 + (size_t)l * D;
+  p.out = h->u;
+  p.out_bs = F;
+  return launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wbf, h->cfg.batch, s, pdl);
+}
+
+cudaError_t op_gate_out(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
+  const size_t D = h->cfg.dim, F = h->cfg.hidden;
+  GemvParams p = base_params(h, h->p_gout, woff(h->w.gate_out, (size_t)l * D * F, h->wes));
+  p.in = h->u;
+  p.in_bs = F;
+  p.out = h->x;
+  p.out_bs = D;
+  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, h->cfg.batch, s, pdl);
+}
+
+// out_norm + text head + first-wins argmax ("moshi_lm.rs", `step_ext` steps 4-5)
+cudaError_t op_head(const rq_handle* h, cudaStream_t s, bool pdl) {
+  const size_t D = h->cfg.dim, V = h->cfg.text_card;
+  GemvParams p = base_params(h, h->p_head, h->w.text_linear);
+  p.in = h->x;
+  p.in_bs = D;
+  p.alpha = h->w.out_norm;
+  p.side_out = h->tout;
+  p.side_bs = D;
+  p.out = h->text_logits;
+  p.out_bs = V;
+  p.key_index = 0;
+  return launch_gemv(p, PRO_RMS, EPI_ARGMAX, h->wbf, h->cfg.batch, s, pdl);
+}
+
+// ---- depformer step cb ("moshi_lm.rs", `depformer_cycle`)
+// per-frame K/V layout [B][DL][2][8][DD]: K of (layer l, step j) at ((l*2+0)*8+j)*DD
+size_t dkv_off(const rq_handle* h, int l, int kv, int j) {
+  const size_t DD = h->cfg.ddim;
+  return (((size_t)l * 2 + kv) * 8 + j) * DD;
+}
+
+cudaError_t op_dep_in(const rq_handle* h, int cb, cudaStream_t s, bool pdl) {
+  const rq_config& c = h->cfg;
+  const size_t D = c.dim, DD = c.ddim, A = c.audio_card;
+  GemvParams p = base_params(h, h->p_depin, woff(h->w.dep_in, (size_t)cb * DD * D, h->wes));
+  p.in = h->tout;
+  p.in_bs = D;
+  p.out = h->dx;
+  p.out_bs = DD;
+  p.emb = cb == 0 ? h->w.dep_text_emb : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, h->wes);
+  p.key_index = cb;  // text token for cb 0, else audio cb-1 (key 1 + (cb-1))
+  return launch_gemv(p, PRO_PLAIN, EPI_DEPIN, h->wbf, c.batch, s, pdl);
+}
+
+cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pdl) {
+  const rq_config& c = h->cfg;
+  const size_t DD = c.ddim, DF = c.dhidden;
+  const size_t ls = (size_t)l * 8 + cb;
+  const long long dkv_bs = (long long)c.dlayers * 2 * 8 * DD;
+  cudaError_t e;
+  {  // rms_norm + in_projs[cb] -> q, per-frame K/V entry cb
+    GemvParams p = base_params(h, h->p_dqkv, woff(h->w.d_in_proj, ls * 3 * DD * DD, h->wes));
+    p.in = h->dx;
+    p.in_bs = DD;
+    p.alpha = h->w.dnorm1 + (size_t)l * DD;
+    p.out = h->dq;
+    p.out_bs = DD;
+    p.dk_out = h->dkv + dkv_off(h, l, 0, cb);
+    p.dv_out = h->dkv + dkv_off(h, l, 1, cb);
+    p.dkv_bs = dkv_bs;
+    if ((e = launch_gemv(p, PRO_RMS, EPI_DQKV, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+  }
+  {  // attention over entries 0..cb fused as the prologue of out_projs[cb] + residual
+    GemvParams p = base_params(h, h->p_dout, woff(h->w.d_out_proj, ls * DD * DD, h->wes));
+    p.dq = h->dq;
+    p.dq_bs = DD;
+    p.dk = h->dkv + dkv_off(h, l, 0, 0);
+    p.dv = h->dkv + dkv_off(h, l, 1, 0);
+    p.dkv_bs = dkv_bs;
+    p.n_keys = cb + 1;
+    p.dheads = c.dheads;
+    p.dhead_dim = c.dhead_dim;
+    p.in = h->dq;  // unused by this prologue
+    p.out = h->dx;
+    p.out_bs = DD;
+    if ((e = launch_gemv(p, PRO_DATTN, EPI_RESID, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+  }
+  {  // rms_norm + gating[cb].linear_in + silu gate
+    GemvParams p = base_params(h, h->p_dgin, woff(h->w.d_gate_in, ls * 2 * DF * DD, h->wes));
+    p.w_half = (long long)(DF * DD);
+    p.in = h->dx;
+    p.in_bs = DD;
+    p.alpha = h->w.dnorm2 + (size_t)l * DD;
+    p.out = h->du;
+    p.out_bs = DF;
+    if ((e = launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+  }
+  {  // gating[cb].linear_out + residual
+    GemvParams p = base_params(h, h->p_dgout, woff(h->w.d_gate_out, ls * DD * DF, h->wes));
+    p.in = h->du;
+    p.in_bs = DF;
+    p.out = h->dx;
+    p.out_bs = DD;
+    if ((e = launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t op_linear(const rq_handle* h, int cb, cudaStream_t s, bool pdl) {
+  const rq_config& c = h->cfg;
+  const size_t DD = c.ddim, A = c.audio_card;
+  GemvParams p = base_params(h, h->p_lin, woff(h->w.linears, (size_t)cb * A * DD, h->wes));
+  p.in = h->dx;
+  p.in_bs = DD;
+  p.out = h->audio_logits + (size_t)cb * A;
+  p.out_bs = 8 * A;
+  p.key_index = 1 + cb;
+  return launch_gemv(p, PRO_PLAIN, EPI_ARGMAX, h->wbf, c.batch, s, pdl);
+}
+
+FrameParams frame_params(const rq_handle* h) {
+  FrameParams f{};
+  f.B = h->cfg.batch;
+  f.D = h->cfg.dim;
+  f.V = h->cfg.text_card;
+  f.A = h->cfg.audio_card;
+  f.ring = h->ring;
+  f.offsets = h->offsets;
+  f.d_in = h->d_in;
+  f.d_out = h->d_out_words();
+  f.d_has = h->d_has();
+  f.keys = h->keys;
+  f.emb = h->w.emb;
+  f.text_emb = h->w.text_emb;
+  f.x = h->x;
+  f.emb_sum = h->emb_sum;
+  return f;
+}
+
+// One whole frame, in the page's order ("moshi_lm.rs", `step_ext` steps 1-8).
+cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
+  cudaError_t e;
+  const FrameParams f = frame_params(h);
+  if ((e = launch_frame_begin(f, h->wbf, s)) != cudaSuccess) return e;
+  for (int l = 0; l < h->cfg.layers; ++l) {
+    if ((e = op_qkv(h, l, s, true)) != cudaSuccess) return e;
+    if ((e = op_attn(h, l, s, true)) != cudaSuccess) return e;
+    if ((e = op_out(h, l, s, true)) != cudaSuccess) return e;
+    if ((e = op_gate_in(h, l, s, true)) != cudaSuccess) return e;
+    if ((e = op_gate_out(h, l, s, true)) != cudaSuccess) return e;
+  }
+  if ((e = op_head(h, s, true)) != cudaSuccess) return e;
+  for (int cb = 0; cb < 8; ++cb) {
+    if ((e = op_dep_in(h, cb, s, true)) != cudaSuccess) return e;
+    for (int l = 0; l < h->cfg.dlayers; ++l)
+      if ((e = op_dlayer(h, cb, l, s, true)) != cudaSuccess) return e;
+    if ((e = op_linear(h, cb, s, true)) != cudaSuccess) return e;
+  }
+  return launch_frame_end(f, s, true);
+}
+
+}  // namespace
+
+namespace {
+
+void free_all(rq_handle* h) {
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  void* dev[] = {h->ring, h->offsets, h->kcache, h->vcache, h->d_in, h->d_outb, h->x,
+                 h->emb_sum, h->q, h->attn, h->u, h->tout, h->text_logits, h->audio_logits,
+                 h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters};
+  for (void* p : dev)
+    if (p) cudaFree(p);
+  if (h->h_in) cudaFreeHost(h->h_in);
+  if (h->h_out) cudaFreeHost(h->h_out);
+  if (h->cap) cudaStreamDestroy(h->cap);
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t bytes) {
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes < 16 ? 16 : bytes);
+}
+
+rq_status plan_all(rq_handle* h, std::string* why) {
+  const rq_config& c = h->cfg;
+  const int es = h->wes, sms = h->num_sms;
+  h->p_qkv = plan_gemv(3 * c.dim, c.dim, es, false, true, sms);
+  h->p_out = plan_gemv(c.dim, c.dim, es, false, false, sms);
+  h->p_gin = plan_gemv(c.hidden, c.dim, es, true, false, sms);
+  h->p_gout = plan_gemv(c.dim, c.hidden, es, false, false, sms);
+  h->p_head = plan_gemv(c.text_card, c.dim, es, false, false, sms);
+  h->p_depin = plan_gemv(c.ddim, c.dim, es, false, false, sms);
+  h->p_dqkv = plan_gemv(3 * c.ddim, c.ddim, es, false, false, sms);
+  h->p_dout = plan_gemv(c.ddim, c.ddim, es, false, false, sms);
+  h->p_dgin = plan_gemv(c.dhidden, c.ddim, es, true, false, sms);
+  h->p_dgout = plan_gemv(c.ddim, c.dhidden, es, false, false, sms);
+  h->p_lin = plan_gemv(c.audio_card, c.ddim, es, false, false, sms);
+  const GemvPlan* all[] = {&h->p_qkv, &h->p_out, &h->p_gin, &h->p_gout, &h->p_head, &h->p_depin,
+                           &h->p_dqkv, &h->p_dout, &h->p_dgin, &h->p_dgout, &h->p_lin};
+  for (const GemvPlan* p : all) {
+    if (gemv_chunks_per_thread(*p, es) > kGemvMaxChunks) {
+      *why = "a reduction length is too long for the GEMV kernel";
+      return RQ_ERR_UNSUPPORTED;
+    }
+    if (p->smem > 200 * 1024) {
+      *why = "a GEMV tile does not fit in shared memory";
+      return RQ_ERR_UNSUPPORTED;
+    }
+  }
+  h->kps = 64;
+  h->nsplit = (c.context + h->kps - 1) / h->kps;
+  return RQ_OK;
+}
+
+rq_status create_impl(rq_handle* h) {
+  const rq_config& c = h->cfg;
+  const size_t B = c.batch, D = c.dim, L = c.layers, C = c.context, F = c.hidden;
+  const size_t V = c.text_card, A = c.audio_card, DD = c.ddim, DL = c.dlayers, DF = c.dhidden;
+  RQ_CUDA(h, cudaGetDevice(&h->device));
+  RQ_CUDA(h, cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
+  std::string why;
+  rq_status st = plan_all(h, &why);
+  if (st != RQ_OK) return fail(h, st, why);
+  RQ_CUDA(h, gemv_configure_all());
+  RQ_CUDA(h, cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
+  auto A_ = [&](cudaError_t e, const char* what) -> rq_status {
+    if (e == cudaSuccess) return RQ_OK;
+    h->err = std::string("allocation failed: ") + what + ": " + cudaGetErrorString(e);
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? RQ_ERR_OOM : RQ_ERR_CUDA;
+  };
+#define RQ_ALLOC(ptr, bytes)                                   \
+  if ((st = A_(dalloc(&(ptr), (bytes)), #ptr)) != RQ_OK) return st;
+  RQ_ALLOC(h->ring, B * kStreams * kRing * 4);
+  RQ_ALLOC(h->offsets, B * 4);
+  RQ_ALLOC(h->kcache, B * L * C * D * h->kves);
+  RQ_ALLOC(h->vcache, B * L * C * D * h->kves);
+  RQ_ALLOC(h->d_in, h->io.in_words() * 4);
+  RQ_ALLOC(h->d_outb, h->io.out_bytes());
+  RQ_ALLOC(h->x, B * D * 4);
+  RQ_ALLOC(h->emb_sum, B * D * 4);
+  RQ_ALLOC(h->q, B * D * 4);
+  RQ_ALLOC(h->attn, B * D * 4);
+  RQ_ALLOC(h->u, B * F * 4);
+  RQ_ALLOC(h->tout, B * D * 4);
+  RQ_ALLOC(h->text_logits, B * V * 4);
+  RQ_ALLOC(h->audio_logits, B * 8 * A * 4);
+  RQ_ALLOC(h->keys, B * 9 * 8);
+  RQ_ALLOC(h->dx, B * DD * 4);
+  RQ_ALLOC(h->dq, B * DD * 4);
+  RQ_ALLOC(h->dkv, B * DL * 2 * 8 * DD * 4);
+  RQ_ALLOC(h->du, B * DF * 4);
+  RQ_ALLOC(h->part, B * (size_t)c.heads * h->nsplit * (c.head_dim + 2) * 4);
+  RQ_ALLOC(h->counters, B * (size_t)c.heads * 4);
+#undef RQ_ALLOC
+  if ((st = A_(cudaMallocHost(reinterpret_cast<void**>(&h->h_in), h->io.in_words() * 4), "h_in")) != RQ_OK)
+    return st;
+  if ((st = A_(cudaMallocHost(reinterpret_cast<void**>(&h->h_out), h->io.out_bytes()), "h_out")) != RQ_OK)
+    return st;
+  std::memset(h->h_in, 0, h->io.in_words() * 4);
+  // fresh sessions, zeroed scratch, cleared status
+  RQ_CUDA(h, cudaMemsetAsync(h->counters, 0, B * (size_t)c.heads * 4, h->cap));
+  RQ_CUDA(h, cudaMemsetAsync(h->d_outb, 0, h->io.out_bytes(), h->cap));
+  RQ_CUDA(h, cudaMemsetAsync(h->d_in, 0, h->io.in_words() * 4, h->cap));
+  RQ_CUDA(h, cudaMemsetAsync(h->keys, 0, B * 9 * 8, h->cap));
+  RQ_CUDA(h, launch_reset(h->ring, h->offsets, (int)B, -1, h->cap));
+  RQ_CUDA(h, cudaStreamSynchronize(h->cap));
+  h->host_off.assign(B, 0);
+  // capture one frame as a graph (programmatic edges between consecutive kernels)
+  RQ_CUDA(h, cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue_frame(h, h->cap);
+  cudaGraph_t g = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(h->cap, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(h, e, "frame capture");
+  }
+  if (e2 != cudaSuccess) return cuda_fail(h, e2, "cudaStreamEndCapture");
+  h->graph = g;
+  RQ_CUDA(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
+  size_t n = 0;
+  RQ_CUDA(h, cudaGraphGetNodes(h->graph, nullptr, &n));
+  std::vector<cudaGraphNode_t> nodes(n);
+  RQ_CUDA(h, cudaGraphGetNodes(h->graph, nodes.data(), &n));
+  int k = 0;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType t;
+    RQ_CUDA(h, cudaGraphNodeGetType(nodes[i], &t));
+    if (t == cudaGraphNodeTypeKernel) ++k;
+  }
+  h->n_kernels = k;
+  RQ_CUDA(h, cudaGraphUpload(h->exec, h->stream));
+  return RQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rq_status rq_create(const rq_config* cfg, const rq_weights* w, void* cuda_stream,
+                    rq_handle** out) {
+  if (!out) return RQ_ERR_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return RQ_ERR_ARG;
+  std::string why;
+  rq_status st = validate_config(cfg, &why);
+  if (st != RQ_OK) {
+    g_create_err = why;
+    return st;
+  }
+  const void* ptrs[] = {w->emb, w->text_emb, w->norm1, w->in_proj, w->out_proj, w->norm2,
+                        w->gate_in, w->gate_out, w->out_norm, w->text_linear, w->dep_in,
+                        w->dep_text_emb, w->dep_emb, w->dnorm1, w->dnorm2, w->d_in_proj,
+                        w->d_out_proj, w->d_gate_in, w->d_gate_out, w->linears};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) {
+      g_create_err = "a weight pointer is NULL or not 16-byte aligned";
+      return RQ_ERR_ARG;
+    }
+  rq_handle* h = new (std::nothrow) rq_handle();
+  if (!h) return RQ_ERR_OOM;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  h->wbf = cfg->weight_dtype == RQ_BF16;
+  h->kvbf = cfg->kv_dtype == RQ_BF16;
+  h->wes = h->wbf ? 2 : 4;
+  h->kves = h->kvbf ? 2 : 4;
+  h->io = IoLayout{cfg->batch};
+  st = create_impl(h);
+  if (st != RQ_OK) {
+    g_create_err = h->err;
+    free_all(h);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return RQ_OK;
+}
+
+void rq_destroy(rq_handle* h) {
+  if (!h) return;
+  cudaStreamSynchronize(h->stream);
+  free_all(h);
+  delete h;
+}
+
+}  // extern "C"
+
+namespace {
+
+rq_status check_usable(rq_handle* h) {
+  if (!h) return RQ_ERR_ARG;
+  if (h->poisoned) return RQ_ERR_POISONED;
+  return RQ_OK;
+}
+
+// read the status word of the last frame (already copied to h_out) and poison on error
+rq_status absorb_status(rq_handle* h, uint32_t status) {
+  if (status == 0) return RQ_OK;
+  h->poisoned = true;
+  if (status & kDevTimeout) {
+    h->err = "a bounded device-side wait timed out";
+    return RQ_ERR_TIMEOUT;
+  }
+  h->err = "device reported bad input";
+  return RQ_ERR_CUDA;
+}
+
+rq_status run_frame_host(rq_handle* h, const int32_t* user, const int32_t* forced,
+                         int32_t* own, int32_t* out_tokens, uint8_t* has_output) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  const int B = c.batch;
+  if (!user) return fail(h, RQ_ERR_ARG, "user_tokens is NULL");
+  for (int i = 0; i < B * 8; ++i)
+    if (user[i] < -1 || user[i] > c.audio_card)
+      return fail(h, RQ_ERR_TOKEN, "user token outside [-1, audio_card]");
+  if (forced) {
+    for (int b = 0; b < B; ++b) {
+      if (forced[b * 9] < 0 || forced[b * 9] >= c.text_card)
+        return fail(h, RQ_ERR_TOKEN, "forced text token outside [0, text_card)");
+      for (int k = 1; k < 9; ++k)
+        if (forced[b * 9 + k] < 0 || forced[b * 9 + k] >= c.audio_card)
+          return fail(h, RQ_ERR_TOKEN, "forced audio token outside [0, audio_card)");
+    }
+  }
+  const IoLayout& io = h->io;
+  std::memcpy(h->h_in + io.user_off(), user, (size_t)B * 8 * 4);
+  if (forced) {
+    std::memcpy(h->h_in + io.forced_off(), forced, (size_t)B * 9 * 4);
+    for (int b = 0; b < B; ++b) h->h_in[io.flag_off() + b] = 1;
+  } else {
+    for (int b = 0; b < B; ++b) h->h_in[io.flag_off() + b] = 0;
+  }
+  RQ_CUDA(h, cudaMemcpyAsync(h->d_in, h->h_in, io.in_words() * 4, cudaMemcpyHostToDevice, h->stream));
+  h->forcing_dirty = forced != nullptr;
+  RQ_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  RQ_CUDA(h, cudaMemcpyAsync(h->h_out, h->d_outb, io.out_bytes(), cudaMemcpyDeviceToHost, h->stream));
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  for (int b = 0; b < B; ++b) h->host_off[b] += 1;
+  uint32_t status;
+  std::memcpy(&status, h->h_out + io.status_off_bytes(), 4);
+  if ((st = absorb_status(h, status)) != RQ_OK) return st;
+  const int32_t* words = reinterpret_cast<const int32_t*>(h->h_out);
+  if (own) std::memcpy(own, words + io.own_off(), (size_t)B * 9 * 4);
+  if (out_tokens) std::memcpy(out_tokens, words + io.out_off(), (size_t)B * 9 * 4);
+  if (has_output) std::memcpy(has_output, h->h_out + io.has_off_bytes(), (size_t)B);
+  return RQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rq_status rq_step(rq_handle* h, const int32_t* user_tokens, int32_t* out_tokens,
+                  uint8_t* has_output) {
+  return run_frame_host(h, user_tokens, nullptr, nullptr, out_tokens, has_output);
+}
+
+rq_status rq_step_forced(rq_handle* h, const int32_t* user_tokens, const int32_t* forced,
+                         int32_t* own_tokens, int32_t* out_tokens, uint8_t* has_output) {
+  if (!forced) return fail(h, RQ_ERR_ARG, "forced is NULL");
+  return run_frame_host(h, user_tokens, forced, own_tokens, out_tokens, has_output);
+}
+
+rq_status rq_step_device(rq_handle* h, const int32_t* d_user, int32_t* d_out_tokens,
+                         uint8_t* d_has_output) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  if (!d_user) return fail(h, RQ_ERR_ARG, "d_user is NULL");
+  const IoLayout& io = h->io;
+  const int B = h->cfg.batch;
+  RQ_CUDA(h, cudaMemcpyAsync(h->d_in + io.user_off(), d_user, (size_t)B * 8 * 4,
+                             cudaMemcpyDeviceToDevice, h->stream));
+  if (h->forcing_dirty) {
+    RQ_CUDA(h, cudaMemsetAsync(h->d_in + io.flag_off(), 0, (size_t)B * 4, h->stream));
+    h->forcing_dirty = false;
+  }
+  RQ_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  if (d_out_tokens)
+    RQ_CUDA(h, cudaMemcpyAsync(d_out_tokens, h->d_out_words() + io.out_off(), (size_t)B * 9 * 4,
+                               cudaMemcpyDeviceToDevice, h->stream));
+  if (d_has_output)
+    RQ_CUDA(h, cudaMemcpyAsync(d_has_output, h->d_has(), (size_t)B, cudaMemcpyDeviceToDevice,
+                               h->stream));
+  for (int b = 0; b < B; ++b) h->host_off[b] += 1;
+  return RQ_OK;
+}
+
+rq_status rq_sync(rq_handle* h) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  uint32_t status = 0;
+  RQ_CUDA(h, cudaMemcpy(&status, h->d_status(), 4, cudaMemcpyDeviceToHost));
+  return absorb_status(h, status);
+}
+
+rq_status rq_get_logits(rq_handle* h, float* text, float* audio) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  if (text)
+    RQ_CUDA(h, cudaMemcpy(text, h->text_logits, (size_t)c.batch * c.text_card * 4, cudaMemcpyDeviceToHost));
+  if (audio)
+    RQ_CUDA(h, cudaMemcpy(audio, h->audio_logits, (size_t)c.batch * 8 * c.audio_card * 4,
+                          cudaMemcpyDeviceToHost));
+  return RQ_OK;
+}
+
+rq_status rq_get_trace(rq_handle* h, float* emb_sum, float* transformer_out) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const size_t n = (size_t)h->cfg.batch * h->cfg.dim * 4;
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  if (emb_sum) RQ_CUDA(h, cudaMemcpy(emb_sum, h->emb_sum, n, cudaMemcpyDeviceToHost));
+  if (transformer_out) RQ_CUDA(h, cudaMemcpy(transformer_out, h->tout, n, cudaMemcpyDeviceToHost));
+  return RQ_OK;
+}
+
+rq_status rq_get_ring(rq_handle* h, int32_t* ring, int32_t* offsets) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const int B = h->cfg.batch;
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  if (ring) RQ_CUDA(h, cudaMemcpy(ring, h->ring, (size_t)B * kStreams * kRing * 4, cudaMemcpyDeviceToHost));
+  if (offsets) RQ_CUDA(h, cudaMemcpy(offsets, h->offsets, (size_t)B * 4, cudaMemcpyDeviceToHost));
+  return RQ_OK;
+}
+
+rq_status rq_reset(rq_handle* h, int32_t session) {
+  if (!h) return RQ_ERR_ARG;
+  const int B = h->cfg.batch;
+  if (session < -1 || session >= B) return fail(h, RQ_ERR_ARG, "session out of range");
+  if (h->poisoned && session != -1) return RQ_ERR_POISONED;
+  if (session == -1) {
+    // clear the sticky CUDA error state of this thread, then every scratch word
+    cudaGetLastError();
+    RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->d_outb, 0, h->io.out_bytes(), h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->counters, 0, (size_t)B * h->cfg.heads * 4, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->keys, 0, (size_t)B * 9 * 8, h->stream));
+  }
+  RQ_CUDA(h, launch_reset(h->ring, h->offsets, B, session, h->stream));
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  for (int b = 0; b < B; ++b)
+    if (session == -1 || b == session) h->host_off[b] = 0;
+  if (session == -1) {
+    h->poisoned = false;
+    h->err.clear();
+  }
+  return RQ_OK;
+}
+
+rq_status rq_set_kv(rq_handle* h, int32_t session, int32_t n_pos, const void* k, const void* v) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (session < 0 || session >= c.batch) return fail(h, RQ_ERR_ARG, "session out of range");
+  if (n_pos < 0 || n_pos > c.context) return fail(h, RQ_ERR_ARG, "n_pos outside [0, context]");
+  if (n_pos > 0 && (!k || !v)) return fail(h, RQ_ERR_ARG, "k or v is NULL");
+  const size_t D = c.dim, C = c.context, L = c.layers, es = h->kves;
+  if (n_pos > 0) {
+    const size_t dst0 = (size_t)session * L * C * D * es;
+    RQ_CUDA(h, cudaMemcpy2DAsync(static_cast<char*>(h->kcache) + dst0, C * D * es, k,
+                                 (size_t)n_pos * D * es, (size_t)n_pos * D * es, L,
+                                 cudaMemcpyDefault, h->stream));
+    RQ_CUDA(h, cudaMemcpy2DAsync(static_cast<char*>(h->vcache) + dst0, C * D * es, v,
+                                 (size_t)n_pos * D * es, (size_t)n_pos * D * es, L,
+                                 cudaMemcpyDefault, h->stream));
+  }
+  RQ_CUDA(h, launch_set_offset(h->offsets, session, n_pos, h->stream));
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->host_off[session] = n_pos;
+  return RQ_OK;
+}
+
+rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
+                       double* bytes_per_launch) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (layer < 0 || layer >= c.layers || count < 0) return fail(h, RQ_ERR_ARG, "bad layer or count");
+  double bytes = 0;
+  switch (op) {
+    case RQ_OP_QKV: bytes = h->p_qkv.bytes; break;
+    case RQ_OP_OUT: bytes = h->p_out.bytes; break;
+    case RQ_OP_GATE_IN: bytes = h->p_gin.bytes; break;
+    case RQ_OP_GATE_OUT: bytes = h->p_gout.bytes; break;
+    case RQ_OP_HEAD: bytes = h->p_head.bytes; break;
+    case RQ_OP_ATTN:
+      for (int b = 0; b < c.batch; ++b) {
+        const int len = h->host_off[b] + 1 < c.context ? h->host_off[b] + 1 : c.context;
+        bytes += 2.0 * len * c.dim * h->kves;
+      }
+      break;
+    default: return fail(h, RQ_ERR_ARG, "unknown op");
+  }
+  if (bytes_per_launch) *bytes_per_launch = bytes;
+  for (int i = 0; i < count; ++i) {
+    cudaError_t e = cudaSuccess;
+    switch (op) {
+      case RQ_OP_QKV: e = op_qkv(h, layer, h->stream, true); break;
+      case RQ_OP_ATTN: e = op_attn(h, layer, h->stream, true); break;
+      case RQ_OP_OUT: e = op_out(h, layer, h->stream, true); break;
+      case RQ_OP_GATE_IN: e = op_gate_in(h, layer, h->stream, true); break;
+      case RQ_OP_GATE_OUT: e = op_gate_out(h, layer, h->stream, true); break;
+      case RQ_OP_HEAD: e = op_head(h, h->stream, true); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "rq_launch_op");
+  }
+  return RQ_OK;
+}
+
+int32_t rq_frame_kernel_count(const rq_handle* h) { return h ? h->n_kernels : 0; }
+
+const char* rq_last_error(const rq_handle* h) {
+  if (!h) return g_create_err.c_str();
+  return h->err.c_str();
+}
+
+const char* rq_status_string(rq_status s) {
+  switch (s) {
+    case RQ_OK: return "ok";
+    case RQ_ERR_ARG: return "invalid argument";
+    case RQ_ERR_TOKEN: return "token out of range";
+    case RQ_ERR_CUDA: return "CUDA error";
+    case RQ_ERR_OOM: return "out of memory";
+    case RQ_ERR_TIMEOUT: return "device-side wait timed out";
+    case RQ_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case RQ_ERR_POISONED: return "handle poisoned by an earlier error";
+  }
+  return "unknown status";
+}
+
+int32_t rq_abi_version(void) { return RQ_ABI_VERSION; }
+
+}  // extern "C"
