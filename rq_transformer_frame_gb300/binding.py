@@ -1,0 +1,218 @@
+"""ctypes binding of the C ABI in include/rq.h (argument marshalling only).
+
+Every step of the decode path runs in the CUDA library (_lib/librq.so); this module
+only moves pointers and sizes across the boundary.  There is no fallback: if the
+library is missing, loading it raises.  PyTorch is used for device memory and
+streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+from .configs import RQConfig
+
+LIBPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "librq.so")
+
+RQ_OK, RQ_ERR_ARG, RQ_ERR_TOKEN, RQ_ERR_CUDA = 0, 1, 2, 3
+RQ_ERR_OOM, RQ_ERR_TIMEOUT, RQ_ERR_UNSUPPORTED, RQ_ERR_POISONED = 4, 5, 6, 7
+RQ_F32, RQ_BF16 = 0, 1
+RQ_OP_QKV, RQ_OP_ATTN, RQ_OP_OUT, RQ_OP_GATE_IN, RQ_OP_GATE_OUT, RQ_OP_HEAD = range(6)
+
+WEIGHT_FIELDS = [
+    "emb", "text_emb", "norm1", "in_proj", "out_proj", "norm2", "gate_in",
+    "gate_out", "out_norm", "text_linear", "dep_in", "dep_text_emb", "dep_emb",
+    "dnorm1", "dnorm2", "d_in_proj", "d_out_proj", "d_gate_in", "d_gate_out",
+    "linears",
+]
+
+_CFG_INT_FIELDS = ["batch", "dim", "layers", "heads", "head_dim", "hidden", "context",
+                   "text_card", "audio_card", "ddim", "dlayers", "dheads", "dhead_dim",
+                   "dhidden", "weight_dtype", "kv_dtype"]
+
+
+class RqConfig(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in _CFG_INT_FIELDS] + \
+        [("rms_eps", C.c_float), ("rope_theta", C.c_float)]
+
+
+class RqWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class RQError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("rq status %d: %s" % (status, msg))
+        self.status = status
+
+
+_LIB = None
+
+
+def load() -> C.CDLL:
+    """Load librq.so; raises if it has not been built (no CPU fallback exists)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIBPATH):
+        raise RuntimeError("CUDA library %s is not built; run __graft_entry__.build()" % LIBPATH)
+    L = C.CDLL(LIBPATH)
+    P, I32 = C.c_void_p, C.c_int32
+    L.rq_create.argtypes = [C.POINTER(RqConfig), C.POINTER(RqWeights), P, C.POINTER(P)]
+    L.rq_destroy.argtypes = [P]
+    L.rq_destroy.restype = None
+    L.rq_reset.argtypes = [P, I32]
+    L.rq_step.argtypes = [P, P, P, P]
+    L.rq_step_forced.argtypes = [P, P, P, P, P, P]
+    L.rq_step_device.argtypes = [P, P, P, P]
+    L.rq_sync.argtypes = [P]
+    L.rq_get_logits.argtypes = [P, P, P]
+    L.rq_get_trace.argtypes = [P, P, P]
+    L.rq_get_ring.argtypes = [P, P, P]
+    L.rq_set_kv.argtypes = [P, I32, I32, P, P]
+    L.rq_launch_op.argtypes = [P, I32, I32, I32, C.POINTER(C.c_double)]
+    L.rq_frame_kernel_count.argtypes = [P]
+    L.rq_frame_kernel_count.restype = I32
+    L.rq_last_error.argtypes = [P]
+    L.rq_last_error.restype = C.c_char_p
+    L.rq_status_string.argtypes = [C.c_int]
+    L.rq_status_string.restype = C.c_char_p
+    L.rq_abi_version.restype = I32
+    for f in ("rq_create", "rq_reset", "rq_step", "rq_step_forced", "rq_step_device",
+              "rq_sync", "rq_get_logits", "rq_get_trace", "rq_get_ring", "rq_set_kv",
+              "rq_launch_op"):
+        getattr(L, f).restype = C.c_int
+    _LIB = L
+    return L
+
+
+def make_config(cfg: RQConfig) -> RqConfig:
+    c = RqConfig()
+    for n in _CFG_INT_FIELDS:
+        if n == "weight_dtype":
+            v = RQ_BF16 if cfg.weight_dtype == "bf16" else RQ_F32
+        elif n == "kv_dtype":
+            v = RQ_BF16 if cfg.kv_dtype == "bf16" else RQ_F32
+        else:
+            v = getattr(cfg, n)
+        setattr(c, n, int(v))
+    c.rms_eps = cfg.eps
+    c.rope_theta = cfg.rope_theta
+    return c
+
+
+def upload_weights(host: dict, device="cuda") -> dict:
+    """Copy host weight tensors (synth.make_weights) to contiguous device tensors."""
+    return {k: v.to(device, non_blocking=False).contiguous() for k, v in host.items()}
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        assert t.flags["C_CONTIGUOUS"]
+        return t.ctypes.data
+    assert t.is_contiguous()
+    return t.data_ptr()
+
+
+class Decoder:
+    """One rq_handle: B sessions of the per-frame decode step on the current device.
+
+    `weights` are device tensors in the layout of include/rq.h (kept referenced for
+    the handle's lifetime).  `stream` is a torch.cuda.Stream (default: the current
+    stream)."""
+
+    def __init__(self, cfg: RQConfig, weights: dict, stream=None):
+        self.L = load()
+        self.cfg = cfg
+        self.weights = weights
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self._c = make_config(cfg)
+        self._w = RqWeights(**{n: weights[n].data_ptr() for n in WEIGHT_FIELDS})
+        h = C.c_void_p()
+        st = self.L.rq_create(C.byref(self._c), C.byref(self._w),
+                              C.c_void_p(self.stream.cuda_stream), C.byref(h))
+        if st != RQ_OK:
+            raise RQError(st, self.L.rq_last_error(None).decode())
+        self.h = h
+        B = cfg.batch
+        self._out = np.zeros((B, 9), np.int32)
+        self._own = np.zeros((B, 9), np.int32)
+        self._has = np.zeros(B, np.uint8)
+
+    def _check(self, st):
+        if st != RQ_OK:
+            raise RQError(st, self.L.rq_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.rq_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def step(self, user):
+        """user [B][8] int32 -> (out [B][9], has_output [B] bool)."""
+        u = np.ascontiguousarray(user, dtype=np.int32).reshape(self.cfg.batch, 8)
+        self._check(self.L.rq_step(self.h, _p(u), _p(self._out), _p(self._has)))
+        return self._out.copy(), self._has.astype(bool)
+
+    def step_forced(self, user, forced):
+        """-> (own [B][9], out [B][9], has_output [B])."""
+        u = np.ascontiguousarray(user, dtype=np.int32).reshape(self.cfg.batch, 8)
+        f = np.ascontiguousarray(forced, dtype=np.int32).reshape(self.cfg.batch, 9)
+        self._check(self.L.rq_step_forced(self.h, _p(u), _p(f), _p(self._own), _p(self._out),
+                                          _p(self._has)))
+        return self._own.copy(), self._out.copy(), self._has.astype(bool)
+
+    def step_device(self, d_user, d_out=None, d_has=None):
+        """Enqueue a frame with device-resident int32 [B][8] input; no sync."""
+        self._check(self.L.rq_step_device(self.h, _p(d_user), _p(d_out), _p(d_has)))
+
+    def sync(self):
+        self._check(self.L.rq_sync(self.h))
+
+    def reset(self, session: int = -1):
+        self._check(self.L.rq_reset(self.h, int(session)))
+
+    def logits(self):
+        c = self.cfg
+        text = np.zeros((c.batch, c.text_card), np.float32)
+        audio = np.zeros((c.batch, 8, c.audio_card), np.float32)
+        self._check(self.L.rq_get_logits(self.h, _p(text), _p(audio)))
+        return text, audio
+
+    def trace(self):
+        c = self.cfg
+        emb = np.zeros((c.batch, c.dim), np.float32)
+        tout = np.zeros((c.batch, c.dim), np.float32)
+        self._check(self.L.rq_get_trace(self.h, _p(emb), _p(tout)))
+        return emb, tout
+
+    def ring(self):
+        ring = np.zeros((self.cfg.batch, 17, 3), np.int32)
+        off = np.zeros(self.cfg.batch, np.int32)
+        self._check(self.L.rq_get_ring(self.h, _p(ring), _p(off)))
+        return ring, off
+
+    def set_kv(self, session: int, k, v):
+        """k, v: [layers][n_pos][dim] tensors in the K/V dtype (host or device)."""
+        k, v = k.contiguous(), v.contiguous()
+        self._check(self.L.rq_set_kv(self.h, int(session), int(k.shape[1]), _p(k), _p(v)))
+
+    def launch_op(self, op: int, layer: int, count: int) -> float:
+        b = C.c_double(0)
+        self._check(self.L.rq_launch_op(self.h, int(op), int(layer), int(count), C.byref(b)))
+        return b.value
+
+    @property
+    def kernels_per_frame(self) -> int:
+        return int(self.L.rq_frame_kernel_count(self.h))

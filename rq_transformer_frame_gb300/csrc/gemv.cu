@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
       }
       s_issued = i;
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ consumer warps
     pdl_wait();
