@@ -1,0 +1,372 @@
+"""Benchmark of the per-frame RQ-Transformer decode step on GB300.
+
+One step = one frame of the whole hot path for every session (ring cache,
+embedding sum, temporal decoder, text head, 8 depformer codebook steps, realign).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl native|reference]
+
+Prints ONE JSON line (rank 0).  `value` = session-frames/s with the user tokens
+already resident in HBM (rq_step_device), timed with CUDA events on the decode
+stream, max over ranks; `e2e` = the same through rq_step with host buffers (the
+host->device copy of the step's codes and the device->host read of its tokens inside
+the timed region).  N > 1 runs N independent replicas (sessions shard across GPUs;
+no collective on the data path), so scaling is weak.  The reference arm times the
+CPU oracle on the host cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {1: "moshi7b", 16: "moshi7b_b16", 64: "moshi7b_b64"}
+
+
+def frame_bytes(c, offsets) -> dict:
+    """Algorithmic bytes of one frame: every weight streamed once, the gathered
+    embedding rows, the live K/V window read once and one K/V row written."""
+    es, kv = c.weight_bytes, c.kv_bytes
+    D, L, F, V, A = c.dim, c.layers, c.hidden, c.text_card, c.audio_card
+    DD, DL, DF = c.ddim, c.dlayers, c.dhidden
+    temporal = L * (3 * D * D + D * D + 2 * F * D + D * F) * es
+    head = V * D * es
+    dep = 8 * DL * (3 * DD * DD + DD * DD + 2 * DF * DD + DD * DF) * es
+    dep_in = 8 * DD * D * es
+    lin = 8 * A * DD * es
+    emb = c.batch * (17 * D + 8 * DD) * es
+    kv_read = sum(2 * min(o + 1, c.context) * D * kv * L for o in offsets)
+    kv_write = c.batch * 2 * D * kv * L
+    w = temporal + head + dep + dep_in + lin
+    return {"weights": w, "temporal": temporal, "kv": kv_read + kv_write,
+            "total": w + emb + kv_read + kv_write}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def gemv_source_hash() -> str:
+    h = hashlib.sha256()
+    for n in ("gemv.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "rq_transformer_frame_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (the summary records the source hash)."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    hsh = re.search(r"gemv_source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not hsh or hsh.group(1) != gemv_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self) -> dict:
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": mx or None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- ranks
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_frames(cfg, w, users, max_frames: int, budget_s: float):
+    """Run oracle frames of session 0 until max_frames or the time budget; returns
+    (frames, seconds, threads)."""
+    import oracle
+    orc = oracle.Oracle(cfg, w)
+    st = orc.new_state()
+    n, t0 = 0, time.perf_counter()
+    while n < max_frames:
+        orc.step(st, users[n % len(users), 0])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return n, time.perf_counter() - t0, oracle.max_threads()
+
+
+def run_reference(args, cfg):
+    from rq_transformer_frame_gb300 import synth
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.make_weights(cfg.with_(batch=1), seed=0)
+    users = synth.batch_user_tokens(cfg, args.steps + args.warmup).numpy()
+    import oracle
+    orc = oracle.Oracle(cfg.with_(batch=1), w)
+    st = orc.new_state()
+    for t in range(args.warmup):
+        orc.step(st, users[t, 0])
+    t0 = time.perf_counter()
+    for t in range(args.steps):
+        orc.step(st, users[args.warmup + t, 0])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt  # session-frames/s of one session on the host cores
+    line = {
+        "impl": "reference", "metric": "frames/s", "value": value, "unit": "session-frames/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": 1,
+                   "note": "oracle timed on one session of the workload"},
+        "cpu_baseline": {"value": value, "unit": "session-frames/s",
+                         "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": "frames %d..%d of session 0" % (args.warmup, args.warmup + args.steps)},
+        "e2e": {"value": value, "unit": "session-frames/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- native arm
+def run_native(args, cfg):
+    import numpy as np
+    import torch
+
+    from rq_transformer_frame_gb300 import binding, synth
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    K, W, B = args.steps, args.warmup, cfg.batch
+    w_host = synth.make_weights(cfg, seed=0)
+    w_dev = binding.upload_weights(w_host, dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dec = binding.Decoder(cfg, w_dev, stream=stream)
+        if cfg.prefill:
+            for b in range(B):
+                k, v = synth.kv_prefill(cfg, b, device=dev)
+                dec.set_kv(b, k, v)
+                del k, v
+    users = synth.batch_user_tokens(cfg, W + 2 * K)
+    d_users = users.to(dev)
+    d_out = torch.zeros((B, 9), dtype=torch.int32, device=dev)
+    d_has = torch.zeros(B, dtype=torch.uint8, device=dev)
+    start0 = cfg.prefill
+
+    # ---- warm-up, then K device-resident frames timed with events on the stream
+    for t in range(W):
+        dec.step_device(d_users[t], d_out, d_has)
+    dec.sync()
+    barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for t in range(K):
+            dec.step_device(d_users[W + t], d_out, d_has)
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize(dev)
+    dec.sync()
+    barrier(ws)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    sec_max = max_over_ranks(sec, ws, dev)
+    value = ws * B * K / sec_max
+    clocks = clk.summary()
+    offs = [[start0 + W + t] * B for t in range(K)]
+    fb = [frame_bytes(cfg, o) for o in offs]
+    bytes_frame = sum(f["total"] for f in fb) / K
+
+    # ---- end to end through rq_step: host codes in, host tokens out, every step
+    users_h = users.numpy()
+    t0 = time.perf_counter()
+    for t in range(K):
+        dec.step(users_h[W + K + t])
+    e2e_sec = max_over_ranks(time.perf_counter() - t0, ws, dev)
+    e2e_value = ws * B * K / e2e_sec
+    h2d = B * 18 * 4
+    d2h = B * 18 * 4 + ((B + 3) // 4) * 4 + 4
+
+    # ---- per-kernel timing of the GEMVs (distinct layers, so nothing is L2-resident)
+    hbm_peak, peak_kind = peaks()
+    kernels = {}
+    names = {binding.RQ_OP_QKV: "qkv", binding.RQ_OP_OUT: "out_proj",
+             binding.RQ_OP_GATE_IN: "gate_in", binding.RQ_OP_GATE_OUT: "gate_out",
+             binding.RQ_OP_HEAD: "text_head"}
+    reps = 3
+    for op, name in names.items():
+        layers = range(cfg.layers) if op != binding.RQ_OP_HEAD else range(1)
+        nb = dec.launch_op(op, 0, 0)
+        dec.launch_op(op, 0, 1)  # warm
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = 0
+        for _ in range(reps if op != binding.RQ_OP_HEAD else 20):
+            for l in layers:
+                dec.launch_op(op, l, 1)
+                n += 1
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        kernels[name] = {"us_per_launch": round(us, 2), "bytes_per_launch": nb,
+                         "GB/s": round(nb / us / 1e3, 1),
+                         "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4)}
+    dec.reset(-1)
+    dom = kernels["gate_in"]
+    roof = {"kernel": "gemv_kernel<bf16, RMS, SWIGLU> (gate_in + SiLU gate, one layer)",
+            "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak, "unit": "GB/s",
+            "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
+            "traffic": profiled_traffic("gemv_moshi7b_b1.md")}
+
+    # ---- the oracle on this machine's host cores, on a bounded sample (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        c1 = cfg.with_(batch=1)
+        import oracle
+        orc_users = users_h
+        n, s, thr = oracle_frames(c1, w_host, orc_users, 200, args.cpu_budget)
+        cpu = {"value": n / s, "unit": "session-frames/s", "cores": thr, "kind": "oracle",
+               "sample": "first %d frames of session 0 of %s (%.1f s)" % (n, cfg.name, s)}
+
+    line = {
+        "metric": "frames/s", "value": value, "unit": "session-frames/s", "n_gpus": ws,
+        "steps": K, "warmup": W, "ms_per_step": 1e3 * sec_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": B, "frames_timed": K,
+                   "start_offset": start0 + W,
+                   "parallelism": "replicas" if ws > 1 else "single-gpu",
+                   "l2": "not flushed: %.1f GB of weights streamed per frame >> 126 MB L2"
+                         % (fb[0]["weights"] / 1e9),
+                   "arith": "bf16 weights and K/V, f32 activations and accumulation"},
+        "tokens_per_s": 9 * value,
+        "hbm": {"bytes_per_frame": bytes_frame, "GB/s": round(bytes_frame / (sec_max / K) / 1e9, 1),
+                "frac_of_measured": round(bytes_frame / (sec_max / K) / 1e9 / hbm_peak, 4),
+                "frac_of_8TBs": round(bytes_frame / (sec_max / K) / 8e12, 4)},
+        "roofline": roof, "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "session-frames/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * dec.kernels_per_frame,
+        "clocks": clocks,
+    }
+    dec.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=1, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None, help="override: a name from configs.CONFIGS")
+    args = ap.parse_args(argv)
+    from rq_transformer_frame_gb300 import configs
+    cfg = configs.CONFIGS[WORKLOADS[args.batch]]
+    if args.workload:
+        cfg = configs.CONFIGS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    import __graft_entry__
+    __graft_entry__.build()
+    return run_native(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
