@@ -75,3 +75,8 @@ MOSHI7B_B64 = MOSHI7B.with_(name="moshi7b_b64", batch=64, frames=100, prefill=29
                             user_seed=2000)
 
 CONFIGS = {c.name: c for c in (TINY, SMALL, MOSHI7B, MOSHI7B_B16, MOSHI7B_B64)}
+
+# Moshi-7B layer shapes with only 2 temporal layers: every kernel of the full model at
+# its real size, in ~3 GB of device memory (used for profiler captures).
+MOSHI7B_2L = MOSHI7B.with_(name="moshi7b_2layer", layers=2, frames=16)
+CONFIGS[MOSHI7B_2L.name] = MOSHI7B_2L

@@ -28,6 +28,12 @@ constexpr int kConsumers = 256;  // 8 consumer warps
 constexpr int kThreads = 288;    // + 1 producer warp
 constexpr int kXch = 6;          // max 16-byte chunks of x held per thread
 constexpr int kMaxAttPairs = 32 * 8;
+#ifndef RQ_GEMV_STAGE_BUDGET
+#define RQ_GEMV_STAGE_BUDGET (96 * 1024)  // shared-memory bytes of the weight ring
+#endif
+#ifndef RQ_GEMV_MAX_STAGES
+#define RQ_GEMV_MAX_STAGES 8
+#endif
 
 template <typename WT>
 struct Chunk;
@@ -201,20 +207,35 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
       }
     }
     if (PRO == PRO_DATTN) {
-      // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1
+      // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1.
+      // Scores: `tp` threads per (head, key) pair, float4 loads issued together, so
+      // the whole prologue costs two dependent round trips to L2.
       const int nk = p.n_keys, dh = p.dheads, hd = p.dhead_dim;
       const float* q = p.dq + (size_t)b * p.dq_bs;
       const float* dk = p.dk + (size_t)b * p.dkv_bs;
       const float* dv = p.dv + (size_t)b * p.dkv_bs;
       const float scale = 1.0f / sqrtf((float)hd);
-      for (int pr = warp; pr < dh * nk; pr += kConsumers / 32) {
+      const int npairs = dh * nk;
+      int tp = 32;
+      while (tp > 1 && tp * npairs > kConsumers) tp >>= 1;
+      if (tp > hd / 4) tp = hd / 4;
+      const int pr = tid / tp, sub = tid % tp;
+      float d = 0.f;
+      if (pr < npairs) {
         const int h = pr / nk, jk = pr % nk;
-        float d = 0.f;
-        for (int e = lane; e < hd; e += 32)
-          d = fmaf(q[h * hd + e], dk[(size_t)jk * K + h * hd + e], d);
-        d = warp_sum(d);
-        if (lane == 0) s_att[h * 8 + jk] = d * scale;
+        const float4* q4 = reinterpret_cast<const float4*>(q + h * hd);
+        const float4* k4 = reinterpret_cast<const float4*>(dk + (size_t)jk * K + h * hd);
+#pragma unroll 8
+        for (int e = sub; e < hd / 4; e += tp) {
+          const float4 a = q4[e], c4 = k4[e];
+          d = fmaf(a.x, c4.x, d);
+          d = fmaf(a.y, c4.y, d);
+          d = fmaf(a.z, c4.z, d);
+          d = fmaf(a.w, c4.w, d);
+        }
       }
+      for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
       bar_sync(1, kConsumers);
       if (tid < dh) {
         float mx = -__int_as_float(0x7f800000);
@@ -232,14 +253,26 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
       for (int j = 0; j < kXch; ++j) {
         const int c = tig + j * pl.tpr;
         if (c < CC) {
+          const int h = (c * V) / hd;  // a chunk never straddles two heads
+          float o[V];
 #pragma unroll
-          for (int v = 0; v < V; ++v) {
-            const int col = c * V + v;
-            const int h = col / hd;
-            float o = 0.f;
-            for (int jk = 0; jk < nk; ++jk) o += s_att[h * 8 + jk] * dv[(size_t)jk * K + col];
-            xr[j][v] = o;
+          for (int v = 0; v < V; ++v) o[v] = 0.f;
+#pragma unroll
+          for (int jk = 0; jk < 8; ++jk) {
+            if (jk < nk) {
+              const float pw = s_att[h * 8 + jk];
+#pragma unroll
+              for (int v = 0; v < V; v += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(dv + (size_t)jk * K + c * V + v);
+                o[v] += pw * f.x;
+                o[v + 1] += pw * f.y;
+                o[v + 2] += pw * f.z;
+                o[v + 3] += pw * f.w;
+              }
+            }
           }
+#pragma unroll
+          for (int v = 0; v < V; ++v) xr[j][v] = o[v];
         }
       }
     }
@@ -424,8 +457,8 @@ GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int nu
   pl.grid = pl.tiles < num_sms ? pl.tiles : num_sms;
   pl.max_tiles = (pl.tiles + pl.grid - 1) / pl.grid;
   const int tile_bytes = pl.tile_rows * row_bytes;
-  int ns = (96 * 1024) / tile_bytes;
-  ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+  int ns = (RQ_GEMV_STAGE_BUDGET) / tile_bytes;
+  ns = ns < 2 ? 2 : (ns > RQ_GEMV_MAX_STAGES ? RQ_GEMV_MAX_STAGES : ns);
   if (ns > pl.max_tiles) ns = pl.max_tiles < 1 ? 1 : pl.max_tiles;
   pl.n_stages = ns;
   const int wpg = tpr / 32;

@@ -1,0 +1,62 @@
+"""Time single operations of the decode step through the C ABI (rq_launch_op).
+
+  python -m rq_transformer_frame_gb300.op_probe --workload moshi7b_2layer \
+      --ops gate_in,qkv --reps 3 [--frames 4]
+
+Builds the decoder for the workload (seeded synthetic weights), runs `--frames`
+whole frames, then for each op launches it once per temporal layer `--reps` times,
+timed with CUDA events on the decoder's stream, and prints one JSON line per op.
+Used as the command under the profiler for the kernel summaries in profiles/.
+"""
+import argparse
+import json
+
+import torch
+
+from . import binding, configs, synth
+
+OPS = {"qkv": binding.RQ_OP_QKV, "attn": binding.RQ_OP_ATTN, "out_proj": binding.RQ_OP_OUT,
+       "gate_in": binding.RQ_OP_GATE_IN, "gate_out": binding.RQ_OP_GATE_OUT,
+       "text_head": binding.RQ_OP_HEAD}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="moshi7b_2layer")
+    ap.add_argument("--ops", default="gate_in")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--frames", type=int, default=2)
+    a = ap.parse_args(argv)
+    cfg = configs.CONFIGS[a.workload]
+    torch.cuda.set_device(0)
+    w = binding.upload_weights(synth.make_weights(cfg, seed=0))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dec = binding.Decoder(cfg, w, stream=stream)
+    users = synth.batch_user_tokens(cfg, max(a.frames, 1)).numpy()
+    for t in range(a.frames):
+        dec.step(users[t])
+    for name in a.ops.split(","):
+        op = OPS[name]
+        layers = range(1) if name == "text_head" else range(cfg.layers)
+        nb = dec.launch_op(op, 0, 0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = 0
+        for _ in range(a.reps):
+            for l in layers:
+                dec.launch_op(op, l, 1)
+                n += 1
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / max(n, 1)
+        print(json.dumps({"workload": cfg.name, "op": name, "launches": n,
+                          "us_per_launch": round(us, 2), "bytes_per_launch": nb,
+                          "GB/s": round(nb / max(us, 1e-9) / 1e3, 1)}), flush=True)
+    dec.reset(-1)
+    dec.close()
+
+
+if __name__ == "__main__":
+    main()
