@@ -1,441 +1,35 @@
-// gemv.cu -- weight-streaming GEMV with fused prologues and epilogues (sm_103a).
-//
-// Every linear of the decode step at batch 1 is y = W x with W [rows][K] read exactly
-// once per frame ("inferencelayer 0.2.4 -- src/moshi_lm.rs", `Band::mv`), so the
-// kernel is bound by HBM bandwidth.  Design:
-//   * one CTA per SM (grid = #SMs; two CTAs of consecutive kernels fit on an SM),
-//     each owning a contiguous run of row tiles, i.e. one contiguous byte range of W;
-//   * a producer warp streams tiles with cp.async.bulk into an mbarrier ring of
-//     shared-memory stages (L2 evict-first: weights are not reused within a frame);
-//     the first stages are issued BEFORE griddepcontrol.wait, so with programmatic
-//     dependent launch the weight stream of this GEMV overlaps the tail of the
-//     previous kernel;
-//   * 8 consumer warps keep their slice of x in registers (formed by the fused
-//     prologue: plain, RMSNorm, or the depformer's tiny attention) and read each
-//     weight element once from shared memory; per-warp partial sums of each row are
-//     kept in shared memory and reduced in a fixed order (deterministic);
-//   * the epilogue fuses what follows the linear on the page: residual add, SiLU gate,
-//     rotary embedding + K/V append, depformer K/V append, logits + first-wins argmax,
-//     depformer conditioning embedding.
-#include <cuda_bf16.h>
-
-#include "common.cuh"
+// gemv.cu -- host side of the streaming GEMV: tile plan and dispatch to the kernel
+// instantiations compiled in gemv_bf16.cu / gemv_f32.cu.
 #include "kernels.h"
 
-namespace rqk {
-
-constexpr int kConsumers = 256;  // 8 consumer warps
-constexpr int kThreads = 288;    // + 1 producer warp
-constexpr int kXch = 6;          // max 16-byte chunks of x held per thread
-constexpr int kMaxAttPairs = 32 * 8;
 #ifndef RQ_GEMV_STAGE_BUDGET
-#define RQ_GEMV_STAGE_BUDGET (96 * 1024)  // shared-memory bytes of the weight ring
+#define RQ_GEMV_STAGE_BUDGET (48 * 1024)  // shared-memory bytes of one CTA's weight ring
 #endif
 #ifndef RQ_GEMV_MAX_STAGES
 #define RQ_GEMV_MAX_STAGES 8
 #endif
+#ifndef RQ_GEMV_CTAS_PER_SM
+#define RQ_GEMV_CTAS_PER_SM 2
+#endif
+
+namespace rqk {
 
 template <typename WT>
-struct Chunk;
+cudaError_t gemv_dispatch(const GemvParams& p, int pro, int epi, int batch, cudaStream_t s,
+                          bool pdl);
+template <typename WT>
+cudaError_t gemv_configure(int max_smem);
 
-template <>
-struct Chunk<uint16_t> {  // bf16 bit patterns
-  static constexpr int V = 8;
-  static __device__ __forceinline__ float dot(const uint4 w, const float (&x)[8], float acc) {
-    acc = fmaf(bf16lo(w.x), x[0], acc);
-    acc = fmaf(bf16hi(w.x), x[1], acc);
-    acc = fmaf(bf16lo(w.y), x[2], acc);
-    acc = fmaf(bf16hi(w.y), x[3], acc);
-    acc = fmaf(bf16lo(w.z), x[4], acc);
-    acc = fmaf(bf16hi(w.z), x[5], acc);
-    acc = fmaf(bf16lo(w.w), x[6], acc);
-    acc = fmaf(bf16hi(w.w), x[7], acc);
-    return acc;
-  }
-  static __device__ __forceinline__ float elem(const void* base, size_t i) {
-    return __uint_as_float(((uint32_t)(static_cast<const uint16_t*>(base)[i])) << 16);
-  }
-};
+constexpr int kMaxDynSmem = 200 * 1024;
 
-template <>
-struct Chunk<float> {
-  static constexpr int V = 4;
-  static __device__ __forceinline__ float dot(const uint4 w, const float (&x)[4], float acc) {
-    acc = fmaf(__uint_as_float(w.x), x[0], acc);
-    acc = fmaf(__uint_as_float(w.y), x[1], acc);
-    acc = fmaf(__uint_as_float(w.z), x[2], acc);
-    acc = fmaf(__uint_as_float(w.w), x[3], acc);
-    return acc;
-  }
-  static __device__ __forceinline__ float elem(const void* base, size_t i) {
-    return static_cast<const float*>(base)[i];
-  }
-};
-
-__device__ __forceinline__ void store_kv(void* base, size_t i, float v, int bf16) {
-  if (bf16)
-    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
-  else
-    static_cast<float*>(base)[i] = v;
+static int nch_bucket(int n) {
+  if (n <= 1) return 1;
+  if (n <= 2) return 2;
+  if (n <= 3) return 3;
+  if (n <= 4) return 4;
+  if (n <= 6) return 6;
+  return 0;  // unsupported
 }
-
-template <typename WT, int PRO, int EPI>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
-  constexpr int V = Chunk<WT>::V;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_red[kConsumers / 32];
-  __shared__ float s_att[kMaxAttPairs];
-  __shared__ unsigned long long s_key[kThreads / 32];
-  __shared__ volatile int s_abort;
-  __shared__ int s_issued;
-
-  const GemvPlan& pl = p.pl;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
-  const int G = gridDim.x;
-  const int t0 = (int)(((long long)pl.tiles * blockIdx.x) / G);
-  const int t1 = (int)(((long long)pl.tiles * (blockIdx.x + 1)) / G);
-  const int nt = t1 - t0;
-  const int K = pl.K;
-  const uint32_t row_bytes = (uint32_t)K * (uint32_t)sizeof(WT);
-  const uint32_t tile_bytes = row_bytes * (uint32_t)pl.tile_rows;
-  const int NS = pl.n_stages;
-  const int wpg = pl.tpr >> 5;
-  const int out_per_tile = (EPI == EPI_SWIGLU) ? (pl.tile_rows >> 1) : pl.tile_rows;
-
-  uint8_t* stages = smem;
-  float* part = reinterpret_cast<float*>(smem + (size_t)NS * tile_bytes);
-  const int part_n = (pl.max_tiles * pl.tile_rows * wpg + 3) & ~3;
-  uint64_t* full = reinterpret_cast<uint64_t*>(part + part_n);
-  uint64_t* empty = full + NS;
-
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers / 32);
-    }
-    fence_barrier_init();
-    s_abort = 0;
-    s_issued = 0;
-  }
-  __syncthreads();
-  pdl_trigger();
-
-  if (warp == kConsumers / 32) {
-    // ------------------------------------------------------------ producer warp
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      const uint8_t* W = static_cast<const uint8_t*>(p.W);
-      int i = 0;
-      for (; i < nt; ++i) {
-        const int s = i % NS;
-        if (i >= NS) {
-          if (!mbar_wait(&empty[s], (uint32_t)(((i / NS) - 1) & 1))) {
-            atomicOr(p.status, kDevTimeout);
-            s_abort = 1;
-            break;
-          }
-        }
-        if (s_abort) break;
-        const int r0 = (t0 + i) * out_per_tile;
-        const int nv = min(out_per_tile, pl.n_out - r0);
-        const uint32_t bytes = (uint32_t)nv * row_bytes;
-        uint8_t* dst = stages + (size_t)s * tile_bytes;
-        if (EPI == EPI_SWIGLU) {
-          mbar_arrive_expect_tx(&full[s], 2u * bytes);
-          bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-          bulk_g2s(dst + (size_t)out_per_tile * row_bytes,
-                   W + (size_t)p.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes, &full[s],
-                   pol);
-        } else {
-          mbar_arrive_expect_tx(&full[s], bytes);
-          bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-        }
-      }
-      s_issued = i;
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ consumer warps
-    pdl_wait();
-    const int g = tid / pl.tpr, tig = tid % pl.tpr;
-    const int CC = K / V;
-    float xr[kXch][V];
-    const float* in = p.in + (size_t)b * p.in_bs;
-#pragma unroll
-    for (int j = 0; j < kXch; ++j) {
-      const int c = tig + j * pl.tpr;
-#pragma unroll
-      for (int v = 0; v < V; ++v) xr[j][v] = 0.f;
-      if (PRO != PRO_DATTN && c < CC) {
-#pragma unroll
-        for (int v = 0; v < V; v += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(in + (size_t)c * V + v);
-          xr[j][v] = f.x;
-          xr[j][v + 1] = f.y;
-          xr[j][v + 2] = f.z;
-          xr[j][v + 3] = f.w;
-        }
-      }
-    }
-    if (PRO == PRO_RMS) {
-      // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n))
-      float ss = 0.f;
-      for (int k = tid; k < K; k += kConsumers) {
-        const float v = in[k];
-        ss = fmaf(v, v, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_red[warp] = ss;
-      bar_sync(1, kConsumers);
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumers / 32; ++w) tot += s_red[w];
-      const float inv = 1.0f / sqrtf(p.eps + tot / (float)K);
-      const bool side = p.side_out != nullptr && blockIdx.x == 0 && g == 0;
-#pragma unroll
-      for (int j = 0; j < kXch; ++j) {
-        const int c = tig + j * pl.tpr;
-        if (c < CC) {
-#pragma unroll
-          for (int v = 0; v < V; ++v) xr[j][v] = xr[j][v] * p.alpha[c * V + v] * inv;
-          if (side) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) p.side_out[(size_t)b * p.side_bs + c * V + v] = xr[j][v];
-          }
-        }
-      }
-    }
-    if (PRO == PRO_DATTN) {
-      // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1.
-      // Scores: `tp` threads per (head, key) pair, float4 loads issued together, so
-      // the whole prologue costs two dependent round trips to L2.
-      const int nk = p.n_keys, dh = p.dheads, hd = p.dhead_dim;
-      const float* q = p.dq + (size_t)b * p.dq_bs;
-      const float* dk = p.dk + (size_t)b * p.dkv_bs;
-      const float* dv = p.dv + (size_t)b * p.dkv_bs;
-      const float scale = 1.0f / sqrtf((float)hd);
-      const int npairs = dh * nk;
-      int tp = 32;
-      while (tp > 1 && tp * npairs > kConsumers) tp >>= 1;
-      if (tp > hd / 4) tp = hd / 4;
-      const int pr = tid / tp, sub = tid % tp;
-      float d = 0.f;
-      if (pr < npairs) {
-        const int h = pr / nk, jk = pr % nk;
-        const float4* q4 = reinterpret_cast<const float4*>(q + h * hd);
-        const float4* k4 = reinterpret_cast<const float4*>(dk + (size_t)jk * K + h * hd);
-#pragma unroll 8
-        for (int e = sub; e < hd / 4; e += tp) {
-          const float4 a = q4[e], c4 = k4[e];
-          d = fmaf(a.x, c4.x, d);
-          d = fmaf(a.y, c4.y, d);
-          d = fmaf(a.z, c4.z, d);
-          d = fmaf(a.w, c4.w, d);
-        }
-      }
-      for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
-      bar_sync(1, kConsumers);
-      if (tid < dh) {
-        float mx = -__int_as_float(0x7f800000);
-        for (int jk = 0; jk < nk; ++jk) mx = fmaxf(mx, s_att[tid * 8 + jk]);
-        float den = 0.f;
-        for (int jk = 0; jk < nk; ++jk) {
-          const float e = expf(s_att[tid * 8 + jk] - mx);
-          s_att[tid * 8 + jk] = e;
-          den += e;
-        }
-        for (int jk = 0; jk < nk; ++jk) s_att[tid * 8 + jk] = s_att[tid * 8 + jk] / den;
-      }
-      bar_sync(1, kConsumers);
-#pragma unroll
-      for (int j = 0; j < kXch; ++j) {
-        const int c = tig + j * pl.tpr;
-        if (c < CC) {
-          const int h = (c * V) / hd;  // a chunk never straddles two heads
-          float o[V];
-#pragma unroll
-          for (int v = 0; v < V; ++v) o[v] = 0.f;
-#pragma unroll
-          for (int jk = 0; jk < 8; ++jk) {
-            if (jk < nk) {
-              const float pw = s_att[h * 8 + jk];
-#pragma unroll
-              for (int v = 0; v < V; v += 4) {
-                const float4 f = *reinterpret_cast<const float4*>(dv + (size_t)jk * K + c * V + v);
-                o[v] += pw * f.x;
-                o[v + 1] += pw * f.y;
-                o[v + 2] += pw * f.z;
-                o[v + 3] += pw * f.w;
-              }
-            }
-          }
-#pragma unroll
-          for (int v = 0; v < V; ++v) xr[j][v] = o[v];
-        }
-      }
-    }
-
-    const int rg = pl.rg;
-    for (int i = 0; i < nt; ++i) {
-      if (s_abort) break;
-      const int s = i % NS;
-      if (!mbar_wait(&full[s], (uint32_t)((i / NS) & 1))) {
-        atomicOr(p.status, kDevTimeout);
-        s_abort = 1;
-        break;
-      }
-      const uint8_t* row0 = stages + (size_t)s * tile_bytes + (size_t)(g * rg) * row_bytes;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < kXch; ++j) {
-        const int c = tig + j * pl.tpr;
-        if (c < CC) {
-          const uint4 w0 = *reinterpret_cast<const uint4*>(row0 + (size_t)c * 16);
-          acc0 = Chunk<WT>::dot(w0, xr[j], acc0);
-          if (rg > 1) {
-            const uint4 w1 = *reinterpret_cast<const uint4*>(row0 + row_bytes + (size_t)c * 16);
-            acc1 = Chunk<WT>::dot(w1, xr[j], acc1);
-          }
-        }
-      }
-      acc0 = warp_sum(acc0);
-      if (rg > 1) acc1 = warp_sum(acc1);
-      if (lane == 0) {
-        float* pp = part + (size_t)(i * pl.tile_rows + g * rg) * wpg + (warp % wpg);
-        pp[0] = acc0;
-        if (rg > 1) pp[wpg] = acc1;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-  }
-  __syncthreads();
-
-  if (s_abort) {
-    // wind down: wait (bounded) for the copies still in flight into this CTA's stages
-    if (tid == 0) {
-      const int issued = s_issued;
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        (void)mbar_wait(&full[i % NS], (uint32_t)((i / NS) & 1));
-    }
-    __syncthreads();
-    return;
-  }
-
-  // ------------------------------------------------------------ epilogue
-  const int tr = pl.tile_rows;
-  const int nrows = nt * tr;
-  auto yrow = [&](int lr) {
-    float y = 0.f;
-    for (int w = 0; w < wpg; ++w) y += part[(size_t)lr * wpg + w];
-    return y;
-  };
-  auto grow = [&](int lr) { return (t0 + lr / tr) * tr + lr % tr; };
-
-  if (EPI == EPI_STORE || EPI == EPI_RESID || EPI == EPI_DEPIN) {
-    float* out = p.out + (size_t)b * p.out_bs;
-    int prev = -1;
-    if (EPI == EPI_DEPIN) {
-      const IoLayout io{p.batch};
-      const int forcing = p.d_in[io.flag_off() + b];
-      prev = forcing ? p.d_in[io.forced_off() + (size_t)b * 9 + p.key_index]
-                     : argmax_key_index(p.keys[(size_t)b * 9 + p.key_index]);
-    }
-    for (int lr = tid; lr < nrows; lr += kThreads) {
-      const int row = grow(lr);
-      if (row >= pl.n_out) continue;
-      const float y = yrow(lr);
-      if (EPI == EPI_STORE) out[row] = y;
-      if (EPI == EPI_RESID) out[row] += y;
-      if (EPI == EPI_DEPIN) {
-        // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
-        if (prev != -1)
-          out[row] = y + Chunk<WT>::elem(p.emb, (size_t)max(prev, 0) * pl.n_out + row);
-        else
-          out[row] = y;
-      }
-    }
-  } else if (EPI == EPI_SWIGLU) {
-    // "moshi_lm.rs", `temporal_step`: silu(gate_j) * mult_j
-    float* out = p.out + (size_t)b * p.out_bs;
-    const int half = tr >> 1;
-    for (int lr = tid; lr < nrows; lr += kThreads) {
-      const int r = lr % tr;
-      if (r >= half) continue;
-      const int j = (t0 + lr / tr) * half + r;
-      if (j >= pl.n_out) continue;
-      const float gt = yrow(lr), mu = yrow(lr + half);
-      out[j] = gt / (1.0f + expf(-gt)) * mu;
-    }
-  } else if (EPI == EPI_QKV) {
-    // "moshi_lm.rs", `rope_row` on q and k at pos, then the K/V push at slot pos % C
-    const int D = pl.n_out / 3;
-    const int pos = p.offsets[b];
-    const int slot = pos % p.context;
-    const int hd = p.head_dim;
-    for (int lr = 2 * tid; lr < nrows; lr += 2 * kThreads) {
-      const int row = grow(lr);
-      if (row >= pl.n_out) continue;
-      float a = yrow(lr), c = yrow(lr + 1);
-      const int region = row / D, col = row % D;
-      if (region < 2) {
-        const int ip = (col % hd) >> 1;
-        const float freq = expf(-logf(p.rope_theta) * 2.0f * (float)ip / (float)hd);
-        const float ang = freq * (float)pos;
-        const float sn = sinf(ang), cs = cosf(ang);
-        const float ra = a * cs - c * sn;
-        const float rc = a * sn + c * cs;
-        a = ra;
-        c = rc;
-      }
-      if (region == 0) {
-        p.out[(size_t)b * p.out_bs + col] = a;
-        p.out[(size_t)b * p.out_bs + col + 1] = c;
-      } else {
-        void* cache = region == 1 ? p.kcache : p.vcache;
-        const size_t base = (size_t)b * p.kv_bs + (size_t)slot * D + col;
-        store_kv(cache, base, a, p.kv_bf16);
-        store_kv(cache, base + 1, c, p.kv_bf16);
-      }
-    }
-  } else if (EPI == EPI_DQKV) {
-    const int DD = pl.n_out / 3;
-    for (int lr = tid; lr < nrows; lr += kThreads) {
-      const int row = grow(lr);
-      if (row >= pl.n_out) continue;
-      const float y = yrow(lr);
-      if (row < DD)
-        p.out[(size_t)b * p.out_bs + row] = y;
-      else if (row < 2 * DD)
-        p.dk_out[(size_t)b * p.dkv_bs + row - DD] = y;
-      else
-        p.dv_out[(size_t)b * p.dkv_bs + row - 2 * DD] = y;
-    }
-  } else if (EPI == EPI_ARGMAX) {
-    float* out = p.out + (size_t)b * p.out_bs;
-    unsigned long long best = 0ull;
-    for (int lr = tid; lr < nrows; lr += kThreads) {
-      const int row = grow(lr);
-      if (row >= pl.n_out) continue;
-      const float y = yrow(lr);
-      out[row] = y;
-      const unsigned long long k = argmax_key(y, (uint32_t)row);
-      best = k > best ? k : best;
-    }
-    best = warp_max_u64(best);
-    if (lane == 0) s_key[warp] = best;
-    __syncthreads();
-    if (tid == 0 && nt > 0) {
-      unsigned long long m = 0ull;
-      for (int w = 0; w < kThreads / 32; ++w) m = s_key[w] > m ? s_key[w] : m;
-      atomicMax(p.keys + (size_t)b * 9 + p.key_index, m);
-    }
-  }
-}
-
-// ---------------------------------------------------------------- host side
 
 GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int num_sms) {
   GemvPlan pl{};
@@ -443,18 +37,19 @@ GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int nu
   pl.K = K;
   const int V = 16 / es;
   const int CC = K / V;
-  int tpr = 256;
+  int tpr = kGemvConsumers;
   while (tpr > 32 && tpr > CC) tpr >>= 1;
-  const int ng = kConsumers / tpr;
+  const int ng = kGemvConsumers / tpr;
+  pl.nch = nch_bucket((CC + tpr - 1) / tpr);
+  pl.rg = pl.nch <= 2 ? 2 : 1;
+  if ((paired || even_rows) && ((ng * pl.rg) & 1)) pl.nch = 0;
   const int row_bytes = K * es;
-  int rg = (2 * ng * row_bytes <= 16384) ? 2 : 1;
-  if ((paired || even_rows) && ((ng * rg) & 1)) rg = 2;
   pl.tpr = tpr;
-  pl.rg = rg;
-  pl.tile_rows = ng * rg;
+  pl.tile_rows = ng * pl.rg;
   const int out_per_tile = paired ? pl.tile_rows / 2 : pl.tile_rows;
   pl.tiles = (n_out + out_per_tile - 1) / out_per_tile;
-  pl.grid = pl.tiles < num_sms ? pl.tiles : num_sms;
+  const int max_grid = num_sms * RQ_GEMV_CTAS_PER_SM;
+  pl.grid = pl.tiles < max_grid ? pl.tiles : max_grid;
   pl.max_tiles = (pl.tiles + pl.grid - 1) / pl.grid;
   const int tile_bytes = pl.tile_rows * row_bytes;
   int ns = (RQ_GEMV_STAGE_BUDGET) / tile_bytes;
@@ -468,81 +63,23 @@ GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int nu
   return pl;
 }
 
-int gemv_chunks_per_thread(const GemvPlan& pl, int es) {
-  const int CC = pl.K / (16 / es);
-  return (CC + pl.tpr - 1) / pl.tpr;
-}
-
-constexpr int kMaxDynSmem = 200 * 1024;
-
-template <typename WT, int PRO, int EPI>
-static cudaError_t configure_t() {
-  return cudaFuncSetAttribute(gemv_kernel<WT, PRO, EPI>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-}
-
-template <typename WT>
-static cudaError_t configure_all_t() {
-  cudaError_t e = cudaSuccess, r;
-#define RQ_CFG(P, E) if ((r = configure_t<WT, P, E>()) != cudaSuccess) e = r;
-  RQ_CFG(PRO_RMS, EPI_QKV) RQ_CFG(PRO_PLAIN, EPI_RESID) RQ_CFG(PRO_RMS, EPI_SWIGLU)
-  RQ_CFG(PRO_RMS, EPI_ARGMAX) RQ_CFG(PRO_PLAIN, EPI_DEPIN) RQ_CFG(PRO_RMS, EPI_DQKV)
-  RQ_CFG(PRO_DATTN, EPI_RESID) RQ_CFG(PRO_PLAIN, EPI_ARGMAX) RQ_CFG(PRO_PLAIN, EPI_STORE)
-#undef RQ_CFG
-  return e;
+int gemv_chunks_per_thread(const GemvPlan& pl, int) {
+  return pl.nch == 0 ? 1 << 20 : pl.nch;
 }
 
 // Raise the dynamic shared-memory limit of every instantiation once per device,
 // before any launch is captured into a graph.
 cudaError_t gemv_configure_all() {
-  cudaError_t e = configure_all_t<uint16_t>();
-  cudaError_t f = configure_all_t<float>();
+  cudaError_t e = gemv_configure<uint16_t>(kMaxDynSmem);
+  cudaError_t f = gemv_configure<float>(kMaxDynSmem);
   return e != cudaSuccess ? e : f;
-}
-
-template <typename WT, int PRO, int EPI>
-static cudaError_t launch_t(const GemvParams& p, int batch, cudaStream_t s, bool pdl) {
-  auto k = gemv_kernel<WT, PRO, EPI>;
-  if (p.pl.smem > kMaxDynSmem) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.pl.grid, (unsigned)batch, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)p.pl.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k, p);
-}
-
-template <typename WT>
-static cudaError_t dispatch(const GemvParams& p, int pro, int epi, int batch, cudaStream_t s,
-                            bool pdl) {
-  if (pro == PRO_RMS && epi == EPI_QKV) return launch_t<WT, PRO_RMS, EPI_QKV>(p, batch, s, pdl);
-  if (pro == PRO_PLAIN && epi == EPI_RESID)
-    return launch_t<WT, PRO_PLAIN, EPI_RESID>(p, batch, s, pdl);
-  if (pro == PRO_RMS && epi == EPI_SWIGLU)
-    return launch_t<WT, PRO_RMS, EPI_SWIGLU>(p, batch, s, pdl);
-  if (pro == PRO_RMS && epi == EPI_ARGMAX)
-    return launch_t<WT, PRO_RMS, EPI_ARGMAX>(p, batch, s, pdl);
-  if (pro == PRO_PLAIN && epi == EPI_DEPIN)
-    return launch_t<WT, PRO_PLAIN, EPI_DEPIN>(p, batch, s, pdl);
-  if (pro == PRO_RMS && epi == EPI_DQKV) return launch_t<WT, PRO_RMS, EPI_DQKV>(p, batch, s, pdl);
-  if (pro == PRO_DATTN && epi == EPI_RESID)
-    return launch_t<WT, PRO_DATTN, EPI_RESID>(p, batch, s, pdl);
-  if (pro == PRO_PLAIN && epi == EPI_ARGMAX)
-    return launch_t<WT, PRO_PLAIN, EPI_ARGMAX>(p, batch, s, pdl);
-  if (pro == PRO_PLAIN && epi == EPI_STORE)
-    return launch_t<WT, PRO_PLAIN, EPI_STORE>(p, batch, s, pdl);
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
                         cudaStream_t s, bool pdl) {
-  return bf16 ? dispatch<uint16_t>(p, pro, epi, batch, s, pdl)
-              : dispatch<float>(p, pro, epi, batch, s, pdl);
+  if (p.pl.smem > kMaxDynSmem || p.pl.nch == 0) return cudaErrorInvalidValue;
+  return bf16 ? gemv_dispatch<uint16_t>(p, pro, epi, batch, s, pdl)
+              : gemv_dispatch<float>(p, pro, epi, batch, s, pdl);
 }
 
 }  // namespace rqk

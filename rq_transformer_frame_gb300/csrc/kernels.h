@@ -35,6 +35,7 @@ struct GemvPlan {
   int n_stages;    // pipeline depth
   int tpr;         // threads per row group (power of two, 32..256)
   int rg;          // rows per thread per tile (1 or 2)
+  int nch;         // 16-byte chunks of x per thread (kernel template parameter)
   int max_tiles;   // tiles of the busiest CTA
   int smem;        // dynamic shared memory bytes
   double bytes;    // weight bytes one launch streams
@@ -83,6 +84,7 @@ GemvPlan plan_gemv(int n_out, int K, int elem_bytes, bool paired, bool even_rows
 int gemv_chunks_per_thread(const GemvPlan& pl, int elem_bytes);
 cudaError_t gemv_configure_all();
 constexpr int kGemvMaxChunks = 6;  // 16-byte chunks of x per thread
+constexpr int kGemvConsumers = 256;  // consumer threads of a GEMV CTA (+1 producer warp)
 cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
                         cudaStream_t s, bool pdl);
 
