@@ -213,6 +213,24 @@ enum {
 rq_status rq_launch_op(rq_handle *h, int32_t op, int32_t layer, int32_t count,
                        double *bytes_per_launch);
 
+/* Standalone decode attention, the kernel the frame runs after each qkv projection
+ * ("moshi_lm.rs", `attend`): for each of `batch` single queries and each head,
+ * softmax((q . k_j) / sqrt(head_dim)) weighted sum of v_j over the window of the
+ * last min(pos + 1, context) positions, position j stored in cache slot j % context.
+ *   q          device [batch][heads*head_dim] f32
+ *   k, v       device [batch][context][heads*head_dim] in kv_dtype (RQ_F32 / RQ_BF16)
+ *   positions  device [batch] int32, the query's own position (>= 0)
+ *   out        device [batch][heads*head_dim] f32
+ *   workspace  device scratch of at least rq_attention_workspace_size(...) bytes,
+ *              owned by the caller; its contents need no initialisation.
+ * head_dim must be 32, 64 or 128.  Enqueued on `cuda_stream`; no synchronization. */
+size_t rq_attention_workspace_size(int32_t batch, int32_t heads, int32_t head_dim,
+                                   int32_t context);
+rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim, int32_t context,
+                       int32_t kv_dtype, const float *q, const void *k, const void *v,
+                       const int32_t *positions, float *out, void *workspace,
+                       size_t workspace_bytes, void *cuda_stream);
+
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 

@@ -81,6 +81,10 @@ def load() -> C.CDLL:
     L.rq_status_string.argtypes = [C.c_int]
     L.rq_status_string.restype = C.c_char_p
     L.rq_abi_version.restype = I32
+    L.rq_attention_workspace_size.argtypes = [I32, I32, I32, I32]
+    L.rq_attention_workspace_size.restype = C.c_size_t
+    L.rq_attention.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P, P, C.c_size_t, P]
+    L.rq_attention.restype = C.c_int
     for f in ("rq_create", "rq_reset", "rq_step", "rq_step_forced", "rq_step_device",
               "rq_sync", "rq_get_logits", "rq_get_trace", "rq_get_ring", "rq_set_kv",
               "rq_launch_op"):
@@ -216,3 +220,20 @@ class Decoder:
     @property
     def kernels_per_frame(self) -> int:
         return int(self.L.rq_frame_kernel_count(self.h))
+
+
+def attention(q, k, v, positions, heads: int, head_dim: int, stream=None):
+    """Standalone decode attention through rq_attention (device tensors):
+    q [B][H*hd] f32, k/v [B][C][H*hd] f32 or bf16, positions [B] int32 -> [B][H*hd]."""
+    L = load()
+    B, ctx = int(k.shape[0]), int(k.shape[1])
+    out = torch.empty((B, heads * head_dim), dtype=torch.float32, device=q.device)
+    nbytes = L.rq_attention_workspace_size(B, heads, head_dim, ctx)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    kvt = RQ_BF16 if k.dtype == torch.bfloat16 else RQ_F32
+    rc = L.rq_attention(B, heads, head_dim, ctx, kvt, _p(q), _p(k), _p(v), _p(positions), _p(out),
+                        _p(ws), nbytes, C.c_void_p(st.cuda_stream))
+    if rc != RQ_OK:
+        raise RQError(rc, "rq_attention")
+    return out

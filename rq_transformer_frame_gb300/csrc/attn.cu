@@ -159,3 +159,58 @@ cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool 
 }
 
 }  // namespace rqk
+
+// ---------------------------------------------------------------- standalone entry
+#include "../../include/rq.h"
+
+namespace {
+constexpr int kStandaloneKps = 64;  // positions per split, as in the frame
+
+size_t partial_bytes(int B, int H, int hd, int C) {
+  const size_t nsplit = (size_t)(C + kStandaloneKps - 1) / kStandaloneKps;
+  return ((size_t)B * H * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+}
+}  // namespace
+
+extern "C" size_t rq_attention_workspace_size(int32_t batch, int32_t heads, int32_t head_dim,
+                                              int32_t context) {
+  if (batch < 1 || heads < 1 || head_dim < 1 || context < 1) return 0;
+  return partial_bytes(batch, heads, head_dim, context) + (size_t)batch * heads * sizeof(int);
+}
+
+extern "C" rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim,
+                                  int32_t context, int32_t kv_dtype, const float* q,
+                                  const void* k, const void* v, const int32_t* positions,
+                                  float* out, void* workspace, size_t workspace_bytes,
+                                  void* cuda_stream) {
+  using namespace rqk;
+  if (batch < 1 || heads < 1 || context < 1 || batch > 65535 || heads > 65535)
+    return RQ_ERR_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return RQ_ERR_UNSUPPORTED;
+  if (kv_dtype != RQ_F32 && kv_dtype != RQ_BF16) return RQ_ERR_ARG;
+  if (!q || !k || !v || !positions || !out || !workspace) return RQ_ERR_ARG;
+  if (workspace_bytes < rq_attention_workspace_size(batch, heads, head_dim, context))
+    return RQ_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  AttnParams a{};
+  a.q = q;
+  a.kc = k;
+  a.vc = v;
+  a.kv_bs = (long long)context * heads * head_dim;
+  a.offsets = positions;
+  a.part = static_cast<float*>(workspace);
+  a.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                      partial_bytes(batch, heads, head_dim, context));
+  a.out = out;
+  a.D = heads * head_dim;
+  a.H = heads;
+  a.hd = head_dim;
+  a.C = context;
+  a.kps = kStandaloneKps;
+  a.nsplit = (context + kStandaloneKps - 1) / kStandaloneKps;
+  a.batch = batch;
+  a.status = nullptr;
+  if (cudaMemsetAsync(a.counters, 0, (size_t)batch * heads * sizeof(int), s) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  return launch_attn(a, kv_dtype == RQ_BF16, s, false) == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
