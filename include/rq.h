@@ -231,6 +231,26 @@ rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim, int32_t c
                        const int32_t *positions, float *out, void *workspace,
                        size_t workspace_bytes, void *cuda_stream);
 
+/* rq_attention without a workspace argument, for callers that cannot allocate device
+ * memory -- e.g. a real-time audio thread, where cudaMalloc may wait on device-wide
+ * synchronization for an unbounded time, or a plug-in whose host grants a fixed memory
+ * budget at start-up and forbids allocation later.  The pages have no counterpart; this
+ * is an addition of this library.  Arguments and results are those of rq_attention.
+ *   Scratch: a fixed 4 MiB array in the library's device image (present on every GPU
+ *   that loads the library until the process exits).  Calls whose scratch need,
+ *   rq_attention_workspace_size(batch, heads, head_dim, context), exceeds 4 MiB are
+ *   refused with RQ_ERR_UNSUPPORTED before anything is enqueued.
+ *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   The first call on a device looks up the array's device address for that device;
+ *   make that first call before any stream capture.
+ *   Every call shares the one array and leaves its contents behind; the call clears
+ *   what must start at zero itself.  Calls that overlap on the GPU (other streams or
+ *   threads) race on the array: serialize them. */
+rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t head_dim,
+                               int32_t context, int32_t kv_dtype, const float *q,
+                               const void *k, const void *v, const int32_t *positions,
+                               float *out, void *cuda_stream);
+
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 
