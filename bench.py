@@ -62,7 +62,7 @@ def peaks():
 
 def gemv_source_hash() -> str:
     h = hashlib.sha256()
-    for n in ("gemv.cu", "common.cuh", "kernels.h"):
+    for n in ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "common.cuh", "kernels.h"):
         with open(os.path.join(ROOT, "rq_transformer_frame_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
