@@ -84,7 +84,14 @@ typedef struct {
   int32_t kv_dtype;     /* rq_dtype of the temporal K/V cache [RQ_BF16] */
   float rms_eps;        /* [1e-8], inside the mean */
   float rope_theta;     /* [10000] */
+  int32_t schedule;     /* RQ_SCHEDULE_*: how a frame is launched [RQ_SCHEDULE_AUTO] */
 } rq_config;
+
+/* Frame schedules.  PERSISTENT runs all linears and attentions of a frame as one
+ * cooperative kernel with grid barriers between dependent ops (batch 1, same weight and
+ * K/V dtype); GRAPH launches one kernel per op inside a CUDA graph.  AUTO picks
+ * PERSISTENT when it applies, else GRAPH.  Results agree within the parity tolerance. */
+enum { RQ_SCHEDULE_AUTO = 0, RQ_SCHEDULE_GRAPH = 1, RQ_SCHEDULE_PERSISTENT = 2 };
 
 /* Device pointers to the weights, row-major, matrices [out][in] ("moshi_lm.rs",
  * structs TemporalLayer, DepLayer, MoshiLm and `load_band`).  Matrices and tables are
@@ -253,6 +260,9 @@ rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t head_dim,
 
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
+
+/* The schedule the handle runs: RQ_SCHEDULE_GRAPH or RQ_SCHEDULE_PERSISTENT. */
+int32_t rq_schedule(const rq_handle *h);
 
 const char *rq_last_error(const rq_handle *h);
 const char *rq_status_string(rq_status s);

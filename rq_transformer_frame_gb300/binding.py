@@ -34,9 +34,12 @@ _CFG_INT_FIELDS = ["batch", "dim", "layers", "heads", "head_dim", "hidden", "con
                    "dhidden", "weight_dtype", "kv_dtype"]
 
 
+RQ_SCHEDULE_AUTO, RQ_SCHEDULE_GRAPH, RQ_SCHEDULE_PERSISTENT = 0, 1, 2
+
+
 class RqConfig(C.Structure):
     _fields_ = [(n, C.c_int32) for n in _CFG_INT_FIELDS] + \
-        [("rms_eps", C.c_float), ("rope_theta", C.c_float)]
+        [("rms_eps", C.c_float), ("rope_theta", C.c_float), ("schedule", C.c_int32)]
 
 
 class RqWeights(C.Structure):
@@ -76,6 +79,8 @@ def load() -> C.CDLL:
     L.rq_launch_op.argtypes = [P, I32, I32, I32, C.POINTER(C.c_double)]
     L.rq_frame_kernel_count.argtypes = [P]
     L.rq_frame_kernel_count.restype = I32
+    L.rq_schedule.argtypes = [P]
+    L.rq_schedule.restype = I32
     L.rq_last_error.argtypes = [P]
     L.rq_last_error.restype = C.c_char_p
     L.rq_status_string.argtypes = [C.c_int]
@@ -93,7 +98,7 @@ def load() -> C.CDLL:
     return L
 
 
-def make_config(cfg: RQConfig) -> RqConfig:
+def make_config(cfg: RQConfig, schedule: int = RQ_SCHEDULE_AUTO) -> RqConfig:
     c = RqConfig()
     for n in _CFG_INT_FIELDS:
         if n == "weight_dtype":
@@ -105,6 +110,7 @@ def make_config(cfg: RQConfig) -> RqConfig:
         setattr(c, n, int(v))
     c.rms_eps = cfg.eps
     c.rope_theta = cfg.rope_theta
+    c.schedule = int(schedule)
     return c
 
 
@@ -130,12 +136,13 @@ class Decoder:
     the handle's lifetime).  `stream` is a torch.cuda.Stream (default: the current
     stream)."""
 
-    def __init__(self, cfg: RQConfig, weights: dict, stream=None):
+    def __init__(self, cfg: RQConfig, weights: dict, stream=None,
+                 schedule: int = RQ_SCHEDULE_AUTO):
         self.L = load()
         self.cfg = cfg
         self.weights = weights
         self.stream = stream if stream is not None else torch.cuda.current_stream()
-        self._c = make_config(cfg)
+        self._c = make_config(cfg, schedule)
         self._w = RqWeights(**{n: weights[n].data_ptr() for n in WEIGHT_FIELDS})
         h = C.c_void_p()
         st = self.L.rq_create(C.byref(self._c), C.byref(self._w),
@@ -216,6 +223,11 @@ class Decoder:
         b = C.c_double(0)
         self._check(self.L.rq_launch_op(self.h, int(op), int(layer), int(count), C.byref(b)))
         return b.value
+
+    @property
+    def schedule(self) -> int:
+        """The schedule the handle runs (RQ_SCHEDULE_GRAPH or RQ_SCHEDULE_PERSISTENT)."""
+        return int(self.L.rq_schedule(self.h))
 
     @property
     def kernels_per_frame(self) -> int:

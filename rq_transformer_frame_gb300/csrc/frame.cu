@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) frame_begin_kernel(const FrameParams p) {
       ring[s * kRing + (off + stream_delay(s)) % kRing] = user[tid];
     }
     if (tid < 9) p.keys[(size_t)b * 9 + tid] = 0ull;
+    if (tid == 0 && b == 0 && p.grid_bar) *p.grid_bar = 0u;
   }
   __syncthreads();
   pdl_trigger();

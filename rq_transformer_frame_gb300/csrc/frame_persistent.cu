@@ -1,0 +1,689 @@
+// frame_persistent.cu -- the whole frame's linears and attentions in one cooperative
+// launch (batch 1).
+//
+// Every CTA walks the same op table (temporal layers, text head, the 8 depformer
+// steps).  Between dependent ops the CTAs meet at a grid barrier (one atomic counter,
+// bounded spin).  The weights of every op are known before the frame starts, so each
+// CTA's producer warp streams the weight tiles it owns for ALL ops, in order, into one
+// shared-memory ring with cp.async.bulk, running ahead of the consumers across op
+// boundaries: HBM keeps streaming the next ops' weights while the consumers wait on a
+// barrier, which removes the per-kernel drain and fill of a launch-per-op schedule.
+// Consumers run the prologues / epilogues of the streaming GEMV (gemv_kernel.cuh)
+// selected per op at run time, and the split-K decode attention as work items.
+// Activations written by other CTAs are read with L2-only loads (ld.global.cg).
+#include <cuda_bf16.h>
+
+#include "gemv_kernel.cuh"
+
+namespace rqk {
+namespace pers {
+
+constexpr int kCons = 256;    // consumer threads
+constexpr int kThr = 288;     // + 1 producer warp
+constexpr int kMaxNch = 6;
+
+// ---------------------------------------------------------------- grid barrier
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// thread 0 of the consumers: wait until `target` CTAs have arrived (bounded)
+__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target) {
+  if (ld_acquire(bar) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ld_acquire(bar) >= target) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------- tile consumer
+// Consume this CTA's `nt` tiles of one GEMV op from the ring (slots advance with the
+// CTA-wide tile counter `gi`), leaving one partial per (row, warp) in `part`.
+template <typename WT, int NCH>
+__device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int nt, uint32_t& gi,
+                                              uint8_t* ring, int slot_bytes, int NS,
+                                              uint64_t* full, uint64_t* empty, float* part,
+                                              const float (&xr)[kMaxNch][Chunk<WT>::V],
+                                              int g, int tig, int warp, int lane) {
+  constexpr int RG = GemvShape<NCH>::RG;
+  const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
+  const int CC = pl.K / Chunk<WT>::V;
+  const int wpg = pl.tpr >> 5;
+  for (int i = 0; i < nt; ++i, ++gi) {
+    const int s = (int)(gi % (uint32_t)NS);
+    if (!mbar_wait(&full[s], (gi / (uint32_t)NS) & 1u)) return false;
+    const uint8_t* row0 = ring + (size_t)s * slot_bytes + (size_t)(g * RG) * row_bytes;
+    float acc[RG][2];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) acc[r][0] = acc[r][1] = 0.f;
+    uint4 w[NCH][RG];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = tig + j * pl.tpr;
+#pragma unroll
+      for (int r = 0; r < RG; ++r)
+        w[j][r] = (c < CC) ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
+                                                             (size_t)c * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < NCH; ++j)
+#pragma unroll
+      for (int r = 0; r < RG; ++r) Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    float* pp = part + (size_t)(i * pl.tile_rows + g * RG) * wpg + (warp % wpg);
+    if (RG == 2) {
+      const bool up = (lane & 16) != 0;
+      const float r0 = acc[0][0] + acc[0][1];
+      const float r1 = acc[RG - 1][0] + acc[RG - 1][1];
+      float keep = up ? r1 : r0;
+      const float send = up ? r0 : r1;
+      keep += __shfl_xor_sync(0xffffffffu, send, 16);
+      keep += __shfl_xor_sync(0xffffffffu, keep, 8);
+      keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+      keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+      keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+      if (lane == 0) pp[0] = keep;
+      if (lane == 16) pp[wpg] = keep;
+    } else {
+      const float r0 = warp_sum(acc[0][0] + acc[0][1]);
+      if (lane == 0) pp[0] = r0;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tile_range(const GemvPlan& pl, int& t0, int& t1) {
+  t0 = (int)(((long long)pl.tiles * blockIdx.x) / gridDim.x);
+  t1 = (int)(((long long)pl.tiles * (blockIdx.x + 1)) / gridDim.x);
+}
+
+// ---------------------------------------------------------------- prologue
+// x for this op into registers: chunk j of thread (g, tig) covers columns
+// [(tig + j*tpr)*V, +V).  Returns nothing; uses consumer barrier 1.
+template <typename WT>
+__device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
+                                       const GemvPlan& pl, int nch,
+                                       float (&xr)[kMaxNch][Chunk<WT>::V], int g, int tig,
+                                       int tid, int warp, int lane, float* s_red,
+                                       float* s_att) {
+  constexpr int V = Chunk<WT>::V;
+  const int K = pl.K, CC = K / V;
+  const float* in = op.in;
+#pragma unroll
+  for (int j = 0; j < kMaxNch; ++j) {
+    const int c = tig + j * pl.tpr;
+#pragma unroll
+    for (int v = 0; v < V; ++v) xr[j][v] = 0.f;
+    if (op.pro != PRO_DATTN && j < nch && c < CC) {
+#pragma unroll
+      for (int v = 0; v < V; v += 4) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(in + (size_t)c * V + v));
+        xr[j][v] = f.x;
+        xr[j][v + 1] = f.y;
+        xr[j][v + 2] = f.z;
+        xr[j][v + 3] = f.w;
+      }
+    }
+  }
+  if (op.pro == PRO_RMS) {
+    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n))
+    float ss = 0.f;
+    for (int k = tid; k < K; k += kCons) {
+      const float v = ldcg(in + k);
+      ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_red[warp] = ss;
+    bar_sync(1, kCons);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCons / 32; ++w) tot += s_red[w];
+    bar_sync(1, kCons);  // s_red is reused by the next op
+    const float inv = 1.0f / sqrtf(P.eps + tot / (float)K);
+    const bool side = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
+#pragma unroll
+    for (int j = 0; j < kMaxNch; ++j) {
+      const int c = tig + j * pl.tpr;
+      if (j < nch && c < CC) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) xr[j][v] = xr[j][v] * op.alpha[c * V + v] * inv;
+        if (side) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) op.side_out[c * V + v] = xr[j][v];
+        }
+      }
+    }
+  } else if (op.pro == PRO_DATTN) {
+    // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1
+    const int nk = op.n_keys, dh = P.dheads, hd = P.dhead_dim;
+    const float scale = 1.0f / sqrtf((float)hd);
+    const int npairs = dh * nk;
+    int tp = 32;
+    while (tp > 1 && tp * npairs > kCons) tp >>= 1;
+    if (tp > hd / 4) tp = hd / 4;
+    const int pr = tid / tp, sub = tid % tp;
+    float d = 0.f;
+    if (pr < npairs) {
+      const int h = pr / nk, jk = pr % nk;
+      const float4* q4 = reinterpret_cast<const float4*>(in + h * hd);
+      const float4* k4 = reinterpret_cast<const float4*>(op.dk + (size_t)jk * K + h * hd);
+#pragma unroll 8
+      for (int e = sub; e < hd / 4; e += tp) {
+        const float4 a = __ldcg(q4 + e), c4 = __ldcg(k4 + e);
+        d = fmaf(a.x, c4.x, d);
+        d = fmaf(a.y, c4.y, d);
+        d = fmaf(a.z, c4.z, d);
+        d = fmaf(a.w, c4.w, d);
+      }
+    }
+    for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
+    bar_sync(1, kCons);
+    if (tid < dh) {
+      float mx = -__int_as_float(0x7f800000);
+      for (int jk = 0; jk < nk; ++jk) mx = fmaxf(mx, s_att[tid * 8 + jk]);
+      float den = 0.f;
+      for (int jk = 0; jk < nk; ++jk) {
+        const float e = expf(s_att[tid * 8 + jk] - mx);
+        s_att[tid * 8 + jk] = e;
+        den += e;
+      }
+      for (int jk = 0; jk < nk; ++jk) s_att[tid * 8 + jk] = s_att[tid * 8 + jk] / den;
+    }
+    bar_sync(1, kCons);
+#pragma unroll
+    for (int j = 0; j < kMaxNch; ++j) {
+      const int c = tig + j * pl.tpr;
+      if (j < nch && c < CC) {
+        const int h = (c * V) / hd;
+        float o[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) o[v] = 0.f;
+#pragma unroll
+        for (int jk = 0; jk < 8; ++jk) {
+          if (jk < nk) {
+            const float pw = s_att[h * 8 + jk];
+#pragma unroll
+            for (int v = 0; v < V; v += 4) {
+              const float4 f =
+                  __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)jk * K + c * V + v));
+              o[v] += pw * f.x;
+              o[v + 1] += pw * f.y;
+              o[v + 2] += pw * f.z;
+              o[v + 3] += pw * f.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) xr[j][v] = o[v];
+      }
+    }
+    bar_sync(1, kCons);  // s_att is reused by the next op
+  }
+}
+
+// ---------------------------------------------------------------- epilogue
+// Finish rows [t0*tr, (t0+nt)*tr) of one GEMV op from the per-warp partials (batch 1).
+template <typename WT>
+__device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
+                                         const GemvPlan& pl, int t0, int nt, const float* part,
+                                         int tid, int warp, int lane,
+                                         unsigned long long* s_key) {
+  const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
+  const int nrows = nt * tr;
+  auto yrow = [&](int lr) {
+    float y = 0.f;
+    for (int w = 0; w < wpg; ++w) y += part[(size_t)lr * wpg + w];
+    return y;
+  };
+  auto grow = [&](int lr) { return (t0 + lr / tr) * tr + lr % tr; };
+  const int epi = op.epi;
+  if (epi == EPI_STORE || epi == EPI_RESID || epi == EPI_DEPIN) {
+    int prev = -1;
+    if (epi == EPI_DEPIN) {
+      const IoLayout io{1};
+      const int forcing = P.d_in[io.flag_off()];
+      prev = forcing ? P.d_in[io.forced_off() + op.key_index]
+                     : argmax_key_index(__ldcg(P.keys + op.key_index));
+    }
+    for (int lr = tid; lr < nrows; lr += kCons) {
+      const int row = grow(lr);
+      if (row >= pl.n_out) continue;
+      const float y = yrow(lr);
+      if (epi == EPI_STORE) op.out[row] = y;
+      if (epi == EPI_RESID) op.out[row] = ldcg(op.out + row) + y;
+      if (epi == EPI_DEPIN) {
+        // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
+        op.out[row] = (prev != -1)
+                          ? y + Chunk<WT>::elem(op.emb, (size_t)max(prev, 0) * pl.n_out + row)
+                          : y;
+      }
+    }
+  } else if (epi == EPI_SWIGLU) {
+    const int half = tr >> 1;
+    for (int lr = tid; lr < nrows; lr += kCons) {
+      const int r = lr % tr;
+      if (r >= half) continue;
+      const int j = (t0 + lr / tr) * half + r;
+      if (j >= pl.n_out) continue;
+      const float gt = yrow(lr), mu = yrow(lr + half);
+      op.out[j] = gt / (1.0f + expf(-gt)) * mu;
+    }
+  } else if (epi == EPI_QKV) {
+    const int D = pl.n_out / 3;
+    const int pos = P.offsets[0];
+    const int slot = pos % P.context;
+    const int hd = P.head_dim;
+    for (int lr = 2 * tid; lr < nrows; lr += 2 * kCons) {
+      const int row = grow(lr);
+      if (row >= pl.n_out) continue;
+      float a = yrow(lr), c = yrow(lr + 1);
+      const int region = row / D, col = row % D;
+      if (region < 2) {
+        const int ip = (col % hd) >> 1;
+        const float freq = expf(-logf(P.rope_theta) * 2.0f * (float)ip / (float)hd);
+        const float ang = freq * (float)pos;
+        const float sn = sinf(ang), cs = cosf(ang);
+        const float ra = a * cs - c * sn;
+        const float rc = a * sn + c * cs;
+        a = ra;
+        c = rc;
+      }
+      if (region == 0) {
+        op.out[col] = a;
+        op.out[col + 1] = c;
+      } else {
+        void* cache = region == 1 ? op.kcache : op.vcache;
+        const size_t base = (size_t)slot * D + col;
+        store_kv(cache, base, a, P.kv_bf16);
+        store_kv(cache, base + 1, c, P.kv_bf16);
+      }
+    }
+  } else if (epi == EPI_DQKV) {
+    const int DD = pl.n_out / 3;
+    for (int lr = tid; lr < nrows; lr += kCons) {
+      const int row = grow(lr);
+      if (row >= pl.n_out) continue;
+      const float y = yrow(lr);
+      if (row < DD)
+        op.out[row] = y;
+      else if (row < 2 * DD)
+        op.dk_out[row - DD] = y;
+      else
+        op.dv_out[row - 2 * DD] = y;
+    }
+  } else if (epi == EPI_ARGMAX) {
+    unsigned long long best = 0ull;
+    for (int lr = tid; lr < nrows; lr += kCons) {
+      const int row = grow(lr);
+      if (row >= pl.n_out) continue;
+      const float y = yrow(lr);
+      op.out[row] = y;
+      const unsigned long long k = argmax_key(y, (uint32_t)row);
+      best = k > best ? k : best;
+    }
+    best = warp_max_u64(best);
+    if (lane == 0) s_key[warp] = best;
+    bar_sync(1, kCons);
+    if (tid == 0) {
+      unsigned long long m = 0ull;
+      for (int w = 0; w < kCons / 32; ++w) m = s_key[w] > m ? s_key[w] : m;
+      atomicMax(P.keys + op.key_index, m);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- attention items
+template <typename KT, int EPL>
+__device__ __forceinline__ void load_row(const KT* p, float (&o)[EPL]);
+template <>
+__device__ __forceinline__ void load_row<float, 4>(const float* p, float (&o)[4]) {
+  const float4 f = __ldcg(reinterpret_cast<const float4*>(p));
+  o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+}
+template <>
+__device__ __forceinline__ void load_row<float, 2>(const float* p, float (&o)[2]) {
+  const float2 f = __ldcg(reinterpret_cast<const float2*>(p));
+  o[0] = f.x; o[1] = f.y;
+}
+template <>
+__device__ __forceinline__ void load_row<float, 1>(const float* p, float (&o)[1]) {
+  o[0] = __ldcg(p);
+}
+template <>
+__device__ __forceinline__ void load_row<uint16_t, 4>(const uint16_t* p, float (&o)[4]) {
+  const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
+  o[0] = bf16lo(u.x); o[1] = bf16hi(u.x); o[2] = bf16lo(u.y); o[3] = bf16hi(u.y);
+}
+template <>
+__device__ __forceinline__ void load_row<uint16_t, 2>(const uint16_t* p, float (&o)[2]) {
+  const unsigned u = __ldcg(reinterpret_cast<const unsigned*>(p));
+  o[0] = bf16lo(u); o[1] = bf16hi(u);
+}
+template <>
+__device__ __forceinline__ void load_row<uint16_t, 1>(const uint16_t* p, float (&o)[1]) {
+  o[0] = __uint_as_float(((unsigned)__ldcg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+// "moshi_lm.rs", `attend` for one session: work item (head, split of kps positions)
+// per group of 4 warps; the last group to finish a head merges its splits in order.
+template <typename KT, int EPL>
+__device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op, int tid,
+                                           int warp, int lane, float (*s_am)[4],
+                                           float (*s_al)[4], float (*s_aacc)[4][EPL * 32],
+                                           int* s_last) {
+  constexpr int HD = EPL * 32;
+  const int group = warp >> 2, wig = warp & 3, gt = tid & 127;
+  const int pos = P.offsets[0];
+  const int len = min(pos + 1, P.context);
+  const int first = pos + 1 - len;
+  const int nsplit = (len + P.kps - 1) / P.kps;
+  const int items = P.H * nsplit;
+  const float scale = 1.0f / sqrtf((float)HD);
+  const float ninf = -__int_as_float(0x7f800000);
+  const size_t pstride = (size_t)HD + 2;
+  for (int it = blockIdx.x * 2 + group; it < items; it += gridDim.x * 2) {
+    const int h = it % P.H, split = it / P.H;
+    const int j0 = first + split * P.kps;
+    const int j1 = min(j0 + P.kps, pos + 1);
+    float q[EPL];
+    const float* qp = P.attn_q + (size_t)h * HD + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) q[e] = ldcg(qp + e);
+    float m = ninf, l = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    const KT* kb = static_cast<const KT*>(op.kcache) + (size_t)h * HD + lane * EPL;
+    const KT* vb = static_cast<const KT*>(op.vcache) + (size_t)h * HD + lane * EPL;
+    for (int j = j0 + wig; j < j1; j += 4) {
+      const size_t off = (size_t)(j % P.context) * P.D;
+      float k[EPL], v[EPL];
+      load_row<KT, EPL>(kb + off, k);
+      load_row<KT, EPL>(vb + off, v);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s = fmaf(q[e], k[e], s);
+      s = warp_sum(s) * scale;
+      const float mn = fmaxf(m, s);
+      const float corr = expf(m - mn);
+      const float pe = expf(s - mn);
+      l = l * corr + pe;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * corr + pe * v[e];
+      m = mn;
+    }
+    if (lane == 0) {
+      s_am[group][wig] = m;
+      s_al[group][wig] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s_aacc[group][wig][lane * EPL + e] = acc[e];
+    bar_sync(2 + group, 128);
+    float* part = P.part + ((size_t)h * P.nsplit + split) * pstride;
+    if (gt < HD) {
+      float M = ninf;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, s_am[group][w]);
+      float L = 0.f, A = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if (s_al[group][w] > 0.f) {
+          const float c = expf(s_am[group][w] - M);
+          L += s_al[group][w] * c;
+          A += s_aacc[group][w][gt] * c;
+        }
+      }
+      part[2 + gt] = A;
+      if (gt == 0) {
+        part[0] = M;
+        part[1] = L;
+      }
+    }
+    __threadfence();
+    bar_sync(2 + group, 128);
+    if (gt == 0) s_last[group] = (atomicAdd(&P.counters[h], 1) == nsplit - 1);
+    bar_sync(2 + group, 128);
+    if (s_last[group]) {
+      __threadfence();
+      const float* pb = P.part + (size_t)h * P.nsplit * pstride;
+      if (gt < HD) {
+        float M = ninf;
+        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ldcg(pb + s * pstride));
+        float L = 0.f, A = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+          const float c = expf(ldcg(pb + s * pstride) - M);
+          L += ldcg(pb + s * pstride + 1) * c;
+          A += ldcg(pb + s * pstride + 2 + gt) * c;
+        }
+        P.attn_out[(size_t)h * HD + gt] = A / L;
+      }
+      if (gt == 0) P.counters[h] = 0;
+    }
+    bar_sync(2 + group, 128);
+  }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <typename WT, typename KT, int EPL>
+__global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersParams P) {
+  constexpr int V = Chunk<WT>::V;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_red[kCons / 32];
+  __shared__ float s_att[kMaxAttPairs];
+  __shared__ unsigned long long s_key[kCons / 32];
+  __shared__ float s_am[2][4], s_al[2][4];
+  __shared__ float s_aacc[2][4][EPL * 32];
+  __shared__ int s_last[2];
+  __shared__ volatile int s_abort;
+  __shared__ unsigned s_issued;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NS = P.n_slots;
+  uint8_t* ring = smem;
+  float* part = reinterpret_cast<float*>(smem + (size_t)NS * P.slot_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + P.part_floats);
+  uint64_t* empty = full + NS;
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCons / 32);
+    }
+    fence_barrier_init();
+    s_abort = 0;
+    s_issued = 0;
+  }
+  __syncthreads();
+
+  if (warp == kCons / 32) {
+    // ------------------------------------------------ producer: every op's weight tiles
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t gi = 0;
+      bool stop = false;
+      for (int k = 0; k < P.n_ops && !stop; ++k) {
+        const PersOp& op = P.ops[k];
+        if (op.type != OPT_GEMV) continue;
+        const GemvPlan& pl = P.plans[op.plan];
+        int t0, t1;
+        tile_range(pl, t0, t1);
+        const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
+        const bool paired = op.epi == EPI_SWIGLU;
+        const int opt = paired ? pl.tile_rows / 2 : pl.tile_rows;
+        const uint8_t* W = static_cast<const uint8_t*>(op.W);
+        for (int t = t0; t < t1; ++t) {
+          const int s = (int)(gi % (uint32_t)NS);
+          if (gi >= (uint32_t)NS && !mbar_wait(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u)) {
+            atomicOr(P.status, kDevTimeout);
+            s_abort = 1;
+          }
+          if (s_abort) {
+            stop = true;
+            break;
+          }
+          const int r0 = t * opt;
+          const int nv = min(opt, pl.n_out - r0);
+          const uint32_t bytes = (uint32_t)nv * row_bytes;
+          uint8_t* dst = ring + (size_t)s * P.slot_bytes;
+          if (paired) {
+            mbar_arrive_expect_tx(&full[s], 2u * bytes);
+            bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
+            bulk_g2s(dst + (size_t)opt * row_bytes,
+                     W + (size_t)op.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes,
+                     &full[s], pol);
+          } else {
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
+          }
+          ++gi;
+        }
+      }
+      s_issued = gi;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ consumers: ops in order
+    pdl_wait();
+    const unsigned G = gridDim.x;
+    uint32_t gi = 0;
+    float xr[kMaxNch][V];
+    for (int k = 0; k < P.n_ops; ++k) {
+      if (k > 0) {
+        if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * G)) {
+          atomicOr(P.status, kDevTimeout);
+          s_abort = 1;
+        }
+        bar_sync(1, kCons);
+        if (s_abort) break;
+      }
+      const PersOp& op = P.ops[k];
+      if (op.type == OPT_ATTN) {
+        attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last);
+      } else {
+        const GemvPlan& pl = P.plans[op.plan];
+        int t0, t1;
+        tile_range(pl, t0, t1);
+        const int nt = t1 - t0;
+        if (nt > 0) {
+          const int g = tid / pl.tpr, tig = tid % pl.tpr;
+          form_x<WT>(P, op, pl, pl.nch, xr, g, tig, tid, warp, lane, s_red, s_att);
+          bool ok = true;
+          switch (pl.nch) {
+            case 1: ok = consume_tiles<WT, 1>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+            case 2: ok = consume_tiles<WT, 2>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+            case 3: ok = consume_tiles<WT, 3>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+            case 4: ok = consume_tiles<WT, 4>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+            default: ok = consume_tiles<WT, 6>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+          }
+          if (!ok) {
+            atomicOr(P.status, kDevTimeout);
+            s_abort = 1;
+          }
+          bar_sync(1, kCons);
+          if (s_abort) break;
+          epilogue<WT>(P, op, pl, t0, nt, part, tid, warp, lane, s_key);
+        }
+      }
+      bar_sync(1, kCons);
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(P.grid_bar, 1u);
+      }
+    }
+  }
+  __syncthreads();
+  pdl_trigger();
+  if (s_abort) {
+    // wind down: wait (bounded) for this CTA's copies still in flight
+    if (tid == 0) {
+      const unsigned issued = s_issued;
+      for (unsigned i = issued > (unsigned)NS ? issued - NS : 0u; i < issued; ++i)
+        (void)mbar_wait(&full[i % NS], (i / NS) & 1u);
+    }
+    __syncthreads();
+  }
+}
+
+template <typename WT, typename KT, int EPL>
+cudaError_t launch_t(const PersParams& p, int grid, int smem, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThr, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, frame_persistent_kernel<WT, KT, EPL>, p);
+}
+
+template <typename WT, typename KT, int EPL>
+int max_grid_t(int smem) {
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, frame_persistent_kernel<WT, KT, EPL>,
+                                                    kThr, (size_t)smem) != cudaSuccess)
+    return 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return per_sm * sms;
+}
+
+template <typename WT, typename KT, int EPL>
+cudaError_t configure_t(int smem) {
+  return cudaFuncSetAttribute(frame_persistent_kernel<WT, KT, EPL>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace pers
+
+#define RQ_PERS_DISPATCH(CALL)                                                  \
+  switch (hd) {                                                                 \
+    case 32: return bf16 ? CALL(uint16_t, uint16_t, 1) : CALL(float, float, 1); \
+    case 64: return bf16 ? CALL(uint16_t, uint16_t, 2) : CALL(float, float, 2); \
+    default: return bf16 ? CALL(uint16_t, uint16_t, 4) : CALL(float, float, 4); \
+  }
+
+cudaError_t launch_persistent(const PersParams& p, bool bf16, bool kv_bf16, int grid, int smem,
+                              cudaStream_t s, bool pdl) {
+  if (bf16 != kv_bf16) return cudaErrorInvalidValue;
+  const int hd = p.head_dim;
+#define RQ_L(W, K, E) pers::launch_t<W, K, E>(p, grid, smem, s, pdl)
+  RQ_PERS_DISPATCH(RQ_L)
+#undef RQ_L
+}
+
+int persistent_max_grid(bool bf16, bool kv_bf16, int smem, int hd) {
+  if (bf16 != kv_bf16) return 0;
+#define RQ_M(W, K, E) pers::max_grid_t<W, K, E>(smem)
+  RQ_PERS_DISPATCH(RQ_M)
+#undef RQ_M
+}
+
+cudaError_t persistent_configure(bool bf16, bool kv_bf16, int smem, int hd) {
+  if (bf16 != kv_bf16) return cudaErrorInvalidValue;
+#define RQ_C(W, K, E) pers::configure_t<W, K, E>(smem)
+  RQ_PERS_DISPATCH(RQ_C)
+#undef RQ_C
+}
+
+GemvPlan plan_persistent(int n_out, int K, int es, bool paired, bool even_rows, int grid) {
+  GemvPlan pl = plan_gemv(n_out, K, es, paired, even_rows, 1 << 24);
+  pl.grid = grid;
+  pl.max_tiles = (pl.tiles + grid - 1) / grid;
+  pl.n_stages = 0;
+  pl.smem = 0;
+  return pl;
+}
+
+}  // namespace rqk

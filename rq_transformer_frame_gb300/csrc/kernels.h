@@ -104,6 +104,67 @@ struct AttnParams {
 };
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
 
+// ---------------------------------------------------------------- persistent frame
+// The whole frame's linears and attentions as one cooperative launch: an op table
+// executed in order by every CTA, a bounded grid barrier between dependent ops, and
+// a per-CTA producer warp that streams the weight tiles of all ops ahead of the
+// consumers through one shared-memory ring.
+enum PersOpType : int { OPT_GEMV = 0, OPT_ATTN = 1 };
+
+struct PersOp {
+  int type;       // PersOpType
+  int pro, epi;   // GEMV prologue / epilogue (GemvPro / GemvEpi)
+  int plan;       // index into PersParams::plans
+  const void* W;  // weights of this op
+  long long w_half;
+  const float* in;      // prologue input (PRO_DATTN: the query)
+  const float* alpha;
+  float* side_out;
+  const float* dk;      // PRO_DATTN keys / values [n][DD]
+  const float* dv;
+  int n_keys;
+  float* out;
+  void* kcache;         // EPI_QKV / OPT_ATTN: this layer's cache [C][D]
+  void* vcache;
+  float* dk_out;        // EPI_DQKV
+  float* dv_out;
+  int key_index;
+  const void* emb;      // EPI_DEPIN
+};
+
+constexpr int kPersMaxPlans = 12;
+
+struct PersParams {
+  const PersOp* ops;
+  int n_ops;
+  GemvPlan plans[kPersMaxPlans];
+  int slot_bytes;   // bytes of one ring slot (>= every op's tile)
+  int n_slots;
+  int part_floats;  // per-op partial-sum buffer (floats)
+  float eps;
+  int kv_bf16, head_dim, context;
+  float rope_theta;
+  int dheads, dhead_dim;
+  const int* offsets;
+  unsigned long long* keys;
+  const int* d_in;
+  // attention
+  const float* attn_q;
+  float* attn_out;
+  float* part;
+  int* counters;
+  int D, H, kps, nsplit;
+  unsigned int* grid_bar;  // zero at launch
+  uint32_t* status;
+};
+
+GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
+                         int grid);
+cudaError_t launch_persistent(const PersParams& p, bool bf16, bool kv_bf16, int grid,
+                              int smem, cudaStream_t s, bool pdl);
+cudaError_t persistent_configure(bool bf16, bool kv_bf16, int smem, int head_dim);
+int persistent_max_grid(bool bf16, bool kv_bf16, int smem, int head_dim);
+
 // ---------------------------------------------------------------- frame begin / end
 struct FrameParams {
   int B, D, V, A;
@@ -117,6 +178,7 @@ struct FrameParams {
   const void* text_emb; // [V+1][D]
   float* x;             // [B][D]
   float* emb_sum;       // [B][D]
+  unsigned int* grid_bar;  // persistent schedule's barrier counter (nullable)
 };
 cudaError_t launch_frame_begin(const FrameParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_frame_end(const FrameParams& p, cudaStream_t s, bool pdl);

@@ -52,6 +52,12 @@ struct rq_handle {
   GemvPlan p_qkv{}, p_out{}, p_gin{}, p_gout{}, p_head{};
   GemvPlan p_depin{}, p_dqkv{}, p_dout{}, p_dgin{}, p_dgout{}, p_lin{};
   int kps = 64, nsplit = 1;
+  // persistent schedule
+  int schedule = RQ_SCHEDULE_GRAPH;
+  PersOp* d_ops = nullptr;
+  unsigned int* grid_bar = nullptr;
+  PersParams pers{};
+  int pers_grid = 0, pers_smem = 0;
   std::vector<int> host_off;  // host mirror of the offsets (for byte accounting)
   bool poisoned = false;
   bool forcing_dirty = true;
@@ -109,6 +115,8 @@ rq_status validate_config(const rq_config* c, std::string* why) {
   if (c->dim % 8 || c->hidden % 8 || c->ddim % 8 || c->dhidden % 8)
     return uns("dim, hidden, ddim and dhidden must be multiples of 8");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
+  if (c->schedule < RQ_SCHEDULE_AUTO || c->schedule > RQ_SCHEDULE_PERSISTENT)
+    return bad("unknown schedule");
   return RQ_OK;
 }
 
@@ -321,6 +329,7 @@ FrameParams frame_params(const rq_handle* h) {
   f.text_emb = h->w.text_emb;
   f.x = h->x;
   f.emb_sum = h->emb_sum;
+  f.grid_bar = h->grid_bar;
   return f;
 }
 
@@ -329,6 +338,12 @@ cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
   cudaError_t e;
   const FrameParams f = frame_params(h);
   if ((e = launch_frame_begin(f, h->wbf, s)) != cudaSuccess) return e;
+  if (h->schedule == RQ_SCHEDULE_PERSISTENT) {
+    if ((e = launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
+        cudaSuccess)
+      return e;
+    return launch_frame_end(f, s, true);
+  }
   for (int l = 0; l < h->cfg.layers; ++l) {
     if ((e = op_qkv(h, l, s, true)) != cudaSuccess) return e;
     if ((e = op_attn(h, l, s, true)) != cudaSuccess) return e;
@@ -358,6 +373,8 @@ void free_all(rq_handle* h) {
                  h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters};
   for (void* p : dev)
     if (p) cudaFree(p);
+  if (h->d_ops) cudaFree(h->d_ops);
+  if (h->grid_bar) cudaFree(h->grid_bar);
   if (h->h_in) cudaFreeHost(h->h_in);
   if (h->h_out) cudaFreeHost(h->h_out);
   if (h->cap) cudaStreamDestroy(h->cap);
@@ -396,6 +413,201 @@ rq_status plan_all(rq_handle* h, std::string* why) {
   }
   h->kps = 64;
   h->nsplit = (c.context + h->kps - 1) / h->kps;
+  return RQ_OK;
+}
+
+
+// ---- persistent schedule: plans for one cooperative grid and the frame's op table
+constexpr int kPersSlotBudget = 96 * 1024;
+
+void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
+  const rq_config& c = h->cfg;
+  const int es = h->wes;
+  pl[0] = plan_persistent(3 * c.dim, c.dim, es, false, true, G);
+  pl[1] = plan_persistent(c.dim, c.dim, es, false, false, G);
+  pl[2] = plan_persistent(c.hidden, c.dim, es, true, false, G);
+  pl[3] = plan_persistent(c.dim, c.hidden, es, false, false, G);
+  pl[4] = plan_persistent(c.text_card, c.dim, es, false, false, G);
+  pl[5] = plan_persistent(c.ddim, c.dim, es, false, false, G);
+  pl[6] = plan_persistent(3 * c.ddim, c.ddim, es, false, false, G);
+  pl[7] = plan_persistent(c.ddim, c.ddim, es, false, false, G);
+  pl[8] = plan_persistent(c.dhidden, c.ddim, es, true, false, G);
+  pl[9] = plan_persistent(c.ddim, c.dhidden, es, false, false, G);
+  pl[10] = plan_persistent(c.audio_card, c.ddim, es, false, false, G);
+}
+constexpr int kPersPlans = 11;
+
+std::vector<PersOp> pers_ops(const rq_handle* h) {
+  const rq_config& c = h->cfg;
+  const size_t D = c.dim, C = c.context, F = c.hidden, A = c.audio_card;
+  const size_t DD = c.ddim, DF = c.dhidden;
+  const int es = h->wes;
+  std::vector<PersOp> ops;
+  auto gemv = [](int pro, int epi, int plan, const void* W) {
+    PersOp o{};
+    o.type = OPT_GEMV;
+    o.pro = pro;
+    o.epi = epi;
+    o.plan = plan;
+    o.W = W;
+    return o;
+  };
+  for (int l = 0; l < c.layers; ++l) {
+    void* kc = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
+    void* vc = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
+    PersOp o = gemv(PRO_RMS, EPI_QKV, 0, woff(h->w.in_proj, (size_t)l * 3 * D * D, es));
+    o.in = h->x;
+    o.alpha = h->w.norm1 + (size_t)l * D;
+    o.out = h->q;
+    o.kcache = kc;
+    o.vcache = vc;
+    ops.push_back(o);
+    PersOp a{};
+    a.type = OPT_ATTN;
+    a.kcache = kc;
+    a.vcache = vc;
+    ops.push_back(a);
+    o = gemv(PRO_PLAIN, EPI_RESID, 1, woff(h->w.out_proj, (size_t)l * D * D, es));
+    o.in = h->attn;
+    o.out = h->x;
+    ops.push_back(o);
+    o = gemv(PRO_RMS, EPI_SWIGLU, 2, woff(h->w.gate_in, (size_t)l * 2 * F * D, es));
+    o.w_half = (long long)(F * D);
+    o.in = h->x;
+    o.alpha = h->w.norm2 + (size_t)l * D;
+    o.out = h->u;
+    ops.push_back(o);
+    o = gemv(PRO_PLAIN, EPI_RESID, 3, woff(h->w.gate_out, (size_t)l * D * F, es));
+    o.in = h->u;
+    o.out = h->x;
+    ops.push_back(o);
+  }
+  PersOp hd = gemv(PRO_RMS, EPI_ARGMAX, 4, h->w.text_linear);
+  hd.in = h->x;
+  hd.alpha = h->w.out_norm;
+  hd.side_out = h->tout;
+  hd.out = h->text_logits;
+  hd.key_index = 0;
+  ops.push_back(hd);
+  for (int cb = 0; cb < 8; ++cb) {
+    PersOp o = gemv(PRO_PLAIN, EPI_DEPIN, 5, woff(h->w.dep_in, (size_t)cb * DD * D, es));
+    o.in = h->tout;
+    o.out = h->dx;
+    o.emb = cb == 0 ? h->w.dep_text_emb : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, es);
+    o.key_index = cb;
+    ops.push_back(o);
+    for (int l = 0; l < c.dlayers; ++l) {
+      const size_t ls = (size_t)l * 8 + cb;
+      o = gemv(PRO_RMS, EPI_DQKV, 6, woff(h->w.d_in_proj, ls * 3 * DD * DD, es));
+      o.in = h->dx;
+      o.alpha = h->w.dnorm1 + (size_t)l * DD;
+      o.out = h->dq;
+      o.dk_out = h->dkv + dkv_off(h, l, 0, cb);
+      o.dv_out = h->dkv + dkv_off(h, l, 1, cb);
+      ops.push_back(o);
+      o = gemv(PRO_DATTN, EPI_RESID, 7, woff(h->w.d_out_proj, ls * DD * DD, es));
+      o.in = h->dq;
+      o.dk = h->dkv + dkv_off(h, l, 0, 0);
+      o.dv = h->dkv + dkv_off(h, l, 1, 0);
+      o.n_keys = cb + 1;
+      o.out = h->dx;
+      ops.push_back(o);
+      o = gemv(PRO_RMS, EPI_SWIGLU, 8, woff(h->w.d_gate_in, ls * 2 * DF * DD, es));
+      o.w_half = (long long)(DF * DD);
+      o.in = h->dx;
+      o.alpha = h->w.dnorm2 + (size_t)l * DD;
+      o.out = h->du;
+      ops.push_back(o);
+      o = gemv(PRO_PLAIN, EPI_RESID, 9, woff(h->w.d_gate_out, ls * DD * DF, es));
+      o.in = h->du;
+      o.out = h->dx;
+      ops.push_back(o);
+    }
+    o = gemv(PRO_PLAIN, EPI_ARGMAX, 10, woff(h->w.linears, (size_t)cb * A * DD, es));
+    o.in = h->dx;
+    o.out = h->audio_logits + (size_t)cb * A;
+    o.key_index = 1 + cb;
+    ops.push_back(o);
+  }
+  return ops;
+}
+
+// Decide the schedule; for the persistent one build plans, ring geometry and op table.
+rq_status setup_schedule(rq_handle* h) {
+  const rq_config& c = h->cfg;
+  const bool can = c.batch == 1 && h->wbf == h->kvbf;
+  if (c.schedule == RQ_SCHEDULE_GRAPH || (c.schedule == RQ_SCHEDULE_AUTO && !can)) {
+    h->schedule = RQ_SCHEDULE_GRAPH;
+    return RQ_OK;
+  }
+  if (!can)
+    return fail(h, RQ_ERR_UNSUPPORTED,
+                "the persistent schedule needs batch 1 and one dtype for weights and K/V");
+  GemvPlan pl[kPersMaxPlans];
+  int G = 2 * h->num_sms, slot = 0, part = 0, ns = 0, smem = 0;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    pers_plans(h, G, pl);
+    slot = 0;
+    part = 0;
+    for (int i = 0; i < kPersPlans; ++i) {
+      if (pl[i].nch == 0) return fail(h, RQ_ERR_UNSUPPORTED, "GEMV shape unsupported");
+      const int tb = pl[i].tile_rows * pl[i].K * h->wes;
+      slot = tb > slot ? tb : slot;
+      const int pf = (pl[i].max_tiles * pl[i].tile_rows * (pl[i].tpr / 32) + 3) & ~3;
+      part = pf > part ? pf : part;
+    }
+    slot = (slot + 127) & ~127;
+    ns = kPersSlotBudget / slot;
+    if (ns < 2) ns = 2;
+    smem = ns * slot + part * 4 + 2 * ns * 8;
+    cudaError_t e = persistent_configure(h->wbf, h->kvbf, smem, c.head_dim);
+    if (e != cudaSuccess) return cuda_fail(h, e, "persistent_configure");
+    const int maxg = persistent_max_grid(h->wbf, h->kvbf, smem, c.head_dim);
+    if (maxg >= G) break;
+    if (attempt == 1 || maxg < h->num_sms) {
+      if (c.schedule == RQ_SCHEDULE_PERSISTENT)
+        return fail(h, RQ_ERR_UNSUPPORTED, "the persistent grid does not fit on this device");
+      h->schedule = RQ_SCHEDULE_GRAPH;
+      return RQ_OK;
+    }
+    G = h->num_sms;
+  }
+  std::vector<PersOp> ops = pers_ops(h);
+  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->d_ops), ops.size() * sizeof(PersOp)));
+  RQ_CUDA(h, cudaMemcpy(h->d_ops, ops.data(), ops.size() * sizeof(PersOp), cudaMemcpyHostToDevice));
+  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->grid_bar), 256));
+  RQ_CUDA(h, cudaMemset(h->grid_bar, 0, 256));
+  PersParams& P = h->pers;
+  P = PersParams{};
+  P.ops = h->d_ops;
+  P.n_ops = (int)ops.size();
+  for (int i = 0; i < kPersPlans; ++i) P.plans[i] = pl[i];
+  P.slot_bytes = slot;
+  P.n_slots = ns;
+  P.part_floats = part;
+  P.eps = c.rms_eps;
+  P.kv_bf16 = h->kvbf ? 1 : 0;
+  P.head_dim = c.head_dim;
+  P.context = c.context;
+  P.rope_theta = c.rope_theta;
+  P.dheads = c.dheads;
+  P.dhead_dim = c.dhead_dim;
+  P.offsets = h->offsets;
+  P.keys = h->keys;
+  P.d_in = h->d_in;
+  P.attn_q = h->q;
+  P.attn_out = h->attn;
+  P.part = h->part;
+  P.counters = h->counters;
+  P.D = c.dim;
+  P.H = c.heads;
+  P.kps = h->kps;
+  P.nsplit = h->nsplit;
+  P.grid_bar = h->grid_bar;
+  P.status = h->d_status();
+  h->pers_grid = G;
+  h->pers_smem = smem;
+  h->schedule = RQ_SCHEDULE_PERSISTENT;
   return RQ_OK;
 }
 
@@ -453,6 +665,7 @@ rq_status create_impl(rq_handle* h) {
   RQ_CUDA(h, launch_reset(h->ring, h->offsets, (int)B, -1, h->cap));
   RQ_CUDA(h, cudaStreamSynchronize(h->cap));
   h->host_off.assign(B, 0);
+  if ((st = setup_schedule(h)) != RQ_OK) return st;
   // capture one frame as a graph (programmatic edges between consecutive kernels)
   RQ_CUDA(h, cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
   cudaError_t e = enqueue_frame(h, h->cap);
@@ -763,6 +976,8 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
 }
 
 int32_t rq_frame_kernel_count(const rq_handle* h) { return h ? h->n_kernels : 0; }
+
+int32_t rq_schedule(const rq_handle* h) { return h ? h->schedule : 0; }
 
 const char* rq_last_error(const rq_handle* h) {
   if (!h) return g_create_err.c_str();

@@ -53,10 +53,25 @@ def check_logits_and_tokens(c, own_gpu, r, text, audio, where):
             assert own_gpu[1 + cb] == r["own"][1 + cb], (where, cb)
 
 
-def run_free(c, frames, w=None, prefill=None):
+SCHEDULES = [binding.RQ_SCHEDULE_GRAPH, binding.RQ_SCHEDULE_PERSISTENT]
+SCHED_IDS = ["graph", "persistent"]
+_WEIGHTS = {}
+
+
+def weights_of(c):
+    key = (c.name, c.weight_dtype)
+    if key not in _WEIGHTS:
+        _WEIGHTS.clear()
+        _WEIGHTS[key] = synth.make_weights(c, seed=0)
+    return _WEIGHTS[key]
+
+
+def run_free(c, frames, w=None, prefill=None, schedule=binding.RQ_SCHEDULE_AUTO):
     """Both sides run free; every token, the ring and the offset must agree."""
-    w = w if w is not None else synth.make_weights(c, seed=0)
-    dec = binding.Decoder(c, binding.upload_weights(w))
+    w = w if w is not None else weights_of(c)
+    dec = binding.Decoder(c, binding.upload_weights(w), schedule=schedule)
+    if schedule != binding.RQ_SCHEDULE_AUTO:
+        assert dec.schedule == schedule
     orc = oracle.Oracle(c, w)
     st = orc.new_state()
     if prefill is not None:
@@ -84,10 +99,12 @@ def run_free(c, frames, w=None, prefill=None):
     dec.close()
 
 
-def run_forced(c, frames, w=None, session_users=None):
+def run_forced(c, frames, w=None, schedule=binding.RQ_SCHEDULE_AUTO):
     """The GPU is forced with the oracle's own tokens; compare own tokens + logits."""
-    w = w if w is not None else synth.make_weights(c, seed=0)
-    dec = binding.Decoder(c, binding.upload_weights(w))
+    w = w if w is not None else weights_of(c)
+    dec = binding.Decoder(c, binding.upload_weights(w), schedule=schedule)
+    if schedule != binding.RQ_SCHEDULE_AUTO:
+        assert dec.schedule == schedule
     orc = oracle.Oracle(c, w)
     st = orc.new_state()
     users = synth.user_tokens(c, frames).numpy()
@@ -105,29 +122,48 @@ def run_forced(c, frames, w=None, session_users=None):
     dec.close()
 
 
-def test_tiny_f32_free_run_bit_exact():
-    run_free(configs.TINY, 32)
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_tiny_f32_free_run_bit_exact(schedule):
+    run_free(configs.TINY, 32, schedule=schedule)
 
 
-def test_tiny_f32_past_context_window():
-    run_free(configs.TINY, 70)  # context 64: the window slides from frame 64 on
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_tiny_f32_past_context_window(schedule):
+    run_free(configs.TINY, 70, schedule=schedule)  # context 64: the window slides
 
 
-def test_tiny_prefilled_start_and_eviction():
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_tiny_prefilled_start_and_eviction(schedule):
     c = configs.TINY
     g = torch.Generator().manual_seed(3)
     n = 62  # offset % 3 == 2 as in the batch-64 workload; frames 2.. evict
     k = torch.randn(c.layers, n, c.dim, generator=g)
     v = torch.randn(c.layers, n, c.dim, generator=g)
-    run_free(c, 8, prefill=(k, v))
+    run_free(c, 8, prefill=(k, v), schedule=schedule)
 
 
-def test_tiny_bf16_forced():
-    run_forced(configs.TINY.with_(name="tiny_bf16", weight_dtype="bf16", kv_dtype="bf16"), 20)
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_tiny_bf16_forced(schedule):
+    run_forced(configs.TINY.with_(name="tiny_bf16", weight_dtype="bf16", kv_dtype="bf16"), 20,
+               schedule=schedule)
 
 
-def test_small_bf16_forced_full_run():
-    run_forced(configs.SMALL, configs.SMALL.frames)
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_small_bf16_forced_full_run(schedule):
+    run_forced(configs.SMALL, configs.SMALL.frames, schedule=schedule)
+
+
+def test_auto_schedule_choice():
+    c = configs.TINY
+    w = binding.upload_weights(weights_of(c))
+    d1 = binding.Decoder(c, w)
+    assert d1.schedule == binding.RQ_SCHEDULE_PERSISTENT
+    d3 = binding.Decoder(c.with_(batch=3), w)
+    assert d3.schedule == binding.RQ_SCHEDULE_GRAPH
+    with pytest.raises(binding.RQError):
+        binding.Decoder(c.with_(batch=3), w, schedule=binding.RQ_SCHEDULE_PERSISTENT)
+    d1.close()
+    d3.close()
 
 
 def test_batch_sessions_are_independent():
@@ -223,7 +259,8 @@ def test_bad_tokens_rejected_before_any_state_change():
     dec.close()
 
 
-def test_moshi7b_full_size_forced_frames():
-    """The Moshi-7B shape at batch 1, in the launch configuration the benchmark
-    times, against the oracle on the first frames."""
-    run_forced(configs.MOSHI7B, 4)
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
+def test_moshi7b_full_size_forced_frames(schedule):
+    """The Moshi-7B shape at batch 1 (the benchmark's workload; AUTO runs the
+    persistent schedule) against the oracle on the first frames."""
+    run_forced(configs.MOSHI7B, 4, schedule=schedule)
