@@ -101,9 +101,12 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int nt, uint32
   return true;
 }
 
+// Tiles [ceil(T*c/G), ceil(T*(c+1)/G)) for CTA c: contiguous, balanced, and CTA 0
+// always owns tile 0 (it writes the op's side output) even when T < G.
 __device__ __forceinline__ void tile_range(const GemvPlan& pl, int& t0, int& t1) {
-  t0 = (int)(((long long)pl.tiles * blockIdx.x) / gridDim.x);
-  t1 = (int)(((long long)pl.tiles * (blockIdx.x + 1)) / gridDim.x);
+  const long long T = pl.tiles, G = gridDim.x;
+  t0 = (int)((T * blockIdx.x + G - 1) / G);
+  t1 = (int)((T * (blockIdx.x + 1) + G - 1) / G);
 }
 
 // ---------------------------------------------------------------- prologue
