@@ -264,6 +264,15 @@ int32_t rq_frame_kernel_count(const rq_handle *h);
 /* The schedule the handle runs: RQ_SCHEDULE_GRAPH or RQ_SCHEDULE_PERSISTENT. */
 int32_t rq_schedule(const rq_handle *h);
 
+/* Per-op timeline of the last frame under the persistent schedule: us[i] = time from the
+ * start of op i to the start of op i+1 (the last: to the end of all ops), in
+ * microseconds, stamped on the device with %globaltimer (synchronizes the stream).  Ops
+ * in frame order: per temporal layer [qkv, attention, out_proj, gate_in, gate_out], the
+ * text head, then per depformer step [input, per layer (qkv, attention+out_proj,
+ * gate_in, gate_out), head].  us == NULL returns the op count; returns the number
+ * written, 0 under the graph schedule.  -1 marks an op that was not stamped. */
+int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
+
 const char *rq_last_error(const rq_handle *h);
 const char *rq_status_string(rq_status s);
 int32_t rq_abi_version(void);

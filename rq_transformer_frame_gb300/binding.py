@@ -81,6 +81,8 @@ def load() -> C.CDLL:
     L.rq_frame_kernel_count.restype = I32
     L.rq_schedule.argtypes = [P]
     L.rq_schedule.restype = I32
+    L.rq_get_op_times.argtypes = [P, P, I32]
+    L.rq_get_op_times.restype = I32
     L.rq_last_error.argtypes = [P]
     L.rq_last_error.restype = C.c_char_p
     L.rq_status_string.argtypes = [C.c_int]
@@ -223,6 +225,15 @@ class Decoder:
         b = C.c_double(0)
         self._check(self.L.rq_launch_op(self.h, int(op), int(layer), int(count), C.byref(b)))
         return b.value
+
+    def op_times(self):
+        """Per-op microseconds of the last frame (persistent schedule), else None."""
+        n = self.L.rq_get_op_times(self.h, None, 0)
+        if n <= 0:
+            return None
+        us = np.zeros(n, np.float32)
+        self.L.rq_get_op_times(self.h, _p(us), n)
+        return us
 
     @property
     def schedule(self) -> int:

@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
     const unsigned G = gridDim.x;
     uint32_t gi = 0;
     float xr[kMaxNch][V];
+    const bool stamp = P.trace != nullptr && blockIdx.x == 0 && tid == 0;
     for (int k = 0; k < P.n_ops; ++k) {
       if (k > 0) {
         if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * G)) {
@@ -566,6 +567,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         bar_sync(1, kCons);
         if (s_abort) break;
       }
+      if (stamp) P.trace[k] = global_timer_ns();
       const PersOp& op = P.ops[k];
       if (op.type == OPT_ATTN) {
         attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last);
@@ -600,6 +602,8 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         atomicAdd(P.grid_bar, 1u);
       }
     }
+    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * G))
+      P.trace[P.n_ops] = global_timer_ns();
   }
   __syncthreads();
   pdl_trigger();

@@ -156,6 +156,7 @@ struct PersParams {
   int D, H, kps, nsplit;
   unsigned int* grid_bar;  // zero at launch
   uint32_t* status;
+  unsigned long long* trace;  // [n_ops + 1] op start times (ns), CTA 0 (nullable)
 };
 
 GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,

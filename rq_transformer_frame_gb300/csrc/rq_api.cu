@@ -56,6 +56,7 @@ struct rq_handle {
   int schedule = RQ_SCHEDULE_GRAPH;
   PersOp* d_ops = nullptr;
   unsigned int* grid_bar = nullptr;
+  unsigned long long* trace = nullptr;
   PersParams pers{};
   int pers_grid = 0, pers_smem = 0;
   std::vector<int> host_off;  // host mirror of the offsets (for byte accounting)
@@ -375,6 +376,7 @@ void free_all(rq_handle* h) {
     if (p) cudaFree(p);
   if (h->d_ops) cudaFree(h->d_ops);
   if (h->grid_bar) cudaFree(h->grid_bar);
+  if (h->trace) cudaFree(h->trace);
   if (h->h_in) cudaFreeHost(h->h_in);
   if (h->h_out) cudaFreeHost(h->h_out);
   if (h->cap) cudaStreamDestroy(h->cap);
@@ -418,7 +420,10 @@ rq_status plan_all(rq_handle* h, std::string* why) {
 
 
 // ---- persistent schedule: plans for one cooperative grid and the frame's op table
-constexpr int kPersSlotBudget = 96 * 1024;
+#ifndef RQ_PERS_SLOT_BUDGET
+#define RQ_PERS_SLOT_BUDGET (96 * 1024)
+#endif
+constexpr int kPersSlotBudget = RQ_PERS_SLOT_BUDGET;
 
 void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
   const rq_config& c = h->cfg;
@@ -577,6 +582,8 @@ rq_status setup_schedule(rq_handle* h) {
   RQ_CUDA(h, cudaMemcpy(h->d_ops, ops.data(), ops.size() * sizeof(PersOp), cudaMemcpyHostToDevice));
   RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->grid_bar), 256));
   RQ_CUDA(h, cudaMemset(h->grid_bar, 0, 256));
+  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->trace), (ops.size() + 1) * 8));
+  RQ_CUDA(h, cudaMemset(h->trace, 0, (ops.size() + 1) * 8));
   PersParams& P = h->pers;
   P = PersParams{};
   P.ops = h->d_ops;
@@ -605,6 +612,7 @@ rq_status setup_schedule(rq_handle* h) {
   P.nsplit = h->nsplit;
   P.grid_bar = h->grid_bar;
   P.status = h->d_status();
+  P.trace = h->trace;
   h->pers_grid = G;
   h->pers_smem = smem;
   h->schedule = RQ_SCHEDULE_PERSISTENT;
@@ -978,6 +986,20 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
 int32_t rq_frame_kernel_count(const rq_handle* h) { return h ? h->n_kernels : 0; }
 
 int32_t rq_schedule(const rq_handle* h) { return h ? h->schedule : 0; }
+
+int32_t rq_get_op_times(rq_handle* h, float* us, int32_t max_ops) {
+  if (!h || h->schedule != RQ_SCHEDULE_PERSISTENT || !h->trace) return 0;
+  const int n = h->pers.n_ops;
+  if (!us) return n;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return 0;
+  std::vector<unsigned long long> t((size_t)n + 1);
+  if (cudaMemcpy(t.data(), h->trace, t.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return 0;
+  const int m = n < max_ops ? n : max_ops;
+  for (int i = 0; i < m; ++i)
+    us[i] = (t[i + 1] >= t[i] && t[i] != 0) ? (float)((t[i + 1] - t[i]) * 1e-3) : -1.f;
+  return m;
+}
 
 const char* rq_last_error(const rq_handle* h) {
   if (!h) return g_create_err.c_str();
