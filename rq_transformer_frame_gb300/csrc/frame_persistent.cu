@@ -115,7 +115,8 @@ __device__ __forceinline__ void tile_range(const GemvPlan& pl, int& t0, int& t1)
 template <typename WT>
 __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                        const GemvPlan& pl, int nch,
-                                       float (&xr)[kMaxNch][Chunk<WT>::V], int g, int tig,
+                                       float (&xr)[kMaxNch][Chunk<WT>::V],
+                                       const float (&ar)[2][Chunk<WT>::V], int g, int tig,
                                        int tid, int warp, int lane, float* s_red,
                                        float* s_att) {
   constexpr int V = Chunk<WT>::V;
@@ -138,18 +139,19 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     }
   }
   if (op.pro == PRO_RMS) {
-    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n))
+    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).
+    // Every row group holds the whole vector: group 0's warps sum the squares from
+    // registers; alpha (a constant) was loaded before the grid barrier.
     float ss = 0.f;
-    for (int k = tid; k < K; k += kCons) {
-      const float v = ldcg(in + k);
-      ss = fmaf(v, v, ss);
-    }
+#pragma unroll
+    for (int j = 0; j < kMaxNch; ++j)
+#pragma unroll
+      for (int v = 0; v < V; ++v) ss = fmaf(xr[j][v], xr[j][v], ss);
     ss = warp_sum(ss);
     if (lane == 0) s_red[warp] = ss;
     bar_sync(1, kCons);
     float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCons / 32; ++w) tot += s_red[w];
+    for (int w = 0; w < pl.tpr / 32; ++w) tot += s_red[w];
     bar_sync(1, kCons);  // s_red is reused by the next op
     const float inv = 1.0f / sqrtf(P.eps + tot / (float)K);
     const bool side = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
@@ -158,7 +160,10 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
       const int c = tig + j * pl.tpr;
       if (j < nch && c < CC) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) xr[j][v] = xr[j][v] * op.alpha[c * V + v] * inv;
+        for (int v = 0; v < V; ++v) {
+          const float a = j < 2 ? ar[j < 2 ? j : 0][v] : op.alpha[c * V + v];
+          xr[j][v] = xr[j][v] * a * inv;
+        }
         if (side) {
 #pragma unroll
           for (int v = 0; v < V; ++v) op.side_out[c * V + v] = xr[j][v];
@@ -170,26 +175,35 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     const int nk = op.n_keys, dh = P.dheads, hd = P.dhead_dim;
     const float scale = 1.0f / sqrtf((float)hd);
     const int npairs = dh * nk;
-    int tp = 32;
-    while (tp > 1 && tp * npairs > kCons) tp >>= 1;
-    if (tp > hd / 4) tp = hd / 4;
-    const int pr = tid / tp, sub = tid % tp;
-    float d = 0.f;
-    if (pr < npairs) {
-      const int h = pr / nk, jk = pr % nk;
-      const float4* q4 = reinterpret_cast<const float4*>(in + h * hd);
-      const float4* k4 = reinterpret_cast<const float4*>(op.dk + (size_t)jk * K + h * hd);
-#pragma unroll 8
-      for (int e = sub; e < hd / 4; e += tp) {
-        const float4 a = __ldcg(q4 + e), c4 = __ldcg(k4 + e);
-        d = fmaf(a.x, c4.x, d);
-        d = fmaf(a.y, c4.y, d);
-        d = fmaf(a.z, c4.z, d);
-        d = fmaf(a.w, c4.w, d);
+    // tp = hd/16 threads per (head, key) pair, each with 4 float4 pairs of q and k;
+    // rounds of 256/tp pairs, every load of a round issued before its first use
+    const int tp = hd / 16;
+    const int ppr = kCons / tp;
+    const int sub = tid % tp;
+    for (int base = 0; base < npairs; base += ppr) {
+      const int pr = base + tid / tp;
+      float d = 0.f;
+      if (pr < npairs) {
+        const int h = pr / nk, jk = pr % nk;
+        const float4* q4 = reinterpret_cast<const float4*>(in + h * hd);
+        const float4* k4 = reinterpret_cast<const float4*>(op.dk + (size_t)jk * K + h * hd);
+        float4 qa[4], ka[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qa[i] = __ldcg(q4 + sub + i * tp);
+          ka[i] = __ldcg(k4 + sub + i * tp);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          d = fmaf(qa[i].x, ka[i].x, d);
+          d = fmaf(qa[i].y, ka[i].y, d);
+          d = fmaf(qa[i].z, ka[i].z, d);
+          d = fmaf(qa[i].w, ka[i].w, d);
+        }
       }
+      for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
     }
-    for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
     bar_sync(1, kCons);
     if (tid < dh) {
       float mx = -__int_as_float(0x7f800000);
@@ -558,7 +572,21 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
     uint32_t gi = 0;
     float xr[kMaxNch][V];
     const bool stamp = P.trace != nullptr && blockIdx.x == 0 && tid == 0;
+    float ar[2][V];
     for (int k = 0; k < P.n_ops; ++k) {
+      {  // constant alpha of an RMSNorm prologue: load it before waiting
+        const PersOp& op = P.ops[k];
+        if (op.type == OPT_GEMV && op.pro == PRO_RMS) {
+          const GemvPlan& pl = P.plans[op.plan];
+          const int tig = tid % pl.tpr, CC = pl.K / V;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int c = tig + j * pl.tpr;
+#pragma unroll
+            for (int v = 0; v < V; ++v) ar[j][v] = (c < CC) ? op.alpha[c * V + v] : 0.f;
+          }
+        }
+      }
       if (k > 0) {
         if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * G)) {
           atomicOr(P.status, kDevTimeout);
@@ -578,7 +606,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         const int nt = t1 - t0;
         if (nt > 0) {
           const int g = tid / pl.tpr, tig = tid % pl.tpr;
-          form_x<WT>(P, op, pl, pl.nch, xr, g, tig, tid, warp, lane, s_red, s_att);
+          form_x<WT>(P, op, pl, pl.nch, xr, ar, g, tig, tid, warp, lane, s_red, s_att);
           bool ok = true;
           switch (pl.nch) {
             case 1: ok = consume_tiles<WT, 1>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
