@@ -20,7 +20,8 @@ namespace pers {
 
 constexpr int kCons = 256;    // consumer threads
 constexpr int kThr = 288;     // + 1 producer warp
-constexpr int kMaxNch = 6;
+constexpr int kMaxNch = 2;  // long reductions are split into parts (GemvPlan::kparts)
+constexpr int kMaxStage = 1024;  // depformer attention output staged in shared memory (DD <= 1024)
 
 // ---------------------------------------------------------------- grid barrier
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -47,14 +48,15 @@ __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 // Consume this CTA's `nt` tiles of one GEMV op from the ring (slots advance with the
 // CTA-wide tile counter `gi`), leaving one partial per (row, warp) in `part`.
 template <typename WT, int NCH>
-__device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int nt, uint32_t& gi,
+__device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool accumulate,
+                                              int nt, uint32_t& gi,
                                               uint8_t* ring, int slot_bytes, int NS,
                                               uint64_t* full, uint64_t* empty, float* part,
                                               const float (&xr)[kMaxNch][Chunk<WT>::V],
                                               int g, int tig, int warp, int lane) {
   constexpr int RG = GemvShape<NCH>::RG;
-  const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
-  const int CC = pl.K / Chunk<WT>::V;
+  const uint32_t row_bytes = (uint32_t)Kw * (uint32_t)sizeof(WT);
+  const int CC = Kw / Chunk<WT>::V;
   const int wpg = pl.tpr >> 5;
   for (int i = 0; i < nt; ++i, ++gi) {
     const int s = (int)(gi % (uint32_t)NS);
@@ -63,20 +65,28 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int nt, uint32
     float acc[RG][2];
 #pragma unroll
     for (int r = 0; r < RG; ++r) acc[r][0] = acc[r][1] = 0.f;
-    uint4 w[NCH][RG];
+    // weights in batches of two chunks: loads of a batch issue together, and the
+    // register footprint stays small for long rows
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int c = tig + j * pl.tpr;
+    for (int jb = 0; jb < NCH; jb += 2) {
+      uint4 w[2][RG];
 #pragma unroll
-      for (int r = 0; r < RG; ++r)
-        w[j][r] = (c < CC) ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
-                                                             (size_t)c * 16)
-                           : make_uint4(0u, 0u, 0u, 0u);
+      for (int jj = 0; jj < 2; ++jj) {
+        const int c = tig + (jb + jj) * pl.tpr;
+#pragma unroll
+        for (int r = 0; r < RG; ++r)
+          w[jj][r] = (jb + jj < NCH && c < CC)
+                         ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
+                                                           (size_t)c * 16)
+                         : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+        if (jb + jj < NCH)
+#pragma unroll
+          for (int r = 0; r < RG; ++r)
+            Chunk<WT>::dot2(w[jj][r], xr[jb + jj < NCH ? jb + jj : 0], acc[r][0], acc[r][1]);
     }
-#pragma unroll
-    for (int j = 0; j < NCH; ++j)
-#pragma unroll
-      for (int r = 0; r < RG; ++r) Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     float* pp = part + (size_t)(i * pl.tile_rows + g * RG) * wpg + (warp % wpg);
@@ -91,11 +101,11 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int nt, uint32
       keep += __shfl_xor_sync(0xffffffffu, keep, 4);
       keep += __shfl_xor_sync(0xffffffffu, keep, 2);
       keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-      if (lane == 0) pp[0] = keep;
-      if (lane == 16) pp[wpg] = keep;
+      if (lane == 0) pp[0] = accumulate ? pp[0] + keep : keep;
+      if (lane == 16) pp[wpg] = accumulate ? pp[wpg] + keep : keep;
     } else {
       const float r0 = warp_sum(acc[0][0] + acc[0][1]);
-      if (lane == 0) pp[0] = r0;
+      if (lane == 0) pp[0] = accumulate ? pp[0] + r0 : r0;
     }
   }
   return true;
@@ -114,14 +124,14 @@ __device__ __forceinline__ void tile_range(const GemvPlan& pl, int& t0, int& t1)
 // [(tig + j*tpr)*V, +V).  Returns nothing; uses consumer barrier 1.
 template <typename WT>
 __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
-                                       const GemvPlan& pl, int nch,
+                                       const GemvPlan& pl, int nch, int k0, int Kw,
                                        float (&xr)[kMaxNch][Chunk<WT>::V],
                                        const float (&ar)[2][Chunk<WT>::V], int g, int tig,
                                        int tid, int warp, int lane, float* s_red,
                                        float* s_att) {
   constexpr int V = Chunk<WT>::V;
-  const int K = pl.K, CC = K / V;
-  const float* in = op.in;
+  const int K = pl.K, CC = Kw / V;
+  const float* in = op.in + k0;  // this part's columns [k0, k0 + Kw)
 #pragma unroll
   for (int j = 0; j < kMaxNch; ++j) {
     const int c = tig + j * pl.tpr;
@@ -171,80 +181,74 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
       }
     }
   } else if (op.pro == PRO_DATTN) {
-    // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1
+    // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1.
+    // hd/4 threads per head, one float4 of dimensions each: q and every key in one
+    // round trip, scores reduced with shuffles, the softmax in registers, then the
+    // values in one more round trip; the output is staged in shared memory and read
+    // back in the chunk layout of x.
     const int nk = op.n_keys, dh = P.dheads, hd = P.dhead_dim;
     const float scale = 1.0f / sqrtf((float)hd);
-    const int npairs = dh * nk;
-    // tp = hd/16 threads per (head, key) pair, each with 4 float4 pairs of q and k;
-    // rounds of 256/tp pairs, every load of a round issued before its first use
-    const int tp = hd / 16;
-    const int ppr = kCons / tp;
-    const int sub = tid % tp;
-    for (int base = 0; base < npairs; base += ppr) {
-      const int pr = base + tid / tp;
-      float d = 0.f;
-      if (pr < npairs) {
-        const int h = pr / nk, jk = pr % nk;
-        const float4* q4 = reinterpret_cast<const float4*>(in + h * hd);
-        const float4* k4 = reinterpret_cast<const float4*>(op.dk + (size_t)jk * K + h * hd);
-        float4 qa[4], ka[4];
+    const int tph = hd / 4;
+    const int hpp = kCons / tph;
+    for (int h0 = 0; h0 < dh; h0 += hpp) {
+      const int h = h0 + tid / tph, sub = tid % tph;
+      const bool act = h < dh;
+      const size_t col = (size_t)h * hd + 4 * sub;
+      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 kk[8];
+      if (act) q4 = __ldcg(reinterpret_cast<const float4*>(in + col));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          qa[i] = __ldcg(q4 + sub + i * tp);
-          ka[i] = __ldcg(k4 + sub + i * tp);
-        }
+      for (int j = 0; j < 8; ++j)
+        kk[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dk + (size_t)j * K + col))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      float sc[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          d = fmaf(qa[i].x, ka[i].x, d);
-          d = fmaf(qa[i].y, ka[i].y, d);
-          d = fmaf(qa[i].z, ka[i].z, d);
-          d = fmaf(qa[i].w, ka[i].w, d);
-        }
+      for (int j = 0; j < 8; ++j) {
+        float d = q4.x * kk[j].x;
+        d = fmaf(q4.y, kk[j].y, d);
+        d = fmaf(q4.z, kk[j].z, d);
+        d = fmaf(q4.w, kk[j].w, d);
+        for (int o = tph >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        sc[j] = d * scale;
       }
-      for (int o = tp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (pr < npairs && sub == 0) s_att[(pr / nk) * 8 + pr % nk] = d * scale;
-    }
-    bar_sync(1, kCons);
-    if (tid < dh) {
       float mx = -__int_as_float(0x7f800000);
-      for (int jk = 0; jk < nk; ++jk) mx = fmaxf(mx, s_att[tid * 8 + jk]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < nk) mx = fmaxf(mx, sc[j]);
       float den = 0.f;
-      for (int jk = 0; jk < nk; ++jk) {
-        const float e = expf(s_att[tid * 8 + jk] - mx);
-        s_att[tid * 8 + jk] = e;
-        den += e;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j] = (j < nk) ? expf(sc[j] - mx) : 0.f;
+        den += sc[j];
       }
-      for (int jk = 0; jk < nk; ++jk) s_att[tid * 8 + jk] = s_att[tid * 8 + jk] / den;
+      float4 vv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        vv[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)j * K + col))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < nk) {
+          const float w = sc[j] / den;
+          o.x += w * vv[j].x;
+          o.y += w * vv[j].y;
+          o.z += w * vv[j].z;
+          o.w += w * vv[j].w;
+        }
+      }
+      if (act) *reinterpret_cast<float4*>(s_att + col) = o;
     }
     bar_sync(1, kCons);
 #pragma unroll
     for (int j = 0; j < kMaxNch; ++j) {
       const int c = tig + j * pl.tpr;
       if (j < nch && c < CC) {
-        const int h = (c * V) / hd;
-        float o[V];
 #pragma unroll
-        for (int v = 0; v < V; ++v) o[v] = 0.f;
-#pragma unroll
-        for (int jk = 0; jk < 8; ++jk) {
-          if (jk < nk) {
-            const float pw = s_att[h * 8 + jk];
-#pragma unroll
-            for (int v = 0; v < V; v += 4) {
-              const float4 f =
-                  __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)jk * K + c * V + v));
-              o[v] += pw * f.x;
-              o[v + 1] += pw * f.y;
-              o[v + 2] += pw * f.z;
-              o[v + 3] += pw * f.w;
-            }
-          }
-        }
-#pragma unroll
-        for (int v = 0; v < V; ++v) xr[j][v] = o[v];
+        for (int v = 0; v < V; ++v) xr[j][v] = s_att[c * V + v];
       }
     }
-    bar_sync(1, kCons);  // s_att is reused by the next op
+    bar_sync(1, kCons);  // the staging buffer is reused by the next op
   }
 }
 
@@ -254,7 +258,8 @@ template <typename WT>
 __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
                                          const GemvPlan& pl, int t0, int nt, const float* part,
                                          int tid, int warp, int lane,
-                                         unsigned long long* s_key) {
+                                         unsigned long long* s_key, const float2* s_rope,
+                                         float resid_old) {
   const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
   const int nrows = nt * tr;
   auto yrow = [&](int lr) {
@@ -277,7 +282,7 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
       if (epi == EPI_STORE) op.out[row] = y;
-      if (epi == EPI_RESID) op.out[row] = ldcg(op.out + row) + y;
+      if (epi == EPI_RESID) op.out[row] = (lr == tid ? resid_old : ldcg(op.out + row)) + y;
       if (epi == EPI_DEPIN) {
         // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
         op.out[row] = (prev != -1)
@@ -306,10 +311,8 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       float a = yrow(lr), c = yrow(lr + 1);
       const int region = row / D, col = row % D;
       if (region < 2) {
-        const int ip = (col % hd) >> 1;
-        const float freq = expf(-logf(P.rope_theta) * 2.0f * (float)ip / (float)hd);
-        const float ang = freq * (float)pos;
-        const float sn = sinf(ang), cs = cosf(ang);
+        const float2 r = s_rope[(col % hd) >> 1];  // (cos, sin) of this pair at pos
+        const float cs = r.x, sn = r.y;
         const float ra = a * cs - c * sn;
         const float rc = a * sn + c * cs;
         a = ra;
@@ -491,12 +494,14 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
 
 // ---------------------------------------------------------------- the kernel
 template <typename WT, typename KT, int EPL>
+// two CTAs per SM: the register cap follows from 2 x 288 threads
 __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersParams P) {
   constexpr int V = Chunk<WT>::V;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_red[kCons / 32];
-  __shared__ float s_att[kMaxAttPairs];
+  __shared__ __align__(16) float s_att[kMaxStage];
   __shared__ unsigned long long s_key[kCons / 32];
+  __shared__ float2 s_rope[64];  // (cos, sin) of each rotary pair at this frame's position
   __shared__ float s_am[2][4], s_al[2][4];
   __shared__ float s_aacc[2][4][EPL * 32];
   __shared__ int s_last[2];
@@ -535,31 +540,44 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         const bool paired = op.epi == EPI_SWIGLU;
         const int opt = paired ? pl.tile_rows / 2 : pl.tile_rows;
         const uint8_t* W = static_cast<const uint8_t*>(op.W);
-        for (int t = t0; t < t1; ++t) {
-          const int s = (int)(gi % (uint32_t)NS);
-          if (gi >= (uint32_t)NS && !mbar_wait(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u)) {
-            atomicOr(P.status, kDevTimeout);
-            s_abort = 1;
+        for (int kp = 0; kp < pl.kparts && !stop; ++kp) {
+          const int k0 = kp * pl.kp_width;
+          const int Kw = kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
+          const uint32_t seg = (uint32_t)Kw * (uint32_t)sizeof(WT);  // bytes of one row part
+          for (int t = t0; t < t1; ++t) {
+            const int s = (int)(gi % (uint32_t)NS);
+            if (gi >= (uint32_t)NS && !mbar_wait(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u)) {
+              atomicOr(P.status, kDevTimeout);
+              s_abort = 1;
+            }
+            if (s_abort) {
+              stop = true;
+              break;
+            }
+            const int r0 = t * opt;
+            const int nv = min(opt, pl.n_out - r0);
+            uint8_t* dst = ring + (size_t)s * P.slot_bytes;
+            if (pl.kparts > 1) {
+              // one copy per row: the part's columns are a strided window of W
+              mbar_arrive_expect_tx(&full[s], (uint32_t)nv * seg);
+              for (int r = 0; r < nv; ++r)
+                bulk_g2s(dst + (size_t)r * seg,
+                         W + (size_t)(r0 + r) * row_bytes + (size_t)k0 * sizeof(WT), seg,
+                         &full[s], pol);
+            } else if (paired) {
+              const uint32_t bytes = (uint32_t)nv * row_bytes;
+              mbar_arrive_expect_tx(&full[s], 2u * bytes);
+              bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
+              bulk_g2s(dst + (size_t)opt * row_bytes,
+                       W + (size_t)op.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes,
+                       &full[s], pol);
+            } else {
+              const uint32_t bytes = (uint32_t)nv * row_bytes;
+              mbar_arrive_expect_tx(&full[s], bytes);
+              bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
+            }
+            ++gi;
           }
-          if (s_abort) {
-            stop = true;
-            break;
-          }
-          const int r0 = t * opt;
-          const int nv = min(opt, pl.n_out - r0);
-          const uint32_t bytes = (uint32_t)nv * row_bytes;
-          uint8_t* dst = ring + (size_t)s * P.slot_bytes;
-          if (paired) {
-            mbar_arrive_expect_tx(&full[s], 2u * bytes);
-            bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-            bulk_g2s(dst + (size_t)opt * row_bytes,
-                     W + (size_t)op.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes,
-                     &full[s], pol);
-          } else {
-            mbar_arrive_expect_tx(&full[s], bytes);
-            bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-          }
-          ++gi;
         }
       }
       s_issued = gi;
@@ -568,6 +586,14 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
   } else {
     // ------------------------------------------------ consumers: ops in order
     pdl_wait();
+    if (tid < P.head_dim / 2) {
+      // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos;
+      // every layer rotates at the same position, so the pairs are computed once
+      const float freq = expf(-logf(P.rope_theta) * 2.0f * (float)tid / (float)P.head_dim);
+      const float ang = freq * (float)P.offsets[0];
+      s_rope[tid] = make_float2(cosf(ang), sinf(ang));
+    }
+    bar_sync(1, kCons);
     const unsigned G = gridDim.x;
     uint32_t gi = 0;
     float xr[kMaxNch][V];
@@ -606,14 +632,24 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         const int nt = t1 - t0;
         if (nt > 0) {
           const int g = tid / pl.tpr, tig = tid % pl.tpr;
-          form_x<WT>(P, op, pl, pl.nch, xr, ar, g, tig, tid, warp, lane, s_red, s_att);
+          float resid_old = 0.f;  // the residual's old value, fetched before the tiles
+          if (op.epi == EPI_RESID && tid < nt * pl.tile_rows) {
+            const int row = (t0 + tid / pl.tile_rows) * pl.tile_rows + tid % pl.tile_rows;
+            if (row < pl.n_out) resid_old = ldcg(op.out + row);
+          }
           bool ok = true;
-          switch (pl.nch) {
-            case 1: ok = consume_tiles<WT, 1>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
-            case 2: ok = consume_tiles<WT, 2>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
-            case 3: ok = consume_tiles<WT, 3>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
-            case 4: ok = consume_tiles<WT, 4>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
-            default: ok = consume_tiles<WT, 6>(pl, nt, gi, ring, P.slot_bytes, NS, full, empty, part, xr, g, tig, warp, lane); break;
+          for (int kp = 0; kp < pl.kparts && ok; ++kp) {
+            // reduction part kp covers columns [k0, k0 + Kw); partials accumulate
+            const int k0 = kp * pl.kp_width;
+            const int Kw = kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
+            const int nch = (Kw / V + pl.tpr - 1) / pl.tpr;
+            form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, s_att);
+            if (nch <= 1)
+              ok = consume_tiles<WT, 1>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
+                                        empty, part, xr, g, tig, warp, lane);
+            else
+              ok = consume_tiles<WT, 2>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
+                                        empty, part, xr, g, tig, warp, lane);
           }
           if (!ok) {
             atomicOr(P.status, kDevTimeout);
@@ -621,7 +657,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           }
           bar_sync(1, kCons);
           if (s_abort) break;
-          epilogue<WT>(P, op, pl, t0, nt, part, tid, warp, lane, s_key);
+          epilogue<WT>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope, resid_old);
         }
       }
       bar_sync(1, kCons);
@@ -714,6 +750,20 @@ cudaError_t persistent_configure(bool bf16, bool kv_bf16, int smem, int hd) {
 
 GemvPlan plan_persistent(int n_out, int K, int es, bool paired, bool even_rows, int grid) {
   GemvPlan pl = plan_gemv(n_out, K, es, paired, even_rows, 1 << 24);
+  const int V = 16 / es, CC = K / V;
+  const int need = (CC + pl.tpr - 1) / pl.tpr;  // chunks per thread over the whole row
+  if (need > 2 && !paired) {
+    // parts of at most 2 chunks per thread; widths are multiples of 8 columns
+    pl.kparts = (need + 1) / 2;
+    int w = (K + pl.kparts - 1) / pl.kparts;
+    w = (w + 7) & ~7;
+    pl.kp_width = w;
+    pl.nch = 2;
+    pl.rg = 2;
+    pl.tile_rows = (kGemvConsumers / pl.tpr) * 2;
+    pl.tiles = (n_out + pl.tile_rows - 1) / pl.tile_rows;
+    if ((K - (pl.kparts - 1) * w) <= 0 || (w / V + pl.tpr - 1) / pl.tpr > 2) pl.nch = 0;
+  }
   pl.grid = grid;
   pl.max_tiles = (pl.tiles + grid - 1) / grid;
   pl.n_stages = 0;

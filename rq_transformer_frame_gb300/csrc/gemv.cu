@@ -60,6 +60,8 @@ GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int nu
   const int part_n = (pl.max_tiles * pl.tile_rows * wpg + 3) & ~3;
   pl.smem = ns * tile_bytes + part_n * 4 + 2 * ns * 8;
   pl.bytes = (double)n_out * (paired ? 2.0 : 1.0) * row_bytes;
+  pl.kparts = 1;
+  pl.kp_width = K;
   return pl;
 }
 

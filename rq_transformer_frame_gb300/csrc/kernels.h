@@ -36,6 +36,8 @@ struct GemvPlan {
   int tpr;         // threads per row group (power of two, 32..256)
   int rg;          // rows per thread per tile (1 or 2)
   int nch;         // 16-byte chunks of x per thread (kernel template parameter)
+  int kparts;      // persistent schedule: reduction split into parts of <= 2 chunks/thread
+  int kp_width;    // columns of every part but the last
   int max_tiles;   // tiles of the busiest CTA
   int smem;        // dynamic shared memory bytes
   double bytes;    // weight bytes one launch streams

@@ -556,7 +556,7 @@ rq_status setup_schedule(rq_handle* h) {
     part = 0;
     for (int i = 0; i < kPersPlans; ++i) {
       if (pl[i].nch == 0) return fail(h, RQ_ERR_UNSUPPORTED, "GEMV shape unsupported");
-      const int tb = pl[i].tile_rows * pl[i].K * h->wes;
+      const int tb = pl[i].tile_rows * pl[i].kp_width * h->wes;
       slot = tb > slot ? tb : slot;
       const int pf = (pl[i].max_tiles * pl[i].tile_rows * (pl[i].tpr / 32) + 3) & ~3;
       part = pf > part ? pf : part;
