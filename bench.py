@@ -60,26 +60,37 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def gemv_source_hash() -> str:
+KERNEL_SOURCES = {
+    "gemv": ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "common.cuh", "kernels.h"),
+    "frame": ("frame_persistent.cu", "gemv_kernel.cuh", "common.cuh", "kernels.h"),
+}
+
+
+def source_hash(kind: str) -> str:
     h = hashlib.sha256()
-    for n in ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "common.cuh", "kernels.h"):
+    for n in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "rq_transformer_frame_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (the summary records the source hash)."""
+def profiled_traffic(name: str, kind: str, bytes_per_launch: float = None):
+    """DRAM bytes per launch from a committed ncu summary, only if it was taken on the
+    current kernel source (the summary records the source hash).  A capture of a
+    smaller case is scaled by algorithmic bytes (traffic grows in proportion)."""
     p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    hsh = re.search(r"gemv_source_hash:\s*([0-9a-f]+)", txt)
-    if not m or not hsh or hsh.group(1) != gemv_source_hash():
+    hsh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not hsh or hsh.group(1) != source_hash(kind):
         return None
-    return float(m.group(1))
+    t = float(m.group(1))
+    a = re.search(r"algorithmic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if bytes_per_launch is not None and a:
+        t *= bytes_per_launch / float(a.group(1))
+    return t
 
 
 class ClockSampler:
@@ -300,11 +311,42 @@ def run_native(args, cfg):
                          "GB/s": round(nb / us / 1e3, 1),
                          "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4)}
     dec.reset(-1)
-    dom = kernels["gate_in"]
-    roof = {"kernel": "gemv_kernel<bf16, RMS, SWIGLU> (gate_in + SiLU gate, one layer)",
-            "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak, "unit": "GB/s",
-            "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
-            "traffic": profiled_traffic("gemv_moshi7b_b1.md")}
+    stages = None
+    if dec.schedule == binding.RQ_SCHEDULE_PERSISTENT:
+        # the frame's dominant kernel is the persistent whole-frame kernel itself
+        for t in range(W):
+            dec.step_device(d_users[t], d_out, d_has)
+        dec.sync()
+        us_ops = dec.op_times()
+        nb = dec.launch_op(binding.RQ_OP_FRAME, 0, 0)
+        dec.launch_op(binding.RQ_OP_FRAME, 0, 2)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nrep = 10
+        e0.record(stream)
+        dec.launch_op(binding.RQ_OP_FRAME, 0, nrep)
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / nrep
+        roof = {"kernel": "frame_persistent_kernel (all linears and attentions of a frame)",
+                "bound": "hbm", "achieved": round(nb / us / 1e3, 1), "peak": hbm_peak,
+                "unit": "GB/s", "peak_kind": peak_kind,
+                "frac": round(nb / us / 1e3 / hbm_peak, 4), "us_per_launch": round(us, 1),
+                "bytes_per_launch": nb,
+                "traffic": profiled_traffic("frame_persistent_moshi7b.md", "frame", nb)}
+        if us_ops is not None:
+            L, DL = cfg.layers, cfg.dlayers
+            stages = {"temporal_ms": round(float(us_ops[:5 * L].sum()) / 1e3, 3),
+                      "text_head_ms": round(float(us_ops[5 * L]) / 1e3, 3),
+                      "depformer_ms": round(float(us_ops[5 * L + 1:].sum()) / 1e3, 3),
+                      "ops": int(len(us_ops))}
+        dec.reset(-1)
+    else:
+        dom = kernels["gate_in"]
+        roof = {"kernel": "gemv_kernel<bf16, RMS, SWIGLU> (gate_in + SiLU gate, one layer)",
+                "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak, "unit": "GB/s",
+                "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
+                "traffic": profiled_traffic("gemv_moshi7b_b1.md", "gemv")}
 
     # ---- the oracle on this machine's host cores, on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -330,7 +372,8 @@ def run_native(args, cfg):
         "hbm": {"bytes_per_frame": bytes_frame, "GB/s": round(bytes_frame / (sec_max / K) / 1e9, 1),
                 "frac_of_measured": round(bytes_frame / (sec_max / K) / 1e9 / hbm_peak, 4),
                 "frac_of_8TBs": round(bytes_frame / (sec_max / K) / 8e12, 4)},
-        "roofline": roof, "kernels": kernels,
+        "roofline": roof, "kernels": kernels, "stages": stages,
+        "schedule": {1: "graph", 2: "persistent"}.get(dec.schedule, "?"),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "session-frames/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -215,7 +215,9 @@ enum {
   RQ_OP_OUT = 2,      /* out_proj GEMV + residual */
   RQ_OP_GATE_IN = 3,  /* RMSNorm + gate_in GEMV + SiLU gate */
   RQ_OP_GATE_OUT = 4, /* gate_out GEMV + residual */
-  RQ_OP_HEAD = 5      /* out_norm + text head GEMV + argmax */
+  RQ_OP_HEAD = 5,     /* out_norm + text head GEMV + argmax */
+  RQ_OP_FRAME = 6     /* the persistent schedule's whole-frame kernel (layer ignored);
+                         *bytes_per_launch = every weight once + the live K/V window */
 };
 rq_status rq_launch_op(rq_handle *h, int32_t op, int32_t layer, int32_t count,
                        double *bytes_per_launch);

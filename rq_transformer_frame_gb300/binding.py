@@ -20,7 +20,7 @@ LIBPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libr
 RQ_OK, RQ_ERR_ARG, RQ_ERR_TOKEN, RQ_ERR_CUDA = 0, 1, 2, 3
 RQ_ERR_OOM, RQ_ERR_TIMEOUT, RQ_ERR_UNSUPPORTED, RQ_ERR_POISONED = 4, 5, 6, 7
 RQ_F32, RQ_BF16 = 0, 1
-RQ_OP_QKV, RQ_OP_ATTN, RQ_OP_OUT, RQ_OP_GATE_IN, RQ_OP_GATE_OUT, RQ_OP_HEAD = range(6)
+RQ_OP_QKV, RQ_OP_ATTN, RQ_OP_OUT, RQ_OP_GATE_IN, RQ_OP_GATE_OUT, RQ_OP_HEAD, RQ_OP_FRAME = range(7)
 
 WEIGHT_FIELDS = [
     "emb", "text_emb", "norm1", "in_proj", "out_proj", "norm2", "gate_in",

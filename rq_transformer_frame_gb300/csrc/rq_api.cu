@@ -953,6 +953,23 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
   const rq_config& c = h->cfg;
   if (layer < 0 || layer >= c.layers || count < 0) return fail(h, RQ_ERR_ARG, "bad layer or count");
   double bytes = 0;
+  if (op == RQ_OP_FRAME) {
+    if (h->schedule != RQ_SCHEDULE_PERSISTENT)
+      return fail(h, RQ_ERR_UNSUPPORTED, "RQ_OP_FRAME needs the persistent schedule");
+    const double es = h->wes, D = c.dim, F = c.hidden, DD = c.ddim, DF = c.dhidden;
+    bytes = es * (c.layers * (3 * D * D + D * D + 2 * F * D + D * F) + (double)c.text_card * D +
+                  8.0 * c.dlayers * (3 * DD * DD + DD * DD + 2 * DF * DD + DD * DF) +
+                  8.0 * DD * D + 8.0 * c.audio_card * DD);
+    const int len = h->host_off[0] + 1 < c.context ? h->host_off[0] + 1 : c.context;
+    bytes += 2.0 * len * c.dim * h->kves * c.layers;
+    if (bytes_per_launch) *bytes_per_launch = bytes;
+    for (int i = 0; i < count; ++i) {
+      RQ_CUDA(h, cudaMemsetAsync(h->grid_bar, 0, 4, h->stream));
+      RQ_CUDA(h, launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem,
+                                   h->stream, false));
+    }
+    return RQ_OK;
+  }
   switch (op) {
     case RQ_OP_QKV: bytes = h->p_qkv.bytes; break;
     case RQ_OP_OUT: bytes = h->p_out.bytes; break;
