@@ -17,7 +17,7 @@ from . import binding, configs, synth
 
 OPS = {"qkv": binding.RQ_OP_QKV, "attn": binding.RQ_OP_ATTN, "out_proj": binding.RQ_OP_OUT,
        "gate_in": binding.RQ_OP_GATE_IN, "gate_out": binding.RQ_OP_GATE_OUT,
-       "text_head": binding.RQ_OP_HEAD}
+       "text_head": binding.RQ_OP_HEAD, "frame": binding.RQ_OP_FRAME}
 
 
 def main(argv=None):
@@ -38,7 +38,7 @@ def main(argv=None):
         dec.step(users[t])
     for name in a.ops.split(","):
         op = OPS[name]
-        layers = range(1) if name == "text_head" else range(cfg.layers)
+        layers = range(1) if name in ("text_head", "frame") else range(cfg.layers)
         nb = dec.launch_op(op, 0, 0)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
