@@ -89,9 +89,18 @@ typedef struct {
 
 /* Frame schedules.  PERSISTENT runs all linears and attentions of a frame as one
  * cooperative kernel with grid barriers between dependent ops (batch 1, same weight and
- * K/V dtype); GRAPH launches one kernel per op inside a CUDA graph.  AUTO picks
- * PERSISTENT when it applies, else GRAPH.  Results agree within the parity tolerance. */
-enum { RQ_SCHEDULE_AUTO = 0, RQ_SCHEDULE_GRAPH = 1, RQ_SCHEDULE_PERSISTENT = 2 };
+ * K/V dtype); GRAPH launches one streaming-GEMV kernel per op inside a CUDA graph;
+ * TENSOR (batch 16..64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
+ * runs every linear as one tcgen05 tensor-core GEMM over all sessions, with the GEMM
+ * operands (the normalised activations) rounded to bf16, inside a CUDA graph.  AUTO
+ * picks PERSISTENT when it applies, TENSOR at batch >= 16 when it applies, else GRAPH.
+ * Results agree within the parity tolerance. */
+enum {
+  RQ_SCHEDULE_AUTO = 0,
+  RQ_SCHEDULE_GRAPH = 1,
+  RQ_SCHEDULE_PERSISTENT = 2,
+  RQ_SCHEDULE_TENSOR = 3
+};
 
 /* Device pointers to the weights, row-major, matrices [out][in] ("moshi_lm.rs",
  * structs TemporalLayer, DepLayer, MoshiLm and `load_band`).  Matrices and tables are
@@ -207,6 +216,8 @@ rq_status rq_set_kv(rq_handle *h, int32_t session, int32_t n_pos, const void *k,
  * alone with events on the handle's stream.  Repeating an operation repeats its side
  * effects on activations and caches: call rq_reset(h, -1) before decoding again.
  *   op     one of RQ_OP_*;  layer  temporal layer index.
+ * Under RQ_SCHEDULE_TENSOR the linear ops launch the tensor-core GEMM alone, on the bf16
+ * operands the last frame left (the normalisation kernel in front of it is not repeated).
  * *bytes_per_launch (may be NULL) receives the weight + K/V bytes one launch must
  * stream. */
 enum {
@@ -263,7 +274,7 @@ rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t head_dim,
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 
-/* The schedule the handle runs: RQ_SCHEDULE_GRAPH or RQ_SCHEDULE_PERSISTENT. */
+/* The schedule the handle runs: RQ_SCHEDULE_GRAPH, _PERSISTENT or _TENSOR. */
 int32_t rq_schedule(const rq_handle *h);
 
 /* Per-op timeline of the last frame under the persistent schedule: us[i] = time from the

@@ -34,7 +34,7 @@ _CFG_INT_FIELDS = ["batch", "dim", "layers", "heads", "head_dim", "hidden", "con
                    "dhidden", "weight_dtype", "kv_dtype"]
 
 
-RQ_SCHEDULE_AUTO, RQ_SCHEDULE_GRAPH, RQ_SCHEDULE_PERSISTENT = 0, 1, 2
+RQ_SCHEDULE_AUTO, RQ_SCHEDULE_GRAPH, RQ_SCHEDULE_PERSISTENT, RQ_SCHEDULE_TENSOR = 0, 1, 2, 3
 
 
 class RqConfig(C.Structure):
@@ -237,7 +237,7 @@ class Decoder:
 
     @property
     def schedule(self) -> int:
-        """The schedule the handle runs (RQ_SCHEDULE_GRAPH or RQ_SCHEDULE_PERSISTENT)."""
+        """The schedule the handle runs (RQ_SCHEDULE_GRAPH, _PERSISTENT or _TENSOR)."""
         return int(self.L.rq_schedule(self.h))
 
     @property

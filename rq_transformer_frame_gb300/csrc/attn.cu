@@ -125,7 +125,11 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnParams p) {
       L += __ldcg(pb + s * pstride + 1) * c;
       A += __ldcg(pb + s * pstride + 2 + tid) * c;
     }
-    p.out[(size_t)b * p.D + (size_t)h * HD + tid] = A / L;
+    const float o = A / L;
+    p.out[(size_t)b * p.D + (size_t)h * HD + tid] = o;
+    if (p.out_bf16)
+      p.out_bf16[(size_t)b * p.D + (size_t)h * HD + tid] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(o));
   }
   if (tid == 0) p.counters[b * p.H + h] = 0;
 }
@@ -214,3 +218,60 @@ extern "C" rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim
     return RQ_ERR_CUDA;
   return launch_attn(a, kv_dtype == RQ_BF16, s, false) == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------- batched depformer attention
+namespace rqk {
+
+// "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1, for every
+// session: one warp per (session, head), the head's dimensions spread over the lanes;
+// writes the bf16 operand of the next tensor-core GEMM.
+__global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long long dq_bs,
+                                                           const float* dk, const float* dv,
+                                                           long long dkv_bs, int n_keys,
+                                                           int hd, int DD, uint16_t* out,
+                                                           long long out_bs) {
+  const int b = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const float* q = dq + (size_t)b * dq_bs + (size_t)h * hd;
+  const float* K = dk + (size_t)b * dkv_bs + (size_t)h * hd;
+  const float* Vv = dv + (size_t)b * dkv_bs + (size_t)h * hd;
+  const float scale = 1.0f / sqrtf((float)hd);
+  float sc[8];
+  float mx = -__int_as_float(0x7f800000);
+  for (int j = 0; j < n_keys; ++j) {
+    float d = 0.f;
+    for (int e = lane; e < hd; e += 32) d = fmaf(q[e], K[(size_t)j * DD + e], d);
+    sc[j] = warp_sum(d) * scale;
+    mx = fmaxf(mx, sc[j]);
+  }
+  float den = 0.f;
+  for (int j = 0; j < n_keys; ++j) {
+    sc[j] = expf(sc[j] - mx);
+    den += sc[j];
+  }
+  for (int e = lane; e < hd; e += 32) {
+    float o = 0.f;
+    for (int j = 0; j < n_keys; ++j) o += sc[j] / den * Vv[(size_t)j * DD + e];
+    out[(size_t)b * out_bs + (size_t)h * hd + e] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+  }
+}
+
+cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
+                                 const float* dv, long long dkv_bs, int n_keys, int B,
+                                 int heads, int hd, uint16_t* out, long long out_bs,
+                                 cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B, (unsigned)heads, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, dattn_batched_kernel, dq, dq_bs, dk, dv, dkv_bs, n_keys, hd,
+                            heads * hd, out, out_bs);
+}
+
+}  // namespace rqk

@@ -40,6 +40,12 @@ __global__ void __launch_bounds__(256) frame_begin_kernel(const FrameParams p) {
     }
     if (tid < 9) p.keys[(size_t)b * 9 + tid] = 0ull;
     if (tid == 0 && b == 0 && p.grid_bar) *p.grid_bar = 0u;
+    if (p.rope && tid < p.head_dim / 2) {
+      // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos
+      const float freq = expf(-logf(p.rope_theta) * 2.0f * (float)tid / (float)p.head_dim);
+      const float ang = freq * (float)off;
+      p.rope[(size_t)b * (p.head_dim / 2) + tid] = make_float2(cosf(ang), sinf(ang));
+    }
   }
   __syncthreads();
   pdl_trigger();

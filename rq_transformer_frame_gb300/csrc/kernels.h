@@ -2,6 +2,7 @@
 // Shared by the kernel translation units and the C-ABI engine (rq_api.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -100,11 +101,69 @@ struct AttnParams {
   float* part;          // [B][H][nsplit][hd + 2]
   int* counters;        // [B][H], zero between uses
   float* out;           // [B][D]
+  uint16_t* out_bf16;   // nullable: the same output rounded to bf16, [B][D]
   int D, H, hd, C, kps, nsplit;
   int batch;
   uint32_t* status;
 };
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
+cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
+                                 const float* dv, long long dkv_bs, int n_keys, int B,
+                                 int heads, int hd, uint16_t* out, long long out_bs,
+                                 cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- tensor-core GEMM
+// Y[b][n] = X[b][:] . W[n][:] for all sessions b at once (batch >= 16): a CTA computes a
+// 128-row tile of W against NB (padded) sessions on the tcgen05 tensor cores, operands
+// fed by TMA, accumulator in tensor memory; optional split-K merged in split order.
+struct TcPlan {
+  int n_out, K;       // output rows (paired: F), reduction length (multiple of 64)
+  int NB;             // padded batch: multiple of 16, <= 64
+  int paired;         // SiLU-gated: tile rows 0-63 gate, 64-127 multiplier
+  int tiles_m, splits, ksteps, ksteps_split;
+  int n_stages, smem;
+  double bytes;       // weight bytes one launch streams
+};
+
+struct TcParams {
+  TcPlan pl;
+  int epi;            // GemvEpi
+  int B;              // sessions (<= NB)
+  float* out;         // f32 outputs [B][..] (stride out_bs)
+  long long out_bs;
+  uint16_t* out_bf16; // EPI_SWIGLU: bf16 [NB][F] (stride outb_bs)
+  long long outb_bs;
+  void* kcache;       // EPI_QKV
+  void* vcache;
+  long long kv_bs;
+  int kv_bf16, head_dim, context;
+  const float2* rope; // [B][head_dim/2] (cos, sin) at each session's position
+  const int* offsets;
+  float* dk_out;      // EPI_DQKV
+  float* dv_out;
+  long long dkv_bs;
+  unsigned long long* keys;
+  int key_index;
+  const void* emb;    // EPI_DEPIN
+  const int* d_in;
+  float* partial;     // split-K scratch [tiles_m][splits][NB][128]
+  int* tickets;       // [tiles_m], zero between uses
+  uint32_t* status;
+};
+
+TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms);
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                      cudaStream_t s, bool pdl);
+cudaError_t tc_configure();
+// encode a 2-D bf16 tensor map: rows x cols (row-major), box {64 cols, box_rows}
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
+                           int box_rows);
+
+// prep: X bf16 [NB][K] = cast(in) or RMSNorm(in, alpha) for sessions < B (rows >= B zero);
+// side (nullable) receives the f32 normalized rows
+cudaError_t launch_prep_bf16(const float* in, long long in_bs, const float* alpha, float eps,
+                             int B, int NB, int K, uint16_t* xb, float* side, long long side_bs,
+                             cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- persistent frame
 // The whole frame's linears and attentions as one cooperative launch: an op table
@@ -163,6 +222,49 @@ struct PersParams {
 
 GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
                          int grid);
+// ---------------------------------------------------------------- tensor-core frame
+// Everything a batched frame needs between frame_begin and frame_end: the per-op plans,
+// the bf16 operand buffers [NB][K] (rows >= B stay zero) and one TMA map per weight
+// matrix and per operand buffer.
+struct TcFrame {
+  int B, NB, D, L, C, F, V, A, DD, DL, DF, H, hd, dH, dhd;
+  float eps;
+  int kv_bf16;
+  // bf16 matrices, f32 alphas (layout of rq_weights)
+  const void *in_proj, *out_proj, *gate_in, *gate_out, *text_linear, *dep_in, *dep_text_emb,
+      *dep_emb, *d_in_proj, *d_out_proj, *d_gate_in, *d_gate_out, *linears;
+  const float *norm1, *norm2, *out_norm, *dnorm1, *dnorm2;
+  // f32 state and outputs
+  float *x, *q, *attn, *tout, *text_logits, *audio_logits, *dx, *dq, *dkv;
+  void *kcache, *vcache;
+  int32_t* offsets;
+  const int32_t* d_in;
+  unsigned long long* keys;
+  float* attn_part;
+  int* attn_counters;
+  int kps, nsplit;
+  uint32_t* status;
+  float2* rope;  // [B][hd/2]
+  // bf16 operands
+  uint16_t *xb, *attn_b, *u_b, *tout_b, *dxb, *do_b, *du_b;
+  float* part;   // split-K partial tiles
+  int* tickets;  // per tile, zero between uses
+  TcPlan p_qkv, p_out, p_gin, p_gout, p_head, p_depin, p_dqkv, p_dout, p_dgin, p_dgout, p_lin;
+  CUtensorMap* wm;  // per weight matrix, see tc_frame_wmap_index
+  int n_wm;
+  CUtensorMap xm_x, xm_attn, xm_u, xm_tout, xm_dx, xm_do, xm_du;
+};
+// plans for every op; returns the split-K scratch floats and ticket count needed
+void tc_frame_plan(TcFrame& f, int num_sms, size_t* part_floats, int* n_tickets);
+// encode every tensor map (buffers and weights set, f.wm holds f.n_wm entries)
+cudaError_t tc_frame_maps(TcFrame& f);
+int tc_frame_n_maps(const TcFrame& f);
+// the frame's ops after frame_begin, each launched with a programmatic edge
+cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s);
+// one op of a temporal layer alone (0 qkv, 1 attention, 2 out_proj, 3 gate_in, 4 gate_out,
+// 5 text head): the GEMM on the operands left by the last frame
+cudaError_t tc_frame_launch_op(const TcFrame& f, int op, int layer, cudaStream_t s);
+
 cudaError_t launch_persistent(const PersParams& p, bool bf16, bool kv_bf16, int grid,
                               int smem, cudaStream_t s, bool pdl);
 cudaError_t persistent_configure(bool bf16, bool kv_bf16, int smem, int head_dim);
@@ -182,6 +284,9 @@ struct FrameParams {
   float* x;             // [B][D]
   float* emb_sum;       // [B][D]
   unsigned int* grid_bar;  // persistent schedule's barrier counter (nullable)
+  float2* rope;         // [B][head_dim/2] (cos, sin) at each session's position (nullable)
+  int head_dim;
+  float rope_theta;
 };
 cudaError_t launch_frame_begin(const FrameParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_frame_end(const FrameParams& p, cudaStream_t s, bool pdl);

@@ -59,6 +59,14 @@ struct rq_handle {
   unsigned long long* trace = nullptr;
   PersParams pers{};
   int pers_grid = 0, pers_smem = 0;
+  // tensor-core schedule
+  TcFrame tcf{};
+  std::vector<CUtensorMap> tc_maps;
+  float2* rope = nullptr;
+  uint16_t *xb = nullptr, *attn_b = nullptr, *u_b = nullptr, *tout_b = nullptr;
+  uint16_t *dxb = nullptr, *do_b = nullptr, *du_b = nullptr;
+  float* tc_part = nullptr;
+  int* tc_tickets = nullptr;
   std::vector<int> host_off;  // host mirror of the offsets (for byte accounting)
   bool poisoned = false;
   bool forcing_dirty = true;
@@ -116,7 +124,7 @@ rq_status validate_config(const rq_config* c, std::string* why) {
   if (c->dim % 8 || c->hidden % 8 || c->ddim % 8 || c->dhidden % 8)
     return uns("dim, hidden, ddim and dhidden must be multiples of 8");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
-  if (c->schedule < RQ_SCHEDULE_AUTO || c->schedule > RQ_SCHEDULE_PERSISTENT)
+  if (c->schedule < RQ_SCHEDULE_AUTO || c->schedule > RQ_SCHEDULE_TENSOR)
     return bad("unknown schedule");
   return RQ_OK;
 }
@@ -331,6 +339,9 @@ FrameParams frame_params(const rq_handle* h) {
   f.x = h->x;
   f.emb_sum = h->emb_sum;
   f.grid_bar = h->grid_bar;
+  f.rope = h->rope;
+  f.head_dim = h->cfg.head_dim;
+  f.rope_theta = h->cfg.rope_theta;
   return f;
 }
 
@@ -343,6 +354,10 @@ cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
     if ((e = launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
         cudaSuccess)
       return e;
+    return launch_frame_end(f, s, true);
+  }
+  if (h->schedule == RQ_SCHEDULE_TENSOR) {
+    if ((e = tc_frame_enqueue(h->tcf, s)) != cudaSuccess) return e;
     return launch_frame_end(f, s, true);
   }
   for (int l = 0; l < h->cfg.layers; ++l) {
@@ -373,6 +388,10 @@ void free_all(rq_handle* h) {
                  h->emb_sum, h->q, h->attn, h->u, h->tout, h->text_logits, h->audio_logits,
                  h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters};
   for (void* p : dev)
+    if (p) cudaFree(p);
+  void* tcb[] = {h->rope, h->xb, h->attn_b, h->u_b, h->tout_b, h->dxb, h->do_b, h->du_b,
+                 h->tc_part, h->tc_tickets};
+  for (void* p : tcb)
     if (p) cudaFree(p);
   if (h->d_ops) cudaFree(h->d_ops);
   if (h->grid_bar) cudaFree(h->grid_bar);
@@ -538,8 +557,128 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
 }
 
 // Decide the schedule; for the persistent one build plans, ring geometry and op table.
+bool tensor_eligible(const rq_handle* h) {
+  const rq_config& c = h->cfg;
+  return h->wbf && c.batch >= 1 && c.batch <= 64 && c.dim % 64 == 0 && c.hidden % 64 == 0 &&
+         c.ddim % 64 == 0 && c.dhidden % 64 == 0;
+}
+
+rq_status setup_tensor(rq_handle* h) {
+  const rq_config& c = h->cfg;
+  TcFrame& f = h->tcf;
+  f = TcFrame{};
+  f.B = c.batch;
+  f.NB = (c.batch + 15) / 16 * 16;
+  f.D = c.dim;
+  f.L = c.layers;
+  f.C = c.context;
+  f.F = c.hidden;
+  f.V = c.text_card;
+  f.A = c.audio_card;
+  f.DD = c.ddim;
+  f.DL = c.dlayers;
+  f.DF = c.dhidden;
+  f.H = c.heads;
+  f.hd = c.head_dim;
+  f.dH = c.dheads;
+  f.dhd = c.dhead_dim;
+  f.eps = c.rms_eps;
+  f.kv_bf16 = h->kvbf ? 1 : 0;
+  const rq_weights& w = h->w;
+  f.in_proj = w.in_proj;
+  f.out_proj = w.out_proj;
+  f.gate_in = w.gate_in;
+  f.gate_out = w.gate_out;
+  f.text_linear = w.text_linear;
+  f.dep_in = w.dep_in;
+  f.dep_text_emb = w.dep_text_emb;
+  f.dep_emb = w.dep_emb;
+  f.d_in_proj = w.d_in_proj;
+  f.d_out_proj = w.d_out_proj;
+  f.d_gate_in = w.d_gate_in;
+  f.d_gate_out = w.d_gate_out;
+  f.linears = w.linears;
+  f.norm1 = w.norm1;
+  f.norm2 = w.norm2;
+  f.out_norm = w.out_norm;
+  f.dnorm1 = w.dnorm1;
+  f.dnorm2 = w.dnorm2;
+  f.x = h->x;
+  f.q = h->q;
+  f.attn = h->attn;
+  f.tout = h->tout;
+  f.text_logits = h->text_logits;
+  f.audio_logits = h->audio_logits;
+  f.dx = h->dx;
+  f.dq = h->dq;
+  f.dkv = h->dkv;
+  f.kcache = h->kcache;
+  f.vcache = h->vcache;
+  f.offsets = h->offsets;
+  f.d_in = h->d_in;
+  f.keys = h->keys;
+  f.attn_part = h->part;
+  f.attn_counters = h->counters;
+  f.kps = h->kps;
+  f.nsplit = h->nsplit;
+  f.status = h->d_status();
+  size_t part_floats = 0;
+  int n_tickets = 0;
+  tc_frame_plan(f, h->num_sms, &part_floats, &n_tickets);
+  const size_t NB = f.NB;
+  auto A_ = [&](void** p, size_t bytes, const char* what) -> rq_status {
+    cudaError_t e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+    if (e == cudaSuccess) e = cudaMemset(*p, 0, bytes < 16 ? 16 : bytes);
+    if (e == cudaSuccess) return RQ_OK;
+    h->err = std::string("allocation failed: ") + what + ": " + cudaGetErrorString(e);
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? RQ_ERR_OOM : RQ_ERR_CUDA;
+  };
+  rq_status st;
+#define TC_ALLOC(ptr, bytes) \
+  if ((st = A_(reinterpret_cast<void**>(&(ptr)), (bytes), #ptr)) != RQ_OK) return st;
+  TC_ALLOC(h->rope, (size_t)c.batch * (c.head_dim / 2) * sizeof(float2));
+  TC_ALLOC(h->xb, NB * c.dim * 2);
+  TC_ALLOC(h->attn_b, NB * c.dim * 2);
+  TC_ALLOC(h->u_b, NB * c.hidden * 2);
+  TC_ALLOC(h->tout_b, NB * c.dim * 2);
+  TC_ALLOC(h->dxb, NB * c.ddim * 2);
+  TC_ALLOC(h->do_b, NB * c.ddim * 2);
+  TC_ALLOC(h->du_b, NB * c.dhidden * 2);
+  TC_ALLOC(h->tc_part, part_floats * 4);
+  TC_ALLOC(h->tc_tickets, (size_t)n_tickets * 4);
+#undef TC_ALLOC
+  f.rope = h->rope;
+  f.xb = h->xb;
+  f.attn_b = h->attn_b;
+  f.u_b = h->u_b;
+  f.tout_b = h->tout_b;
+  f.dxb = h->dxb;
+  f.do_b = h->do_b;
+  f.du_b = h->du_b;
+  f.part = h->tc_part;
+  f.tickets = h->tc_tickets;
+  f.n_wm = tc_frame_n_maps(f);
+  h->tc_maps.assign((size_t)f.n_wm, CUtensorMap{});
+  f.wm = h->tc_maps.data();
+  cudaError_t e = tc_configure();
+  if (e != cudaSuccess) return cuda_fail(h, e, "tc_configure");
+  e = tc_frame_maps(f);
+  if (e != cudaSuccess) return cuda_fail(h, e, "tensor map encoding");
+  h->schedule = RQ_SCHEDULE_TENSOR;
+  return RQ_OK;
+}
+
 rq_status setup_schedule(rq_handle* h) {
   const rq_config& c = h->cfg;
+  if (c.schedule == RQ_SCHEDULE_TENSOR ||
+      (c.schedule == RQ_SCHEDULE_AUTO && c.batch >= 16 && tensor_eligible(h))) {
+    if (!tensor_eligible(h))
+      return fail(h, RQ_ERR_UNSUPPORTED,
+                  "the tensor schedule needs batch <= 64, bf16 weights and dim, hidden, ddim, "
+                  "dhidden multiples of 64");
+    return setup_tensor(h);
+  }
   const bool can = c.batch == 1 && h->wbf == h->kvbf;
   if (c.schedule == RQ_SCHEDULE_GRAPH || (c.schedule == RQ_SCHEDULE_AUTO && !can)) {
     h->schedule = RQ_SCHEDULE_GRAPH;
@@ -985,6 +1124,19 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
     default: return fail(h, RQ_ERR_ARG, "unknown op");
   }
   if (bytes_per_launch) *bytes_per_launch = bytes;
+  if (h->schedule == RQ_SCHEDULE_TENSOR) {
+    if (op == RQ_OP_QKV) bytes = h->tcf.p_qkv.bytes;
+    if (op == RQ_OP_OUT) bytes = h->tcf.p_out.bytes;
+    if (op == RQ_OP_GATE_IN) bytes = h->tcf.p_gin.bytes;
+    if (op == RQ_OP_GATE_OUT) bytes = h->tcf.p_gout.bytes;
+    if (op == RQ_OP_HEAD) bytes = h->tcf.p_head.bytes;
+    if (bytes_per_launch) *bytes_per_launch = bytes;
+    for (int i = 0; i < count; ++i) {
+      cudaError_t e = tc_frame_launch_op(h->tcf, op, layer, h->stream);
+      if (e != cudaSuccess) return cuda_fail(h, e, "rq_launch_op");
+    }
+    return RQ_OK;
+  }
   for (int i = 0; i < count; ++i) {
     cudaError_t e = cudaSuccess;
     switch (op) {

@@ -1,0 +1,489 @@
+// tc_gemm.cu -- weights x batch on the tcgen05 tensor cores (batch >= 16).
+//
+// At batch B the linears of a frame become Y[b][n] = sum_k X[b][k] W[n][k], a real dense
+// contraction (B flops per weight byte... still below the tensor ridge, so the kernel
+// stays bound by streaming W once).  One CTA owns a 128-row tile of W (or 64 gate + 64
+// multiplier rows for the SiLU-gated layers) and a range of 64-wide K steps:
+//   warp 0 (one lane)  TMA: W tile box {64, 128} and X box {64, NB} per K step, 128-byte
+//                      swizzle, into a ring of shared-memory stages (mbarrier tx count);
+//   warp 1             allocates NB tensor-memory columns; one lane issues 4
+//                      tcgen05.mma.kind::f16 (M 128, N NB, K 16) per stage and commits
+//                      each stage back to its "empty" barrier;
+//   warps 2-5          read the 128 x NB f32 accumulator from tensor memory
+//                      (tcgen05.ld, one lane = one W row) and run the fused epilogue.
+// With split-K each split stores its partial tile; the last split to finish (atomic
+// ticket) adds all splits in split order -- deterministic -- and runs the epilogue.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace rqk {
+namespace tcg {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;  // rows of W per tile
+constexpr int kBK = 64;   // K elements per stage (128 bytes of bf16)
+constexpr int kABytes = kBM * kBK * 2;
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ void store_kv_tc(void* base, size_t i, float v, int bf16) {
+  if (bf16)
+    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(base)[i] = v;
+}
+
+
+// Fused epilogue of columns c0..c0+15 (sessions) of one 128-row tile, this thread's row m
+// of the tile = tensor-memory lane m.  Mirrors the streaming GEMV's epilogues, batched.
+struct EpiShared {
+  float ex[2][64][16];                 // SiLU gate: multiplier rows -> gate rows
+  unsigned long long key[4][64];       // argmax: best key per lane quarter and session
+};
+
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&d)[16], int c0,
+                                               int tile, int m, int lane, int q, EpiShared& es) {
+  const TcPlan& pl = p.pl;
+  const int B = p.B;
+  const int epi = p.epi;
+  if (epi == EPI_SWIGLU) {
+    // "moshi_lm.rs": silu(gate_j) * mult_j; the multiplier rows (64..127) hand their
+    // values to the gate rows (0..63) through shared memory (double-buffered by chunk)
+    float(*ex)[16] = es.ex[(c0 >> 4) & 1];
+    if (m >= 64) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ex[m - 64][i] = d[i];
+    }
+    bar_sync(1, 128);
+    const int j = tile * 64 + m;
+    if (m < 64 && j < pl.n_out) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float g = d[i], mu = ex[m][i];
+        p.out_bf16[(size_t)(c0 + i) * p.outb_bs + j] = f2bf(g / (1.0f + expf(-g)) * mu);
+      }
+    }
+    return;
+  }
+  const int row = tile * kBM + m;
+  const bool valid = row < pl.n_out;
+  if (epi == EPI_RESID || epi == EPI_STORE) {
+    if (valid)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < B) {
+          float* o = p.out + (size_t)(c0 + i) * p.out_bs + row;
+          *o = (epi == EPI_RESID ? *o : 0.f) + d[i];
+        }
+  } else if (epi == EPI_QKV) {
+    // "moshi_lm.rs", `rope_row` on q, k at each session's position, K/V append
+    const int D = pl.n_out / 3;
+    const int region = row / D, col = row % D;
+    const bool odd = (lane & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int b = c0 + i;
+      const float partner = __shfl_xor_sync(0xffffffffu, d[i], 1);
+      if (!valid || b >= B) continue;
+      float v = d[i];
+      if (region < 2) {
+        const float2 r = p.rope[(size_t)b * (p.head_dim / 2) + (col % p.head_dim) / 2];
+        const float re = odd ? partner : v, im = odd ? v : partner;
+        v = odd ? re * r.y + im * r.x : re * r.x - im * r.y;
+      }
+      if (region == 0) {
+        p.out[(size_t)b * p.out_bs + col] = v;
+      } else {
+        const int slot = p.offsets[b] % p.context;
+        store_kv_tc(region == 1 ? p.kcache : p.vcache,
+                    (size_t)b * p.kv_bs + (size_t)slot * D + col, v, p.kv_bf16);
+      }
+    }
+  } else if (epi == EPI_DQKV) {
+    const int DD = pl.n_out / 3;
+    if (valid)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int b = c0 + i;
+        if (b >= B) continue;
+        if (row < DD)
+          p.out[(size_t)b * p.out_bs + row] = d[i];
+        else if (row < 2 * DD)
+          p.dk_out[(size_t)b * p.dkv_bs + row - DD] = d[i];
+        else
+          p.dv_out[(size_t)b * p.dkv_bs + row - 2 * DD] = d[i];
+      }
+  } else if (epi == EPI_DEPIN) {
+    // "moshi_lm.rs", `embed` of the previous step's token: -1 adds nothing
+    const IoLayout io{p.B};
+    if (valid)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int b = c0 + i;
+        if (b >= B) continue;
+        const int prev = p.d_in[io.flag_off() + b]
+                             ? p.d_in[io.forced_off() + (size_t)b * 9 + p.key_index]
+                             : argmax_key_index(p.keys[(size_t)b * 9 + p.key_index]);
+        float e = 0.f;
+        if (prev != -1)
+          e = __uint_as_float(((uint32_t)static_cast<const uint16_t*>(
+                                   p.emb)[(size_t)max(prev, 0) * pl.n_out + row])
+                              << 16);
+        p.out[(size_t)b * p.out_bs + row] = d[i] + e;
+      }
+  } else if (epi == EPI_ARGMAX) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int b = c0 + i;
+      unsigned long long k = 0ull;
+      if (valid && b < B) {
+        p.out[(size_t)b * p.out_bs + row] = d[i];
+        k = argmax_key(d[i], (uint32_t)row);
+      }
+      k = warp_max_u64(k);
+      if (lane == 0) es.key[q][b] = k;
+    }
+  }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 2)
+    tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap wmap,
+                   const __grid_constant__ CUtensorMap xmap) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t s_full[8], s_empty[8], s_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_last;
+  __shared__ volatile int s_abort;
+  __shared__ int s_issued, s_consumed;
+  __shared__ EpiShared s_epi;
+  constexpr uint32_t kCols = NB <= 32 ? 32u : 64u;  // power of two >= 32
+  const TcPlan& pl = p.pl;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NS = pl.n_stages;
+  constexpr int kBBytes = NB * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;  // both multiples of 1024
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tile = blockIdx.x / pl.splits, split = blockIdx.x % pl.splits;
+  const int ks0 = split * pl.ksteps_split;
+  const int ks1 = min(ks0 + pl.ksteps_split, pl.ksteps);
+  const int nk = ks1 - ks0;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 1);
+    }
+    mbar_init(&s_done, 1);
+    fence_barrier_init();
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    tc::prefetch_tmap(&wmap);
+    tc::prefetch_tmap(&xmap);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&s_tmem, kCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();  // weights: read once per frame
+      const uint64_t pol_x = l2_policy_evict_last();  // operands: read by every tile
+      const int row_a = pl.paired ? tile * 64 : tile * kBM;
+      auto load_w = [&](int i) {
+        uint8_t* a = smem + (size_t)(i % NS) * kStage;
+        const int kx = (ks0 + i) * kBK;
+        tc::tma_load_2d(a, &wmap, kx, row_a, &s_full[i % NS], pol);
+        if (pl.paired)
+          tc::tma_load_2d(a + kABytes / 2, &wmap, kx, pl.n_out + row_a, &s_full[i % NS], pol);
+      };
+      auto load_x = [&](int i) {
+        uint8_t* b = smem + (size_t)(i % NS) * kStage + kABytes;
+        tc::tma_load_2d(b, &xmap, (ks0 + i) * kBK, 0, &s_full[i % NS], pol_x);
+      };
+      // the weights do not depend on the previous kernel: stream the first stages now,
+      // the activations once that kernel has finished
+      const int pre = min(NS, nk);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&s_full[i], (uint32_t)kStage);
+        load_w(i);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      int i = pre;
+      for (; i < nk; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(&s_empty[s], (uint32_t)((i / NS) - 1) & 1u)) {
+          atomicOr(p.status, kDevTimeout);
+          s_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&s_full[s], (uint32_t)kStage);
+        load_w(i);
+        load_x(i);
+      }
+      s_issued = i;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(kBM, NB);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % NS;
+        if (s_abort || !mbar_wait(&s_full[s], (uint32_t)(i / NS) & 1u)) {
+          atomicOr(p.status, kDevTimeout);
+          s_abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t a = smem_u32(smem + (size_t)s * kStage);
+        const uint32_t b = a + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc::mma_bf16(tmem, tc::sw128_desc(a + kk * 32), tc::sw128_desc(b + kk * 32), idesc,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&s_empty[s]);
+        s_consumed = i + 1;
+      }
+      tc::commit(&s_done);  // after every MMA issued above (also on abort)
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    pdl_wait();
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int m = q * 32 + lane;
+    const int et = tid - 64;  // 0..127 among the epilogue warps
+    if (!mbar_wait(&s_done, 0u)) s_abort = 1;
+    bar_sync(1, 128);
+    const bool ok = !s_abort;  // the same for all epilogue threads
+    tc::fence_after_sync();
+    bool run = ok;
+    if (!ok) atomicOr(p.status, kDevTimeout);
+    if (ok && pl.splits > 1) {
+      // store this split's partial, then the last split of the tile merges in order
+      float* mine = p.partial + ((size_t)(tile * pl.splits + split) * NB) * kBM;
+#pragma unroll
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mine[(size_t)(c0 + i) * kBM + m] = v[i];
+      }
+      __threadfence();
+      bar_sync(1, 128);
+      if (et == 0) s_last = (atomicAdd(&p.tickets[tile], 1) == pl.splits - 1);
+      bar_sync(1, 128);
+      run = s_last != 0;
+      if (run) __threadfence();
+    }
+    if (run) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        float v[16];
+        if (pl.splits > 1) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int sp = 0; sp < pl.splits; ++sp) {
+            const float* src =
+                p.partial + ((size_t)(tile * pl.splits + sp) * NB + c0) * kBM + m;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += __ldcg(src + (size_t)i * kBM);
+          }
+        } else {
+          tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        }
+        epilogue_chunk(p, v, c0, tile, m, lane, q, s_epi);
+      }
+      if (p.epi == EPI_ARGMAX) {
+        bar_sync(1, 128);
+        if (et < NB && et < p.B) {
+          unsigned long long k = s_epi.key[0][et];
+          for (int w = 1; w < 4; ++w) k = s_epi.key[w][et] > k ? s_epi.key[w][et] : k;
+          atomicMax(p.keys + (size_t)et * 9 + p.key_index, k);
+        }
+      }
+      if (pl.splits > 1 && et == 0) p.tickets[tile] = 0;
+    }
+    tc::fence_before_sync();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kCols);
+  }
+  if (s_abort && tid == 0) {
+    // wind down: wait (bounded) for TMA loads that no MMA consumed
+    for (int i = s_consumed; i < s_issued; ++i)
+      (void)mbar_wait(&s_full[i % NS], (uint32_t)(i / NS) & 1u);
+  }
+}
+
+}  // namespace tcg
+}  // namespace rqk
+
+// ---------------------------------------------------------------- activation prep
+namespace rqk {
+namespace tcg {
+
+// one CTA per padded session row: xb[b] = bf16(in[b] (* alpha * 1/sqrt(eps + mean(in^2))))
+// ("moshi_lm.rs", `rms_norm`), zero rows for b >= B; side[b] = the f32 result
+__global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long long in_bs,
+                                                        const float* alpha, float eps, int B,
+                                                        int K, uint16_t* xb, float* side,
+                                                        long long side_bs) {
+  __shared__ float s_red[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  uint16_t* dst = xb + (size_t)b * K;
+  if (b >= B) {
+    for (int k = tid; k < K; k += 256) dst[k] = 0;
+    return;
+  }
+  const float* x = in + (size_t)b * in_bs;
+  float inv = 1.f;
+  if (alpha) {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += 256) ss = fmaf(x[k], x[k], ss);
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) s_red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += s_red[w];
+    inv = 1.0f / sqrtf(eps + tot / (float)K);
+  }
+  for (int k = tid; k < K; k += 256) {
+    const float v = alpha ? x[k] * alpha[k] * inv : x[k];
+    dst[k] = f2bf(v);
+    if (side) side[(size_t)b * side_bs + k] = v;
+  }
+}
+
+}  // namespace tcg
+
+cudaError_t launch_prep_bf16(const float* in, long long in_bs, const float* alpha, float eps,
+                             int B, int NB, int K, uint16_t* xb, float* side, long long side_bs,
+                             cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)NB, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tcg::prep_bf16_kernel, in, in_bs, alpha, eps, B, K, xb, side,
+                            side_bs);
+}
+
+// ---------------------------------------------------------------- host side
+TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
+  TcPlan pl{};
+  pl.n_out = n_out;
+  pl.K = K;
+  pl.NB = NB;
+  pl.paired = paired ? 1 : 0;
+  const int rows = paired ? 64 : tcg::kBM;
+  pl.tiles_m = (n_out + rows - 1) / rows;
+  pl.ksteps = K / tcg::kBK;
+  // split K until the grid covers ~2 CTAs per SM, keeping >= 4 K steps per split
+  int splits = (2 * num_sms + pl.tiles_m - 1) / pl.tiles_m;
+  const int max_splits = pl.ksteps / 4 > 0 ? pl.ksteps / 4 : 1;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  pl.ksteps_split = (pl.ksteps + splits - 1) / splits;
+  pl.splits = (pl.ksteps + pl.ksteps_split - 1) / pl.ksteps_split;
+  const int stage = tcg::kABytes + NB * tcg::kBK * 2;
+  int ns = (96 * 1024) / stage;
+  ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+  pl.n_stages = ns;
+  pl.smem = ns * stage + 1024;
+  pl.bytes = (double)n_out * (paired ? 2.0 : 1.0) * K * 2.0;
+  return pl;
+}
+
+template <int NB>
+static cudaError_t launch_nb(const TcParams& p, const CUtensorMap& w, const CUtensorMap& x,
+                             cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.pl.tiles_m * p.pl.splits), 1, 1);
+  cfg.blockDim = dim3(tcg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)p.pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tcg::tc_gemm_kernel<NB>, p, w, x);
+}
+
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                      cudaStream_t s, bool pdl) {
+  switch (p.pl.NB) {
+    case 16: return launch_nb<16>(p, wmap, xmap, s, pdl);
+    case 32: return launch_nb<32>(p, wmap, xmap, s, pdl);
+    case 48: return launch_nb<48>(p, wmap, xmap, s, pdl);
+    case 64: return launch_nb<64>(p, wmap, xmap, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t tc_configure() {
+  const int smem = 200 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(tcg::tc_gemm_kernel<16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tcg::tc_gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tcg::tc_gemm_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tcg::tc_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
+                           int box_rows) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) return cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  if (cols % 64 || box_rows < 1 || box_rows > 256) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace rqk

@@ -13,6 +13,8 @@ import torch
 import oracle
 from rq_transformer_frame_gb300 import binding, configs, synth
 
+from parity_util import check_logits_and_tokens, rel_err, tol_of, weights_of  # noqa: F401
+
 pytestmark = pytest.mark.gpu
 
 
@@ -25,47 +27,8 @@ def _gpu():
     torch.cuda.set_device(0)
 
 
-def tol_of(c):
-    return 1e-3 if c.weight_dtype == "f32" else 2e-2
-
-
-def rel_err(got, want):
-    return float(np.max(np.abs(got - want)) / max(np.max(np.abs(want)), 1e-30))
-
-
-def margin(v):
-    s = np.sort(v)
-    return s[-1] - s[-2]
-
-
-def check_logits_and_tokens(c, own_gpu, r, text, audio, where):
-    tol = tol_of(c)
-    assert rel_err(text, r["text_logits"]) <= tol, (where, rel_err(text, r["text_logits"]))
-    for cb in range(8):
-        e = rel_err(audio[cb], r["audio_logits"][cb])
-        assert e <= tol, (where, cb, e)
-    tl = r["text_logits"]
-    if margin(tl) > tol * np.max(np.abs(tl)):
-        assert own_gpu[0] == r["own"][0], (where, "text")
-    for cb in range(8):
-        lg = r["audio_logits"][cb]
-        if margin(lg) > tol * np.max(np.abs(lg)):
-            assert own_gpu[1 + cb] == r["own"][1 + cb], (where, cb)
-
-
 SCHEDULES = [binding.RQ_SCHEDULE_GRAPH, binding.RQ_SCHEDULE_PERSISTENT]
 SCHED_IDS = ["graph", "persistent"]
-_WEIGHTS = {}
-
-
-def weights_of(c):
-    key = (c.name, c.weight_dtype)
-    if key not in _WEIGHTS:
-        _WEIGHTS.clear()
-        _WEIGHTS[key] = synth.make_weights(c, seed=0)
-    return _WEIGHTS[key]
-
-
 def run_free(c, frames, w=None, prefill=None, schedule=binding.RQ_SCHEDULE_AUTO):
     """Both sides run free; every token, the ring and the offset must agree."""
     w = w if w is not None else weights_of(c)

@@ -1,0 +1,135 @@
+"""Parity of the batched tensor-core schedule (RQ_SCHEDULE_TENSOR: every linear one
+tcgen05 GEMM over all sessions, bf16 operands) with the CPU oracle, session by session.
+
+Same bar as the other parity tests: ring, offsets and delayed outputs bit-exact; logits
+within 2e-2 * max|logit| (bf16 weights); a token may differ only where the oracle's
+top-2 margin is inside that tolerance.  Teacher-forced runs force every session with a
+seeded synthetic token stream on both sides, so a near-tie cannot fork a trajectory;
+free runs compare a session until its first near-tie.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rq_transformer_frame_gb300 import binding, configs, synth
+
+from parity_util import check_logits_and_tokens, margin, tol_of, weights_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def forced_tokens(c, frames, seed=77):
+    """int32 [frames][B][9]: text in [0, V), audio in [0, A), one generator per session."""
+    out = np.zeros((frames, c.batch, 9), np.int32)
+    for b in range(c.batch):
+        g = torch.Generator().manual_seed(seed * 1000 + b)
+        out[:, b, 0] = torch.randint(0, c.text_card, (frames,), generator=g).numpy()
+        out[:, b, 1:] = torch.randint(0, c.audio_card, (frames, 8), generator=g).numpy()
+    return out
+
+
+def run_batch_forced(c, frames, sessions):
+    w = weights_of(c)
+    dec = binding.Decoder(c, binding.upload_weights(w), schedule=binding.RQ_SCHEDULE_TENSOR)
+    assert dec.schedule == binding.RQ_SCHEDULE_TENSOR
+    orc = oracle.Oracle(c, w)
+    sts = {b: orc.new_state() for b in sessions}
+    users = synth.batch_user_tokens(c, frames).numpy()
+    forced = forced_tokens(c, frames)
+    for t in range(frames):
+        rs = {b: orc.step(sts[b], users[t, b], forced=forced[t, b], trace=True)
+              for b in sessions}
+        own, out, has = dec.step_forced(users[t], forced[t])
+        text, audio = dec.logits()
+        ring, off = dec.ring()
+        for b in sessions:
+            r = rs[b]
+            oring, ooff = sts[b].ring()
+            assert int(off[b]) == ooff and np.array_equal(ring[b], oring), (t, b)
+            assert bool(has[b]) == r["has_out"], (t, b)
+            if r["has_out"]:
+                assert np.array_equal(out[b], r["out"]), (t, b)
+            check_logits_and_tokens(c, own[b], r, text[b], audio[b], (t, b))
+    dec.close()
+
+
+def test_small_batch16_all_sessions_forced():
+    run_batch_forced(configs.SMALL.with_(batch=16), 6, range(16))
+
+
+@pytest.mark.parametrize("batch", [20, 64])
+def test_small_padded_and_full_tiles(batch):
+    """batch 20 pads the session tile to 32 (rows 20..31 stay zero); 64 fills it."""
+    run_batch_forced(configs.SMALL.with_(batch=batch), 4, [0, batch // 2, batch - 1])
+
+
+def test_small_batch16_free_run():
+    """No forcing: the argmax feeds the next depformer step and the ring; a session is
+    compared until the oracle meets its first near-tie."""
+    c = configs.SMALL.with_(batch=16)
+    w = weights_of(c)
+    dec = binding.Decoder(c, binding.upload_weights(w), schedule=binding.RQ_SCHEDULE_TENSOR)
+    orc = oracle.Oracle(c, w)
+    sts = [orc.new_state() for _ in range(16)]
+    alive = [True] * 16
+    users = synth.batch_user_tokens(c, 8).numpy()
+    tol = tol_of(c)
+    compared = 0
+    for t in range(8):
+        out, has = dec.step(users[t])
+        text, audio = dec.logits()
+        ring, off = dec.ring()
+        for b in range(16):
+            if not alive[b]:
+                continue
+            r = orc.step(sts[b], users[t, b], trace=True)
+            ties = [margin(r["text_logits"]) <= tol * np.max(np.abs(r["text_logits"]))] + [
+                margin(r["audio_logits"][k]) <= tol * np.max(np.abs(r["audio_logits"][k]))
+                for k in range(8)]
+            own = ring[b][np.arange(9), (int(off[b])) % 3]
+            check_logits_and_tokens(c, own, r, text[b], audio[b], (t, b))
+            if any(ties):
+                alive[b] = False
+                continue
+            oring, ooff = sts[b].ring()
+            assert int(off[b]) == ooff and np.array_equal(ring[b], oring), (t, b)
+            assert bool(has[b]) == r["has_out"], (t, b)
+            if r["has_out"]:
+                assert np.array_equal(out[b], r["out"]), (t, b)
+            compared += 1
+    assert compared >= 32
+    dec.close()
+
+
+def test_auto_picks_tensor_at_batch16():
+    c = configs.SMALL.with_(batch=16)
+    w = binding.upload_weights(weights_of(c))
+    d = binding.Decoder(c, w)
+    assert d.schedule == binding.RQ_SCHEDULE_TENSOR
+    d.close()
+    t = configs.TINY.with_(batch=16)  # f32 weights: the tensor schedule does not apply
+    wt = binding.upload_weights(weights_of(t))
+    d = binding.Decoder(t, wt)
+    assert d.schedule == binding.RQ_SCHEDULE_GRAPH
+    d.close()
+    with pytest.raises(binding.RQError):
+        binding.Decoder(t, wt, schedule=binding.RQ_SCHEDULE_TENSOR)
+
+
+def test_moshi7b_batch16_forced_frames():
+    """The batch-16 workload's shapes (M = 16 session tile) on the first frames."""
+    run_batch_forced(configs.MOSHI7B_B16, 3, [0, 15])
+
+
+def test_moshi7b_batch64_forced_frames():
+    run_batch_forced(configs.MOSHI7B.with_(batch=64), 2, [0, 63])
