@@ -31,8 +31,7 @@ class OrcCfg(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "dim", "layers", "heads", "head_dim", "hidden", "context", "text_card",
         "audio_card", "ddim", "dlayers", "dheads", "dhead_dim", "dhidden", "w_bf16",
-        "kv_bf16")] + [("eps", C.c_float), ("rope_theta", C.c_float),
-                       ("act_bf16", C.c_int32)]
+        "kv_bf16")] + [("eps", C.c_float), ("rope_theta", C.c_float)]
 
 
 class OrcWeights(C.Structure):
@@ -155,9 +154,7 @@ def round_to_bf16(x: float) -> float:
 class Oracle:
     """One model (config + host weights); sessions are `new_state()` handles."""
 
-    def __init__(self, cfg, weights: dict, act_bf16: bool = False):
-        """act_bf16: round each matrix product's activation operand to bf16 (the
-        operand precision of a bf16 tensor-core product); off = all f32."""
+    def __init__(self, cfg, weights: dict):
         self.cfg = cfg
         self.weights = weights  # keep the host tensors alive
         self.c = OrcCfg(
@@ -166,7 +163,7 @@ class Oracle:
             audio_card=cfg.audio_card, ddim=cfg.ddim, dlayers=cfg.dlayers,
             dheads=cfg.dheads, dhead_dim=cfg.dhead_dim, dhidden=cfg.dhidden,
             w_bf16=int(cfg.weight_dtype == "bf16"), kv_bf16=int(cfg.kv_dtype == "bf16"),
-            eps=cfg.eps, rope_theta=cfg.rope_theta, act_bf16=int(act_bf16))
+            eps=cfg.eps, rope_theta=cfg.rope_theta)
         self.w = OrcWeights(**{n: _ptr(weights[n]) for n in WEIGHT_FIELDS})
 
     def new_state(self) -> "OracleState":

@@ -28,11 +28,7 @@
  *     nearest even) when they are appended to the window, as the GPU cache stores
  *     them; the depformer's per-frame K/V stay f32;
  *   - forcing: `forced` = [text, audio0..7] conditions the depformer chain and is
- *     what the ring records, while the step still reports its own argmax tokens;
- *   - act_bf16 (off unless asked for): the vector each matrix product consumes (the
- *     normalised activations, the attention output, the SiLU-gated hidden vector,
- *     out_norm's output, the depformer's last residual) is rounded to bf16 first;
- *     residuals, K/V, logits and every sum stay f32.
+ *     what the ring records, while the step still reports its own argmax tokens.
  *
  * Parity pins (tests/test_oracle_pins.py): RMSNorm closed forms, RoPE hand vectors,
  * argmax tie/NaN cases, one-key attention, attention and GEMV against independent
@@ -66,8 +62,6 @@ typedef struct {
   int32_t kv_bf16; /* 1: temporal K/V rows are rounded to bf16 when appended */
   float eps;       /* RMSNorm epsilon (1e-8) */
   float rope_theta;/* 10000 */
-  int32_t act_bf16;/* 1: every matrix product takes its activation operand rounded to
-                      bf16 (the precision of a bf16 x bf16 tensor-core product) */
 } orc_cfg;
 
 typedef struct {
@@ -128,12 +122,6 @@ static float round_to_bf16(float f) {
   float r;
   memcpy(&r, &u, 4);
   return r;
-}
-
-/* act_bf16: round the operand of a matrix product to bf16 in place (into `dst`) */
-static float *operand(const orc_cfg *c, const float *x, int n, float *dst) {
-  for (int i = 0; i < n; i++) dst[i] = c->act_bf16 ? round_to_bf16(x[i]) : x[i];
-  return dst;
 }
 
 /* element i of a weight array stored as bf16 bits or f32 */
@@ -329,7 +317,6 @@ void orc_temporal_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
   float *gated = (float *)malloc(sizeof(float) * F);
   for (int l = 0; l < c->layers; l++) {
     orc_rms_norm(x, w->norm1 + (size_t)l * D, D, c->eps, h);
-    operand(c, h, D, h);
     orc_gemv(woff(w->in_proj, bf, (size_t)l * 3 * D * D), bf, 3 * D, D, h, qkv);
     float *q = qkv, *k = qkv + D, *v = qkv + 2 * D;
     orc_rope_row(q, D, pos, c->head_dim, c->rope_theta);
@@ -348,14 +335,11 @@ void orc_temporal_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
     }
     st->kv_len[l] = n + 1;
     orc_attend(q, K, V, n + 1, c->heads, c->head_dim, attn);
-    operand(c, attn, D, attn);
     orc_gemv(woff(w->out_proj, bf, (size_t)l * D * D), bf, D, D, attn, proj);
     for (int d = 0; d < D; d++) x[d] += proj[d];
     orc_rms_norm(x, w->norm2 + (size_t)l * D, D, c->eps, h);
-    operand(c, h, D, h);
     orc_gemv(woff(w->gate_in, bf, (size_t)l * 2 * F * D), bf, 2 * F, D, h, gate);
     for (int j = 0; j < F; j++) gated[j] = orc_silu(gate[j]) * gate[F + j];
-    operand(c, gated, F, gated);
     orc_gemv(woff(w->gate_out, bf, (size_t)l * D * F), bf, D, F, gated, proj);
     for (int d = 0; d < D; d++) x[d] += proj[d];
   }
@@ -384,10 +368,9 @@ void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *to
   float *proj = (float *)malloc(sizeof(float) * DD);
   float *gate = (float *)malloc(sizeof(float) * 2 * DF);
   float *gated = (float *)malloc(sizeof(float) * DF);
-  float *tin = operand(c, tout, D, (float *)malloc(sizeof(float) * D));
   int64_t prev = forced ? (int64_t)forced[0] : text_token;
   for (int cb = 0; cb < Q; cb++) {
-    orc_gemv(woff(w->dep_in, bf, (size_t)cb * DD * D), bf, DD, D, tin, x);
+    orc_gemv(woff(w->dep_in, bf, (size_t)cb * DD * D), bf, DD, D, tout, x);
     if (cb == 0)
       orc_embed(w->dep_text_emb, bf, DD, prev, x);
     else
@@ -395,30 +378,26 @@ void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *to
     for (int l = 0; l < DL; l++) {
       size_t ls = (size_t)l * Q + cb; /* [DL][8] weight set index */
       orc_rms_norm(x, w->dnorm1 + (size_t)l * DD, DD, c->eps, h);
-      operand(c, h, DD, h);
       orc_gemv(woff(w->d_in_proj, bf, ls * 3 * DD * DD), bf, 3 * DD, DD, h, qkv);
       float *K = kc + (size_t)l * Q * DD, *V = vc + (size_t)l * Q * DD;
       memcpy(K + (size_t)cb * DD, qkv + DD, sizeof(float) * DD);
       memcpy(V + (size_t)cb * DD, qkv + 2 * DD, sizeof(float) * DD);
       orc_attend(qkv, K, V, cb + 1, c->dheads, c->dhead_dim, attn);
-      operand(c, attn, DD, attn);
       orc_gemv(woff(w->d_out_proj, bf, ls * DD * DD), bf, DD, DD, attn, proj);
       for (int d = 0; d < DD; d++) x[d] += proj[d];
       orc_rms_norm(x, w->dnorm2 + (size_t)l * DD, DD, c->eps, h);
-      operand(c, h, DD, h);
       orc_gemv(woff(w->d_gate_in, bf, ls * 2 * DF * DD), bf, 2 * DF, DD, h, gate);
       for (int j = 0; j < DF; j++) gated[j] = orc_silu(gate[j]) * gate[DF + j];
-      operand(c, gated, DF, gated);
       orc_gemv(woff(w->d_gate_out, bf, ls * DD * DF), bf, DD, DF, gated, proj);
       for (int d = 0; d < DD; d++) x[d] += proj[d];
     }
     float *lg = logits + (size_t)cb * A;
-    orc_gemv(woff(w->linears, bf, (size_t)cb * A * DD), bf, A, DD, operand(c, x, DD, h), lg);
+    orc_gemv(woff(w->linears, bf, (size_t)cb * A * DD), bf, A, DD, x, lg);
     tokens[cb] = (int32_t)orc_argmax(lg, A);
     prev = forced ? (int64_t)forced[1 + cb] : (int64_t)tokens[cb];
   }
   free(kc); free(vc); free(x); free(h); free(qkv); free(attn); free(proj);
-  free(gate); free(gated); free(tin);
+  free(gate); free(gated);
 }
 
 /* moshi_lm.rs, `step_ext` (steps 1-8) for one session.
@@ -458,9 +437,7 @@ void orc_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
   float *tl = (float *)malloc(sizeof(float) * V);
   float *al = (float *)malloc(sizeof(float) * ORC_DEP_Q * A);
   orc_temporal_step(c, w, st, x, tout);
-  float *tin = operand(c, tout, D, (float *)malloc(sizeof(float) * D));
-  orc_gemv(w->text_linear, bf, V, D, tin, tl);
-  free(tin);
+  orc_gemv(w->text_linear, bf, V, D, tout, tl);
   int32_t text_token = (int32_t)orc_argmax(tl, V);
   /* 6. depformer cycle */
   int32_t audio[ORC_DEP_Q];

@@ -128,8 +128,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnParams p) {
     const float o = A / L;
     p.out[(size_t)b * p.D + (size_t)h * HD + tid] = o;
     if (p.out_bf16)
-      p.out_bf16[(size_t)b * p.D + (size_t)h * HD + tid] =
-          __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, (size_t)b * p.D + (size_t)h * HD + tid, o);
   }
   if (tid == 0) p.counters[b * p.H + h] = 0;
 }
@@ -224,12 +223,12 @@ namespace rqk {
 
 // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1, for every
 // session: one warp per (session, head), the head's dimensions spread over the lanes;
-// writes the bf16 operand of the next tensor-core GEMM.
+// writes the bf16x3 operand of the next tensor-core GEMM (parts nb rows apart).
 __global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long long dq_bs,
                                                            const float* dk, const float* dv,
                                                            long long dkv_bs, int n_keys,
                                                            int hd, int DD, uint16_t* out,
-                                                           long long out_bs) {
+                                                           long long out_bs, int nb) {
   const int b = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -253,13 +252,13 @@ __global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long
   for (int e = lane; e < hd; e += 32) {
     float o = 0.f;
     for (int j = 0; j < n_keys; ++j) o += sc[j] / den * Vv[(size_t)j * DD + e];
-    out[(size_t)b * out_bs + (size_t)h * hd + e] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    store_bf16x3(out, (size_t)nb * out_bs, (size_t)b * out_bs + (size_t)h * hd + e, o);
   }
 }
 
 cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
                                  const float* dv, long long dkv_bs, int n_keys, int B,
-                                 int heads, int hd, uint16_t* out, long long out_bs,
+                                 int heads, int hd, uint16_t* out, long long out_bs, int nb,
                                  cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B, (unsigned)heads, 1);
@@ -271,7 +270,7 @@ cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* 
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, dattn_batched_kernel, dq, dq_bs, dk, dv, dkv_bs, n_keys, hd,
-                            heads * hd, out, out_bs);
+                            heads * hd, out, out_bs, nb);
 }
 
 }  // namespace rqk

@@ -7,6 +7,7 @@
 // of spinning forever.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -140,6 +141,21 @@ __device__ __forceinline__ void bar_sync(int id, int n) {
 }
 
 // ---------------------------------------------------------------- numerics
+// Three-term bf16 expansion of an f32: hi = bf16(x), mid = bf16(x - hi), lo = x - hi - mid.
+// Both differences are exact (Sterbenz) and lo needs at most 8 significant bits, so
+// hi + mid + lo == x for every normal-range x: a bf16 x bf16 tensor-core product over the
+// three parts, accumulated in f32, sees the f32 operand itself.  Parts go to
+// base[idx], base[ps + idx], base[2 ps + idx].
+__device__ __forceinline__ void store_bf16x3(uint16_t* base, size_t ps, size_t idx, float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(m);
+  base[idx] = __bfloat16_as_ushort(h);
+  base[ps + idx] = __bfloat16_as_ushort(m);
+  base[2 * ps + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

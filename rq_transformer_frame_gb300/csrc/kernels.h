@@ -101,7 +101,8 @@ struct AttnParams {
   float* part;          // [B][H][nsplit][hd + 2]
   int* counters;        // [B][H], zero between uses
   float* out;           // [B][D]
-  uint16_t* out_bf16;   // nullable: the same output rounded to bf16, [B][D]
+  uint16_t* out_bf16;   // nullable: the same output as a bf16x3 operand [3][nb][D]
+  int nb;               // rows per bf16x3 part
   int D, H, hd, C, kps, nsplit;
   int batch;
   uint32_t* status;
@@ -109,7 +110,7 @@ struct AttnParams {
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
                                  const float* dv, long long dkv_bs, int n_keys, int B,
-                                 int heads, int hd, uint16_t* out, long long out_bs,
+                                 int heads, int hd, uint16_t* out, long long out_bs, int nb,
                                  cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- tensor-core GEMM
@@ -118,7 +119,7 @@ cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* 
 // fed by TMA, accumulator in tensor memory; optional split-K merged in split order.
 struct TcPlan {
   int n_out, K;       // output rows (paired: F), reduction length (multiple of 64)
-  int NB;             // padded batch: multiple of 16, <= 64
+  int NB;             // padded batch: multiple of 16, <= 64 (operand rows: 3 NB)
   int paired;         // SiLU-gated: tile rows 0-63 gate, 64-127 multiplier
   int tiles_m, splits, ksteps, ksteps_split;
   int n_stages, smem;
@@ -131,7 +132,7 @@ struct TcParams {
   int B;              // sessions (<= NB)
   float* out;         // f32 outputs [B][..] (stride out_bs)
   long long out_bs;
-  uint16_t* out_bf16; // EPI_SWIGLU: bf16 [NB][F] (stride outb_bs)
+  uint16_t* out_bf16; // EPI_SWIGLU: bf16x3 operand [3][NB][F] (row stride outb_bs)
   long long outb_bs;
   void* kcache;       // EPI_QKV
   void* vcache;
@@ -159,7 +160,7 @@ cudaError_t tc_configure();
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
                            int box_rows);
 
-// prep: X bf16 [NB][K] = cast(in) or RMSNorm(in, alpha) for sessions < B (rows >= B zero);
+// prep: X bf16x3 [3][NB][K] = in or RMSNorm(in, alpha) for sessions < B (rows >= B zero);
 // side (nullable) receives the f32 normalized rows
 cudaError_t launch_prep_bf16(const float* in, long long in_bs, const float* alpha, float eps,
                              int B, int NB, int K, uint16_t* xb, float* side, long long side_bs,
@@ -224,8 +225,8 @@ GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool eve
                          int grid);
 // ---------------------------------------------------------------- tensor-core frame
 // Everything a batched frame needs between frame_begin and frame_end: the per-op plans,
-// the bf16 operand buffers [NB][K] (rows >= B stay zero) and one TMA map per weight
-// matrix and per operand buffer.
+// the bf16x3 operand buffers [3][NB][K] (hi, mid, lo parts; rows >= B stay zero) and one
+// TMA map per weight matrix and per operand buffer.
 struct TcFrame {
   int B, NB, D, L, C, F, V, A, DD, DL, DF, H, hd, dH, dhd;
   float eps;

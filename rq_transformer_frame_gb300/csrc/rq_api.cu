@@ -638,13 +638,14 @@ rq_status setup_tensor(rq_handle* h) {
 #define TC_ALLOC(ptr, bytes) \
   if ((st = A_(reinterpret_cast<void**>(&(ptr)), (bytes), #ptr)) != RQ_OK) return st;
   TC_ALLOC(h->rope, (size_t)c.batch * (c.head_dim / 2) * sizeof(float2));
-  TC_ALLOC(h->xb, NB * c.dim * 2);
-  TC_ALLOC(h->attn_b, NB * c.dim * 2);
-  TC_ALLOC(h->u_b, NB * c.hidden * 2);
-  TC_ALLOC(h->tout_b, NB * c.dim * 2);
-  TC_ALLOC(h->dxb, NB * c.ddim * 2);
-  TC_ALLOC(h->do_b, NB * c.ddim * 2);
-  TC_ALLOC(h->du_b, NB * c.dhidden * 2);
+  const size_t R = 3 * NB;  // bf16x3 operands: [3][NB][K]
+  TC_ALLOC(h->xb, R * c.dim * 2);
+  TC_ALLOC(h->attn_b, R * c.dim * 2);
+  TC_ALLOC(h->u_b, R * c.hidden * 2);
+  TC_ALLOC(h->tout_b, R * c.dim * 2);
+  TC_ALLOC(h->dxb, R * c.ddim * 2);
+  TC_ALLOC(h->do_b, R * c.ddim * 2);
+  TC_ALLOC(h->du_b, R * c.dhidden * 2);
   TC_ALLOC(h->tc_part, part_floats * 4);
   TC_ALLOC(h->tc_tickets, (size_t)n_tickets * 4);
 #undef TC_ALLOC

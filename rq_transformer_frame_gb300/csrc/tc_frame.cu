@@ -84,13 +84,14 @@ cudaError_t tc_frame_maps(TcFrame& f) {
   cudaError_t e;
 #define MAP(slot, base, rows, cols, box) \
   if ((e = make_tmap_bf16(&(slot), (base), (rows), (cols), (box))) != cudaSuccess) return e;
-  MAP(f.xm_x, f.xb, f.NB, D, f.NB);
-  MAP(f.xm_attn, f.attn_b, f.NB, D, f.NB);
-  MAP(f.xm_u, f.u_b, f.NB, F, f.NB);
-  MAP(f.xm_tout, f.tout_b, f.NB, D, f.NB);
-  MAP(f.xm_dx, f.dxb, f.NB, DD, f.NB);
-  MAP(f.xm_do, f.do_b, f.NB, DD, f.NB);
-  MAP(f.xm_du, f.du_b, f.NB, DF, f.NB);
+  const int R = 3 * f.NB;  // bf16x3 operand rows: hi, mid, lo parts of each session
+  MAP(f.xm_x, f.xb, R, D, R);
+  MAP(f.xm_attn, f.attn_b, R, D, R);
+  MAP(f.xm_u, f.u_b, R, F, R);
+  MAP(f.xm_tout, f.tout_b, R, D, R);
+  MAP(f.xm_dx, f.dxb, R, DD, R);
+  MAP(f.xm_do, f.do_b, R, DD, R);
+  MAP(f.xm_du, f.du_b, R, DF, R);
   for (int l = 0; l < f.L; ++l) {
     MAP(f.wm[wi_layer(l, 0)], bf(f.in_proj, (size_t)l * 3 * D * D), 3 * D, D, 128);
     MAP(f.wm[wi_layer(l, 1)], bf(f.out_proj, (size_t)l * D * D), D, D, 128);
@@ -142,6 +143,7 @@ cudaError_t tc_attn(const TcFrame& f, int l, cudaStream_t s) {
   a.counters = f.attn_counters;
   a.out = f.attn;
   a.out_bf16 = f.attn_b;
+  a.nb = f.NB;
   a.D = f.D;
   a.H = f.H;
   a.hd = f.hd;
@@ -237,7 +239,7 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
       }
       CK(launch_dattn_batched(f.dq, (long long)DD, f.dkv + dkv_off(l, 0, 0),
                               f.dkv + dkv_off(l, 1, 0), dkv_bs, cb + 1, f.B, f.dH, f.dhd,
-                              f.do_b, (long long)DD, s, true));
+                              f.do_b, (long long)DD, f.NB, s, true));
       {
         TcParams p = base(f, f.p_dout, EPI_RESID);
         p.out = f.dx;

@@ -26,9 +26,6 @@ constexpr int kBM = 128;  // rows of W per tile
 constexpr int kBK = 64;   // K elements per stage (128 bytes of bf16)
 constexpr int kABytes = kBM * kBK * 2;
 
-__device__ __forceinline__ uint16_t f2bf(float f) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
 
 __device__ __forceinline__ void store_kv_tc(void* base, size_t i, float v, int bf16) {
   if (bf16)
@@ -64,7 +61,8 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float g = d[i], mu = ex[m][i];
-        p.out_bf16[(size_t)(c0 + i) * p.outb_bs + j] = f2bf(g / (1.0f + expf(-g)) * mu);
+        store_bf16x3(p.out_bf16, (size_t)pl.NB * p.outb_bs, (size_t)(c0 + i) * p.outb_bs + j,
+                     g / (1.0f + expf(-g)) * mu);
       }
     }
     return;
@@ -150,6 +148,17 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
   }
 }
 
+// columns c0..c0+15 of this lane's accumulator row: (lo + mid) + hi of each session
+template <int NB>
+__device__ __forceinline__ void load_sum3(uint32_t taddr, int c0, float (&v)[16]) {
+  float h[16], m[16];
+  tc::tmem_ld16(taddr + (uint32_t)c0, h);
+  tc::tmem_ld16(taddr + (uint32_t)(NB + c0), m);
+  tc::tmem_ld16(taddr + (uint32_t)(2 * NB + c0), v);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = (v[i] + m[i]) + h[i];
+}
+
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 2)
     tc_gemm_kernel(const TcParams p, const __grid_constant__ CUtensorMap wmap,
@@ -161,11 +170,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ volatile int s_abort;
   __shared__ int s_issued, s_consumed;
   __shared__ EpiShared s_epi;
-  constexpr uint32_t kCols = NB <= 32 ? 32u : 64u;  // power of two >= 32
+  constexpr int kN = 3 * NB;  // MMA columns: the hi, mid and lo parts of each session
+  constexpr uint32_t kCols = kN <= 64 ? 64u : (kN <= 128 ? 128u : 256u);  // power of two
   const TcPlan& pl = p.pl;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NS = pl.n_stages;
-  constexpr int kBBytes = NB * kBK * 2;
+  constexpr int kBBytes = kN * kBK * 2;
   constexpr int kStage = kABytes + kBBytes;  // both multiples of 1024
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(kBM, NB);
+      const uint32_t idesc = tc::idesc_bf16_f32(kBM, kN);
       for (int i = 0; i < nk; ++i) {
         const int s = i % NS;
         if (s_abort || !mbar_wait(&s_full[s], (uint32_t)(i / NS) & 1u)) {
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c0 = 0; c0 < NB; c0 += 16) {
         float v[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        load_sum3<NB>(tmem + ((uint32_t)(q * 32) << 16), c0, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) mine[(size_t)(c0 + i) * kBM + m] = v[i];
       }
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i < 16; ++i) v[i] += __ldcg(src + (size_t)i * kBM);
           }
         } else {
-          tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+          load_sum3<NB>(tmem + ((uint32_t)(q * 32) << 16), c0, v);
         }
         epilogue_chunk(p, v, c0, tile, m, lane, q, s_epi);
       }
@@ -340,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 namespace rqk {
 namespace tcg {
 
-// one CTA per padded session row: xb[b] = bf16(in[b] (* alpha * 1/sqrt(eps + mean(in^2))))
-// ("moshi_lm.rs", `rms_norm`), zero rows for b >= B; side[b] = the f32 result
+// one CTA per padded session row: xb[.][b] = bf16x3(in[b] (* alpha * 1/sqrt(eps +
+// mean(in^2)))) ("moshi_lm.rs", `rms_norm`), zero rows for b >= B; side[b] = the f32 result
 __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long long in_bs,
                                                         const float* alpha, float eps, int B,
                                                         int K, uint16_t* xb, float* side,
@@ -350,9 +360,9 @@ __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long lo
   const int b = blockIdx.x, tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  uint16_t* dst = xb + (size_t)b * K;
+  const size_t ps = (size_t)gridDim.x * K;  // bf16x3 part stride
   if (b >= B) {
-    for (int k = tid; k < K; k += 256) dst[k] = 0;
+    for (int k = tid; k < K; k += 256) store_bf16x3(xb, ps, (size_t)b * K + k, 0.f);
     return;
   }
   const float* x = in + (size_t)b * in_bs;
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long lo
   }
   for (int k = tid; k < K; k += 256) {
     const float v = alpha ? x[k] * alpha[k] * inv : x[k];
-    dst[k] = f2bf(v);
+    store_bf16x3(xb, ps, (size_t)b * K + k, v);
     if (side) side[(size_t)b * side_bs + k] = v;
   }
 }
@@ -409,8 +419,9 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   if (splits < 1) splits = 1;
   pl.ksteps_split = (pl.ksteps + splits - 1) / splits;
   pl.splits = (pl.ksteps + pl.ksteps_split - 1) / pl.ksteps_split;
-  const int stage = tcg::kABytes + NB * tcg::kBK * 2;
-  int ns = (96 * 1024) / stage;
+  // two CTAs per SM: ~104 KB of dynamic shared memory each
+  const int stage = tcg::kABytes + 3 * NB * tcg::kBK * 2;
+  int ns = (104 * 1024) / stage;
   ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
   pl.n_stages = ns;
   pl.smem = ns * stage + 1024;

@@ -25,14 +25,9 @@ def bf16_round(a: np.ndarray) -> np.ndarray:
 
 
 class Ref64:
-    def __init__(self, cfg, weights: dict, act_bf16: bool = False):
+    def __init__(self, cfg, weights: dict):
         self.c = cfg
         self.W = {k: v.float().numpy().astype(np.float64) for k, v in weights.items()}
-        self.act_bf16 = act_bf16
-
-    def op(self, v):
-        """The vector a matrix product consumes: bf16-rounded when act_bf16."""
-        return bf16_round(v) if self.act_bf16 else v
 
     # -- building blocks ---------------------------------------------------
     def rms(self, x, alpha):
@@ -67,9 +62,9 @@ class Ref64:
         return int(np.argmax(v))  # numpy returns the first maximal index
 
     def ffn(self, x, alpha, w_in, w_out, hidden):
-        g = w_in @ self.op(self.rms(x, alpha))
+        g = w_in @ self.rms(x, alpha)
         a, b = g[:hidden], g[hidden:]
-        return w_out @ self.op(a / (1.0 + np.exp(-a)) * b)
+        return w_out @ (a / (1.0 + np.exp(-a)) * b)
 
     # -- session -------------------------------------------------------------
     def new_state(self):
@@ -86,7 +81,7 @@ class Ref64:
         c, W = self.c, self.W
         pos = st["off"]
         for l in range(c.layers):
-            qkv = W["in_proj"][l] @ self.op(self.rms(x, W["norm1"][l]))
+            qkv = W["in_proj"][l] @ self.rms(x, W["norm1"][l])
             q, k, v = np.split(qkv, 3)
             q = self.rope(q, pos, c.head_dim)
             k = self.rope(k, pos, c.head_dim)
@@ -98,14 +93,14 @@ class Ref64:
             st["V"][l] = st["V"][l][-c.context:]
             o = self.attention(q, np.array(st["K"][l]), np.array(st["V"][l]),
                                c.heads, c.head_dim)
-            x = x + W["out_proj"][l] @ self.op(o)
+            x = x + W["out_proj"][l] @ o
             x = x + self.ffn(x, W["norm2"][l], W["gate_in"][l], W["gate_out"][l], c.hidden)
         return self.rms(x, W["out_norm"])
 
     def dep_input(self, tout, cb, prev):
         W = self.W
         table = W["dep_text_emb"] if cb == 0 else W["dep_emb"][cb - 1]
-        return W["dep_in"][cb] @ self.op(tout) + self.embed_row(table, prev)
+        return W["dep_in"][cb] @ tout + self.embed_row(table, prev)
 
     def depformer(self, tout, text, forced=None):
         """Incremental cycle (per-step K/V appended), own argmaxes; forced = [9]."""
@@ -117,15 +112,15 @@ class Ref64:
         for cb in range(8):
             x = self.dep_input(tout, cb, prev)
             for l in range(c.dlayers):
-                qkv = W["d_in_proj"][l, cb] @ self.op(self.rms(x, W["dnorm1"][l]))
+                qkv = W["d_in_proj"][l, cb] @ self.rms(x, W["dnorm1"][l])
                 q, k, v = np.split(qkv, 3)
                 Ks[l].append(k)
                 Vs[l].append(v)
                 o = self.attention(q, np.array(Ks[l]), np.array(Vs[l]), c.dheads, c.dhead_dim)
-                x = x + W["d_out_proj"][l, cb] @ self.op(o)
+                x = x + W["d_out_proj"][l, cb] @ o
                 x = x + self.ffn(x, W["dnorm2"][l], W["d_gate_in"][l, cb],
                                  W["d_gate_out"][l, cb], c.dhidden)
-            lg = W["linears"][cb] @ self.op(x)
+            lg = W["linears"][cb] @ x
             logits.append(lg)
             toks.append(self.first_argmax(lg))
             prev = toks[-1] if forced is None else forced[1 + cb]
@@ -162,7 +157,7 @@ class Ref64:
         x = x + self.embed_row(W["text_emb"], inp[0])
         emb_sum = x.copy()
         tout = self.temporal(st, x)
-        text_logits = W["text_linear"] @ self.op(tout)
+        text_logits = W["text_linear"] @ tout
         text = self.first_argmax(text_logits)
         audio_logits, audio = self.depformer(tout, text, forced)
         st["off"] = off = off + 1
