@@ -63,6 +63,8 @@ def peaks():
 KERNEL_SOURCES = {
     "gemv": ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "common.cuh", "kernels.h"),
     "frame": ("frame_persistent.cu", "gemv_kernel.cuh", "common.cuh", "kernels.h"),
+    "tc": ("tc_gemm.cu", "tc_common.cuh", "common.cuh", "kernels.h"),
+    "attn": ("attn.cu", "common.cuh", "kernels.h"),
 }
 
 
@@ -239,7 +241,10 @@ def run_native(args, cfg):
     w_dev = binding.upload_weights(w_host, dev)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        dec = binding.Decoder(cfg, w_dev, stream=stream)
+        sched = {"auto": binding.RQ_SCHEDULE_AUTO, "graph": binding.RQ_SCHEDULE_GRAPH,
+                 "persistent": binding.RQ_SCHEDULE_PERSISTENT,
+                 "tensor": binding.RQ_SCHEDULE_TENSOR}[args.schedule]
+        dec = binding.Decoder(cfg, w_dev, stream=stream, schedule=sched)
         if cfg.prefill:
             for b in range(B):
                 k, v = synth.kv_prefill(cfg, b, device=dev)
@@ -288,9 +293,9 @@ def run_native(args, cfg):
     # ---- per-kernel timing of the GEMVs (distinct layers, so nothing is L2-resident)
     hbm_peak, peak_kind = peaks()
     kernels = {}
-    names = {binding.RQ_OP_QKV: "qkv", binding.RQ_OP_OUT: "out_proj",
-             binding.RQ_OP_GATE_IN: "gate_in", binding.RQ_OP_GATE_OUT: "gate_out",
-             binding.RQ_OP_HEAD: "text_head"}
+    names = {binding.RQ_OP_QKV: "qkv", binding.RQ_OP_ATTN: "attention",
+             binding.RQ_OP_OUT: "out_proj", binding.RQ_OP_GATE_IN: "gate_in",
+             binding.RQ_OP_GATE_OUT: "gate_out", binding.RQ_OP_HEAD: "text_head"}
     reps = 3
     for op, name in names.items():
         layers = range(cfg.layers) if op != binding.RQ_OP_HEAD else range(1)
@@ -309,7 +314,9 @@ def run_native(args, cfg):
         us = e0.elapsed_time(e1) * 1e3 / n
         kernels[name] = {"us_per_launch": round(us, 2), "bytes_per_launch": nb,
                          "GB/s": round(nb / us / 1e3, 1),
-                         "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4)}
+                         "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4),
+                         "launches_per_frame": len(layers),
+                         "ms_per_frame": round(us * len(layers) / 1e3, 3)}
     dec.reset(-1)
     stages = None
     if dec.schedule == binding.RQ_SCHEDULE_PERSISTENT:
@@ -342,11 +349,25 @@ def run_native(args, cfg):
                       "ops": int(len(us_ops))}
         dec.reset(-1)
     else:
-        dom = kernels["gate_in"]
-        roof = {"kernel": "gemv_kernel<bf16, RMS, SWIGLU> (gate_in + SiLU gate, one layer)",
-                "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak, "unit": "GB/s",
-                "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
-                "traffic": profiled_traffic("gemv_moshi7b_b1.md", "gemv")}
+        # the kernel with the largest share of the frame (time per launch x launches)
+        name = max(kernels, key=lambda k: kernels[k]["ms_per_frame"])
+        dom = kernels[name]
+        tensor = dec.schedule == binding.RQ_SCHEDULE_TENSOR
+        if name == "attention":
+            label = "attn_decode_kernel (split-K decode attention over the K/V window, one layer)"
+            traffic = profiled_traffic("attn_%s.md" % cfg.name, "attn", dom["bytes_per_launch"])
+        elif tensor:
+            label = "tc_gemm_kernel<%d> (%s on the tcgen05 tensor cores, one layer)" % (
+                (B + 15) // 16 * 16, name)
+            traffic = profiled_traffic("tc_gemm_%s.md" % cfg.name, "tc", dom["bytes_per_launch"])
+        else:
+            label = "gemv_kernel<bf16> (%s, one layer)" % name
+            traffic = profiled_traffic("gemv_moshi7b_b1.md", "gemv")
+        roof = {"kernel": label, "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak,
+                "unit": "GB/s", "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
+                "us_per_launch": dom["us_per_launch"], "bytes_per_launch": dom["bytes_per_launch"],
+                "share_of_frame": round(dom["ms_per_frame"] / (1e3 * sec_max / K), 3),
+                "traffic": traffic}
 
     # ---- the oracle on this machine's host cores, on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -367,13 +388,15 @@ def run_native(args, cfg):
                    "parallelism": "replicas" if ws > 1 else "single-gpu",
                    "l2": "not flushed: %.1f GB of weights streamed per frame >> 126 MB L2"
                          % (fb[0]["weights"] / 1e9),
-                   "arith": "bf16 weights and K/V, f32 activations and accumulation"},
+                   "arith": ("bf16 weights and K/V, f32 activations and accumulation" +
+                             ("; tensor-core GEMMs on exact bf16x3 activation operands"
+                              if dec.schedule == binding.RQ_SCHEDULE_TENSOR else ""))},
         "tokens_per_s": 9 * value,
         "hbm": {"bytes_per_frame": bytes_frame, "GB/s": round(bytes_frame / (sec_max / K) / 1e9, 1),
                 "frac_of_measured": round(bytes_frame / (sec_max / K) / 1e9 / hbm_peak, 4),
                 "frac_of_8TBs": round(bytes_frame / (sec_max / K) / 8e12, 4)},
         "roofline": roof, "kernels": kernels, "stages": stages,
-        "schedule": {1: "graph", 2: "persistent"}.get(dec.schedule, "?"),
+        "schedule": {1: "graph", 2: "persistent", 3: "tensor"}.get(dec.schedule, "?"),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "session-frames/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -399,6 +422,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None, help="override: a name from configs.CONFIGS")
+    ap.add_argument("--schedule", default="auto",
+                    choices=["auto", "graph", "persistent", "tensor"])
     args = ap.parse_args(argv)
     from rq_transformer_frame_gb300 import configs
     cfg = configs.CONFIGS[WORKLOADS[args.batch]]
