@@ -238,7 +238,8 @@ rq_status rq_launch_op(rq_handle *h, int32_t op, int32_t layer, int32_t count,
  * softmax((q . k_j) / sqrt(head_dim)) weighted sum of v_j over the window of the
  * last min(pos + 1, context) positions, position j stored in cache slot j % context.
  *   q          device [batch][heads*head_dim] f32
- *   k, v       device [batch][context][heads*head_dim] in kv_dtype (RQ_F32 / RQ_BF16)
+ *   k, v       device [batch][context][heads*head_dim] in kv_dtype (RQ_F32 / RQ_BF16),
+ *              16-byte aligned (RQ_ERR_ARG otherwise)
  *   positions  device [batch] int32, the query's own position (>= 0)
  *   out        device [batch][heads*head_dim] f32
  *   workspace  device scratch of at least rq_attention_workspace_size(...) bytes,

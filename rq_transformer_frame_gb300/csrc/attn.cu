@@ -5,17 +5,17 @@
 // p = softmax(s) with the maximum subtracted, o = sum_j p_j v_j.
 //
 // The window of session b holds positions [pos - len + 1, pos] with
-// len = min(pos + 1, C); position j lives in cache slot j % C.  Grid (split, head,
-// session): each CTA covers `kps` consecutive positions with 4 warps (one key per
-// warp per step, the head's dimensions spread over the lanes), keeps an online
-// softmax (running max m, sum l, weighted values) in registers, merges its warps in a
-// fixed order and writes a partial (m, l, acc).  The last CTA of a (session, head)
-// to finish -- found with an atomic ticket -- merges the partials in split order, so
-// the result does not depend on which CTA finished last.
+// len = min(pos + 1, C); position j lives in cache slot j % C.  A work item is `kps`
+// consecutive positions of one (session, head); a CTA keeps an online softmax
+// (running max m, sum l, weighted values) per warp in registers, merges its warps in a
+// fixed order and writes the item's partial (m, l, acc).  The last CTA of a (session,
+// head) to finish -- found with an atomic ticket -- merges the partials in split order,
+// so the result does not depend on which CTA finished last.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace rqk {
 
@@ -28,124 +28,353 @@ __device__ __forceinline__ float kv_load<uint16_t>(const uint16_t* p) {
   return __uint_as_float(((uint32_t)*p) << 16);
 }
 
+// This lane's EPL consecutive elements of a K or V row in shared memory, widened to f32.
 template <typename KT, int EPL>
-__global__ void __launch_bounds__(128) attn_decode_kernel(const AttnParams p) {
+__device__ __forceinline__ void load_row(const KT* r, float (&v)[EPL]) {
+  if constexpr (sizeof(KT) == 2 && EPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(r);
+    v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  } else if constexpr (sizeof(KT) == 2 && EPL == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(r);
+    v[0] = bf16lo(u); v[1] = bf16hi(u);
+  } else if constexpr (sizeof(KT) == 4 && EPL == 4) {
+    const float4 f = *reinterpret_cast<const float4*>(r);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else if constexpr (sizeof(KT) == 4 && EPL == 2) {
+    const float2 f = *reinterpret_cast<const float2*>(r);
+    v[0] = f.x; v[1] = f.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] = kv_load<KT>(r + e);
+  }
+}
+
+// The 16 elements of a K or V row in shared memory that lane gl of a G-lane group owns,
+// widened to f32: 16-byte chunks c = 0.. at element c * G * EPC + gl * EPC (EPC elements
+// per chunk), so the G lanes of a group read each chunk row contiguously (no bank
+// conflicts).  Element e of the result is dimension dim16<KT>(e, gl, G).
+template <typename KT>
+__device__ __forceinline__ int dim16(int e, int gl, int G) {
+  constexpr int EPC = 16 / sizeof(KT);
+  return (e / EPC) * G * EPC + gl * EPC + (e % EPC);
+}
+
+template <typename KT>
+__device__ __forceinline__ void load16(const KT* row, int gl, int G, float (&v)[16]) {
+  constexpr int EPC = 16 / sizeof(KT);
+#pragma unroll
+  for (int c = 0; c < 16 / EPC; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + c * G * EPC + gl * EPC);
+    if constexpr (sizeof(KT) == 2) {
+      v[8 * c + 0] = bf16lo(u.x); v[8 * c + 1] = bf16hi(u.x);
+      v[8 * c + 2] = bf16lo(u.y); v[8 * c + 3] = bf16hi(u.y);
+      v[8 * c + 4] = bf16lo(u.z); v[8 * c + 5] = bf16hi(u.z);
+      v[8 * c + 6] = bf16lo(u.w); v[8 * c + 7] = bf16hi(u.w);
+    } else {
+      v[4 * c + 0] = __uint_as_float(u.x); v[4 * c + 1] = __uint_as_float(u.y);
+      v[4 * c + 2] = __uint_as_float(u.z); v[4 * c + 3] = __uint_as_float(u.w);
+    }
+  }
+}
+
+// One work item = (session, split, head).  Splits are cut in cache-slot
+// space: the window of session b is every slot when pos >= C, else slots 0..pos, so
+// split s covers slots [s kps, min((s + 1) kps, min(pos + 1, C))) and never wraps.
+// Softmax is order-free, so visiting the window in slot order rather than position
+// order changes only the rounding.
+struct AttnItem {
+  int b, h, split, ns, j0, j1;
+};
+
+__device__ __forceinline__ bool attn_decode_item(const AttnParams& p, int it, AttnItem& x) {
+  // head fastest: the items in flight at once read every head's slice of the same K/V
+  // rows, so each row is fetched from DRAM as a whole
+  x.h = it % p.H;
+  const int bs = it / p.H;
+  x.split = bs % p.nsplit;
+  x.b = bs / p.nsplit;
+  const int lim = min(p.offsets[x.b] + 1, p.C);
+  x.ns = (lim + p.kps - 1) / p.kps;
+  if (x.split >= x.ns) return false;
+  x.j0 = x.split * p.kps;
+  x.j1 = min(x.j0 + p.kps, lim);
+  return true;
+}
+
+#ifndef RQ_ATTN_STAGES
+#define RQ_ATTN_STAGES 2
+#endif
+#ifndef RQ_ATTN_WARPS
+#define RQ_ATTN_WARPS 4
+#endif
+constexpr int kAttnStages = RQ_ATTN_STAGES;  // K/V chunks per CTA (ring depth)
+constexpr int kAttnWarps = RQ_ATTN_WARPS;
+
+// Persistent grid over the work items: each CTA takes items blockIdx.x, + gridDim.x, ...
+// skipping splits beyond a session's window.  Thread 0 loads an item's K and V rows with
+// one 2-D TMA box each ({head_dim, kps} out of the cache viewed as rows of D) into a
+// kAttnStages-deep shared-memory ring, so the next items' chunks stream while this one
+// is computed.  Within a warp, groups of head_dim / 16 lanes each take one key (16
+// dimensions per lane), so a warp steps through 32 / (head_dim / 16) keys at once with
+// log2(head_dim / 16) shuffles; each group keeps an online softmax in registers, the
+// groups merge by a fixed butterfly, the warps in a fixed order into the item's partial
+// (m, l, acc), combined per (session, head) by attn_merge_kernel.
+template <typename KT, int EPL>
+__global__ void __launch_bounds__(kAttnWarps * 32)
+    attn_decode_kernel(const AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
   constexpr int HD = EPL * 32;
-  __shared__ float s_m[4], s_l[4];
-  __shared__ float s_acc[4][HD];
-  __shared__ int s_last;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  constexpr int NS = kAttnStages, NW = kAttnWarps;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t s_full[NS];
+  __shared__ int s_item[NS];
+  __shared__ float s_m[NW], s_l[NW];
+  __shared__ float s_acc[NW][HD];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kps = p.kps;
+  KT* const stage0 = reinterpret_cast<KT*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const size_t stage_elems = (size_t)2 * kps * HD;  // K rows then V rows
+  const uint32_t stage_bytes = (uint32_t)(stage_elems * sizeof(KT));
+  const int total = p.batch * p.H * p.nsplit;
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&s_full[i], 1);
+    fence_barrier_init();
+    tc::prefetch_tmap(&kmap);
+    tc::prefetch_tmap(&vmap);
+  }
+  __syncthreads();
   pdl_trigger();
   pdl_wait();
-  const int pos = p.offsets[b];
-  const int len = min(pos + 1, p.C);
-  const int first = pos + 1 - len;
-  const int nsplit = (len + p.kps - 1) / p.kps;
-  if (split >= nsplit) return;
-  const int j0 = first + split * p.kps;
-  const int j1 = min(j0 + p.kps, pos + 1);
-
-  float q[EPL];
-  const float* qp = p.q + (size_t)b * p.D + (size_t)h * HD + lane * EPL;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) q[e] = qp[e];
+  const uint64_t pol = l2_policy_evict_first();
+  // thread 0 only: the next valid item at or after `it` (stride gridDim.x), then its load
+  int last = blockIdx.x - (int)gridDim.x;  // last item index issued by this CTA
+  auto issue_next = [&](int s) {
+    AttnItem x;
+    int it = last + (int)gridDim.x;
+    while (it < total && !attn_decode_item(p, it, x)) it += gridDim.x;
+    s_item[s] = it;
+    if (it >= total) return;
+    last = it;
+    KT* const st = stage0 + (size_t)s * stage_elems;
+    const int row = (int)(p.row_bs * x.b + p.row0 + x.j0);
+    mbar_arrive_expect_tx(&s_full[s], stage_bytes);  // full boxes; tail rows unused
+    tc::tma_load_2d(st, &kmap, x.h * HD, row, &s_full[s], pol);
+    tc::tma_load_2d(st + (size_t)kps * HD, &vmap, x.h * HD, row, &s_full[s], pol);
+  };
+  if (tid == 0)
+    for (int s = 0; s < NS; ++s) issue_next(s);
+  __syncthreads();
   const float scale = 1.0f / sqrtf((float)HD);
   const float ninf = -__int_as_float(0x7f800000);
-  float m = ninf, l = 0.f, acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  const KT* kb = static_cast<const KT*>(p.kc) + (size_t)b * p.kv_bs + (size_t)h * HD + lane * EPL;
-  const KT* vb = static_cast<const KT*>(p.vc) + (size_t)b * p.kv_bs + (size_t)h * HD + lane * EPL;
-  for (int j = j0 + warp; j < j1; j += 4) {
-    const size_t off = (size_t)(j % p.C) * p.D;
-    float k[EPL], v[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      k[e] = kv_load<KT>(kb + off + e);
-      v[e] = kv_load<KT>(vb + off + e);
+  for (int k = 0;; ++k) {
+    const int s = k % NS;
+    const int item = s_item[s];
+    if (item >= total) break;
+    const bool ok = mbar_wait(&s_full[s], (uint32_t)(k / NS) & 1u);
+    if (__syncthreads_or(!ok)) {
+      // a copy never landed: record it, wait (bounded) for the other stages, stop
+      if (tid == 0) {
+        if (p.status) atomicOr(p.status, kDevTimeout);
+        for (int d = 1; d < NS; ++d)
+          if (s_item[(k + d) % NS] < total)
+            (void)mbar_wait(&s_full[(k + d) % NS], (uint32_t)((k + d) / NS) & 1u);
+      }
+      return;
     }
-    float s = 0.f;
+    AttnItem cur;
+    attn_decode_item(p, item, cur);
+    const int b = cur.b, h = cur.h, n = cur.j1 - cur.j0;
+    // G lanes share one key, 16 dimensions each; a warp covers KPI keys per step
+    constexpr int G = HD / 16, KPI = 32 / G;
+    const int grp = lane / G, gl = lane % G;
+    const KT* ks = stage0 + (size_t)s * stage_elems;
+    const KT* vs = ks + (size_t)kps * HD;
+    float q[16];
+    const float* qp = p.q + (size_t)b * p.D + (size_t)h * HD;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) s = fmaf(q[e], k[e], s);
-    s = warp_sum(s) * scale;
-    const float mn = fmaxf(m, s);
-    const float corr = expf(m - mn);
-    const float pe = expf(s - mn);
-    l = l * corr + pe;
+    for (int e = 0; e < 16; ++e) q[e] = qp[dim16<KT>(e, gl, G)] * scale;
+    float m = ninf, l = 0.f, acc[16];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * corr + pe * v[e];
-    m = mn;
-  }
-  if (lane == 0) {
-    s_m[warp] = m;
-    s_l[warp] = l;
-  }
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int r0 = warp * KPI; r0 < n; r0 += NW * KPI) {
+      const int r = r0 + grp;  // this group's key (uniform within the group)
+      float kv[16];
+      float d = 0.f;
+      if (r < n) {
+        load16<KT>(ks + (size_t)r * HD, gl, G, kv);
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = acc[e];
-  __syncthreads();
-
-  const size_t pstride = (size_t)HD + 2;
-  float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + split) * pstride;
-  if (tid < HD) {
-    float M = ninf;
+        for (int e = 0; e < 16; ++e) d = fmaf(q[e], kv[e], d);
+      }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w]);
-    float L = 0.f, A = 0.f;
+      for (int o = G / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (r < n) {
+        load16<KT>(vs + (size_t)r * HD, gl, G, kv);
+        const float mn = fmaxf(m, d);
+        const float corr = expf(m - mn);  // m = -inf: 0
+        const float pe = expf(d - mn);
+        l = l * corr + pe;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      if (s_l[w] > 0.f) {
-        const float c = expf(s_m[w] - M);
-        L += s_l[w] * c;
-        A += s_acc[w][tid] * c;
+        for (int e = 0; e < 16; ++e) acc[e] = fmaf(pe, kv[e], acc[e] * corr);
+        m = mn;
       }
     }
-    part[2 + tid] = A;
-    if (tid == 0) {
-      part[0] = M;
-      part[1] = L;
+    // merge the KPI key groups of the warp (lanes gl, gl + G, ...): fixed butterfly order
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) {
+      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+      const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+      const float M = fmaxf(m, mo);
+      const float c1 = (l > 0.f) ? expf(m - M) : 0.f;
+      const float c2 = (lo > 0.f) ? expf(mo - M) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float ao = __shfl_xor_sync(0xffffffffu, acc[e], o);
+        acc[e] = acc[e] * c1 + ao * c2;
+      }
+      l = l * c1 + lo * c2;
+      m = M;
     }
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_l[warp] = l;
+    }
+    if (lane < G) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s_acc[warp][dim16<KT>(e, gl, G)] = acc[e];
+    }
+    __syncthreads();  // every warp is done with this stage and has published its state
+    if (tid == 0) issue_next(s);  // refill the stage just consumed
+    // merge the warps in a fixed order into this split's partial (m, l, acc)
+    if (tid < HD) {
+      const size_t pstride = (size_t)HD + 2;
+      float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + cur.split) * pstride;
+      float M = ninf;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
+      float L = 0.f, A = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        if (s_l[w] > 0.f) {
+          const float c = expf(s_m[w] - M);
+          L += s_l[w] * c;
+          A += s_acc[w][tid] * c;
+        }
+      }
+      part[2 + tid] = A;
+      if (tid == 0) {
+        part[0] = M;
+        part[1] = L;
+      }
+    }
+    __syncthreads();  // s_m / s_acc / s_item are reused by the next item
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(&p.counters[b * p.H + h], 1);
-    s_last = (t == nsplit - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+}
+
+// Grid (head, session), head_dim threads: combine the partials of every split of the
+// window in split order (deterministic) into o = sum_s A_s e^(M_s - M) / sum_s L_s e^(M_s - M).
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (tid >= p.hd) return;
+  const int ns = (min(p.offsets[b] + 1, p.C) + p.kps - 1) / p.kps;
+  const size_t pstride = (size_t)p.hd + 2;
   const float* pb = p.part + ((size_t)b * p.H + h) * p.nsplit * pstride;
-  if (tid < HD) {
-    float M = ninf;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(pb + s * pstride));
-    float L = 0.f, A = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float c = expf(__ldcg(pb + s * pstride) - M);
-      L += __ldcg(pb + s * pstride + 1) * c;
-      A += __ldcg(pb + s * pstride + 2 + tid) * c;
-    }
-    const float o = A / L;
-    p.out[(size_t)b * p.D + (size_t)h * HD + tid] = o;
-    if (p.out_bf16)
-      store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, (size_t)b * p.D + (size_t)h * HD + tid, o);
+  float M = -__int_as_float(0x7f800000);
+  for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, pb[sp * pstride]);
+  float L = 0.f, A = 0.f;
+  for (int sp = 0; sp < ns; ++sp) {
+    const float c = expf(pb[sp * pstride] - M);
+    L += pb[sp * pstride + 1] * c;
+    A += pb[sp * pstride + 2 + tid] * c;
   }
-  if (tid == 0) p.counters[b * p.H + h] = 0;
+  const float o = A / L;
+  const size_t i = (size_t)b * p.D + (size_t)h * p.hd + tid;
+  p.out[i] = o;
+  if (p.out_bf16) store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, i, o);
+}
+
+// Resident CTAs per SM of one instantiation at `smem` bytes (sets the shared-memory
+// attribute first).  Called outside stream capture by attn_configure, and lazily by the
+// standalone entry points.
+template <typename KT, int EPL>
+static cudaError_t attn_occupancy(size_t smem, int* per_sm) {
+  static int cached = 0;
+  static size_t cached_smem = 0;
+  if (cached == 0 || cached_smem != smem) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<KT, EPL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<KT, EPL>,
+                                                      kAttnWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    cached = n > 0 ? n : 1;
+    cached_smem = smem;
+  }
+  *per_sm = cached;
+  return cudaSuccess;
+}
+
+template <typename KT, int EPL>
+static size_t attn_smem(int kps) {
+  return (size_t)kAttnStages * 2 * kps * EPL * 32 * sizeof(KT) + 1024;  // K, V stages + align
 }
 
 template <typename KT, int EPL>
 static cudaError_t launch_attn_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+  constexpr int HD = EPL * 32;
+  const size_t smem = attn_smem<KT, EPL>(p.kps);
+  int per_sm = 0, dev = 0, sms = 0;
+  cudaError_t e = attn_occupancy<KT, EPL>(smem, &per_sm);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  CUtensorMap kmap, vmap;
+  const bool bf = sizeof(KT) == 2;
+  if ((e = encode_tmap_2d(&kmap, bf, p.kbase, p.rows, p.D, HD, p.kps, false)) != cudaSuccess)
+    return e;
+  if ((e = encode_tmap_2d(&vmap, bf, p.vbase, p.rows, p.D, HD, p.kps, false)) != cudaSuccess)
+    return e;
+  const long long total = (long long)p.batch * p.H * p.nsplit;
+  const long long grid = total < (long long)per_sm * sms ? total : (long long)per_sm * sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.nsplit, (unsigned)p.H, (unsigned)p.batch);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<KT, EPL>, p);
+  if ((e = cudaLaunchKernelEx(&cfg, attn_decode_kernel<KT, EPL>, p, kmap, vmap)) != cudaSuccess)
+    return e;
+  cudaLaunchConfig_t mc = {};
+  mc.gridDim = dim3((unsigned)p.H, (unsigned)p.batch, 1);
+  mc.blockDim = dim3(128, 1, 1);
+  mc.stream = s;
+  mc.attrs = attr;
+  mc.numAttrs = 1;  // the merge always follows the attention kernel on the stream
+  return cudaLaunchKernelEx(&mc, attn_merge_kernel, p);
+}
+
+cudaError_t attn_configure(int hd, bool kv_bf16, int kps) {
+  int n = 0;
+  switch (hd) {
+    case 32:
+      return kv_bf16 ? attn_occupancy<uint16_t, 1>(attn_smem<uint16_t, 1>(kps), &n)
+                     : attn_occupancy<float, 1>(attn_smem<float, 1>(kps), &n);
+    case 64:
+      return kv_bf16 ? attn_occupancy<uint16_t, 2>(attn_smem<uint16_t, 2>(kps), &n)
+                     : attn_occupancy<float, 2>(attn_smem<float, 2>(kps), &n);
+    case 128:
+      return kv_bf16 ? attn_occupancy<uint16_t, 4>(attn_smem<uint16_t, 4>(kps), &n)
+                     : attn_occupancy<float, 4>(attn_smem<float, 4>(kps), &n);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl) {
@@ -167,7 +396,10 @@ cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool 
 #include "../../include/rq.h"
 
 namespace {
-constexpr int kStandaloneKps = 64;  // positions per split, as in the frame
+#ifndef RQ_ATTN_KPS
+#define RQ_ATTN_KPS 64
+#endif
+constexpr int kStandaloneKps = RQ_ATTN_KPS;  // positions per split, as in the frame
 
 size_t partial_bytes(int B, int H, int hd, int C) {
   const size_t nsplit = (size_t)(C + kStandaloneKps - 1) / kStandaloneKps;
@@ -192,14 +424,18 @@ extern "C" rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return RQ_ERR_UNSUPPORTED;
   if (kv_dtype != RQ_F32 && kv_dtype != RQ_BF16) return RQ_ERR_ARG;
   if (!q || !k || !v || !positions || !out || !workspace) return RQ_ERR_ARG;
+  // the K/V rows are bulk-copied into shared memory: 16-byte aligned sources
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) return RQ_ERR_ARG;
   if (workspace_bytes < rq_attention_workspace_size(batch, heads, head_dim, context))
     return RQ_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   AttnParams a{};
   a.q = q;
-  a.kc = k;
-  a.vc = v;
-  a.kv_bs = (long long)context * heads * head_dim;
+  a.kbase = k;
+  a.vbase = v;
+  a.rows = (long long)batch * context;
+  a.row0 = 0;
+  a.row_bs = context;
   a.offsets = positions;
   a.part = static_cast<float*>(workspace);
   a.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) +

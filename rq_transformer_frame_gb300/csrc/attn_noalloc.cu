@@ -65,6 +65,8 @@ extern "C" rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t 
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return RQ_ERR_UNSUPPORTED;
   if (kv_dtype != RQ_F32 && kv_dtype != RQ_BF16) return RQ_ERR_ARG;
   if (!q || !k || !v || !positions || !out) return RQ_ERR_ARG;
+  // the K/V rows are bulk-copied into shared memory: 16-byte aligned sources
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) return RQ_ERR_ARG;
   const size_t part = partial_bytes(batch, heads, head_dim, context);
   const size_t need = part + (size_t)batch * heads * sizeof(int);
   if (need > kScratchBytes) return RQ_ERR_UNSUPPORTED;  // beyond the fixed scratch
@@ -73,9 +75,11 @@ extern "C" rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   AttnParams a{};
   a.q = q;
-  a.kc = k;
-  a.vc = v;
-  a.kv_bs = (long long)context * heads * head_dim;
+  a.kbase = k;
+  a.vbase = v;
+  a.rows = (long long)batch * context;
+  a.row0 = 0;
+  a.row_bs = context;
   a.offsets = positions;
   a.part = static_cast<float*>(scratch);
   a.counters = reinterpret_cast<int*>(static_cast<char*>(scratch) + part);

@@ -94,9 +94,10 @@ cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int ba
 // ---------------------------------------------------------------- decode attention
 struct AttnParams {
   const float* q;       // [B][D]
-  const void* kc;       // layer's K cache, [C][D] per session (stride kv_bs)
-  const void* vc;
-  long long kv_bs;
+  const void* kbase;    // K cache viewed as rows of D elements; session b, slot j of this
+  const void* vbase;    // layer is row  row_bs * b + row0 + j  (V alike)
+  long long rows;       // rows of that view (the tensor maps' extent)
+  long long row0, row_bs;
   const int* offsets;   // [B]
   float* part;          // [B][H][nsplit][hd + 2]
   int* counters;        // [B][H], zero between uses
@@ -108,6 +109,8 @@ struct AttnParams {
   uint32_t* status;
 };
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
+// shared-memory attribute and occupancy of the attention kernel (call outside capture)
+cudaError_t attn_configure(int hd, bool kv_bf16, int kps);
 cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
                                  const float* dv, long long dkv_bs, int n_keys, int B,
                                  int heads, int hd, uint16_t* out, long long out_bs, int nb,
@@ -156,6 +159,10 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms);
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                       cudaStream_t s, bool pdl);
 cudaError_t tc_configure();
+// encode a 2-D tensor map over a row-major rows x cols array (bf16 or f32), box
+// {box_cols, box_rows}, 128-byte swizzle or none
+cudaError_t encode_tmap_2d(CUtensorMap* map, bool bf16, const void* base, long long rows,
+                           long long cols, int box_cols, int box_rows, bool swizzle128);
 // encode a 2-D bf16 tensor map: rows x cols (row-major), box {64 cols, box_rows}
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
                            int box_rows);

@@ -171,9 +171,11 @@ cudaError_t op_attn(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const size_t D = c.dim, C = c.context, L = c.layers;
   AttnParams a{};
   a.q = h->q;
-  a.kc = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
-  a.vc = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
-  a.kv_bs = (long long)(L * C * D);
+  a.kbase = h->kcache;  // [B][L][C][D]: session b, layer l, slot j is row (b L + l) C + j
+  a.vbase = h->vcache;
+  a.rows = (long long)h->cfg.batch * L * C;
+  a.row0 = (long long)l * C;
+  a.row_bs = (long long)(L * C);
   a.offsets = h->offsets;
   a.part = h->part;
   a.counters = h->counters;
@@ -769,6 +771,7 @@ rq_status create_impl(rq_handle* h) {
   rq_status st = plan_all(h, &why);
   if (st != RQ_OK) return fail(h, st, why);
   RQ_CUDA(h, gemv_configure_all());
+  RQ_CUDA(h, attn_configure(c.head_dim, h->kvbf, h->kps));
   RQ_CUDA(h, cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
   auto A_ = [&](cudaError_t e, const char* what) -> rq_status {
     if (e == cudaSuccess) return RQ_OK;

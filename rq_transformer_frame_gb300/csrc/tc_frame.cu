@@ -135,9 +135,11 @@ cudaError_t tc_qkv(const TcFrame& f, int l, cudaStream_t s) {
 cudaError_t tc_attn(const TcFrame& f, int l, cudaStream_t s) {
   AttnParams a{};
   a.q = f.q;
-  a.kc = layer_cache(f, f.kcache, l);
-  a.vc = layer_cache(f, f.vcache, l);
-  a.kv_bs = (long long)f.L * f.C * f.D;
+  a.kbase = f.kcache;  // [B][L][C][D]: session b, layer l, slot j is row (b L + l) C + j
+  a.vbase = f.vcache;
+  a.rows = (long long)f.B * f.L * f.C;
+  a.row0 = (long long)l * f.C;
+  a.row_bs = (long long)f.L * f.C;
   a.offsets = f.offsets;
   a.part = f.attn_part;
   a.counters = f.attn_counters;

@@ -474,8 +474,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
-                           int box_rows) {
+cudaError_t encode_tmap_2d(CUtensorMap* map, bool bf16, const void* base, long long rows,
+                           long long cols, int box_cols, int box_rows, bool swizzle128) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* f = nullptr;
@@ -485,16 +485,27 @@ cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, l
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) return cudaErrorNotSupported;
     fn = reinterpret_cast<EncodeTiledFn>(f);
   }
-  if (cols % 64 || box_rows < 1 || box_rows > 256) return cudaErrorInvalidValue;
+  const int es = bf16 ? 2 : 4;
+  if (rows < 1 || cols < 1 || rows >= (1ll << 32) || cols >= (1ll << 32) ||
+      (cols * es) % 16 || box_cols < 1 || box_cols > 256 || (box_cols * es) % 16 ||
+      box_rows < 1 || box_rows > 256 || (reinterpret_cast<uintptr_t>(base) & 15u))
+    return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * es};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
+                           int box_rows) {
+  if (cols % 64) return cudaErrorInvalidValue;
+  return encode_tmap_2d(map, true, base, rows, cols, 64, box_rows, true);
 }
 
 }  // namespace rqk
