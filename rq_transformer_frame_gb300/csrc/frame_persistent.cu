@@ -396,6 +396,9 @@ __device__ __forceinline__ void load_row<uint16_t, 1>(const uint16_t* p, float (
 
 // "moshi_lm.rs", `attend` for one session: work item (head, split of kps positions)
 // per group of 4 warps; the last group to finish a head merges its splits in order.
+// The split length follows the window so that every group of the grid gets about one
+// item (16..64 positions, a multiple of 16): short windows give each warp few keys, so
+// the chain of dependent K/V loads per warp stays short.
 template <typename KT, int EPL>
 __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op, int tid,
                                            int warp, int lane, float (*s_am)[4],
@@ -406,19 +409,22 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
   const int pos = P.offsets[0];
   const int len = min(pos + 1, P.context);
   const int first = pos + 1 - len;
-  const int nsplit = (len + P.kps - 1) / P.kps;
+  const int groups = (int)gridDim.x * 2;
+  int kps = (len * P.H + groups - 1) / groups;
+  kps = min(64, max(16, (kps + 15) & ~15));
+  const int nsplit = (len + kps - 1) / kps;  // <= P.nsplit = ceil(C / 16)
   const int items = P.H * nsplit;
   const float scale = 1.0f / sqrtf((float)HD);
   const float ninf = -__int_as_float(0x7f800000);
   const size_t pstride = (size_t)HD + 2;
-  for (int it = blockIdx.x * 2 + group; it < items; it += gridDim.x * 2) {
+  for (int it = blockIdx.x * 2 + group; it < items; it += groups) {
     const int h = it % P.H, split = it / P.H;
-    const int j0 = first + split * P.kps;
-    const int j1 = min(j0 + P.kps, pos + 1);
+    const int j0 = first + split * kps;
+    const int j1 = min(j0 + kps, pos + 1);
     float q[EPL];
     const float* qp = P.attn_q + (size_t)h * HD + lane * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) q[e] = ldcg(qp + e);
+    for (int e = 0; e < EPL; ++e) q[e] = ldcg(qp + e) * scale;
     float m = ninf, l = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -429,13 +435,13 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
       float k[EPL], v[EPL];
       load_row<KT, EPL>(kb + off, k);
       load_row<KT, EPL>(vb + off, v);
-      float s = 0.f;
+      float sc = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s = fmaf(q[e], k[e], s);
-      s = warp_sum(s) * scale;
-      const float mn = fmaxf(m, s);
+      for (int e = 0; e < EPL; ++e) sc = fmaf(q[e], k[e], sc);
+      sc = warp_sum(sc);
+      const float mn = fmaxf(m, sc);
       const float corr = expf(m - mn);
-      const float pe = expf(s - mn);
+      const float pe = expf(sc - mn);
       l = l * corr + pe;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * corr + pe * v[e];

@@ -750,8 +750,8 @@ rq_status setup_schedule(rq_handle* h) {
   P.counters = h->counters;
   P.D = c.dim;
   P.H = c.heads;
-  P.kps = h->kps;
-  P.nsplit = h->nsplit;
+  P.kps = 16;  // shortest split; the kernel sizes splits from the window (16..64)
+  P.nsplit = (c.context + 15) / 16;
   P.grid_bar = h->grid_bar;
   P.status = h->d_status();
   P.trace = h->trace;
@@ -800,7 +800,11 @@ rq_status create_impl(rq_handle* h) {
   RQ_ALLOC(h->dq, B * DD * 4);
   RQ_ALLOC(h->dkv, B * DL * 2 * 8 * DD * 4);
   RQ_ALLOC(h->du, B * DF * 4);
-  RQ_ALLOC(h->part, B * (size_t)c.heads * h->nsplit * (c.head_dim + 2) * 4);
+  {  // attention partials: [B][H][nsplit] at 64 positions per split, or one session's
+     // [H][ceil(C / 16)] for the persistent schedule's shorter splits
+    const size_t n64 = B * (size_t)c.heads * h->nsplit, n16 = (size_t)c.heads * ((C + 15) / 16);
+    RQ_ALLOC(h->part, (n64 > n16 ? n64 : n16) * (c.head_dim + 2) * 4);
+  }
   RQ_ALLOC(h->counters, B * (size_t)c.heads * 4);
 #undef RQ_ALLOC
   if ((st = A_(cudaMallocHost(reinterpret_cast<void**>(&h->h_in), h->io.in_words() * 4), "h_in")) != RQ_OK)
