@@ -1,12 +1,14 @@
 """Time single operations of the decode step through the C ABI (rq_launch_op).
 
   python -m rq_transformer_frame_gb300.op_probe --workload moshi7b_2layer \
-      --ops gate_in,qkv --reps 3 [--frames 4]
+      --ops gate_in,qkv --reps 3 [--frames 4] [--batch 16] [--prefill 2900]
 
-Builds the decoder for the workload (seeded synthetic weights), runs `--frames`
-whole frames, then for each op launches it once per temporal layer `--reps` times,
-timed with CUDA events on the decoder's stream, and prints one JSON line per op.
-Used as the command under the profiler for the kernel summaries in profiles/.
+Builds the decoder for the workload (seeded synthetic weights; `--batch` overrides the
+session count, `--prefill n` fills every session's temporal K/V with the workload's
+synthetic positions 0..n-1), runs `--frames` whole frames, then for each op launches it
+once per temporal layer `--reps` times, timed with CUDA events on the decoder's stream,
+and prints one JSON line per op.  Used as the command under the profiler for the kernel
+summaries in profiles/.
 """
 import argparse
 import json
@@ -26,13 +28,23 @@ def main(argv=None):
     ap.add_argument("--ops", default="gate_in")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--frames", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--prefill", type=int, default=-1)
     a = ap.parse_args(argv)
     cfg = configs.CONFIGS[a.workload]
+    if a.batch > 0:
+        cfg = cfg.with_(batch=a.batch)
+    if a.prefill >= 0:
+        cfg = cfg.with_(prefill=a.prefill)
     torch.cuda.set_device(0)
     w = binding.upload_weights(synth.make_weights(cfg, seed=0))
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dec = binding.Decoder(cfg, w, stream=stream)
+        for b in range(cfg.batch if cfg.prefill else 0):
+            k, v = synth.kv_prefill(cfg, b, device=torch.device("cuda", 0))
+            dec.set_kv(b, k, v)
+            del k, v
     users = synth.batch_user_tokens(cfg, max(a.frames, 1)).numpy()
     for t in range(a.frames):
         dec.step(users[t])
@@ -51,7 +63,8 @@ def main(argv=None):
         e1.record(stream)
         e1.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / max(n, 1)
-        print(json.dumps({"workload": cfg.name, "op": name, "launches": n,
+        print(json.dumps({"workload": cfg.name, "batch": cfg.batch, "prefill": cfg.prefill,
+                          "schedule": dec.schedule, "op": name, "launches": n,
                           "us_per_launch": round(us, 2), "bytes_per_launch": nb,
                           "GB/s": round(nb / max(us, 1e-9) / 1e3, 1)}), flush=True)
     dec.reset(-1)
