@@ -168,7 +168,7 @@ cudaError_t op_qkv(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
 
 cudaError_t op_attn(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const rq_config& c = h->cfg;
-  const size_t D = c.dim, C = c.context, L = c.layers;
+  const size_t C = c.context, L = c.layers;
   AttnParams a{};
   a.q = h->q;
   a.kbase = h->kcache;  // [B][L][C][D]: session b, layer l, slot j is row (b L + l) C + j

@@ -412,8 +412,9 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   const int rows = paired ? 64 : tcg::kBM;
   pl.tiles_m = (n_out + rows - 1) / rows;
   pl.ksteps = K / tcg::kBK;
-  // split K until the grid covers ~2 CTAs per SM, keeping >= 4 K steps per split
-  int splits = (2 * num_sms + pl.tiles_m - 1) / pl.tiles_m;
+  // split K so the grid fills at most one wave of 2 CTAs per SM (a partial second wave
+  // would idle most SMs for its duration), keeping >= 4 K steps per split
+  int splits = (2 * num_sms) / pl.tiles_m;
   const int max_splits = pl.ksteps / 4 > 0 ? pl.ksteps / 4 : 1;
   if (splits > max_splits) splits = max_splits;
   if (splits < 1) splits = 1;
