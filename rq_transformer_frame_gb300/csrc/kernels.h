@@ -153,6 +153,16 @@ struct TcParams {
   float* partial;     // split-K scratch [tiles_m][splits][NB][128]
   int* tickets;       // [tiles_m], zero between uses
   uint32_t* status;
+  // fused RMSNorm.  Producer (EPI_RESID / EPI_DEPIN): also write the next GEMM's operand
+  // bf16x3(new value * alpha_next) [3][NB][n_out] (alpha_next null: the value itself) and,
+  // when ss_out is set, per-tile sums of squares ss_out[tile][NB] of the new values.
+  // Consumer: scale every accumulator column b by 1 / sqrt(eps + sum_t ss_in[t][b] / rms_K).
+  uint16_t* opnd;
+  const float* alpha_next;
+  float* ss_out;
+  const float* ss_in;
+  int ss_tiles, rms_K;
+  float eps;
 };
 
 TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms);
@@ -257,6 +267,7 @@ struct TcFrame {
   uint16_t *xb, *attn_b, *u_b, *tout_b, *dxb, *do_b, *du_b;
   float* part;   // split-K partial tiles
   int* tickets;  // per tile, zero between uses
+  float *ss_x, *ss_dx;  // fused RMSNorm: per-tile sums of squares [D/128][NB], [DD/128][NB]
   TcPlan p_qkv, p_out, p_gin, p_gout, p_head, p_depin, p_dqkv, p_dout, p_dgin, p_dgout, p_lin;
   CUtensorMap* wm;  // per weight matrix, see tc_frame_wmap_index
   int n_wm;

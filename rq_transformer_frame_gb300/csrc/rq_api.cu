@@ -67,6 +67,7 @@ struct rq_handle {
   uint16_t *dxb = nullptr, *do_b = nullptr, *du_b = nullptr;
   float* tc_part = nullptr;
   int* tc_tickets = nullptr;
+  float *ss_x = nullptr, *ss_dx = nullptr;
   std::vector<int> host_off;  // host mirror of the offsets (for byte accounting)
   bool poisoned = false;
   bool forcing_dirty = true;
@@ -392,7 +393,7 @@ void free_all(rq_handle* h) {
   for (void* p : dev)
     if (p) cudaFree(p);
   void* tcb[] = {h->rope, h->xb, h->attn_b, h->u_b, h->tout_b, h->dxb, h->do_b, h->du_b,
-                 h->tc_part, h->tc_tickets};
+                 h->tc_part, h->tc_tickets, h->ss_x, h->ss_dx};
   for (void* p : tcb)
     if (p) cudaFree(p);
   if (h->d_ops) cudaFree(h->d_ops);
@@ -650,6 +651,8 @@ rq_status setup_tensor(rq_handle* h) {
   TC_ALLOC(h->du_b, R * c.dhidden * 2);
   TC_ALLOC(h->tc_part, part_floats * 4);
   TC_ALLOC(h->tc_tickets, (size_t)n_tickets * 4);
+  TC_ALLOC(h->ss_x, (size_t)((c.dim + 127) / 128) * NB * 4);
+  TC_ALLOC(h->ss_dx, (size_t)((c.ddim + 127) / 128) * NB * 4);
 #undef TC_ALLOC
   f.rope = h->rope;
   f.xb = h->xb;
@@ -661,6 +664,8 @@ rq_status setup_tensor(rq_handle* h) {
   f.du_b = h->du_b;
   f.part = h->tc_part;
   f.tickets = h->tc_tickets;
+  f.ss_x = h->ss_x;
+  f.ss_dx = h->ss_dx;
   f.n_wm = tc_frame_n_maps(f);
   h->tc_maps.assign((size_t)f.n_wm, CUtensorMap{});
   f.wm = h->tc_maps.data();

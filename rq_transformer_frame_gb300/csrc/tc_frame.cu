@@ -27,6 +27,7 @@ int wi_lin(const TcFrame& f, int cb) { return 4 * f.L + 9 + 32 * f.DL + cb; }
 
 TcParams base(const TcFrame& f, const TcPlan& pl, int epi) {
   TcParams p{};
+  p.eps = f.eps;
   p.pl = pl;
   p.epi = epi;
   p.B = f.B;
@@ -46,6 +47,21 @@ TcParams base(const TcFrame& f, const TcPlan& pl, int epi) {
 cudaError_t prep(const TcFrame& f, const float* in, int K, const float* alpha, uint16_t* xb,
                  float* side, cudaStream_t s) {
   return launch_prep_bf16(in, K, alpha, f.eps, f.B, f.NB, K, xb, side, K, s, true);
+}
+
+// fused RMSNorm: the consumer scales by 1 / rms from the producer's tile sums
+void rms_in(const TcFrame& f, TcParams& p, bool depformer) {
+  p.ss_in = depformer ? f.ss_dx : f.ss_x;
+  p.rms_K = depformer ? f.DD : f.D;
+  p.ss_tiles = (p.rms_K + 127) / 128;
+}
+
+// the producer writes the next GEMM's operand (value * alpha, or the value) and,
+// when that GEMM normalises, the tile sums of squares
+void feed(const TcFrame& f, TcParams& p, bool depformer, const float* alpha, bool rms) {
+  p.opnd = depformer ? f.dxb : f.xb;
+  p.alpha_next = alpha;
+  p.ss_out = rms ? (depformer ? f.ss_dx : f.ss_x) : nullptr;
 }
 
 }  // namespace
@@ -123,6 +139,7 @@ void* layer_cache(const TcFrame& f, void* base, int l) {
 
 cudaError_t tc_qkv(const TcFrame& f, int l, cudaStream_t s) {
   TcParams p = base(f, f.p_qkv, EPI_QKV);
+  if (l > 0) rms_in(f, p, false);  // layer 0's operand is normalised by the prep kernel
   p.out = f.q;
   p.out_bs = f.D;
   p.kcache = layer_cache(f, f.kcache, l);
@@ -161,11 +178,13 @@ cudaError_t tc_out(const TcFrame& f, int l, cudaStream_t s) {
   TcParams p = base(f, f.p_out, EPI_RESID);
   p.out = f.x;
   p.out_bs = f.D;
+  feed(f, p, false, f.norm2 + (size_t)l * f.D, true);  // gate_in's rms_norm
   return launch_tc(p, f.wm[wi_layer(l, 1)], f.xm_attn, s, true);
 }
 
 cudaError_t tc_gin(const TcFrame& f, int l, cudaStream_t s) {
   TcParams p = base(f, f.p_gin, EPI_SWIGLU);
+  rms_in(f, p, false);
   p.out_bf16 = f.u_b;
   p.outb_bs = f.F;
   return launch_tc(p, f.wm[wi_layer(l, 2)], f.xm_x, s, true);
@@ -175,6 +194,7 @@ cudaError_t tc_gout(const TcFrame& f, int l, cudaStream_t s) {
   TcParams p = base(f, f.p_gout, EPI_RESID);
   p.out = f.x;
   p.out_bs = f.D;
+  if (l + 1 < f.L) feed(f, p, false, f.norm1 + (size_t)(l + 1) * f.D, true);  // next qkv
   return launch_tc(p, f.wm[wi_layer(l, 3)], f.xm_u, s, true);
 }
 
@@ -207,12 +227,12 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
   cudaError_t e;
 #define CK(call) \
   if ((e = (call)) != cudaSuccess) return e;
+  // rms_norm of layer 0's input; later norms are fused (producer epilogue + consumer scale)
+  CK(prep(f, f.x, f.D, f.norm1, f.xb, nullptr, s));
   for (int l = 0; l < f.L; ++l) {
-    CK(prep(f, f.x, f.D, f.norm1 + (size_t)l * D, f.xb, nullptr, s));  // rms_norm
     CK(tc_qkv(f, l, s));
     CK(tc_attn(f, l, s));
     CK(tc_out(f, l, s));
-    CK(prep(f, f.x, f.D, f.norm2 + (size_t)l * D, f.xb, nullptr, s));
     CK(tc_gin(f, l, s));
     CK(tc_gout(f, l, s));
   }
@@ -220,18 +240,19 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
   CK(prep(f, f.x, f.D, f.out_norm, f.tout_b, f.tout, s));
   CK(tc_head(f, s));
   for (int cb = 0; cb < 8; ++cb) {
-    {  // depformer_in[cb](tout) + embedding of the previous token
+    {  // depformer_in[cb](tout) + embedding of the previous token; feeds layer 0's norm
       TcParams p = base(f, f.p_depin, EPI_DEPIN);
       p.out = f.dx;
       p.out_bs = DD;
       p.emb = cb == 0 ? f.dep_text_emb : bf(f.dep_emb, (size_t)(cb - 1) * (A + 1) * DD);
       p.key_index = cb;
+      feed(f, p, true, f.dnorm1, true);
       CK(launch_tc(p, f.wm[wi_depin(f, cb)], f.xm_tout, s, true));
     }
     for (int l = 0; l < f.DL; ++l) {
-      CK(prep(f, f.dx, f.DD, f.dnorm1 + (size_t)l * DD, f.dxb, nullptr, s));
       {
         TcParams p = base(f, f.p_dqkv, EPI_DQKV);
+        rms_in(f, p, true);
         p.out = f.dq;
         p.out_bs = DD;
         p.dk_out = f.dkv + dkv_off(l, 0, cb);
@@ -246,23 +267,28 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
         TcParams p = base(f, f.p_dout, EPI_RESID);
         p.out = f.dx;
         p.out_bs = DD;
+        feed(f, p, true, f.dnorm2 + (size_t)l * DD, true);  // gate_in's rms_norm
         CK(launch_tc(p, f.wm[wi_dep(f, cb, l, 1)], f.xm_do, s, true));
       }
-      CK(prep(f, f.dx, f.DD, f.dnorm2 + (size_t)l * DD, f.dxb, nullptr, s));
       {
         TcParams p = base(f, f.p_dgin, EPI_SWIGLU);
+        rms_in(f, p, true);
         p.out_bf16 = f.du_b;
         p.outb_bs = DF;
         CK(launch_tc(p, f.wm[wi_dep(f, cb, l, 2)], f.xm_dx, s, true));
       }
       {
+        // next layer's rms_norm, or the head's plain operand (no norm before linears)
         TcParams p = base(f, f.p_dgout, EPI_RESID);
         p.out = f.dx;
         p.out_bs = DD;
+        if (l + 1 < f.DL)
+          feed(f, p, true, f.dnorm1 + (size_t)(l + 1) * DD, true);
+        else
+          feed(f, p, true, nullptr, false);
         CK(launch_tc(p, f.wm[wi_dep(f, cb, l, 3)], f.xm_du, s, true));
       }
     }
-    CK(prep(f, f.dx, f.DD, nullptr, f.dxb, nullptr, s));
     {
       TcParams p = base(f, f.p_lin, EPI_ARGMAX);
       p.out = f.audio_logits + (size_t)cb * A;

@@ -40,10 +40,65 @@ __device__ __forceinline__ void store_kv_tc(void* base, size_t i, float v, int b
 struct EpiShared {
   float ex[2][64][16];                 // SiLU gate: multiplier rows -> gate rows
   unsigned long long key[4][64];       // argmax: best key per lane quarter and session
+  float ss[4][64];                     // fused RMSNorm: sum of squares per lane quarter
+  float inv[64];                       // fused RMSNorm: 1 / rms of each session's input
 };
 
+// The next GEMM's operand for a new residual value v of row `row`, session b (fused
+// RMSNorm, see TcParams).
+__device__ __forceinline__ void feed_next(const TcParams& p, int row, bool valid, int b,
+                                          float v) {
+  const TcPlan& pl = p.pl;
+  if (valid)
+    store_bf16x3(p.opnd, (size_t)pl.NB * pl.n_out, (size_t)b * pl.n_out + row,
+                 b < p.B ? (p.alpha_next ? v * p.alpha_next[row] : v) : 0.f);
+}
+
+// Sum over the warp's 32 rows of each of 16 per-lane values with 16 shuffles (a
+// transposing butterfly: every step halves the values a lane keeps); the lanes with bit 0
+// clear end with the sum for column ((lane >> 1) & 15) bit-reversed into place below.
+__device__ __forceinline__ void tile_sumsq(float (&sq)[16], int lane, int q, int c0,
+                                           EpiShared& es) {
+  float w8[8], w4[4], w2[2];
+  {
+    const bool hi = (lane & 16) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = hi ? sq[i] : sq[i + 8];
+      const float keep = hi ? sq[i + 8] : sq[i];
+      w8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool hi = (lane & 8) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = hi ? w8[i] : w8[i + 4];
+      const float keep = hi ? w8[i + 4] : w8[i];
+      w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool hi = (lane & 4) != 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = hi ? w4[i] : w4[i + 2];
+      const float keep = hi ? w4[i + 2] : w4[i];
+      w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  const bool hi = (lane & 2) != 0;
+  float w1 = (hi ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, hi ? w2[0] : w2[1], 2);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+  // column kept: bit 4 of the lane chose 8, bit 3 chose 4, bit 2 chose 2, bit 1 chose 1
+  const int col = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                  ((lane >> 1) & 1);
+  if ((lane & 1) == 0) es.ss[q][c0 + col] = w1;
+}
+
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&d)[16], int c0,
-                                               int tile, int m, int lane, int q, EpiShared& es) {
+                                               int tile, int m, int lane, int q, EpiShared& es,
+                                               const float (&old0)[16]) {
   const TcPlan& pl = p.pl;
   const int B = p.B;
   const int epi = p.epi;
@@ -70,13 +125,19 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
   const int row = tile * kBM + m;
   const bool valid = row < pl.n_out;
   if (epi == EPI_RESID || epi == EPI_STORE) {
-    if (valid)
+    float sq[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (c0 + i < B) {
-          float* o = p.out + (size_t)(c0 + i) * p.out_bs + row;
-          *o = (epi == EPI_RESID ? *o : 0.f) + d[i];
-        }
+    for (int i = 0; i < 16; ++i) {
+      float nv = 0.f;
+      if (valid && c0 + i < B) {
+        float* o = p.out + (size_t)(c0 + i) * p.out_bs + row;
+        nv = (epi == EPI_RESID ? (c0 == 0 ? old0[i] : *o) : 0.f) + d[i];
+        *o = nv;
+      }
+      sq[i] = nv * nv;
+      if (p.opnd) feed_next(p, row, valid, c0 + i, nv);
+    }
+    if (p.ss_out) tile_sumsq(sq, lane, q, c0, es);
   } else if (epi == EPI_QKV) {
     // "moshi_lm.rs", `rope_row` on q, k at each session's position, K/V append
     const int D = pl.n_out / 3;
@@ -118,11 +179,12 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
   } else if (epi == EPI_DEPIN) {
     // "moshi_lm.rs", `embed` of the previous step's token: -1 adds nothing
     const IoLayout io{p.B};
-    if (valid)
+    float sq[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int b = c0 + i;
-        if (b >= B) continue;
+    for (int i = 0; i < 16; ++i) {
+      const int b = c0 + i;
+      float nv = 0.f;
+      if (valid && b < B) {
         const int prev = p.d_in[io.flag_off() + b]
                              ? p.d_in[io.forced_off() + (size_t)b * 9 + p.key_index]
                              : argmax_key_index(p.keys[(size_t)b * 9 + p.key_index]);
@@ -131,8 +193,13 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
           e = __uint_as_float(((uint32_t)static_cast<const uint16_t*>(
                                    p.emb)[(size_t)max(prev, 0) * pl.n_out + row])
                               << 16);
-        p.out[(size_t)b * p.out_bs + row] = d[i] + e;
+        nv = d[i] + e;
+        p.out[(size_t)b * p.out_bs + row] = nv;
       }
+      sq[i] = nv * nv;
+      if (p.opnd) feed_next(p, row, valid, b, nv);
+    }
+    if (p.ss_out) tile_sumsq(sq, lane, q, c0, es);
   } else if (epi == EPI_ARGMAX) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -278,6 +345,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
     const int m = q * 32 + lane;
     const int et = tid - 64;  // 0..127 among the epilogue warps
+    // while the MMAs run: the fused-RMSNorm scales, and the old residual values of the
+    // first 16 sessions
+    if (p.ss_in && et < NB) {
+      float ss = 0.f;
+      for (int t = 0; t < p.ss_tiles; ++t) ss += p.ss_in[(size_t)t * NB + et];
+      s_epi.inv[et] = 1.0f / sqrtf(p.eps + ss / (float)p.rms_K);
+    }
+    float old0[16];
+    {
+      const int row = tile * kBM + m;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        old0[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && i < p.B)
+                      ? p.out[(size_t)i * p.out_bs + row]
+                      : 0.f;
+    }
     if (!mbar_wait(&s_done, 0u)) s_abort = 1;
     bar_sync(1, 128);
     const bool ok = !s_abort;  // the same for all epilogue threads
@@ -317,7 +400,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
           load_sum3<NB>(tmem + ((uint32_t)(q * 32) << 16), c0, v);
         }
-        epilogue_chunk(p, v, c0, tile, m, lane, q, s_epi);
+        if (p.ss_in) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= s_epi.inv[c0 + i];
+        }
+        epilogue_chunk(p, v, c0, tile, m, lane, q, s_epi, old0);
+        if (p.ss_out) {
+          bar_sync(1, 128);
+          if (et < 16) {
+            const float ss = s_epi.ss[0][c0 + et] + s_epi.ss[1][c0 + et] +
+                             s_epi.ss[2][c0 + et] + s_epi.ss[3][c0 + et];
+            p.ss_out[(size_t)tile * NB + c0 + et] = ss;
+          }
+        }
       }
       if (p.epi == EPI_ARGMAX) {
         bar_sync(1, 128);
