@@ -152,7 +152,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   auto issue_next = [&](int s) {
     AttnItem x;
     int it = last + (int)gridDim.x;
-    while (it < total && !attn_decode_item(p, it, x)) it += gridDim.x;
+    const int G = (int)gridDim.x, per_b = p.nsplit * p.H;
+    while (it < total && !attn_decode_item(p, it, x)) {
+      // past session b's window: every later split of b is empty too, so go to the first
+      // item of session b + 1 in this CTA's stride class (it mod G fixed)
+      const int base = (x.b + 1) * per_b;
+      it = base + (((it - base) % G) + G) % G;
+    }
     s_item[s] = it;
     if (it >= total) return;
     last = it;
