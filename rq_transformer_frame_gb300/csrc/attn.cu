@@ -77,6 +77,39 @@ __device__ __forceinline__ void load16(const KT* row, int gl, int G, float (&v)[
   }
 }
 
+// packed pair of f32 (two lanes of one 64-bit register pair) and its FMA
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ void ffma2(f32x2& d, f32x2 a, f32x2 b) {  // d += a * b, per lane
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// load16 as 8 packed pairs: pair i holds elements 2i, 2i + 1 (dimensions dim16(2i), +1)
+template <typename KT>
+__device__ __forceinline__ void load16p(const KT* row, int gl, int G, f32x2 (&v)[8]) {
+  constexpr int EPC = 16 / sizeof(KT);
+#pragma unroll
+  for (int c = 0; c < 16 / EPC; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + c * G * EPC + gl * EPC);
+    if constexpr (sizeof(KT) == 2) {
+      v[4 * c + 0] = pack2(bf16lo(u.x), bf16hi(u.x));
+      v[4 * c + 1] = pack2(bf16lo(u.y), bf16hi(u.y));
+      v[4 * c + 2] = pack2(bf16lo(u.z), bf16hi(u.z));
+      v[4 * c + 3] = pack2(bf16lo(u.w), bf16hi(u.w));
+    } else {
+      v[2 * c + 0] = pack2(__uint_as_float(u.x), __uint_as_float(u.y));
+      v[2 * c + 1] = pack2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+  }
+}
+
 // One work item = (session, split, head).  Splits are cut in cache-slot
 // space: the window of session b is every slot when pos >= C, else slots 0..pos, so
 // split s covers slots [s kps, min((s + 1) kps, min(pos + 1, C))) and never wraps.
@@ -108,6 +141,7 @@ __device__ __forceinline__ bool attn_decode_item(const AttnParams& p, int it, At
 #define RQ_ATTN_WARPS 4
 #endif
 constexpr int kAttnStages = RQ_ATTN_STAGES;  // K/V chunks per CTA (ring depth)
+constexpr int kAttnMaxKps = 64;              // positions per work item, at most
 constexpr int kAttnWarps = RQ_ATTN_WARPS;
 
 // Persistent grid over the work items: each CTA takes items blockIdx.x, + gridDim.x, ...
@@ -196,50 +230,63 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     const int grp = lane / G, gl = lane % G;
     const KT* ks = stage0 + (size_t)s * stage_elems;
     const KT* vs = ks + (size_t)kps * HD;
-    float q[16];
+    f32x2 q2[8];
     const float* qp = p.q + (size_t)b * p.D + (size_t)h * HD;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) q[e] = qp[dim16<KT>(e, gl, G)] * scale;
-    float m = ninf, l = 0.f, acc[16];
+    for (int i = 0; i < 8; ++i)
+      q2[i] = pack2(qp[dim16<KT>(2 * i, gl, G)] * scale, qp[dim16<KT>(2 * i + 1, gl, G)] * scale);
+    // pass 1: this warp's scores (key group grp takes key warp*KPI + st*NW*KPI + grp), max
+    constexpr int kSteps = kAttnMaxKps / (NW * KPI) > 0 ? kAttnMaxKps / (NW * KPI) : 1;
+    float sc[kSteps];
+    float m = ninf;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-    for (int r0 = warp * KPI; r0 < n; r0 += NW * KPI) {
-      const int r = r0 + grp;  // this group's key (uniform within the group)
-      float kv[16];
+    for (int st = 0; st < kSteps; ++st) {
+      const int r = warp * KPI + st * NW * KPI + grp;  // uniform within the group
       float d = 0.f;
       if (r < n) {
-        load16<KT>(ks + (size_t)r * HD, gl, G, kv);
+        f32x2 kv[8];
+        load16p<KT>(ks + (size_t)r * HD, gl, G, kv);
+        f32x2 d2 = pack2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) d = fmaf(q[e], kv[e], d);
+        for (int i = 0; i < 8; ++i) ffma2(d2, q2[i], kv[i]);
+        float dx, dy;
+        unpack2(d2, dx, dy);
+        d = dx + dy;
       }
 #pragma unroll
       for (int o = G / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (r < n) {
-        load16<KT>(vs + (size_t)r * HD, gl, G, kv);
-        const float mn = fmaxf(m, d);
-        const float corr = expf(m - mn);  // m = -inf: 0
-        const float pe = expf(d - mn);
-        l = l * corr + pe;
+      sc[st] = r < n ? d : ninf;
+      m = fmaxf(m, sc[st]);
+    }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = fmaf(pe, kv[e], acc[e] * corr);
-        m = mn;
+    for (int o = G; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    // pass 2: exp against the warp's max (no per-key rescale), weighted values
+    float l = 0.f;
+    f32x2 acc2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc2[i] = pack2(0.f, 0.f);
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const int r = warp * KPI + st * NW * KPI + grp;
+      if (r < n) {
+        const float pe = expf(sc[st] - m);
+        l += pe;
+        const f32x2 p2 = pack2(pe, pe);
+        f32x2 vv[8];
+        load16p<KT>(vs + (size_t)r * HD, gl, G, vv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ffma2(acc2[i], p2, vv[i]);
       }
     }
-    // merge the KPI key groups of the warp (lanes gl, gl + G, ...): fixed butterfly order
+    // merge the key groups (same max): plain sums in a fixed butterfly order
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) unpack2(acc2[i], acc[2 * i], acc[2 * i + 1]);
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-      const float lo = __shfl_xor_sync(0xffffffffu, l, o);
-      const float M = fmaxf(m, mo);
-      const float c1 = (l > 0.f) ? expf(m - M) : 0.f;
-      const float c2 = (lo > 0.f) ? expf(mo - M) : 0.f;
+      l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float ao = __shfl_xor_sync(0xffffffffu, acc[e], o);
-        acc[e] = acc[e] * c1 + ao * c2;
-      }
-      l = l * c1 + lo * c2;
-      m = M;
+      for (int e = 0; e < 16; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
     }
     if (lane == 0) {
       s_m[warp] = m;
@@ -384,6 +431,7 @@ cudaError_t attn_configure(int hd, bool kv_bf16, int kps) {
 }
 
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl) {
+  if (p.kps < 1 || p.kps > kAttnMaxKps) return cudaErrorInvalidValue;
   switch (p.hd) {
     case 32:
       return kv_bf16 ? launch_attn_t<uint16_t, 1>(p, s, pdl) : launch_attn_t<float, 1>(p, s, pdl);
