@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     tc::prefetch_tmap(&vmap);
   }
   __syncthreads();
-  pdl_trigger();
   pdl_wait();
   const uint64_t pol = l2_policy_evict_first();
   // thread 0 only: the next valid item at or after `it` (stride gridDim.x), then its load
@@ -322,6 +321,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     }
     __syncthreads();  // s_m / s_acc / s_item are reused by the next item
   }
+  // dependents launch once this CTA is done: launched early, the merge kernel's blocks
+  // would sit resident beside the streaming CTAs for the whole kernel
+  pdl_trigger();
 }
 
 // Grid (head, session), head_dim threads: combine the partials of every split of the
