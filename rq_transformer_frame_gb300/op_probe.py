@@ -5,7 +5,8 @@
 
 Builds the decoder for the workload (seeded synthetic weights; `--batch` overrides the
 session count, `--prefill n` fills every session's temporal K/V with the workload's
-synthetic positions 0..n-1), runs `--frames` whole frames, then for each op launches it
+synthetic positions 0..n-1; `--context` shrinks the K/V window, e.g. to profile a
+linear on a small device footprint), runs `--frames` whole frames, then for each op launches it
 once per temporal layer `--reps` times, timed with CUDA events on the decoder's stream,
 and prints one JSON line per op.  Used as the command under the profiler for the kernel
 summaries in profiles/.
@@ -30,12 +31,15 @@ def main(argv=None):
     ap.add_argument("--frames", type=int, default=2)
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--prefill", type=int, default=-1)
+    ap.add_argument("--context", type=int, default=0)
     a = ap.parse_args(argv)
     cfg = configs.CONFIGS[a.workload]
     if a.batch > 0:
         cfg = cfg.with_(batch=a.batch)
     if a.prefill >= 0:
         cfg = cfg.with_(prefill=a.prefill)
+    if a.context > 0:
+        cfg = cfg.with_(context=a.context)
     torch.cuda.set_device(0)
     w = binding.upload_weights(synth.make_weights(cfg, seed=0))
     stream = torch.cuda.Stream()
