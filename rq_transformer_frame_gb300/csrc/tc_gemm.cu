@@ -131,7 +131,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
       float nv = 0.f;
       if (valid && c0 + i < B) {
         float* o = p.out + (size_t)(c0 + i) * p.out_bs + row;
-        nv = (epi == EPI_RESID ? (c0 == 0 ? old0[i] : *o) : 0.f) + d[i];
+        nv = (epi == EPI_RESID ? old0[i] : 0.f) + d[i];
         *o = nv;
       }
       sq[i] = nv * nv;
@@ -387,6 +387,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (run) {
 #pragma unroll 1
       for (int c0 = 0; c0 < NB; c0 += 16) {
+        // the residual's old values of the next chunk load while this one is processed
+        float old1[16];
+        {
+          const int row = tile * kBM + m;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            old1[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && c0 + 16 + i < p.B)
+                          ? p.out[(size_t)(c0 + 16 + i) * p.out_bs + row]
+                          : 0.f;
+        }
         float v[16];
         if (pl.splits > 1) {
           // splits added in split order (deterministic); two splits' loads are issued
@@ -418,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; i < 16; ++i) v[i] *= s_epi.inv[c0 + i];
         }
         epilogue_chunk(p, v, c0, tile, m, lane, q, s_epi, old0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) old0[i] = old1[i];
         if (p.ss_out) {
           bar_sync(1, 128);
           if (et < 16) {
@@ -528,10 +540,15 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   if (splits < 1) splits = 1;
   pl.ksteps_split = (pl.ksteps + splits - 1) / splits;
   pl.splits = (pl.ksteps + pl.ksteps_split - 1) / pl.ksteps_split;
-  // two CTAs per SM: ~104 KB of dynamic shared memory each
+  // two CTAs per SM: ~104 KB of dynamic shared memory each; a grid that fits one CTA per
+  // SM (the small depformer GEMMs) takes up to ~200 KB, enough to have all of a CTA's
+  // K steps in flight at once
   const int stage = tcg::kABytes + 3 * NB * tcg::kBK * 2;
-  int ns = (104 * 1024) / stage;
+  const bool one_per_sm = pl.tiles_m * pl.splits <= num_sms;
+  // (two per SM: 2 x (dynamic + ~11.5 KB static + 1 KB reserved) within 228 KB)
+  int ns = ((one_per_sm ? 190 : 100) * 1024) / stage;  // + 1 KB alignment
   ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+  if (one_per_sm && ns > pl.ksteps_split) ns = pl.ksteps_split < 2 ? 2 : pl.ksteps_split;
   pl.n_stages = ns;
   pl.smem = ns * stage + 1024;
   pl.bytes = (double)n_out * (paired ? 2.0 : 1.0) * K * 2.0;
