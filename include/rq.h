@@ -91,8 +91,8 @@ typedef struct {
  * cooperative kernel with grid barriers between dependent ops (batch 1, same weight and
  * K/V dtype); GRAPH launches one streaming-GEMV kernel per op inside a CUDA graph;
  * TENSOR (batch 16..64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
- * runs every linear as one tcgen05 tensor-core GEMM over all sessions, with the GEMM
- * operands (the normalised activations) rounded to bf16, inside a CUDA graph.  AUTO
+ * runs every linear as one tcgen05 tensor-core GEMM over all sessions, the normalised
+ * f32 activations split exactly into three bf16 operand parts, inside a CUDA graph.  AUTO
  * picks PERSISTENT when it applies, TENSOR at batch >= 16 when it applies, else GRAPH.
  * Results agree within the parity tolerance. */
 enum {

@@ -30,6 +30,12 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
+// one arrival of this CTA, after a CTA barrier: the release orders every thread's writes
+// (made visible to it by that barrier) before the count
+__device__ __forceinline__ void grid_arrive(unsigned* bar) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+}
+
 // thread 0 of the consumers: wait until `target` CTAs have arrived (bounded)
 __device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target) {
   if (ld_acquire(bar) >= target) return true;
@@ -600,7 +606,6 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
       s_rope[tid] = make_float2(cosf(ang), sinf(ang));
     }
     bar_sync(1, kCons);
-    const unsigned G = gridDim.x;
     uint32_t gi = 0;
     float xr[kMaxNch][V];
     const bool stamp = P.trace != nullptr && blockIdx.x == 0 && tid == 0;
@@ -620,7 +625,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         }
       }
       if (k > 0) {
-        if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * G)) {
+        if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * gridDim.x)) {
           atomicOr(P.status, kDevTimeout);
           s_abort = 1;
         }
@@ -667,12 +672,9 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         }
       }
       bar_sync(1, kCons);
-      if (tid == 0) {
-        __threadfence();
-        atomicAdd(P.grid_bar, 1u);
-      }
+      if (tid == 0) grid_arrive(P.grid_bar);
     }
-    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * G))
+    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x))
       P.trace[P.n_ops] = global_timer_ns();
   }
   __syncthreads();
