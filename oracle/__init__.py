@@ -68,6 +68,18 @@ def lib():
         L.orc_max_threads.restype = I32
         L.orc_round_to_bf16.argtypes = [F]
         L.orc_round_to_bf16.restype = F
+        U64 = C.c_uint64
+        L.orc_xorshift_next.argtypes = [C.POINTER(U64)]
+        L.orc_xorshift_next.restype = U64
+        L.orc_xorshift_u01.argtypes = [C.POINTER(U64)]
+        L.orc_xorshift_u01.restype = C.c_double
+        L.orc_gumbel_pick.argtypes = [P, I32, F, C.POINTER(U64)]
+        L.orc_gumbel_pick.restype = C.c_uint32
+        L.orc_topk_pick.argtypes = [P, I32, F, I32, C.POINTER(U64)]
+        L.orc_topk_pick.restype = C.c_uint32
+        L.orc_state_set_sampling.argtypes = [P, I32, F, F, I32, I32, U64]
+        L.orc_state_get_rng.argtypes = [P]
+        L.orc_state_get_rng.restype = U64
         _LIB = L
     return _LIB
 
@@ -147,6 +159,37 @@ def embed(table, tok: int, acc):
 
 def round_to_bf16(x: float) -> float:
     return float(lib().orc_round_to_bf16(C.c_float(x)))
+
+
+# sampling ("moshi_lm.rs", `Sampling` / `pick`): modes of a session's sampler
+PICK_GREEDY, PICK_TOPK, PICK_GUMBEL = 0, 1, 2
+
+
+class XorShift:
+    """The page's xorshift64 sampler state (`xorshift_u01`)."""
+
+    def __init__(self, state: int):
+        self.s = C.c_uint64(state)
+
+    def next(self) -> int:
+        return int(lib().orc_xorshift_next(C.byref(self.s)))
+
+    def u01(self) -> float:
+        return float(lib().orc_xorshift_u01(C.byref(self.s)))
+
+    @property
+    def state(self) -> int:
+        return int(self.s.value)
+
+
+def gumbel_pick(logits, temp: float, rng: XorShift) -> int:
+    v = _f32(logits)
+    return int(lib().orc_gumbel_pick(_ptr(v), v.size, C.c_float(temp), C.byref(rng.s)))
+
+
+def topk_pick(logits, temp: float, k: int, rng: XorShift) -> int:
+    v = _f32(logits)
+    return int(lib().orc_topk_pick(_ptr(v), v.size, C.c_float(temp), int(k), C.byref(rng.s)))
 
 
 # ------------------------------------------------------------------ model
@@ -231,6 +274,16 @@ class OracleState:
         rc = lib().orc_state_set_kv(self.p, int(k.shape[1]), _ptr(k), _ptr(v), bits16)
         if rc != 0:
             raise ValueError("n_pos exceeds the context")
+
+    def set_sampling(self, mode: int, temp: float = 0.8, temp_text: float = 0.7,
+                     top_k: int = 250, top_k_text: int = 25, seed: int = 1) -> None:
+        """`MoshiLm::set_sampling` for this session (defaults: the page's `Sampling`)."""
+        lib().orc_state_set_sampling(self.p, int(mode), C.c_float(temp), C.c_float(temp_text),
+                                     int(top_k), int(top_k_text), C.c_uint64(seed))
+
+    @property
+    def rng(self) -> int:
+        return int(lib().orc_state_get_rng(self.p))
 
     def ring(self):
         ring = np.zeros((17, 3), np.int64)

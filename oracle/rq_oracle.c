@@ -4,8 +4,9 @@
  * A plain, slow, scalar CPU restatement (f32, as the page fixes) of the per-frame
  * decode step of a Moshi-style RQ-Transformer, written from the docs.rs page
  * "inferencelayer 0.2.4 -- src/moshi_lm.rs" (module doc comment, `rms_norm`,
- * `silu`, `argmax`, `rope_row`, `attend`, `embed`, `temporal_step`,
- * `depformer_cycle`, `step_ext`, `MoshiState::force_generated`), plus the forced
+ * `silu`, `argmax`, `xorshift_u01`, `topk_sample`, `gumbel_full_pick`, `pick`,
+ * `rope_row`, `attend`, `embed`, `temporal_step`, `depformer_cycle`, `step_ext`,
+ * `MoshiState::force_generated`, `Sampling`, `set_sampling`), plus the forced
  * depformer conditioning of "rlx-moshi -- src/rlx_lm.rs" (`depformer_sample_rlx`,
  * `depformer_forced_logits_rlx`).
  *
@@ -28,10 +29,15 @@
  *     nearest even) when they are appended to the window, as the GPU cache stores
  *     them; the depformer's per-frame K/V stay f32;
  *   - forcing: `forced` = [text, audio0..7] conditions the depformer chain and is
- *     what the ring records, while the step still reports its own argmax tokens.
+ *     what the ring records, while the step still reports its own picked tokens;
+ *   - `topk_sample` walks the k selected logits in descending order, equal logits by
+ *     ascending index (the page's partial selection leaves that order open);
+ *   - each session owns its sampler state (the page has one session per model).
  *
  * Parity pins (tests/test_oracle_pins.py): RMSNorm closed forms, RoPE hand vectors,
- * argmax tie/NaN cases, one-key attention, attention and GEMV against independent
+ * argmax tie/NaN cases, the published xorshift64 sequence, the Gumbel-max and top-k
+ * pick frequencies against the softmax they sample, one-key attention, attention and
+ * GEMV against independent
  * f64 routines, the hand-traced ring schedule, -1 zero embedding, depformer reset
  * versus a from-scratch causal recompute, and an independent NumPy f64
  * restatement of whole frames.
@@ -89,9 +95,20 @@ typedef struct {
 
 /* moshi_lm.rs, struct MoshiState: ring cache, offset, temporal K/V window
  * ([layer][step][dim], oldest first). */
+/* moshi_lm.rs, struct `Sampling` and `MoshiLm::set_sampling`: how `pick` chooses a
+ * token.  mode 0 = greedy argmax (no sampler set), 1 = `topk_sample`, 2 =
+ * `gumbel_full_pick`; text picks use temp_text / top_k_text. */
+typedef struct {
+  int32_t mode;
+  float temp, temp_text;
+  int32_t top_k, top_k_text;
+} orc_sampling;
+
 typedef struct {
   int64_t ring[ORC_STREAMS][ORC_CT];
   int64_t offset;
+  orc_sampling smp; /* greedy unless orc_state_set_sampling was called */
+  uint64_t rng;     /* xorshift64 state of this session's sampler */
   int32_t layers, context, dim;
   int32_t *kv_len; /* [L] entries currently in the window */
   float *k;        /* [L][C][D] */
@@ -180,6 +197,104 @@ uint32_t orc_argmax(const float *v, int32_t n) {
   return bi;
 }
 
+/* moshi_lm.rs, `xorshift_u01`: one xorshift64 step (shifts 13, 7, 17, as in
+ * G. Marsaglia, "Xorshift RNGs", J. Stat. Soft. 8(14), 2003) of the state, returned
+ * raw; orc_xorshift_u01 maps its top 53 bits to [0, 1). */
+uint64_t orc_xorshift_next(uint64_t *st) {
+  uint64_t x = *st;
+  x ^= x << 13;
+  x ^= x >> 7;
+  x ^= x << 17;
+  *st = x;
+  return x;
+}
+
+double orc_xorshift_u01(uint64_t *st) {
+  uint64_t x = orc_xorshift_next(st);
+  return (double)(x >> 11) / (double)(1ull << 53);
+}
+
+/* moshi_lm.rs, `gumbel_full_pick`: argmax over i of logits[i] / temp + g_i with
+ * g_i = -ln(-ln(u_i)) in f64 (u_i the i-th draw, at least 1e-300) rounded to f32;
+ * the first strictly greater score wins.  Consumes n draws. */
+uint32_t orc_gumbel_pick(const float *logits, int32_t n, float temp, uint64_t *st) {
+  float best = -INFINITY;
+  uint32_t bi = 0;
+  for (int32_t i = 0; i < n; i++) {
+    double u = orc_xorshift_u01(st);
+    if (u < 1e-300) u = 1e-300;
+    float g = (float)(-log(-log(u)));
+    float sc = logits[i] / temp + g;
+    if (sc > best) {
+      best = sc;
+      bi = (uint32_t)i;
+    }
+  }
+  return bi;
+}
+
+/* the total order of f32 values (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN) as
+ * an unsigned key */
+static uint32_t total_order_key(float v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+static const float *g_sort_logits;
+/* descending total order of the logit; equal logits by ascending index */
+static int topk_cmp(const void *a, const void *b) {
+  uint32_t ia = *(const uint32_t *)a, ib = *(const uint32_t *)b;
+  uint32_t ka = total_order_key(g_sort_logits[ia]), kb = total_order_key(g_sort_logits[ib]);
+  if (ka != kb) return ka > kb ? -1 : 1;
+  return ia < ib ? -1 : (ia > ib);
+}
+
+/* moshi_lm.rs, `topk_sample`: the k largest logits (reading: taken in descending order,
+ * equal logits by ascending index -- the page leaves the order of the selected k
+ * open), p_i = exp(((l_i - max) / temp) in f32, widened to f64), normalised by their
+ * sequential f64 sum; one draw u, and the first i at which u - p_0 - ... - p_i <= 0 is
+ * the token (the last candidate if none).  Consumes one draw. */
+uint32_t orc_topk_pick(const float *logits, int32_t n, float temp, int32_t k, uint64_t *st) {
+  if (k > n) k = n;
+  if (k < 1) k = 1;
+  uint32_t *idx = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)n);
+  for (int32_t i = 0; i < n; i++) idx[i] = (uint32_t)i;
+  g_sort_logits = logits;
+  qsort(idx, (size_t)n, sizeof(uint32_t), topk_cmp);
+  float mx = -INFINITY;
+  for (int32_t i = 0; i < k; i++) mx = fmaxf(mx, logits[idx[i]]);
+  double *p = (double *)malloc(sizeof(double) * (size_t)k);
+  double sum = 0.0;
+  for (int32_t i = 0; i < k; i++) {
+    p[i] = exp((double)((logits[idx[i]] - mx) / temp));
+    sum += p[i];
+  }
+  for (int32_t i = 0; i < k; i++) p[i] /= sum;
+  double u = orc_xorshift_u01(st);
+  uint32_t tok = idx[k - 1];
+  for (int32_t i = 0; i < k; i++) {
+    u -= p[i];
+    if (u <= 0.0) {
+      tok = idx[i];
+      break;
+    }
+  }
+  free(p);
+  free(idx);
+  return tok;
+}
+
+/* moshi_lm.rs, `pick`: greedy argmax without a sampler, else the configured sampler
+ * with the text or the audio temperature and k. */
+static uint32_t pick(const orc_sampling *smp, uint64_t *rng, const float *logits,
+                     int32_t n, int text) {
+  if (smp == NULL || smp->mode == 0) return orc_argmax(logits, n);
+  float temp = text ? smp->temp_text : smp->temp;
+  if (smp->mode == 2) return orc_gumbel_pick(logits, n, temp, rng);
+  return orc_topk_pick(logits, n, temp, text ? smp->top_k_text : smp->top_k, rng);
+}
+
 /* moshi_lm.rs, `rope_row`: interleaved pairs (2i, 2i+1) of every head rotated by
  * freq_i * pos, freq_i = exp(-ln(theta) * 2i / head_dim), all in f32. */
 void orc_rope_row(float *row, int32_t n, int64_t pos, int32_t head_dim,
@@ -265,8 +380,22 @@ orc_state *orc_state_new(const orc_cfg *c) {
   for (int s = 0; s < ORC_STREAMS; s++)
     for (int j = 0; j < ORC_CT; j++) st->ring[s][j] = ORC_UNGENERATED;
   st->offset = 0;
+  st->rng = 1;
   return st;
 }
+
+/* moshi_lm.rs, `MoshiLm::set_sampling`: the sampler and its seed (at least 1) */
+void orc_state_set_sampling(orc_state *st, int32_t mode, float temp, float temp_text,
+                            int32_t top_k, int32_t top_k_text, uint64_t seed) {
+  st->smp.mode = mode;
+  st->smp.temp = temp;
+  st->smp.temp_text = temp_text;
+  st->smp.top_k = top_k;
+  st->smp.top_k_text = top_k_text;
+  st->rng = seed > 1 ? seed : 1;
+}
+
+uint64_t orc_state_get_rng(const orc_state *st) { return st->rng; }
 
 void orc_state_free(orc_state *st) {
   if (!st) return;
@@ -354,9 +483,10 @@ void orc_temporal_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
  * rotation; then linears[cb] (no norm) and an argmax.
  * `forced` (NULL, or [text, audio0..7]) replaces prev after each step, as in
  * rlx_lm.rs `depformer_forced_logits_rlx`; `tokens` are always the own argmaxes. */
-void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *tout,
-                         int64_t text_token, const int32_t *forced,
-                         float *logits /*[8][A]*/, int32_t *tokens /*[8]*/) {
+static void depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *tout,
+                            int64_t text_token, const int32_t *forced,
+                            float *logits /*[8][A]*/, int32_t *tokens /*[8]*/,
+                            const orc_sampling *smp, uint64_t *rng) {
   const int D = c->dim, DD = c->ddim, DF = c->dhidden, A = c->audio_card;
   const int DL = c->dlayers, bf = c->w_bf16, Q = ORC_DEP_Q;
   float *kc = (float *)calloc((size_t)DL * Q * DD, sizeof(float));
@@ -393,11 +523,17 @@ void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *to
     }
     float *lg = logits + (size_t)cb * A;
     orc_gemv(woff(w->linears, bf, (size_t)cb * A * DD), bf, A, DD, x, lg);
-    tokens[cb] = (int32_t)orc_argmax(lg, A);
+    tokens[cb] = (int32_t)pick(smp, rng, lg, A, 0);
     prev = forced ? (int64_t)forced[1 + cb] : (int64_t)tokens[cb];
   }
   free(kc); free(vc); free(x); free(h); free(qkv); free(attn); free(proj);
   free(gate); free(gated);
+}
+
+void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *tout,
+                         int64_t text_token, const int32_t *forced,
+                         float *logits /*[8][A]*/, int32_t *tokens /*[8]*/) {
+  depformer_cycle(c, w, tout, text_token, forced, logits, tokens, NULL, NULL);
 }
 
 /* moshi_lm.rs, `step_ext` (steps 1-8) for one session.
@@ -438,10 +574,10 @@ void orc_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
   float *al = (float *)malloc(sizeof(float) * ORC_DEP_Q * A);
   orc_temporal_step(c, w, st, x, tout);
   orc_gemv(w->text_linear, bf, V, D, tout, tl);
-  int32_t text_token = (int32_t)orc_argmax(tl, V);
+  int32_t text_token = (int32_t)pick(&st->smp, &st->rng, tl, V, 1);
   /* 6. depformer cycle */
   int32_t audio[ORC_DEP_Q];
-  orc_depformer_cycle(c, w, tout, text_token, forced, al, audio);
+  depformer_cycle(c, w, tout, text_token, forced, al, audio, &st->smp, &st->rng);
   /* 7. advance and self-feed (forced tokens are what the ring records) */
   st->offset += 1;
   int pos = (int)(st->offset % ORC_CT);

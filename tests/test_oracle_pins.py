@@ -289,3 +289,139 @@ def test_threads_do_not_change_bits(tiny):
     oracle.set_threads(oracle.max_threads())
     for k in ("text_logits", "audio_logits", "tout"):
         np.testing.assert_array_equal(outs[0][k], outs[1][k])
+
+
+# ------------------------------------------------------------------ sampling
+XS = _load("xorshift64.json")
+
+
+def test_xorshift_published_sequence():
+    r = oracle.XorShift(XS["seed"])
+    assert [r.next() for _ in range(3)] == XS["outputs"]
+
+
+def test_xorshift_u01_takes_the_top_53_bits():
+    r = oracle.XorShift(XS["seed"])
+    for x in XS["outputs"]:
+        u = r.u01()
+        assert u == (x >> 11) / 2.0 ** 53 and 0.0 <= u < 1.0
+
+
+def _chi2_ok(counts, probs, n):
+    """Pearson chi-square against the expected frequencies, generous 1e-4 tail bound
+    (df <= 7: chi2 < 30)."""
+    exp = np.asarray(probs) * n
+    keep = exp > 0
+    stat = float((((counts - exp) ** 2)[keep] / exp[keep]).sum())
+    return stat < 30.0, stat
+
+
+def test_gumbel_pick_samples_softmax_of_logits_over_temp():
+    # the Gumbel-max property: argmax(l/T + G) is distributed as softmax(l/T)
+    logits = np.array([0.5, -1.0, 2.0, 0.0, 1.0], np.float32)
+    temp = 0.8
+    p = np.exp(logits.astype(np.float64) / temp)
+    p /= p.sum()
+    r = oracle.XorShift(12345)
+    n = 60000
+    counts = np.zeros(5)
+    for _ in range(n):
+        counts[oracle.gumbel_pick(logits, temp, r)] += 1
+    ok, stat = _chi2_ok(counts, p, n)
+    assert ok, (stat, counts / n, p)
+
+
+def test_gumbel_pick_consumes_one_draw_per_logit():
+    logits = np.zeros(37, np.float32)
+    a, b = oracle.XorShift(99), oracle.XorShift(99)
+    oracle.gumbel_pick(logits, 1.0, a)
+    for _ in range(37):
+        b.next()
+    assert a.state == b.state
+
+
+def test_gumbel_pick_tiny_temperature_is_argmax():
+    logits = np.array([0.1, 5.0, -2.0, 4.0], np.float32)
+    assert oracle.gumbel_pick(logits, 1e-6, oracle.XorShift(7)) == 1
+
+
+def test_topk_pick_samples_renormalised_top_k():
+    logits = np.array([0.3, 2.0, -1.0, 1.5, 1.7, -0.5, 0.9, 0.0], np.float32)
+    temp, k = 0.7, 3
+    top = np.argsort(-logits.astype(np.float64), kind="stable")[:k]
+    p = np.zeros(8)
+    p[top] = np.exp((logits[top].astype(np.float64) - logits.max()) / temp)
+    p /= p.sum()
+    r = oracle.XorShift(2024)
+    n = 60000
+    counts = np.zeros(8)
+    for _ in range(n):
+        counts[oracle.topk_pick(logits, temp, k, r)] += 1
+    assert counts[[i for i in range(8) if i not in top]].sum() == 0
+    ok, stat = _chi2_ok(counts, p, n)
+    assert ok, (stat, counts / n, p)
+
+
+def test_topk_pick_consumes_one_draw():
+    a, b = oracle.XorShift(5), oracle.XorShift(5)
+    oracle.topk_pick(np.arange(10, dtype=np.float32), 0.8, 4, a)
+    b.next()
+    assert a.state == b.state
+
+
+def test_topk_k1_is_first_wins_argmax():
+    logits = np.array([1.0, 3.0, 3.0, 2.0], np.float32)
+    for seed in range(1, 20):
+        assert oracle.topk_pick(logits, 0.8, 1, oracle.XorShift(seed)) == 1
+
+
+def test_topk_equal_logits_walk_in_index_order():
+    # two equal logits, k = 2: p = (1/2, 1/2); the draw u picks the lower index when
+    # u <= 1/2 (reading: equal logits in ascending index order)
+    logits = np.array([0.0, 4.0, 4.0, -3.0], np.float32)
+    seen = set()
+    for i in range(1, 40):
+        seed = (i * 0x9E3779B97F4A7C15) & (2 ** 64 - 1)  # spread over all 64 bits
+        u = oracle.XorShift(seed).u01()
+        tok = oracle.topk_pick(logits, 1.0, 2, oracle.XorShift(seed))
+        assert tok == (1 if u <= 0.5 else 2), (seed, u, tok)
+        seen.add(tok)
+    assert seen == {1, 2}
+
+
+@pytest.mark.parametrize("mode,draws", [(oracle.PICK_GREEDY, lambda c: 0),
+                                        (oracle.PICK_TOPK, lambda c: 9),
+                                        (oracle.PICK_GUMBEL,
+                                         lambda c: c.text_card + 8 * c.audio_card)])
+def test_frame_draw_count_per_sampler(tiny, mode, draws):
+    # `pick` runs once for the text token and once per codebook, in that order
+    c, w, o = tiny
+    st = o.new_state()
+    st.set_sampling(mode, seed=77)
+    st.set_sampling(mode, seed=77)
+    ref = oracle.XorShift(77)
+    o.step(st, np.arange(8, dtype=np.int32))
+    for _ in range(draws(c)):
+        ref.next()
+    assert st.rng == (ref.state if mode != oracle.PICK_GREEDY else 77)
+
+
+def test_sampled_step_tokens_follow_pick_on_its_own_logits(tiny):
+    # the frame's text token is the pick over its text logits with the frame-start state
+    c, w, o = tiny
+    for mode in (oracle.PICK_TOPK, oracle.PICK_GUMBEL):
+        st = o.new_state()
+        st.set_sampling(mode, temp=0.9, temp_text=0.6, top_k=5, top_k_text=3, seed=31)
+        r = o.step(st, np.arange(8, dtype=np.int32), trace=True)
+        rng = oracle.XorShift(31)
+        if mode == oracle.PICK_TOPK:
+            tok = oracle.topk_pick(r["text_logits"], 0.6, 3, rng)
+        else:
+            tok = oracle.gumbel_pick(r["text_logits"], 0.6, rng)
+        assert tok == r["own"][0]
+        for cb in range(8):
+            lg = r["audio_logits"][cb]
+            t = (oracle.topk_pick(lg, 0.9, 5, rng) if mode == oracle.PICK_TOPK
+                 else oracle.gumbel_pick(lg, 0.9, rng))
+            assert t == r["own"][1 + cb], (mode, cb)
+        assert rng.state == st.rng
