@@ -272,6 +272,26 @@ rq_status rq_attention_noalloc(int32_t batch, int32_t heads, int32_t head_dim,
                                const void *k, const void *v, const int32_t *positions,
                                float *out, void *cuda_stream);
 
+/* Token picks ("moshi_lm.rs", `Sampling`, `MoshiLm::set_sampling`, `pick`): every frame
+ * picks the text token (temp_text, top_k_text) and then codebooks 0..7 (temp, top_k),
+ * each session from its own xorshift64 state ("moshi_lm.rs", `xorshift_u01`):
+ *   RQ_PICK_GREEDY  first-wins argmax (the default; the parity and benchmark mode);
+ *   RQ_PICK_TOPK    `topk_sample`: the top_k largest logits (taken in descending order,
+ *                   equal logits by ascending index), softmax((l - max) / temp) in f64,
+ *                   one draw per pick; top_k in 1..256;
+ *   RQ_PICK_GUMBEL  `gumbel_full_pick`: argmax of l / temp - ln(-ln u) over the whole
+ *                   vocabulary, one draw per logit.
+ * seeds: host [B], required unless mode is greedy; session b's state becomes
+ * max(seeds[b], 1).  With mode greedy and seeds NULL the states are kept.  Frames
+ * report the picked tokens as their own tokens and feed them back as the argmax would
+ * be.  Waits for the handle's stream and re-captures the frame graph. */
+enum { RQ_PICK_GREEDY = 0, RQ_PICK_TOPK = 1, RQ_PICK_GUMBEL = 2 };
+rq_status rq_set_sampling(rq_handle *h, int32_t mode, float temp, float temp_text,
+                          int32_t top_k, int32_t top_k_text, const uint64_t *seeds);
+
+/* Each session's sampler state after the last frame (host [B]; synchronizes). */
+rq_status rq_get_rng(rq_handle *h, uint64_t *states);
+
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 

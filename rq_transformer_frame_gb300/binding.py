@@ -35,6 +35,7 @@ _CFG_INT_FIELDS = ["batch", "dim", "layers", "heads", "head_dim", "hidden", "con
 
 
 RQ_SCHEDULE_AUTO, RQ_SCHEDULE_GRAPH, RQ_SCHEDULE_PERSISTENT, RQ_SCHEDULE_TENSOR = 0, 1, 2, 3
+RQ_PICK_GREEDY, RQ_PICK_TOPK, RQ_PICK_GUMBEL = 0, 1, 2
 
 
 class RqConfig(C.Structure):
@@ -77,6 +78,8 @@ def load() -> C.CDLL:
     L.rq_get_ring.argtypes = [P, P, P]
     L.rq_set_kv.argtypes = [P, I32, I32, P, P]
     L.rq_launch_op.argtypes = [P, I32, I32, I32, C.POINTER(C.c_double)]
+    L.rq_set_sampling.argtypes = [P, I32, C.c_float, C.c_float, I32, I32, P]
+    L.rq_get_rng.argtypes = [P, P]
     L.rq_frame_kernel_count.argtypes = [P]
     L.rq_frame_kernel_count.restype = I32
     L.rq_schedule.argtypes = [P]
@@ -94,7 +97,7 @@ def load() -> C.CDLL:
     L.rq_attention.restype = C.c_int
     for f in ("rq_create", "rq_reset", "rq_step", "rq_step_forced", "rq_step_device",
               "rq_sync", "rq_get_logits", "rq_get_trace", "rq_get_ring", "rq_set_kv",
-              "rq_launch_op"):
+              "rq_launch_op", "rq_set_sampling", "rq_get_rng"):
         getattr(L, f).restype = C.c_int
     _LIB = L
     return L
@@ -192,6 +195,24 @@ class Decoder:
 
     def sync(self):
         self._check(self.L.rq_sync(self.h))
+
+    def set_sampling(self, mode: int, temp: float = 0.8, temp_text: float = 0.7,
+                     top_k: int = 250, top_k_text: int = 25, seeds=None):
+        """Token picks (rq_set_sampling); defaults are the page's `Sampling` values.
+        seeds: one per session (required unless mode is greedy)."""
+        sd = None
+        if seeds is not None:
+            sd = np.ascontiguousarray(seeds, dtype=np.uint64)
+            assert sd.shape == (self.cfg.batch,)
+        self._check(self.L.rq_set_sampling(self.h, int(mode), float(temp), float(temp_text),
+                                           int(top_k), int(top_k_text),
+                                           None if sd is None else _p(sd)))
+
+    def rng(self) -> np.ndarray:
+        """Each session's sampler state after the last frame."""
+        out = np.zeros(self.cfg.batch, np.uint64)
+        self._check(self.L.rq_get_rng(self.h, _p(out)))
+        return out
 
     def reset(self, session: int = -1):
         self._check(self.L.rq_reset(self.h, int(session)))

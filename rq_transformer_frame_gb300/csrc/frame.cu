@@ -6,6 +6,7 @@
 // `step_ext` steps 1-3 and 7-8; `embed` (ScaledEmbedding).
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 namespace rqk {
 
@@ -105,6 +106,14 @@ __global__ void __launch_bounds__(32) frame_end_kernel(const FrameParams p) {
   if (lane == 0) {
     p.d_has[b] = off1 > kMaxDelay ? 1 : 0;
     p.offsets[b] = off1;
+    // the sampler moves past this frame's draws (one per logit of every Gumbel-max
+    // pick, one per top-k pick)
+    const SampleParams& sp = p.samp;
+    if (sp.mode != SAMPLE_GREEDY) {
+      const uint32_t draws =
+          sp.mode == SAMPLE_GUMBEL ? (uint32_t)sp.V + 8u * (uint32_t)sp.A : 9u;
+      sp.rng[b] = xs_advance(sp.rng[b], draws, sp.jump);
+    }
   }
 }
 

@@ -354,7 +354,7 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
       op.out[row] = y;
-      const unsigned long long k = argmax_key(y, (uint32_t)row);
+      const unsigned long long k = pick_key(P.samp, 0, op.key_index, y, (uint32_t)row);
       best = k > best ? k : best;
     }
     best = warp_max_u64(best);
@@ -636,6 +636,20 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
       const PersOp& op = P.ops[k];
       if (op.type == OPT_ATTN) {
         attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last);
+      } else if (op.type == OPT_TOPK) {
+        // "moshi_lm.rs", `topk_sample` for pick key_index over the logits the previous op
+        // wrote, by CTA 0 (its partial-sum buffer holds the selection's scratch)
+        if (blockIdx.x == 0) {
+          const int pk = op.key_index;
+          const double u = xs_u01(xs_advance(P.samp.rng[0], draws_before(P.samp, pk) + 1u,
+                                             P.samp.jump));
+          TopkShared& S = *reinterpret_cast<TopkShared*>(part);
+          const int tok = topk_pick_block(op.in, pk == 0 ? P.samp.V : P.samp.A,
+                                          pk == 0 ? P.samp.top_k_text : P.samp.top_k,
+                                          pk == 0 ? P.samp.temp_text : P.samp.temp, u, tid,
+                                          kCons, S, SyncNamed<kCons>{});
+          if (tid == 0) P.keys[pk] = argmax_key(__ldcg(op.in + tok), (uint32_t)tok);
+        }
       } else {
         const GemvPlan& pl = P.plans[op.plan];
         int t0, t1;

@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 namespace rqk {
 
@@ -460,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
       out[row] = y;
-      const unsigned long long k = argmax_key(y, (uint32_t)row);
+      const unsigned long long k = pick_key(p.samp, b, p.key_index, y, (uint32_t)row);
       best = k > best ? k : best;
     }
     best = warp_max_u64(best);

@@ -8,6 +8,34 @@
 
 namespace rqk {
 
+// ---------------------------------------------------------------- token picks
+// "moshi_lm.rs", `Sampling` / `pick`: greedy argmax, top-k temperature sampling or
+// full-vocabulary Gumbel-max, driven by one xorshift64 state per session.  Within a
+// frame pick p (0 the text token, 1 + cb codebook cb) draws from a fixed position of the
+// session's stream (Gumbel: one draw per logit, top-k: one draw), so every draw is the
+// frame-start state advanced by a known count (xorshift64 is linear over GF(2): the
+// advance by n is the matrix power M^n, applied from a table of M^(2^k)).
+enum SampleMode : int { SAMPLE_GREEDY = 0, SAMPLE_TOPK = 1, SAMPLE_GUMBEL = 2 };
+constexpr int kXsLevels = 32;  // M^(2^k), k < 32: advances up to 2^32 - 1 draws
+constexpr int kTopKMax = 256;  // largest k of a top-k pick
+struct SampleParams {
+  int mode;              // SampleMode
+  float temp, temp_text;
+  int top_k, top_k_text;
+  int V, A;              // logits of the text pick and of each codebook pick
+  uint64_t* rng;         // [B] sampler state at the start of the frame
+  const uint64_t* jump;  // [kXsLevels][64]: column b of M^(2^k)
+};
+// the table above, computed on the host from the generator's definition
+void xorshift_jump_table(uint64_t* table /*[kXsLevels * 64]*/);
+// one CTA per session: pick p's token from logits [B][n] (row stride ld) by top-k
+// sampling; writes keys[b * 9 + p] (an argmax key of the chosen token)
+cudaError_t launch_topk_pick(const SampleParams& sp, const float* logits, long long ld,
+                             int n, int p, unsigned long long* keys, int B, cudaStream_t s,
+                             bool pdl);
+// the sampler draws one frame consumes
+long long frame_draws(const SampleParams& sp);
+
 // ---------------------------------------------------------------- streaming GEMV
 // y = W x for one weight matrix W [rows][K] streamed once from HBM through a
 // shared-memory ring filled by bulk copies, with a fused prologue (how x is formed)
@@ -80,6 +108,7 @@ struct GemvParams {
   const int* d_in;     // per-step input block (forced tokens / flags)
   int batch;
   uint32_t* status;
+  SampleParams samp;   // EPI_ARGMAX: Gumbel-max scores when samp.mode is SAMPLE_GUMBEL
 };
 
 GemvPlan plan_gemv(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
@@ -163,6 +192,7 @@ struct TcParams {
   const float* ss_in;
   int ss_tiles, rms_K;
   float eps;
+  SampleParams samp;  // EPI_ARGMAX
 };
 
 TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms);
@@ -188,7 +218,7 @@ cudaError_t launch_prep_bf16(const float* in, long long in_bs, const float* alph
 // executed in order by every CTA, a bounded grid barrier between dependent ops, and
 // a per-CTA producer warp that streams the weight tiles of all ops ahead of the
 // consumers through one shared-memory ring.
-enum PersOpType : int { OPT_GEMV = 0, OPT_ATTN = 1 };
+enum PersOpType : int { OPT_GEMV = 0, OPT_ATTN = 1, OPT_TOPK = 2 };  // OPT_TOPK: pick key_index from logits `in`
 
 struct PersOp {
   int type;       // PersOpType
@@ -236,6 +266,7 @@ struct PersParams {
   unsigned int* grid_bar;  // zero at launch
   uint32_t* status;
   unsigned long long* trace;  // [n_ops + 1] op start times (ns), CTA 0 (nullable)
+  SampleParams samp;
 };
 
 GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
@@ -258,6 +289,7 @@ struct TcFrame {
   int32_t* offsets;
   const int32_t* d_in;
   unsigned long long* keys;
+  SampleParams samp;  // token picks (EPI_ARGMAX scores; top-k picks after the heads)
   float* attn_part;
   int* attn_counters;
   int kps, nsplit;
@@ -306,6 +338,7 @@ struct FrameParams {
   float2* rope;         // [B][head_dim/2] (cos, sin) at each session's position (nullable)
   int head_dim;
   float rope_theta;
+  SampleParams samp;    // frame_end advances each session's sampler state
 };
 cudaError_t launch_frame_begin(const FrameParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_frame_end(const FrameParams& p, cudaStream_t s, bool pdl);

@@ -7,11 +7,13 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <cmath>
 #include <vector>
 
 #include "../../include/rq.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 using namespace rqk;
 
@@ -59,6 +61,10 @@ struct rq_handle {
   unsigned long long* trace = nullptr;
   PersParams pers{};
   int pers_grid = 0, pers_smem = 0;
+  // token picks: the sampler configuration and each session's xorshift64 state
+  SampleParams samp{};
+  uint64_t* rng = nullptr;      // [B]
+  uint64_t* xs_jump = nullptr;  // [kXsLevels][64]
   // tensor-core schedule
   TcFrame tcf{};
   std::vector<CUtensorMap> tc_maps;
@@ -148,6 +154,7 @@ GemvParams base_params(const rq_handle* h, const GemvPlan& pl, const void* W) {
   p.d_in = h->d_in;
   p.batch = h->cfg.batch;
   p.status = h->d_status();
+  p.samp = h->samp;
   return p;
 }
 
@@ -345,6 +352,7 @@ FrameParams frame_params(const rq_handle* h) {
   f.rope = h->rope;
   f.head_dim = h->cfg.head_dim;
   f.rope_theta = h->cfg.rope_theta;
+  f.samp = h->samp;
   return f;
 }
 
@@ -370,12 +378,20 @@ cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
     if ((e = op_gate_in(h, l, s, true)) != cudaSuccess) return e;
     if ((e = op_gate_out(h, l, s, true)) != cudaSuccess) return e;
   }
+  const int B = h->cfg.batch, V = h->cfg.text_card, A = h->cfg.audio_card;
+  const bool topk = h->samp.mode == SAMPLE_TOPK;
   if ((e = op_head(h, s, true)) != cudaSuccess) return e;
+  if (topk && (e = launch_topk_pick(h->samp, h->text_logits, V, V, 0, h->keys, B, s, true)) !=
+                  cudaSuccess)
+    return e;
   for (int cb = 0; cb < 8; ++cb) {
     if ((e = op_dep_in(h, cb, s, true)) != cudaSuccess) return e;
     for (int l = 0; l < h->cfg.dlayers; ++l)
       if ((e = op_dlayer(h, cb, l, s, true)) != cudaSuccess) return e;
     if ((e = op_linear(h, cb, s, true)) != cudaSuccess) return e;
+    if (topk && (e = launch_topk_pick(h->samp, h->audio_logits + (size_t)cb * A, 8ll * A, A,
+                                      1 + cb, h->keys, B, s, true)) != cudaSuccess)
+      return e;
   }
   return launch_frame_end(f, s, true);
 }
@@ -389,7 +405,8 @@ void free_all(rq_handle* h) {
   if (h->graph) cudaGraphDestroy(h->graph);
   void* dev[] = {h->ring, h->offsets, h->kcache, h->vcache, h->d_in, h->d_outb, h->x,
                  h->emb_sum, h->q, h->attn, h->u, h->tout, h->text_logits, h->audio_logits,
-                 h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters};
+                 h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters, h->rng,
+                 h->xs_jump};
   for (void* p : dev)
     if (p) cudaFree(p);
   void* tcb[] = {h->rope, h->xb, h->attn_b, h->u_b, h->tout_b, h->dxb, h->do_b, h->du_b,
@@ -516,6 +533,15 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
   hd.out = h->text_logits;
   hd.key_index = 0;
   ops.push_back(hd);
+  auto topk_op = [&](const float* logits, int p) {
+    PersOp t{};
+    t.type = OPT_TOPK;
+    t.in = logits;
+    t.key_index = p;
+    ops.push_back(t);
+  };
+  const bool topk = h->samp.mode == SAMPLE_TOPK;
+  if (topk) topk_op(h->text_logits, 0);
   for (int cb = 0; cb < 8; ++cb) {
     PersOp o = gemv(PRO_PLAIN, EPI_DEPIN, 5, woff(h->w.dep_in, (size_t)cb * DD * D, es));
     o.in = h->tout;
@@ -555,6 +581,7 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
     o.out = h->audio_logits + (size_t)cb * A;
     o.key_index = 1 + cb;
     ops.push_back(o);
+    if (topk) topk_op(h->audio_logits + (size_t)cb * A, 1 + cb);
   }
   return ops;
 }
@@ -620,6 +647,7 @@ rq_status setup_tensor(rq_handle* h) {
   f.offsets = h->offsets;
   f.d_in = h->d_in;
   f.keys = h->keys;
+  f.samp = h->samp;
   f.attn_part = h->part;
   f.attn_counters = h->counters;
   f.kps = h->kps;
@@ -677,6 +705,28 @@ rq_status setup_tensor(rq_handle* h) {
   return RQ_OK;
 }
 
+// the persistent kernel's op table for the current sampler (top-k adds a pick after the
+// text head and after each linears[cb]); the op timeline has room for both tables
+rq_status upload_pers_ops(rq_handle* h) {
+  std::vector<PersOp> ops = pers_ops(h);
+  if (h->d_ops) {
+    cudaFree(h->d_ops);
+    h->d_ops = nullptr;
+  }
+  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->d_ops), ops.size() * sizeof(PersOp)));
+  RQ_CUDA(h, cudaMemcpy(h->d_ops, ops.data(), ops.size() * sizeof(PersOp), cudaMemcpyHostToDevice));
+  if (!h->trace) {
+    const size_t n = ops.size() + (h->samp.mode == SAMPLE_TOPK ? 1 : 10);
+    RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->trace), n * 8));
+    RQ_CUDA(h, cudaMemset(h->trace, 0, n * 8));
+  }
+  h->pers.ops = h->d_ops;
+  h->pers.n_ops = (int)ops.size();
+  h->pers.trace = h->trace;
+  h->pers.samp = h->samp;
+  return RQ_OK;
+}
+
 rq_status setup_schedule(rq_handle* h) {
   const rq_config& c = h->cfg;
   if (c.schedule == RQ_SCHEDULE_TENSOR ||
@@ -708,6 +758,9 @@ rq_status setup_schedule(rq_handle* h) {
       const int pf = (pl[i].max_tiles * pl[i].tile_rows * (pl[i].tpr / 32) + 3) & ~3;
       part = pf > part ? pf : part;
     }
+    // the partial-sum buffer also holds a top-k pick's scratch
+    const int topk_floats = (int)((sizeof(TopkShared) + 15) / 16 * 4);
+    part = part > topk_floats ? part : topk_floats;
     slot = (slot + 127) & ~127;
     ns = kPersSlotBudget / slot;
     if (ns < 2) ns = 2;
@@ -724,17 +777,10 @@ rq_status setup_schedule(rq_handle* h) {
     }
     G = h->num_sms;
   }
-  std::vector<PersOp> ops = pers_ops(h);
-  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->d_ops), ops.size() * sizeof(PersOp)));
-  RQ_CUDA(h, cudaMemcpy(h->d_ops, ops.data(), ops.size() * sizeof(PersOp), cudaMemcpyHostToDevice));
   RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->grid_bar), 256));
   RQ_CUDA(h, cudaMemset(h->grid_bar, 0, 256));
-  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->trace), (ops.size() + 1) * 8));
-  RQ_CUDA(h, cudaMemset(h->trace, 0, (ops.size() + 1) * 8));
   PersParams& P = h->pers;
   P = PersParams{};
-  P.ops = h->d_ops;
-  P.n_ops = (int)ops.size();
   for (int i = 0; i < kPersPlans; ++i) P.plans[i] = pl[i];
   P.slot_bytes = slot;
   P.n_slots = ns;
@@ -759,12 +805,13 @@ rq_status setup_schedule(rq_handle* h) {
   P.nsplit = (c.context + 15) / 16;
   P.grid_bar = h->grid_bar;
   P.status = h->d_status();
-  P.trace = h->trace;
   h->pers_grid = G;
   h->pers_smem = smem;
   h->schedule = RQ_SCHEDULE_PERSISTENT;
-  return RQ_OK;
+  return upload_pers_ops(h);
 }
+
+rq_status capture_frame(rq_handle* h);
 
 rq_status create_impl(rq_handle* h) {
   const rq_config& c = h->cfg;
@@ -801,6 +848,24 @@ rq_status create_impl(rq_handle* h) {
   RQ_ALLOC(h->text_logits, B * V * 4);
   RQ_ALLOC(h->audio_logits, B * 8 * A * 4);
   RQ_ALLOC(h->keys, B * 9 * 8);
+  RQ_ALLOC(h->rng, B * 8);
+  RQ_ALLOC(h->xs_jump, (size_t)kXsLevels * 64 * 8);
+  {  // greedy until rq_set_sampling; the page's `Sampling` defaults otherwise
+    std::vector<uint64_t> table((size_t)kXsLevels * 64), ones(B, 1ull);
+    xorshift_jump_table(table.data());
+    RQ_CUDA(h, cudaMemcpy(h->xs_jump, table.data(), table.size() * 8, cudaMemcpyHostToDevice));
+    RQ_CUDA(h, cudaMemcpy(h->rng, ones.data(), B * 8, cudaMemcpyHostToDevice));
+    h->samp = SampleParams{};
+    h->samp.mode = SAMPLE_GREEDY;
+    h->samp.temp = 0.8f;
+    h->samp.temp_text = 0.7f;
+    h->samp.top_k = 250;
+    h->samp.top_k_text = 25;
+    h->samp.V = (int)V;
+    h->samp.A = (int)A;
+    h->samp.rng = h->rng;
+    h->samp.jump = h->xs_jump;
+  }
   RQ_ALLOC(h->dx, B * DD * 4);
   RQ_ALLOC(h->dq, B * DD * 4);
   RQ_ALLOC(h->dkv, B * DL * 2 * 8 * DD * 4);
@@ -826,7 +891,20 @@ rq_status create_impl(rq_handle* h) {
   RQ_CUDA(h, cudaStreamSynchronize(h->cap));
   h->host_off.assign(B, 0);
   if ((st = setup_schedule(h)) != RQ_OK) return st;
-  // capture one frame as a graph (programmatic edges between consecutive kernels)
+  return capture_frame(h);
+}
+
+// capture one frame as a graph (programmatic edges between consecutive kernels),
+// replacing the previous one
+rq_status capture_frame(rq_handle* h) {
+  if (h->exec) {
+    cudaGraphExecDestroy(h->exec);
+    h->exec = nullptr;
+  }
+  if (h->graph) {
+    cudaGraphDestroy(h->graph);
+    h->graph = nullptr;
+  }
   RQ_CUDA(h, cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
   cudaError_t e = enqueue_frame(h, h->cap);
   cudaGraph_t g = nullptr;
@@ -1162,6 +1240,48 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "rq_launch_op");
   }
+  return RQ_OK;
+}
+
+rq_status rq_set_sampling(rq_handle* h, int32_t mode, float temp, float temp_text,
+                          int32_t top_k, int32_t top_k_text, const uint64_t* seeds) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  if (mode < RQ_PICK_GREEDY || mode > RQ_PICK_GUMBEL)
+    return fail(h, RQ_ERR_ARG, "unknown pick mode");
+  if (mode != RQ_PICK_GREEDY) {
+    if (!(temp > 0.f) || !(temp_text > 0.f) || !std::isfinite(temp) || !std::isfinite(temp_text))
+      return fail(h, RQ_ERR_ARG, "temperatures must be finite and > 0");
+    if (mode == RQ_PICK_TOPK && (top_k < 1 || top_k > kTopKMax || top_k_text < 1 ||
+                                 top_k_text > kTopKMax))
+      return fail(h, RQ_ERR_ARG, "top-k must be in 1..256");
+    if (!seeds) return fail(h, RQ_ERR_ARG, "seeds required");
+  }
+  const int B = h->cfg.batch;
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));  // no frame of the old graph in flight
+  if (seeds) {
+    std::vector<uint64_t> s0(seeds, seeds + B);
+    for (uint64_t& v : s0) v = v > 1 ? v : 1;  // "moshi_lm.rs", `set_sampling`: seed.max(1)
+    RQ_CUDA(h, cudaMemcpy(h->rng, s0.data(), (size_t)B * 8, cudaMemcpyHostToDevice));
+  }
+  h->samp.mode = mode;
+  if (mode != RQ_PICK_GREEDY) {
+    h->samp.temp = temp;
+    h->samp.temp_text = temp_text;
+    h->samp.top_k = top_k;
+    h->samp.top_k_text = top_k_text;
+  }
+  h->tcf.samp = h->samp;
+  if (h->schedule == RQ_SCHEDULE_PERSISTENT && (st = upload_pers_ops(h)) != RQ_OK) return st;
+  return capture_frame(h);
+}
+
+rq_status rq_get_rng(rq_handle* h, uint64_t* states) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  if (!states) return fail(h, RQ_ERR_ARG, "null states");
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  RQ_CUDA(h, cudaMemcpy(states, h->rng, (size_t)h->cfg.batch * 8, cudaMemcpyDeviceToHost));
   return RQ_OK;
 }
 

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "sampling.cuh"
 #include "tc_common.cuh"
 
 namespace rqk {
@@ -197,7 +198,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
       unsigned long long k = 0ull;
       if (valid && b < B) {
         p.out[(size_t)b * p.out_bs + row] = d[i];
-        k = argmax_key(d[i], (uint32_t)row);
+        k = pick_key(p.samp, b, p.key_index, d[i], (uint32_t)row);
       }
       k = warp_max_u64(k);
       if (lane == 0) es.key[q][b] = k;

@@ -33,6 +33,7 @@ TcParams base(const TcFrame& f, const TcPlan& pl, int epi) {
   p.B = f.B;
   p.offsets = f.offsets;
   p.keys = f.keys;
+  p.samp = f.samp;
   p.d_in = f.d_in;
   p.partial = f.part;
   p.tickets = f.tickets;
@@ -239,6 +240,8 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
   // out_norm (kept as the depformer's input) + text head + first-wins argmax
   CK(prep(f, f.x, f.D, f.out_norm, f.tout_b, f.tout, s));
   CK(tc_head(f, s));
+  if (f.samp.mode == SAMPLE_TOPK)
+    CK(launch_topk_pick(f.samp, f.text_logits, f.V, f.V, 0, f.keys, f.B, s, true));
   for (int cb = 0; cb < 8; ++cb) {
     {  // depformer_in[cb](tout) + embedding of the previous token; feeds layer 0's norm
       TcParams p = base(f, f.p_depin, EPI_DEPIN);
@@ -296,6 +299,9 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
       p.key_index = 1 + cb;
       CK(launch_tc(p, f.wm[wi_lin(f, cb)], f.xm_dx, s, true));
     }
+    if (f.samp.mode == SAMPLE_TOPK)
+      CK(launch_topk_pick(f.samp, f.audio_logits + (size_t)cb * A, 8ll * A, A, 1 + cb, f.keys,
+                          f.B, s, true));
   }
 #undef CK
   return cudaSuccess;
