@@ -516,11 +516,16 @@ namespace rqk {
 // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1, for every
 // session: one warp per (session, head), the head's dimensions spread over the lanes;
 // writes the bf16x3 operand of the next tensor-core GEMM (parts nb rows apart).
+// "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1 (<= 8) for
+// session b, head h: one warp, dimension e = lane + 32 i on lane `lane`.  The query, every
+// key and then every value are loaded together (two round trips instead of one per key);
+// the sums run in the same order as a key-by-key loop.
 __global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long long dq_bs,
                                                            const float* dk, const float* dv,
                                                            long long dkv_bs, int n_keys,
                                                            int hd, int DD, uint16_t* out,
                                                            long long out_bs, int nb) {
+  constexpr int kE = 4;  // head_dim <= 128
   const int b = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -528,22 +533,45 @@ __global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long
   const float* K = dk + (size_t)b * dkv_bs + (size_t)h * hd;
   const float* Vv = dv + (size_t)b * dkv_bs + (size_t)h * hd;
   const float scale = 1.0f / sqrtf((float)hd);
+  float qv[kE], kk[8][kE];
+#pragma unroll
+  for (int i = 0; i < kE; ++i) {
+    const int e = lane + 32 * i;
+    qv[i] = e < hd ? q[e] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) kk[j][i] = (j < n_keys && e < hd) ? K[(size_t)j * DD + e] : 0.f;
+  }
   float sc[8];
   float mx = -__int_as_float(0x7f800000);
-  for (int j = 0; j < n_keys; ++j) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
     float d = 0.f;
-    for (int e = lane; e < hd; e += 32) d = fmaf(q[e], K[(size_t)j * DD + e], d);
+#pragma unroll
+    for (int i = 0; i < kE; ++i)
+      if (lane + 32 * i < hd) d = fmaf(qv[i], kk[j][i], d);
     sc[j] = warp_sum(d) * scale;
-    mx = fmaxf(mx, sc[j]);
+    if (j < n_keys) mx = fmaxf(mx, sc[j]);
   }
   float den = 0.f;
-  for (int j = 0; j < n_keys; ++j) {
-    sc[j] = expf(sc[j] - mx);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sc[j] = j < n_keys ? expf(sc[j] - mx) : 0.f;
     den += sc[j];
   }
-  for (int e = lane; e < hd; e += 32) {
+#pragma unroll
+  for (int i = 0; i < kE; ++i) {
+    const int e = lane + 32 * i;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) kk[j][i] = (j < n_keys && e < hd) ? Vv[(size_t)j * DD + e] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kE; ++i) {
+    const int e = lane + 32 * i;
+    if (e >= hd) continue;
     float o = 0.f;
-    for (int j = 0; j < n_keys; ++j) o += sc[j] / den * Vv[(size_t)j * DD + e];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < n_keys) o += sc[j] / den * kk[j][i];
     store_bf16x3(out, (size_t)nb * out_bs, (size_t)b * out_bs + (size_t)h * hd + e, o);
   }
 }
@@ -552,6 +580,7 @@ cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* 
                                  const float* dv, long long dkv_bs, int n_keys, int B,
                                  int heads, int hd, uint16_t* out, long long out_bs, int nb,
                                  cudaStream_t s, bool pdl) {
+  if (n_keys < 1 || n_keys > 8 || hd > 128) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B, (unsigned)heads, 1);
   cfg.blockDim = dim3(32, 1, 1);
