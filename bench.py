@@ -61,9 +61,12 @@ def peaks():
 
 
 KERNEL_SOURCES = {
-    "gemv": ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "common.cuh", "kernels.h"),
-    "frame": ("frame_persistent.cu", "gemv_kernel.cuh", "common.cuh", "kernels.h"),
-    "tc": ("tc_gemm.cu", "tc_epilogue.cuh", "tc_common.cuh", "common.cuh", "kernels.h"),
+    "gemv": ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "sampling.cuh", "common.cuh",
+             "kernels.h"),
+    "frame": ("frame_persistent.cu", "gemv_kernel.cuh", "sampling.cuh", "common.cuh",
+              "kernels.h"),
+    "tc": ("tc_gemm.cu", "tc_epilogue.cuh", "tc_common.cuh", "sampling.cuh", "common.cuh",
+           "kernels.h"),
     "attn": ("attn.cu", "common.cuh", "kernels.h"),
 }
 
