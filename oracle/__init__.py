@@ -80,6 +80,10 @@ def lib():
         L.orc_state_set_sampling.argtypes = [P, I32, F, F, I32, I32, U64]
         L.orc_state_get_rng.argtypes = [P]
         L.orc_state_get_rng.restype = U64
+        L.orc_prime_step.argtypes = [C.POINTER(OrcCfg), C.POINTER(OrcWeights), P, P, P, P]
+        L.orc_replay_step.argtypes = [C.POINTER(OrcCfg), C.POINTER(OrcWeights), P, P]
+        L.orc_state_clone.argtypes = [P]
+        L.orc_state_clone.restype = P
         _LIB = L
     return _LIB
 
@@ -238,6 +242,22 @@ class Oracle:
         r["has_out"] = bool(has[0])
         return r
 
+    def prime_step(self, st: "OracleState", forced, user):
+        """`step_forced`: temporal only, the ring records `forced` [9]; returns the
+        embedding sum the temporal stack consumed."""
+        f = np.ascontiguousarray(forced, dtype=np.int32)
+        u = np.ascontiguousarray(user, dtype=np.int32)
+        assert f.shape == (9,) and u.shape == (8,)
+        e = np.zeros(self.cfg.dim, np.float32)
+        lib().orc_prime_step(C.byref(self.c), C.byref(self.w), st.p, _ptr(f), _ptr(u), _ptr(e))
+        return e
+
+    def replay_step(self, st: "OracleState", x) -> None:
+        """`advance_clock` after the temporal consumed the embedding row x [D]."""
+        x = _f32(x)
+        assert x.shape == (self.cfg.dim,)
+        lib().orc_replay_step(C.byref(self.c), C.byref(self.w), st.p, _ptr(x))
+
     def temporal_step(self, st: "OracleState", x):
         x = _f32(x).copy()
         tout = np.zeros(self.cfg.dim, np.float32)
@@ -280,6 +300,13 @@ class OracleState:
         """`MoshiLm::set_sampling` for this session (defaults: the page's `Sampling`)."""
         lib().orc_state_set_sampling(self.p, int(mode), C.c_float(temp), C.c_float(temp_text),
                                      int(top_k), int(top_k_text), C.c_uint64(seed))
+
+    def clone(self) -> "OracleState":
+        """`MoshiState::snapshot`: an independent copy."""
+        p = lib().orc_state_clone(self.p)
+        if not p:
+            raise MemoryError("oracle state copy failed")
+        return OracleState(p, self.model)
 
     @property
     def rng(self) -> int:

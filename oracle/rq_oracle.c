@@ -536,6 +536,81 @@ void orc_depformer_cycle(const orc_cfg *c, const orc_weights *w, const float *to
   depformer_cycle(c, w, tout, text_token, forced, logits, tokens, NULL, NULL);
 }
 
+/* moshi_lm.rs, `step_ext` steps 1-3 (shared by `step_forced`): write the user stream at
+ * its delays, gather the model input (INITIAL tokens while offset <= delay) and sum the
+ * embeddings, the 16 audio streams in order, then text, into x (zeroed by the caller). */
+static void gather_embed(const orc_cfg *c, const orc_weights *w, orc_state *st,
+                         const int32_t *user, int64_t *input, float *x) {
+  const int D = c->dim, V = c->text_card, A = c->audio_card, bf = c->w_bf16;
+  for (int k = 0; k < ORC_DEP_Q; k++) {
+    int s = ORC_DEP_Q + 1 + k;
+    st->ring[s][(st->offset + ORC_DELAYS[s]) % ORC_CT] = user[k];
+  }
+  for (int s = 0; s < ORC_STREAMS; s++) {
+    if (st->offset <= ORC_DELAYS[s])
+      input[s] = (s == 0) ? (int64_t)V : (int64_t)A;
+    else
+      input[s] = st->ring[s][st->offset % ORC_CT];
+  }
+  for (int k = 0; k < 16; k++)
+    orc_embed(woff(w->emb, bf, (size_t)k * (A + 1) * D), bf, D, input[1 + k], x);
+  orc_embed(w->text_emb, bf, D, input[0], x);
+}
+
+/* moshi_lm.rs, `MoshiLm::step_forced` (the prompt-priming primitive): steps 1-3, the
+ * temporal stack at pos = offset with its output discarded (only its K/V rows stay),
+ * offset + 1, and the ring records the forced [text, agent0..7].  No text head and no
+ * depformer run.  emb_sum: NULL or [D]. */
+void orc_prime_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
+                    const int32_t *forced, const int32_t *user, float *emb_sum) {
+  const int D = c->dim;
+  int64_t input[ORC_STREAMS];
+  float *x = (float *)calloc((size_t)D, sizeof(float));
+  float *tout = (float *)malloc(sizeof(float) * D);
+  gather_embed(c, w, st, user, input, x);
+  if (emb_sum) memcpy(emb_sum, x, sizeof(float) * D);
+  orc_temporal_step(c, w, st, x, tout);
+  st->offset += 1;
+  int pos = (int)(st->offset % ORC_CT);
+  for (int s = 0; s <= ORC_DEP_Q; s++) st->ring[s][pos] = forced[s];
+  free(x);
+  free(tout);
+}
+
+/* moshi_lm.rs, `MoshiState::advance_clock` after the temporal consumed a precomputed
+ * embedding row (the voice-prompt replay): the temporal stack on x at pos = offset, then
+ * offset + 1; the ring is not touched. */
+void orc_replay_step(const orc_cfg *c, const orc_weights *w, orc_state *st, const float *x_in) {
+  const int D = c->dim;
+  float *x = (float *)malloc(sizeof(float) * D);
+  float *tout = (float *)malloc(sizeof(float) * D);
+  memcpy(x, x_in, sizeof(float) * D);
+  orc_temporal_step(c, w, st, x, tout);
+  st->offset += 1;
+  free(x);
+  free(tout);
+}
+
+/* moshi_lm.rs, `MoshiState::snapshot`: an independent copy of the session (ring, offset,
+ * K/V window, sampler). */
+orc_state *orc_state_clone(const orc_state *st) {
+  orc_state *o = (orc_state *)malloc(sizeof(orc_state));
+  if (!o) return NULL;
+  memcpy(o, st, sizeof(orc_state));
+  size_t n = (size_t)st->layers * st->context * st->dim;
+  o->kv_len = (int32_t *)malloc(sizeof(int32_t) * (size_t)st->layers);
+  o->k = (float *)malloc(sizeof(float) * n);
+  o->v = (float *)malloc(sizeof(float) * n);
+  if (!o->kv_len || !o->k || !o->v) {
+    free(o->kv_len); free(o->k); free(o->v); free(o);
+    return NULL;
+  }
+  memcpy(o->kv_len, st->kv_len, sizeof(int32_t) * (size_t)st->layers);
+  memcpy(o->k, st->k, sizeof(float) * n);
+  memcpy(o->v, st->v, sizeof(float) * n);
+  return o;
+}
+
 /* moshi_lm.rs, `step_ext` (steps 1-8) for one session.
  * user: [8] user-audio codes; forced: NULL or [9] = [text, audio0..7].
  * own: [9] the step's own argmax tokens [text, audio0..7].
@@ -548,24 +623,10 @@ void orc_step(const orc_cfg *c, const orc_weights *w, orc_state *st,
               float *emb_sum, float *tout_o, float *text_logits_o,
               float *audio_logits_o) {
   const int D = c->dim, V = c->text_card, A = c->audio_card, bf = c->w_bf16;
-  /* 1. write the user stream at its delays */
-  for (int k = 0; k < ORC_DEP_Q; k++) {
-    int s = ORC_DEP_Q + 1 + k;
-    st->ring[s][(st->offset + ORC_DELAYS[s]) % ORC_CT] = user[k];
-  }
-  /* 2. gather the model input, INITIAL tokens while offset <= delay */
+  /* 1-3. user codes, gathered input, embedding sum */
   int64_t input[ORC_STREAMS];
-  for (int s = 0; s < ORC_STREAMS; s++) {
-    if (st->offset <= ORC_DELAYS[s])
-      input[s] = (s == 0) ? (int64_t)V : (int64_t)A;
-    else
-      input[s] = st->ring[s][st->offset % ORC_CT];
-  }
-  /* 3. embedding sum: the 16 audio streams in order, then text */
   float *x = (float *)calloc((size_t)D, sizeof(float));
-  for (int k = 0; k < 16; k++)
-    orc_embed(woff(w->emb, bf, (size_t)k * (A + 1) * D), bf, D, input[1 + k], x);
-  orc_embed(w->text_emb, bf, D, input[0], x);
+  gather_embed(c, w, st, user, input, x);
   if (emb_sum) memcpy(emb_sum, x, sizeof(float) * D);
   if (input_tokens) memcpy(input_tokens, input, sizeof(input));
   /* 4-5. temporal step and text head */

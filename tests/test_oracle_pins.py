@@ -425,3 +425,59 @@ def test_sampled_step_tokens_follow_pick_on_its_own_logits(tiny):
                  else oracle.gumbel_pick(lg, 0.9, rng))
             assert t == r["own"][1 + cb], (mode, cb)
         assert rng.state == st.rng
+
+
+# ------------------------------------------------------------------ priming, replay, snapshot
+def _prime_inputs(c, t):
+    f = np.array([(5 * t + 2) % c.text_card] + [(3 * cb + 7 * t + 1) % c.audio_card
+                                                 for cb in range(8)], np.int32)
+    return f
+
+
+def test_prime_steps_leave_the_state_of_forced_full_steps(tiny):
+    # `step_forced` (temporal only) and a full step forced with the same tokens differ
+    # only in the outputs they discard: same ring, offset and K/V afterwards
+    c, w, o = tiny
+    a, b = o.new_state(), o.new_state()
+    u = synth.user_tokens(c, 7).numpy()
+    for t in range(6):
+        f = _prime_inputs(c, t)
+        r = o.step(a, u[t], forced=f, trace=True)
+        e = o.prime_step(b, f, u[t])
+        np.testing.assert_array_equal(e, r["emb_sum"])
+    ra, oa = a.ring()
+    rb, ob = b.ring()
+    assert np.array_equal(ra, rb) and oa == ob == 6
+    x, y = o.step(a, u[6], trace=True), o.step(b, u[6], trace=True)
+    for k in ("text_logits", "audio_logits", "tout"):
+        np.testing.assert_array_equal(x[k], y[k])
+
+
+def test_replay_of_the_gathered_embeddings_equals_priming_kv(tiny):
+    c, w, o = tiny
+    a, b = o.new_state(), o.new_state()
+    u = synth.user_tokens(c, 5).numpy()
+    ring0, _ = b.ring()
+    for t in range(5):
+        e = o.prime_step(a, _prime_inputs(c, t), u[t])
+        o.replay_step(b, e)
+    ring1, off = b.ring()
+    assert off == 5 and np.array_equal(ring0, ring1)  # advance_clock: ring untouched
+    probe = np.linspace(-1, 1, c.dim).astype(np.float32)
+    np.testing.assert_array_equal(o.temporal_step(a, probe), o.temporal_step(b, probe))
+
+
+def test_snapshot_copy_is_independent(tiny):
+    c, w, o = tiny
+    a = o.new_state()
+    u = synth.user_tokens(c, 8).numpy()
+    for t in range(3):
+        o.step(a, u[t])
+    snap = a.clone()
+    ra = [o.step(a, u[t], trace=True) for t in range(3, 8)]
+    r0, off0 = snap.ring()
+    assert off0 == 3
+    rs = [o.step(snap, u[t], trace=True) for t in range(3, 8)]
+    for x, y in zip(ra, rs):
+        np.testing.assert_array_equal(x["own"], y["own"])
+        np.testing.assert_array_equal(x["text_logits"], y["text_logits"])
