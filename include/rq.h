@@ -292,6 +292,34 @@ rq_status rq_set_sampling(rq_handle *h, int32_t mode, float temp, float temp_tex
 /* Each session's sampler state after the last frame (host [B]; synchronizes). */
 rq_status rq_get_rng(rq_handle *h, uint64_t *states);
 
+/* Prompt priming ("moshi_lm.rs", `MoshiLm::step_forced`, the prompt-priming primitive):
+ * n teacher-forced steps of session `session`.  Step t writes user[t] ([8], codes in
+ * [-1, A]) at the user streams' delays, gathers and embeds the 17 inputs (INITIAL while
+ * the offset is <= a stream's delay), runs the temporal stack at the session's offset
+ * (only its K/V rows are kept: no text head, no depformer), advances the offset, and the
+ * ring records forced[t] = [text in [0, V), agent codes in [0, A) x 8].  The n positions
+ * run in chunks of up to 64 as the columns of the tensor-core temporal layers (a chunk
+ * never wraps the K/V window).  Needs bf16 weights and dim, hidden, ddim, dhidden
+ * multiples of 64 (else RQ_ERR_UNSUPPORTED); tokens out of range give RQ_ERR_TOKEN
+ * before any state changes.  forced, user: host memory.  Synchronizes the stream. */
+rq_status rq_prime(rq_handle *h, int32_t session, int32_t n, const int32_t *forced,
+                   const int32_t *user);
+
+/* Embedding replay ("moshi_lm.rs", `MoshiState::advance_clock`): the temporal stack
+ * consumes x[t] ([dim] f32, host or device memory) at the session's offset, the offset
+ * advances, the ring is not touched.  Same chunking and requirements as rq_prime. */
+rq_status rq_replay(rq_handle *h, int32_t session, int32_t n, const float *x);
+
+/* Session snapshot ("moshi_lm.rs", `MoshiState::snapshot`): the ring, the offset and the
+ * K/V window of one session (min(offset, context) cache slots per layer, in the K/V
+ * dtype), into a caller buffer of at least rq_snapshot_size bytes (host or device
+ * memory).  rq_restore puts a snapshot of the same model back into any session of the
+ * handle (RQ_ERR_ARG if the layout does not match).  The sampler state is not part of a
+ * session.  Both synchronize the stream. */
+size_t rq_snapshot_size(const rq_handle *h, int32_t session);
+rq_status rq_snapshot(rq_handle *h, int32_t session, void *dst, size_t capacity);
+rq_status rq_restore(rq_handle *h, int32_t session, const void *src, size_t size);
+
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 

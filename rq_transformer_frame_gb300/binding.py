@@ -80,6 +80,12 @@ def load() -> C.CDLL:
     L.rq_launch_op.argtypes = [P, I32, I32, I32, C.POINTER(C.c_double)]
     L.rq_set_sampling.argtypes = [P, I32, C.c_float, C.c_float, I32, I32, P]
     L.rq_get_rng.argtypes = [P, P]
+    L.rq_prime.argtypes = [P, I32, I32, P, P]
+    L.rq_replay.argtypes = [P, I32, I32, P]
+    L.rq_snapshot_size.argtypes = [P, I32]
+    L.rq_snapshot_size.restype = C.c_size_t
+    L.rq_snapshot.argtypes = [P, I32, P, C.c_size_t]
+    L.rq_restore.argtypes = [P, I32, P, C.c_size_t]
     L.rq_frame_kernel_count.argtypes = [P]
     L.rq_frame_kernel_count.restype = I32
     L.rq_schedule.argtypes = [P]
@@ -97,7 +103,8 @@ def load() -> C.CDLL:
     L.rq_attention.restype = C.c_int
     for f in ("rq_create", "rq_reset", "rq_step", "rq_step_forced", "rq_step_device",
               "rq_sync", "rq_get_logits", "rq_get_trace", "rq_get_ring", "rq_set_kv",
-              "rq_launch_op", "rq_set_sampling", "rq_get_rng"):
+              "rq_launch_op", "rq_set_sampling", "rq_get_rng", "rq_prime", "rq_replay",
+              "rq_snapshot", "rq_restore"):
         getattr(L, f).restype = C.c_int
     _LIB = L
     return L
@@ -213,6 +220,34 @@ class Decoder:
         out = np.zeros(self.cfg.batch, np.uint64)
         self._check(self.L.rq_get_rng(self.h, _p(out)))
         return out
+
+    def prime(self, session: int, forced, user):
+        """Teacher-forced prompt steps (rq_prime): forced [n][9], user [n][8] int32."""
+        f = np.ascontiguousarray(forced, dtype=np.int32).reshape(-1, 9)
+        u = np.ascontiguousarray(user, dtype=np.int32).reshape(-1, 8)
+        assert f.shape[0] == u.shape[0]
+        self._check(self.L.rq_prime(self.h, int(session), f.shape[0], _p(f), _p(u)))
+
+    def replay(self, session: int, x):
+        """Embedding replay (rq_replay): x [n][dim] f32 (numpy or a CUDA tensor)."""
+        if isinstance(x, torch.Tensor):
+            assert x.dtype == torch.float32 and x.is_contiguous()
+            n = x.shape[0]
+        else:
+            x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, self.cfg.dim)
+            n = x.shape[0]
+        self._check(self.L.rq_replay(self.h, int(session), int(n), _p(x)))
+
+    def snapshot(self, session: int) -> np.ndarray:
+        """One session's ring, offset and K/V window as bytes (rq_snapshot)."""
+        n = int(self.L.rq_snapshot_size(self.h, int(session)))
+        buf = np.zeros(n, np.uint8)
+        self._check(self.L.rq_snapshot(self.h, int(session), _p(buf), n))
+        return buf
+
+    def restore(self, session: int, snap: np.ndarray):
+        snap = np.ascontiguousarray(snap, dtype=np.uint8)
+        self._check(self.L.rq_restore(self.h, int(session), _p(snap), snap.size))
 
     def reset(self, session: int = -1):
         self._check(self.L.rq_reset(self.h, int(session)))

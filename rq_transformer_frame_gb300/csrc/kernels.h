@@ -304,6 +304,9 @@ struct TcFrame {
   CUtensorMap* wm;  // per weight matrix, see tc_frame_wmap_index
   int n_wm;
   CUtensorMap xm_x, xm_attn, xm_u, xm_tout, xm_dx, xm_do, xm_du;
+  // prefill: the B columns are consecutive positions of ONE session whose K/V region
+  // kcache / vcache point at ([L][C][D]); offsets[b] is column b's position
+  int one_session;
 };
 // plans for every op; returns the split-K scratch floats and ticket count needed
 void tc_frame_plan(TcFrame& f, int num_sms, size_t* part_floats, int* n_tickets);
@@ -312,6 +315,28 @@ cudaError_t tc_frame_maps(TcFrame& f);
 int tc_frame_n_maps(const TcFrame& f);
 // the frame's ops after frame_begin, each launched with a programmatic edge
 cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s);
+// the temporal layers alone (layer-0 norm, then qkv, attention, out, gate_in, gate_out)
+cudaError_t tc_frame_enqueue_temporal(const TcFrame& f, cudaStream_t s);
+
+// ---------------------------------------------------------------- prompt prefill
+// T <= 64 consecutive positions of one session as the columns of the tensor-core
+// temporal layers ("moshi_lm.rs", `MoshiLm::step_forced` priming and the embedding
+// replay of `MoshiState::advance_clock`).
+struct PrefillParams {
+  int session, T, B, D, V, A, head_dim;
+  float rope_theta;
+  int32_t* ring;          // [B][17][3]
+  int32_t* offsets;       // [B]
+  const int32_t* forced;  // [T][9] priming (the ring records them); null: replay
+  const int32_t* user;    // [T][8] priming
+  int32_t* tokens;        // [T][17] scratch: each step's gathered inputs
+  int32_t* pos;           // [T] column positions (written)
+  float2* rope;           // [T][head_dim / 2] (written)
+  const void* emb;        // [16][A+1][D]
+  const void* text_emb;   // [V+1][D]
+  float* x;               // [T][D] priming: the embedding sums (written); replay: given
+};
+cudaError_t launch_prefill_begin(const PrefillParams& p, bool bf16, cudaStream_t s);
 // one op of a temporal layer alone (0 qkv, 1 attention, 2 out_proj, 3 gate_in, 4 gate_out,
 // 5 text head): the GEMM on the operands left by the last frame
 cudaError_t tc_frame_launch_op(const TcFrame& f, int op, int layer, cudaStream_t s);

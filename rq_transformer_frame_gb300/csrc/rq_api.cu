@@ -61,6 +61,12 @@ struct rq_handle {
   unsigned long long* trace = nullptr;
   PersParams pers{};
   int pers_grid = 0, pers_smem = 0;
+  // prompt prefill: up to kPrefillCols positions of one session per tensor-core pass
+  TcFrame pf{};
+  bool pf_ready = false;
+  std::vector<CUtensorMap> pf_maps;
+  std::vector<void*> pf_bufs;  // freed with the handle
+  int32_t *pf_tokens = nullptr, *pf_pos = nullptr, *pf_forced = nullptr, *pf_user = nullptr;
   // token picks: the sampler configuration and each session's xorshift64 state
   SampleParams samp{};
   uint64_t* rng = nullptr;      // [B]
@@ -413,6 +419,8 @@ void free_all(rq_handle* h) {
                  h->tc_part, h->tc_tickets, h->ss_x, h->ss_dx};
   for (void* p : tcb)
     if (p) cudaFree(p);
+  for (void* p : h->pf_bufs)
+    if (p) cudaFree(p);
   if (h->d_ops) cudaFree(h->d_ops);
   if (h->grid_bar) cudaFree(h->grid_bar);
   if (h->trace) cudaFree(h->trace);
@@ -703,6 +711,159 @@ rq_status setup_tensor(rq_handle* h) {
   if (e != cudaSuccess) return cuda_fail(h, e, "tensor map encoding");
   h->schedule = RQ_SCHEDULE_TENSOR;
   return RQ_OK;
+}
+
+constexpr int kPrefillCols = 64;
+
+bool prefill_eligible(const rq_handle* h) {
+  const rq_config& c = h->cfg;
+  return h->wbf && c.dim % 64 == 0 && c.hidden % 64 == 0 && c.ddim % 64 == 0 &&
+         c.dhidden % 64 == 0;
+}
+
+// the prefill frame: the tensor-core temporal layers over kPrefillCols columns, which
+// are consecutive positions of one session (TcFrame::one_session); built on first use
+rq_status setup_prefill(rq_handle* h) {
+  if (h->pf_ready) return RQ_OK;
+  const rq_config& c = h->cfg;
+  TcFrame f{};
+  f.B = kPrefillCols;
+  f.NB = kPrefillCols;
+  f.D = c.dim;
+  f.L = c.layers;
+  f.C = c.context;
+  f.F = c.hidden;
+  f.V = c.text_card;
+  f.A = c.audio_card;
+  f.DD = c.ddim;
+  f.DL = c.dlayers;
+  f.DF = c.dhidden;
+  f.H = c.heads;
+  f.hd = c.head_dim;
+  f.dH = c.dheads;
+  f.dhd = c.dhead_dim;
+  f.eps = c.rms_eps;
+  f.kv_bf16 = h->kvbf ? 1 : 0;
+  const rq_weights& w = h->w;
+  f.in_proj = w.in_proj;
+  f.out_proj = w.out_proj;
+  f.gate_in = w.gate_in;
+  f.gate_out = w.gate_out;
+  f.text_linear = w.text_linear;
+  f.dep_in = w.dep_in;
+  f.dep_text_emb = w.dep_text_emb;
+  f.dep_emb = w.dep_emb;
+  f.d_in_proj = w.d_in_proj;
+  f.d_out_proj = w.d_out_proj;
+  f.d_gate_in = w.d_gate_in;
+  f.d_gate_out = w.d_gate_out;
+  f.linears = w.linears;
+  f.norm1 = w.norm1;
+  f.norm2 = w.norm2;
+  f.out_norm = w.out_norm;
+  f.dnorm1 = w.dnorm1;
+  f.dnorm2 = w.dnorm2;
+  f.d_in = h->d_in;
+  f.keys = h->keys;
+  f.samp = h->samp;
+  f.kps = h->kps;
+  f.nsplit = h->nsplit;
+  f.status = h->d_status();
+  f.one_session = 1;
+  size_t part_floats = 0;
+  int n_tickets = 0;
+  tc_frame_plan(f, h->num_sms, &part_floats, &n_tickets);
+  const size_t NB = kPrefillCols, R = 3 * NB;
+  auto A_ = [&](void** p, size_t bytes, const char* what) -> rq_status {
+    cudaError_t e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+    if (e == cudaSuccess) e = cudaMemset(*p, 0, bytes < 16 ? 16 : bytes);
+    if (e == cudaSuccess) {
+      h->pf_bufs.push_back(*p);
+      return RQ_OK;
+    }
+    h->err = std::string("allocation failed: ") + what + ": " + cudaGetErrorString(e);
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? RQ_ERR_OOM : RQ_ERR_CUDA;
+  };
+  rq_status st;
+#define PF_ALLOC(ptr, bytes) \
+  if ((st = A_(reinterpret_cast<void**>(&(ptr)), (bytes), #ptr)) != RQ_OK) return st;
+  PF_ALLOC(f.x, NB * c.dim * 4);
+  PF_ALLOC(f.q, NB * c.dim * 4);
+  PF_ALLOC(f.attn, NB * c.dim * 4);
+  PF_ALLOC(f.attn_part, NB * c.heads * (size_t)h->nsplit * (c.head_dim + 2) * 4);
+  PF_ALLOC(f.attn_counters, NB * c.heads * 4);
+  PF_ALLOC(f.rope, NB * (c.head_dim / 2) * sizeof(float2));
+  PF_ALLOC(f.xb, R * c.dim * 2);
+  PF_ALLOC(f.attn_b, R * c.dim * 2);
+  PF_ALLOC(f.u_b, R * c.hidden * 2);
+  PF_ALLOC(f.tout_b, R * c.dim * 2);
+  PF_ALLOC(f.dxb, R * c.ddim * 2);
+  PF_ALLOC(f.do_b, R * c.ddim * 2);
+  PF_ALLOC(f.du_b, R * c.dhidden * 2);
+  PF_ALLOC(f.part, part_floats * 4);
+  PF_ALLOC(f.tickets, (size_t)n_tickets * 4);
+  PF_ALLOC(f.ss_x, (size_t)((c.dim + 127) / 128) * NB * 4);
+  PF_ALLOC(f.ss_dx, (size_t)((c.ddim + 127) / 128) * NB * 4);
+  PF_ALLOC(h->pf_tokens, NB * kStreams * 4);
+  PF_ALLOC(h->pf_pos, NB * 4);
+  PF_ALLOC(h->pf_forced, NB * 9 * 4);
+  PF_ALLOC(h->pf_user, NB * 8 * 4);
+#undef PF_ALLOC
+  f.offsets = h->pf_pos;
+  f.n_wm = tc_frame_n_maps(f);
+  h->pf_maps.assign((size_t)f.n_wm, CUtensorMap{});
+  f.wm = h->pf_maps.data();
+  cudaError_t e = tc_configure();
+  if (e != cudaSuccess) return cuda_fail(h, e, "tc_configure");
+  e = tc_frame_maps(f);
+  if (e != cudaSuccess) return cuda_fail(h, e, "tensor map encoding");
+  h->pf = f;
+  h->pf_ready = true;
+  return RQ_OK;
+}
+
+// T prompt steps of one session from the prefill frame's x (replay) or from forced and
+// user codes already in the staging buffers (priming)
+rq_status enqueue_prefill_chunk(rq_handle* h, int session, int T, bool priming) {
+  const rq_config& c = h->cfg;
+  PrefillParams pp{};
+  pp.session = session;
+  pp.T = T;
+  pp.B = c.batch;
+  pp.D = c.dim;
+  pp.V = c.text_card;
+  pp.A = c.audio_card;
+  pp.head_dim = c.head_dim;
+  pp.rope_theta = c.rope_theta;
+  pp.ring = h->ring;
+  pp.offsets = h->offsets;
+  pp.forced = priming ? h->pf_forced : nullptr;
+  pp.user = h->pf_user;
+  pp.tokens = h->pf_tokens;
+  pp.pos = h->pf_pos;
+  pp.rope = h->pf.rope;
+  pp.emb = h->w.emb;
+  pp.text_emb = h->w.text_emb;
+  pp.x = h->pf.x;
+  RQ_CUDA(h, launch_prefill_begin(pp, h->wbf, h->stream));
+  TcFrame f = h->pf;
+  f.B = T;
+  const size_t sess = (size_t)session * c.layers * c.context * c.dim * h->kves;
+  f.kcache = static_cast<char*>(h->kcache) + sess;
+  f.vcache = static_cast<char*>(h->vcache) + sess;
+  RQ_CUDA(h, tc_frame_enqueue_temporal(f, h->stream));
+  h->host_off[session] += T;
+  return RQ_OK;
+}
+
+// positions of the next chunk: up to kPrefillCols, but a chunk of more than one column
+// must not wrap the window (a later column would overwrite a slot an earlier one reads)
+int prefill_chunk(const rq_handle* h, int session, int left) {
+  const int C = h->cfg.context, off = h->host_off[session];
+  int T = left < kPrefillCols ? left : kPrefillCols;
+  if (T > 1 && off + T > C) T = C - off > 1 ? C - off : 1;
+  return T;
 }
 
 // the persistent kernel's op table for the current sampler (top-k adds a pick after the
@@ -1282,6 +1443,144 @@ rq_status rq_get_rng(rq_handle* h, uint64_t* states) {
   if (!states) return fail(h, RQ_ERR_ARG, "null states");
   RQ_CUDA(h, cudaStreamSynchronize(h->stream));
   RQ_CUDA(h, cudaMemcpy(states, h->rng, (size_t)h->cfg.batch * 8, cudaMemcpyDeviceToHost));
+  return RQ_OK;
+}
+
+rq_status rq_prime(rq_handle* h, int32_t session, int32_t n, const int32_t* forced,
+                   const int32_t* user) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (session < 0 || session >= c.batch || n < 0) return fail(h, RQ_ERR_ARG, "bad session or n");
+  if (n == 0) return RQ_OK;
+  if (!forced || !user) return fail(h, RQ_ERR_ARG, "null forced or user codes");
+  if (!prefill_eligible(h))
+    return fail(h, RQ_ERR_UNSUPPORTED, "prefill needs bf16 weights and dim, hidden, ddim, "
+                                       "dhidden multiples of 64");
+  for (int64_t i = 0; i < (int64_t)n * 9; ++i) {  // tokens a frame could have generated
+    const int lim = i % 9 == 0 ? c.text_card : c.audio_card;
+    if (forced[i] < 0 || forced[i] >= lim) return fail(h, RQ_ERR_TOKEN, "forced token out of range");
+  }
+  for (int64_t i = 0; i < (int64_t)n * 8; ++i)
+    if (user[i] < -1 || user[i] > c.audio_card) return fail(h, RQ_ERR_TOKEN, "user code out of range");
+  if ((st = setup_prefill(h)) != RQ_OK) return st;
+  for (int done = 0; done < n;) {
+    const int T = prefill_chunk(h, session, n - done);
+    RQ_CUDA(h, cudaMemcpyAsync(h->pf_forced, forced + (size_t)done * 9, (size_t)T * 9 * 4,
+                               cudaMemcpyHostToDevice, h->stream));
+    RQ_CUDA(h, cudaMemcpyAsync(h->pf_user, user + (size_t)done * 8, (size_t)T * 8 * 4,
+                               cudaMemcpyHostToDevice, h->stream));
+    if ((st = enqueue_prefill_chunk(h, session, T, true)) != RQ_OK) return st;
+    done += T;
+  }
+  return rq_sync(h);
+}
+
+rq_status rq_replay(rq_handle* h, int32_t session, int32_t n, const float* x) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (session < 0 || session >= c.batch || n < 0) return fail(h, RQ_ERR_ARG, "bad session or n");
+  if (n == 0) return RQ_OK;
+  if (!x) return fail(h, RQ_ERR_ARG, "null embedding rows");
+  if (!prefill_eligible(h))
+    return fail(h, RQ_ERR_UNSUPPORTED, "prefill needs bf16 weights and dim, hidden, ddim, "
+                                       "dhidden multiples of 64");
+  if ((st = setup_prefill(h)) != RQ_OK) return st;
+  for (int done = 0; done < n;) {
+    const int T = prefill_chunk(h, session, n - done);
+    RQ_CUDA(h, cudaMemcpyAsync(h->pf.x, x + (size_t)done * c.dim, (size_t)T * c.dim * 4,
+                               cudaMemcpyDefault, h->stream));
+    if ((st = enqueue_prefill_chunk(h, session, T, false)) != RQ_OK) return st;
+    done += T;
+  }
+  return rq_sync(h);
+}
+
+namespace {
+// snapshot layout: this header, then K [L][n][D] and V [L][n][D] in the K/V dtype, where
+// n = min(offset, context) cache slots 0..n-1 (slot p % C holds position p)
+struct SnapHeader {
+  char magic[8];
+  int32_t layers, context, dim, kv_bytes, offset, n;
+  int32_t ring[kStreams * kRing];
+};
+const char kSnapMagic[8] = {'R', 'Q', 'S', 'N', 'A', 'P', '0', '1'};
+
+size_t snap_bytes(const rq_handle* h, int n) {
+  const rq_config& c = h->cfg;
+  return sizeof(SnapHeader) + 2 * (size_t)c.layers * n * c.dim * h->kves;
+}
+}  // namespace
+
+size_t rq_snapshot_size(const rq_handle* h, int32_t session) {
+  if (!h || session < 0 || session >= h->cfg.batch) return 0;
+  const int off = h->host_off[session];
+  return snap_bytes(h, off < h->cfg.context ? off : h->cfg.context);
+}
+
+rq_status rq_snapshot(rq_handle* h, int32_t session, void* dst, size_t capacity) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (session < 0 || session >= c.batch || !dst) return fail(h, RQ_ERR_ARG, "bad session or dst");
+  const int off = h->host_off[session], n = off < c.context ? off : c.context;
+  if (capacity < snap_bytes(h, n)) return fail(h, RQ_ERR_ARG, "snapshot buffer too small");
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  SnapHeader hd{};
+  std::memcpy(hd.magic, kSnapMagic, 8);
+  hd.layers = c.layers;
+  hd.context = c.context;
+  hd.dim = c.dim;
+  hd.kv_bytes = h->kves;
+  hd.offset = off;
+  hd.n = n;
+  RQ_CUDA(h, cudaMemcpy(hd.ring, h->ring + (size_t)session * kStreams * kRing, sizeof(hd.ring),
+                        cudaMemcpyDeviceToHost));
+  RQ_CUDA(h, cudaMemcpy(dst, &hd, sizeof(hd), cudaMemcpyDefault));
+  const size_t rowb = (size_t)c.dim * h->kves, layer = (size_t)c.context * rowb;
+  const size_t sess = (size_t)session * c.layers * layer;
+  char* out = static_cast<char*>(dst) + sizeof(SnapHeader);
+  for (int kv = 0; kv < 2; ++kv) {
+    const char* cache = static_cast<const char*>(kv ? h->vcache : h->kcache) + sess;
+    for (int l = 0; l < c.layers; ++l, out += (size_t)n * rowb)
+      if (n > 0)
+        RQ_CUDA(h, cudaMemcpyAsync(out, cache + (size_t)l * layer, (size_t)n * rowb,
+                                   cudaMemcpyDefault, h->stream));
+  }
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  return RQ_OK;
+}
+
+rq_status rq_restore(rq_handle* h, int32_t session, const void* src, size_t size) {
+  rq_status st = check_usable(h);
+  if (st != RQ_OK) return st;
+  const rq_config& c = h->cfg;
+  if (session < 0 || session >= c.batch || !src || size < sizeof(SnapHeader))
+    return fail(h, RQ_ERR_ARG, "bad session or snapshot");
+  SnapHeader hd{};
+  RQ_CUDA(h, cudaMemcpy(&hd, src, sizeof(hd), cudaMemcpyDefault));
+  if (std::memcmp(hd.magic, kSnapMagic, 8) != 0 || hd.layers != c.layers ||
+      hd.context != c.context || hd.dim != c.dim || hd.kv_bytes != h->kves || hd.offset < 0 ||
+      hd.n != (hd.offset < c.context ? hd.offset : c.context) || size < snap_bytes(h, hd.n))
+    return fail(h, RQ_ERR_ARG, "snapshot does not match this model");
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  const int n = hd.n;
+  const size_t rowb = (size_t)c.dim * h->kves, layer = (size_t)c.context * rowb;
+  const size_t sess = (size_t)session * c.layers * layer;
+  const char* in = static_cast<const char*>(src) + sizeof(SnapHeader);
+  for (int kv = 0; kv < 2; ++kv) {
+    char* cache = static_cast<char*>(kv ? h->vcache : h->kcache) + sess;
+    for (int l = 0; l < c.layers; ++l, in += (size_t)n * rowb)
+      if (n > 0)
+        RQ_CUDA(h, cudaMemcpyAsync(cache + (size_t)l * layer, in, (size_t)n * rowb,
+                                   cudaMemcpyDefault, h->stream));
+  }
+  RQ_CUDA(h, cudaMemcpyAsync(h->ring + (size_t)session * kStreams * kRing, hd.ring,
+                             sizeof(hd.ring), cudaMemcpyHostToDevice, h->stream));
+  RQ_CUDA(h, launch_set_offset(h->offsets, session, hd.offset, h->stream));
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->host_off[session] = hd.offset;
   return RQ_OK;
 }
 

@@ -145,7 +145,7 @@ cudaError_t tc_qkv(const TcFrame& f, int l, cudaStream_t s) {
   p.out_bs = f.D;
   p.kcache = layer_cache(f, f.kcache, l);
   p.vcache = layer_cache(f, f.vcache, l);
-  p.kv_bs = (long long)f.L * f.C * f.D;
+  p.kv_bs = f.one_session ? 0 : (long long)f.L * f.C * f.D;  // columns: sessions or positions
   return launch_tc(p, f.wm[wi_layer(l, 0)], f.xm_x, s, true);
 }
 
@@ -155,9 +155,9 @@ cudaError_t tc_attn(const TcFrame& f, int l, cudaStream_t s) {
   a.q = f.q;
   a.kbase = f.kcache;  // [B][L][C][D]: session b, layer l, slot j is row (b L + l) C + j
   a.vbase = f.vcache;
-  a.rows = (long long)f.B * f.L * f.C;
+  a.rows = (long long)(f.one_session ? 1 : f.B) * f.L * f.C;
   a.row0 = (long long)l * f.C;
-  a.row_bs = (long long)f.L * f.C;
+  a.row_bs = f.one_session ? 0 : (long long)f.L * f.C;
   a.offsets = f.offsets;
   a.part = f.attn_part;
   a.counters = f.attn_counters;
@@ -221,10 +221,7 @@ cudaError_t tc_frame_launch_op(const TcFrame& f, int op, int layer, cudaStream_t
   }
 }
 
-cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
-  const size_t D = f.D, A = f.A, DD = f.DD, DF = f.DF;
-  const long long dkv_bs = (long long)f.DL * 2 * 8 * DD;
-  auto dkv_off = [&](int l, int kv, int j) { return (((size_t)l * 2 + kv) * 8 + j) * DD; };
+cudaError_t tc_frame_enqueue_temporal(const TcFrame& f, cudaStream_t s) {
   cudaError_t e;
 #define CK(call) \
   if ((e = (call)) != cudaSuccess) return e;
@@ -237,6 +234,18 @@ cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
     CK(tc_gin(f, l, s));
     CK(tc_gout(f, l, s));
   }
+#undef CK
+  return cudaSuccess;
+}
+
+cudaError_t tc_frame_enqueue(const TcFrame& f, cudaStream_t s) {
+  const size_t D = f.D, A = f.A, DD = f.DD, DF = f.DF;
+  const long long dkv_bs = (long long)f.DL * 2 * 8 * DD;
+  auto dkv_off = [&](int l, int kv, int j) { return (((size_t)l * 2 + kv) * 8 + j) * DD; };
+  cudaError_t e;
+#define CK(call) \
+  if ((e = (call)) != cudaSuccess) return e;
+  CK(tc_frame_enqueue_temporal(f, s));
   // out_norm (kept as the depformer's input) + text head + first-wins argmax
   CK(prep(f, f.x, f.D, f.out_norm, f.tout_b, f.tout, s));
   CK(tc_head(f, s));
