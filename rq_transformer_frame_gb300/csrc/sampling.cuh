@@ -63,6 +63,8 @@ struct TopkShared {
   unsigned int misc[4];
 };
 
+constexpr int kTkBatch = 8;  // logits loaded per thread before any is used
+
 // f32 total order (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN) as an unsigned key
 __device__ __forceinline__ uint32_t total_key(float v) {
   const uint32_t u = __float_as_uint(v);
@@ -86,9 +88,22 @@ __device__ int topk_pick_block(const float* lg, int n, int k, float temp, double
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += nthr) S.hist[i] = 0u;
     sync();
-    for (int i = tid; i < n; i += nthr) {
-      const uint32_t key = total_key(__ldcg(lg + i));
-      if ((key & mask) == prefix) atomicAdd(&S.hist[(key >> shift) & 255u], 1u);
+    // kTkBatch loads in flight per thread; logits cluster in a few bins, so lanes with
+    // equal bins add once, by their count
+    for (int base = 0; base < n; base += kTkBatch * nthr) {
+      uint32_t key[kTkBatch];
+#pragma unroll
+      for (int j = 0; j < kTkBatch; ++j) {
+        const int i = base + j * nthr + tid;
+        key[j] = i < n ? total_key(__ldcg(lg + i)) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kTkBatch; ++j) {
+        const int i = base + j * nthr + tid;
+        const unsigned bin = (i < n && (key[j] & mask) == prefix) ? (key[j] >> shift) & 255u : 256u;
+        const unsigned same = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && (tid & 31) == __ffs(same) - 1) atomicAdd(&S.hist[bin], __popc(same));
+      }
     }
     sync();
     if (tid == 0) {
@@ -113,12 +128,21 @@ __device__ int topk_pick_block(const float* lg, int n, int k, float temp, double
   if (tid == 0) S.misc[3] = 0u;
   sync();
   const bool all_eq = n_eq == (unsigned)remaining;
-  for (int i = tid; i < n; i += nthr) {
-    const uint32_t key = total_key(__ldcg(lg + i));
-    if (key > T || (all_eq && key == T)) {
-      const unsigned slot = atomicAdd(&S.misc[3], 1u);
-      if (slot < (unsigned)kTopKMax)  // exactly k keys qualify (counted by the passes)
-        S.cand[slot] = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)i);
+  for (int base = 0; base < n; base += kTkBatch * nthr) {
+    uint32_t key[kTkBatch];
+#pragma unroll
+    for (int j = 0; j < kTkBatch; ++j) {
+      const int i = base + j * nthr + tid;
+      key[j] = i < n ? total_key(__ldcg(lg + i)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kTkBatch; ++j) {
+      const int i = base + j * nthr + tid;
+      if (i < n && (key[j] > T || (all_eq && key[j] == T))) {
+        const unsigned slot = atomicAdd(&S.misc[3], 1u);
+        if (slot < (unsigned)kTopKMax)  // exactly k keys qualify (counted by the passes)
+          S.cand[slot] = ((unsigned long long)key[j] << 32) | (0xffffffffu - (uint32_t)i);
+      }
     }
   }
   sync();
@@ -179,13 +203,23 @@ __device__ int topk_pick_block(const float* lg, int n, int k, float temp, double
   const float mx = __uint_as_float(S.misc[1]);
   for (int r = tid; r < k; r += nthr) S.p[r] = exp((double)(((float)S.p[r] - mx) / temp));
   sync();
-  if (tid == 0) {
+  if (tid == 0) {  // the sum in order, then every p_i / sum in parallel
     double sum = 0.0;
     for (int r = 0; r < k; ++r) sum += S.p[r];
+    S.misc[2] = (unsigned)__double2hiint(sum);
+    S.misc[3] = (unsigned)__double2loint(sum);
+  }
+  sync();
+  {
+    const double sum = __hiloint2double((int)S.misc[2], (int)S.misc[3]);
+    for (int r = tid; r < k; r += nthr) S.p[r] = S.p[r] / sum;
+  }
+  sync();
+  if (tid == 0) {
     int tok = (int)(0xffffffffu - (uint32_t)(S.cand[P - k] & 0xffffffffull));
     double left = u;
     for (int r = 0; r < k; ++r) {
-      left -= S.p[r] / sum;
+      left -= S.p[r];
       if (left <= 0.0) {
         tok = (int)(0xffffffffu - (uint32_t)(S.cand[P - 1 - r] & 0xffffffffull));
         break;
