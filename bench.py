@@ -392,7 +392,7 @@ def run_native(args, cfg):
                    "l2": "not flushed: %.1f GB of weights streamed per frame >> 126 MB L2"
                          % (fb[0]["weights"] / 1e9),
                    "arith": ("bf16 weights and K/V, f32 activations and accumulation" +
-                             ("; tensor-core GEMMs on exact bf16x3 activation operands"
+                             ("; tensor-core GEMMs on two-part bf16 activation operands (16 significant bits)"
                               if dec.schedule == binding.RQ_SCHEDULE_TENSOR else ""))},
         "tokens_per_s": 9 * value,
         "hbm": {"bytes_per_frame": bytes_frame, "GB/s": round(bytes_frame / (sec_max / K) / 1e9, 1),

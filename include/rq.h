@@ -92,7 +92,8 @@ typedef struct {
  * K/V dtype); GRAPH launches one streaming-GEMV kernel per op inside a CUDA graph;
  * TENSOR (batch 16..64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
  * runs every linear as one tcgen05 tensor-core GEMM over all sessions, the normalised
- * f32 activations split exactly into three bf16 operand parts, inside a CUDA graph.  AUTO
+ * f32 activations split into two bf16 operand parts (16 significant bits), inside a
+ * CUDA graph.  AUTO
  * picks PERSISTENT when it applies, TENSOR at batch >= 16 when it applies, else GRAPH.
  * Results agree within the parity tolerance. */
 enum {

@@ -8,6 +8,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+
+#include "kernels.h"
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -146,14 +148,17 @@ __device__ __forceinline__ void bar_sync(int id, int n) {
 // hi + mid + lo == x for every normal-range x: a bf16 x bf16 tensor-core product over the
 // three parts, accumulated in f32, sees the f32 operand itself.  Parts go to
 // base[idx], base[ps + idx], base[2 ps + idx].
+// With kOpndParts == 2 only hi and mid = bf16(x - hi) are kept (16 significant bits).
 __device__ __forceinline__ void store_bf16x3(uint16_t* base, size_t ps, size_t idx, float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   const float r1 = x - __bfloat162float(h);
   const __nv_bfloat16 m = __float2bfloat16_rn(r1);
-  const float r2 = r1 - __bfloat162float(m);
   base[idx] = __bfloat16_as_ushort(h);
   base[ps + idx] = __bfloat16_as_ushort(m);
-  base[2 * ps + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+  if (kOpndParts == 3) {
+    const float r2 = r1 - __bfloat162float(m);
+    base[2 * ps + idx] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+  }
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }

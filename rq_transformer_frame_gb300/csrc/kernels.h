@@ -8,6 +8,14 @@
 
 namespace rqk {
 
+// bf16 parts of a tensor-core activation operand: 3 gives the exact f32 value
+// (hi + mid + lo), 2 a 16-significant-bit value (hi + lo)
+#ifndef RQ_OPND_PARTS
+#define RQ_OPND_PARTS 2
+#endif
+constexpr int kOpndParts = RQ_OPND_PARTS;
+static_assert(kOpndParts == 2 || kOpndParts == 3, "two or three bf16 parts");
+
 // ---------------------------------------------------------------- token picks
 // "moshi_lm.rs", `Sampling` / `pick`: greedy argmax, top-k temperature sampling or
 // full-vocabulary Gumbel-max, driven by one xorshift64 state per session.  Within a
@@ -131,8 +139,8 @@ struct AttnParams {
   float* part;          // [B][H][nsplit][hd + 2]
   int* counters;        // [B][H], zero between uses
   float* out;           // [B][D]
-  uint16_t* out_bf16;   // nullable: the same output as a bf16x3 operand [3][nb][D]
-  int nb;               // rows per bf16x3 part
+  uint16_t* out_bf16;   // nullable: the same output as a bf16 operand [parts][nb][D]
+  int nb;               // rows per bf16 part
   int D, H, hd, C, kps, nsplit;
   int batch;
   uint32_t* status;
@@ -164,7 +172,7 @@ struct TcParams {
   int B;              // sessions (<= NB)
   float* out;         // f32 outputs [B][..] (stride out_bs)
   long long out_bs;
-  uint16_t* out_bf16; // EPI_SWIGLU: bf16x3 operand [3][NB][F] (row stride outb_bs)
+  uint16_t* out_bf16; // EPI_SWIGLU: bf16 operand [parts][NB][F] (row stride outb_bs)
   long long outb_bs;
   void* kcache;       // EPI_QKV
   void* vcache;
@@ -183,7 +191,7 @@ struct TcParams {
   int* tickets;       // [tiles_m], zero between uses
   uint32_t* status;
   // fused RMSNorm.  Producer (EPI_RESID / EPI_DEPIN): also write the next GEMM's operand
-  // bf16x3(new value * alpha_next) [3][NB][n_out] (alpha_next null: the value itself) and,
+  // bf16 parts of (new value * alpha_next) [parts][NB][n_out] (alpha_next null: the value) and,
   // when ss_out is set, per-tile sums of squares ss_out[tile][NB] of the new values.
   // Consumer: scale every accumulator column b by 1 / sqrt(eps + sum_t ss_in[t][b] / rms_K).
   uint16_t* opnd;
@@ -207,7 +215,7 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, bool bf16, const void* base, long l
 cudaError_t make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
                            int box_rows);
 
-// prep: X bf16x3 [3][NB][K] = in or RMSNorm(in, alpha) for sessions < B (rows >= B zero);
+// prep: X bf16 parts [parts][NB][K] = in or RMSNorm(in, alpha) for sessions < B (rows >= B zero);
 // side (nullable) receives the f32 normalized rows
 cudaError_t launch_prep_bf16(const float* in, long long in_bs, const float* alpha, float eps,
                              int B, int NB, int K, uint16_t* xb, float* side, long long side_bs,
@@ -273,7 +281,7 @@ GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool eve
                          int grid);
 // ---------------------------------------------------------------- tensor-core frame
 // Everything a batched frame needs between frame_begin and frame_end: the per-op plans,
-// the bf16x3 operand buffers [3][NB][K] (hi, mid, lo parts; rows >= B stay zero) and one
+// the bf16 operand buffers [kOpndParts][NB][K] (hi, mid[, lo] parts; rows >= B stay zero) and one
 // TMA map per weight matrix and per operand buffer.
 struct TcFrame {
   int B, NB, D, L, C, F, V, A, DD, DL, DF, H, hd, dH, dhd;

@@ -677,7 +677,7 @@ rq_status setup_tensor(rq_handle* h) {
 #define TC_ALLOC(ptr, bytes) \
   if ((st = A_(reinterpret_cast<void**>(&(ptr)), (bytes), #ptr)) != RQ_OK) return st;
   TC_ALLOC(h->rope, (size_t)c.batch * (c.head_dim / 2) * sizeof(float2));
-  const size_t R = 3 * NB;  // bf16x3 operands: [3][NB][K]
+  const size_t R = kOpndParts * NB;  // operands: [parts][NB][K]
   TC_ALLOC(h->xb, R * c.dim * 2);
   TC_ALLOC(h->attn_b, R * c.dim * 2);
   TC_ALLOC(h->u_b, R * c.hidden * 2);
@@ -773,7 +773,7 @@ rq_status setup_prefill(rq_handle* h) {
   size_t part_floats = 0;
   int n_tickets = 0;
   tc_frame_plan(f, h->num_sms, &part_floats, &n_tickets);
-  const size_t NB = kPrefillCols, R = 3 * NB;
+  const size_t NB = kPrefillCols, R = kOpndParts * NB;
   auto A_ = [&](void** p, size_t bytes, const char* what) -> rq_status {
     cudaError_t e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
     if (e == cudaSuccess) e = cudaMemset(*p, 0, bytes < 16 ? 16 : bytes);

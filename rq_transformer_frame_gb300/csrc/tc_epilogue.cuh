@@ -212,9 +212,14 @@ __device__ __forceinline__ void load_sum3(uint32_t taddr, int c0, float (&v)[16]
   float h[16], m[16];
   tc::tmem_ld16(taddr + (uint32_t)c0, h);
   tc::tmem_ld16(taddr + (uint32_t)(NB + c0), m);
-  tc::tmem_ld16(taddr + (uint32_t)(2 * NB + c0), v);
+  if (kOpndParts == 3) {
+    tc::tmem_ld16(taddr + (uint32_t)(2 * NB + c0), v);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = (v[i] + m[i]) + h[i];
+    for (int i = 0; i < 16; ++i) v[i] = (v[i] + m[i]) + h[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = m[i] + h[i];
+  }
 }
 
 }  // namespace tcg

@@ -101,7 +101,7 @@ cudaError_t tc_frame_maps(TcFrame& f) {
   cudaError_t e;
 #define MAP(slot, base, rows, cols, box) \
   if ((e = make_tmap_bf16(&(slot), (base), (rows), (cols), (box))) != cudaSuccess) return e;
-  const int R = 3 * f.NB;  // bf16x3 operand rows: hi, mid, lo parts of each session
+  const int R = kOpndParts * f.NB;  // operand rows: the bf16 parts of each session
   MAP(f.xm_x, f.xb, R, D, R);
   MAP(f.xm_attn, f.attn_b, R, D, R);
   MAP(f.xm_u, f.u_b, R, F, R);

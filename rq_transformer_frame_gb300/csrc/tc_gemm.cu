@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ volatile int s_abort;
   __shared__ int s_issued, s_consumed;
   __shared__ EpiShared s_epi;
-  constexpr int kN = 3 * NB;  // MMA columns: the hi, mid and lo parts of each session
+  constexpr int kN = kOpndParts * NB;  // MMA columns: the bf16 parts of each session
   constexpr uint32_t kCols = kN <= 64 ? 64u : (kN <= 128 ? 128u : 256u);  // power of two
   const TcPlan& pl = p.pl;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -335,7 +335,7 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   // two CTAs per SM: ~104 KB of dynamic shared memory each; a grid that fits one CTA per
   // SM (the small depformer GEMMs) takes up to ~200 KB, enough to have all of a CTA's
   // K steps in flight at once
-  const int stage = tcg::kABytes + 3 * NB * tcg::kBK * 2;
+  const int stage = tcg::kABytes + kOpndParts * NB * tcg::kBK * 2;
   const bool one_per_sm = pl.tiles_m * pl.splits <= num_sms;
   // (two per SM: 2 x (dynamic + ~11.5 KB static + 1 KB reserved) within 228 KB)
   int ns = ((one_per_sm ? 190 : 100) * 1024) / stage;  // + 1 KB alignment
