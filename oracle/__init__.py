@@ -80,6 +80,7 @@ def lib():
         L.orc_state_set_sampling.argtypes = [P, I32, F, F, I32, I32, U64]
         L.orc_state_get_rng.argtypes = [P]
         L.orc_state_get_rng.restype = U64
+        L.orc_qn_roundtrip.argtypes = [P, I32, I32, I32, I32]
         L.orc_prime_step.argtypes = [C.POINTER(OrcCfg), C.POINTER(OrcWeights), P, P, P, P]
         L.orc_replay_step.argtypes = [C.POINTER(OrcCfg), C.POINTER(OrcWeights), P, P]
         L.orc_state_clone.argtypes = [P]
@@ -163,6 +164,15 @@ def embed(table, tok: int, acc):
 
 def round_to_bf16(x: float) -> float:
     return float(lib().orc_round_to_bf16(C.c_float(x)))
+
+
+def qn_roundtrip(v, bits: int, group: int = 32):
+    """`qn_roundtrip`: a [rows][cols] f32 copy quantized to `bits` per value with one
+    scale per `group` values of a row, and dequantized."""
+    a = _f32(v).copy()
+    rows, cols = a.shape
+    lib().orc_qn_roundtrip(_ptr(a), rows, cols, int(bits), int(group))
+    return a
 
 
 # sampling ("moshi_lm.rs", `Sampling` / `pick`): modes of a session's sampler

@@ -214,6 +214,37 @@ double orc_xorshift_u01(uint64_t *st) {
   return (double)(x >> 11) / (double)(1ull << 53);
 }
 
+/* moshi_lm.rs, `qn_roundtrip` (the symmetric weight bands): every group of `group`
+ * consecutive values of a row, with mx the first value of the largest magnitude,
+ * d = mx / -(2^(bits-1)), id = 1/d (0 when d == 0), is replaced by
+ * clamp(round(x * id), -(2^(bits-1)), 2^(bits-1) - 1) * d; `round` halves away from zero
+ * as Rust's f32::round.  bits 4 with group 32 is the Q4_0 band (d = max / -8), bits 8 the
+ * q8_0-style band.  In place on an f32 [rows][cols] array. */
+void orc_qn_roundtrip(float *v, int32_t rows, int32_t cols, int32_t bits, int32_t group) {
+  const int32_t qmin = -(1 << (bits - 1)), qmax = (1 << (bits - 1)) - 1;
+  for (int32_t r = 0; r < rows; r++) {
+    for (int32_t b = 0; b < cols / group; b++) {
+      float *blk = v + (size_t)r * cols + (size_t)b * group;
+      float amax = 0.0f, mx = 0.0f;
+      for (int32_t i = 0; i < group; i++) {
+        if (fabsf(blk[i]) > amax) {
+          amax = fabsf(blk[i]);
+          mx = blk[i];
+        }
+      }
+      float d = mx / (float)qmin;
+      float id = d != 0.0f ? 1.0f / d : 0.0f;
+      for (int32_t i = 0; i < group; i++) {
+        float q = roundf(blk[i] * id);
+        int32_t qi = (int32_t)q;
+        if (qi < qmin) qi = qmin;
+        if (qi > qmax) qi = qmax;
+        blk[i] = (float)qi * d;
+      }
+    }
+  }
+}
+
 /* moshi_lm.rs, `gumbel_full_pick`: argmax over i of logits[i] / temp + g_i with
  * g_i = -ln(-ln(u_i)) in f64 (u_i the i-th draw, at least 1e-300) rounded to f32;
  * the first strictly greater score wins.  Consumes n draws. */

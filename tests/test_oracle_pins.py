@@ -481,3 +481,47 @@ def test_snapshot_copy_is_independent(tiny):
     for x, y in zip(ra, rs):
         np.testing.assert_array_equal(x["own"], y["own"])
         np.testing.assert_array_equal(x["text_logits"], y["text_logits"])
+
+
+# ------------------------------------------------------------------ weight bands
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qn_roundtrip_grid_and_error_bound(bits):
+    g = np.random.default_rng(3)
+    v = g.normal(0, 0.02, (5, 96)).astype(np.float32)
+    q = oracle.qn_roundtrip(v, bits)
+    qmin = -(1 << (bits - 1))
+    for r in range(5):
+        for b in range(3):
+            blk, out = v[r, 32 * b:32 * b + 32], q[r, 32 * b:32 * b + 32]
+            mx = blk[np.argmax(np.abs(blk))]
+            d = np.float32(mx / np.float32(qmin))
+            # the largest-magnitude value maps to the end of the grid exactly
+            assert out[np.argmax(np.abs(blk))] == np.float32(qmin) * d
+            k = out / d  # every output is an integer multiple of d in [qmin, qmax]
+            assert np.all(np.abs(k - np.round(k)) < 1e-3)
+            assert k.min() >= qmin - 1e-3 and k.max() <= -qmin - 1 + 1e-3
+            # rounding to the nearest grid point; a value beyond qmax (only possible with the
+            # sign opposite to mx, |x| <= |mx|) is clamped and lands within one step
+            err = np.abs(out - blk)
+            clamped = np.abs(np.round(k) - (-qmin - 1)) < 1e-3
+            assert np.all(err[~clamped] <= np.abs(d) * 0.5 * (1 + 1e-5) + 1e-12)
+            assert np.all(err[clamped] <= np.abs(d) * (1 + 1e-5) + 1e-12)
+
+
+def test_qn_roundtrip_exact_grid_values_and_zero_group():
+    d = np.float32(0.125)
+    ks = np.array([-8, -3, 0, 5, 7, -1, 2, -8] * 4, np.float32)
+    v = (ks * d).reshape(1, 32)
+    np.testing.assert_array_equal(oracle.qn_roundtrip(v, 4), v)  # already on the grid
+    z = np.zeros((2, 32), np.float32)
+    np.testing.assert_array_equal(oracle.qn_roundtrip(z, 4), z)  # d = 0: all zero
+
+
+def test_qn_roundtrip_q4_page_scale():
+    # Q4_0: "d = max / -8" with max the value of largest magnitude, ties to the first
+    v = np.zeros((1, 32), np.float32)
+    v[0, 3], v[0, 9], v[0, 20] = -0.5, 0.5, 0.25
+    q = oracle.qn_roundtrip(v, 4)
+    d = np.float32(-0.5) / np.float32(-8)  # the first of the equal magnitudes, -0.5
+    assert q[0, 3] == -0.5 and q[0, 20] == np.float32(round(0.25 / d)) * d
+    assert q[0, 9] == np.float32(7) * d  # +8 d is past the grid: clamped to qmax
