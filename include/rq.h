@@ -61,7 +61,7 @@ typedef enum {
   RQ_ERR_POISONED = 7     /* an earlier CUDA error or timeout; rq_reset(h, -1) */
 } rq_status;
 
-typedef enum { RQ_F32 = 0, RQ_BF16 = 1 } rq_dtype;
+typedef enum { RQ_F32 = 0, RQ_BF16 = 1, RQ_Q8 = 2, RQ_Q4 = 3 } rq_dtype;
 
 /* Model shape.  Defaults of the Moshi-7B shape ("moshi_lm.rs", consts DIM..DHIDDEN,
  * CARD, TEXT_CARD, RMS_EPS) in brackets. */
@@ -80,7 +80,10 @@ typedef struct {
   int32_t dheads;     /* [16] */
   int32_t dhead_dim;  /* [64]; must be 32, 64 or 128 */
   int32_t dhidden;    /* DF [2816] */
-  int32_t weight_dtype; /* rq_dtype of every matrix and table [RQ_BF16] */
+  int32_t weight_dtype; /* rq_dtype of every matrix and table [RQ_BF16]; with RQ_Q8 or
+                           RQ_Q4 the matrices are in that weight band (rq_quantize) and the
+                           tables are bf16; bands run under RQ_SCHEDULE_GRAPH and need dim,
+                           hidden, ddim, dhidden multiples of 128 */
   int32_t kv_dtype;     /* rq_dtype of the temporal K/V cache [RQ_BF16] */
   float rms_eps;        /* [1e-8], inside the mean */
   float rope_theta;     /* [10000] */
@@ -320,6 +323,21 @@ rq_status rq_replay(rq_handle *h, int32_t session, int32_t n, const float *x);
 size_t rq_snapshot_size(const rq_handle *h, int32_t session);
 rq_status rq_snapshot(rq_handle *h, int32_t session, void *dst, size_t capacity);
 rq_status rq_restore(rq_handle *h, int32_t session, const void *src, size_t size);
+
+/* Weight bands ("moshi_lm.rs", `qn_roundtrip`; Q4_0 as at `q4_roundtrip`): every 32
+ * consecutive values of a matrix row share one f32 scale d = mx / -(2^(bits-1)), mx the
+ * first value of the largest magnitude in the group; value i is stored as the integer
+ * q_i = clamp(round(x_i / d)) in [-2^(bits-1), 2^(bits-1) - 1] (round halves away from
+ * zero; q = 0 where d = 0) and stands for q_i * d.  A row of `cols` values is its codes
+ * followed by its cols/32 scales: RQ_Q8 one two's-complement byte per value, RQ_Q4 16
+ * bytes per group, byte i = (q_i + 8) | (q_(i+16) + 8) << 4.  Stacked weight arrays keep
+ * their row order (rq_weights), each row in this layout.
+ * rq_band_row_bytes: bytes of one stored row (0 if cols is not a positive multiple of
+ * 32).  rq_quantize: rows x cols values (src_dtype RQ_F32 or RQ_BF16, device memory)
+ * into dst (device, rows * rq_band_row_bytes bytes), enqueued on cuda_stream. */
+size_t rq_band_row_bytes(int32_t dtype, int32_t cols);
+rq_status rq_quantize(int32_t dtype, const void *src, int32_t src_dtype, int64_t rows,
+                      int32_t cols, void *dst, void *cuda_stream);
 
 /* Number of kernel launches in one frame (the captured graph's kernel nodes). */
 int32_t rq_frame_kernel_count(const rq_handle *h);

@@ -36,6 +36,10 @@ _CFG_INT_FIELDS = ["batch", "dim", "layers", "heads", "head_dim", "hidden", "con
 
 RQ_SCHEDULE_AUTO, RQ_SCHEDULE_GRAPH, RQ_SCHEDULE_PERSISTENT, RQ_SCHEDULE_TENSOR = 0, 1, 2, 3
 RQ_PICK_GREEDY, RQ_PICK_TOPK, RQ_PICK_GUMBEL = 0, 1, 2
+RQ_F32, RQ_BF16, RQ_Q8, RQ_Q4 = 0, 1, 2, 3
+# stacked weight matrices (the weight bands quantize these; tables and alphas stay)
+MATRIX_FIELDS = ("in_proj", "out_proj", "gate_in", "gate_out", "text_linear", "dep_in",
+                 "d_in_proj", "d_out_proj", "d_gate_in", "d_gate_out", "linears")
 
 
 class RqConfig(C.Structure):
@@ -80,6 +84,10 @@ def load() -> C.CDLL:
     L.rq_launch_op.argtypes = [P, I32, I32, I32, C.POINTER(C.c_double)]
     L.rq_set_sampling.argtypes = [P, I32, C.c_float, C.c_float, I32, I32, P]
     L.rq_get_rng.argtypes = [P, P]
+    L.rq_band_row_bytes.argtypes = [I32, I32]
+    L.rq_band_row_bytes.restype = C.c_size_t
+    L.rq_quantize.argtypes = [I32, P, I32, C.c_int64, I32, P, P]
+    L.rq_quantize.restype = C.c_int
     L.rq_prime.argtypes = [P, I32, I32, P, P]
     L.rq_replay.argtypes = [P, I32, I32, P]
     L.rq_snapshot_size.argtypes = [P, I32]
@@ -114,7 +122,7 @@ def make_config(cfg: RQConfig, schedule: int = RQ_SCHEDULE_AUTO) -> RqConfig:
     c = RqConfig()
     for n in _CFG_INT_FIELDS:
         if n == "weight_dtype":
-            v = RQ_BF16 if cfg.weight_dtype == "bf16" else RQ_F32
+            v = {"bf16": RQ_BF16, "q8": RQ_Q8, "q4": RQ_Q4}.get(cfg.weight_dtype, RQ_F32)
         elif n == "kv_dtype":
             v = RQ_BF16 if cfg.kv_dtype == "bf16" else RQ_F32
         else:
@@ -129,6 +137,30 @@ def make_config(cfg: RQConfig, schedule: int = RQ_SCHEDULE_AUTO) -> RqConfig:
 def upload_weights(host: dict, device="cuda") -> dict:
     """Copy host weight tensors (synth.make_weights) to contiguous device tensors."""
     return {k: v.to(device, non_blocking=False).contiguous() for k, v in host.items()}
+
+
+def quantize(t: torch.Tensor, dtype: int, stream=None) -> torch.Tensor:
+    """rq_quantize: a CUDA f32 / bf16 tensor [..., cols] into weight-band rows (uint8
+    [rows * row_bytes]); cols a multiple of 32."""
+    L = load()
+    assert t.is_cuda and t.is_contiguous() and t.dtype in (torch.float32, torch.bfloat16)
+    cols = int(t.shape[-1])
+    rows = t.numel() // cols
+    rb = int(L.rq_band_row_bytes(int(dtype), cols))
+    if rb == 0:
+        raise ValueError("cols must be a positive multiple of 32")
+    out = torch.empty(rows * rb, dtype=torch.uint8, device=t.device)
+    st = stream if stream is not None else torch.cuda.current_stream(t.device)
+    rc = L.rq_quantize(int(dtype), t.data_ptr(), RQ_BF16 if t.dtype == torch.bfloat16 else RQ_F32,
+                       rows, cols, out.data_ptr(), C.c_void_p(st.cuda_stream))
+    if rc != RQ_OK:
+        raise RQError(rc, "rq_quantize failed")
+    return out
+
+
+def quantize_weights(weights: dict, dtype: int) -> dict:
+    """Device weights (bf16 / f32) with every matrix replaced by its weight-band rows."""
+    return {k: (quantize(v, dtype) if k in MATRIX_FIELDS else v) for k, v in weights.items()}
 
 
 def _p(t):

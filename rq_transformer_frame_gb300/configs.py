@@ -28,7 +28,7 @@ class RQConfig:
     dheads: int
     dhead_dim: int
     dhidden: int
-    weight_dtype: str        # "f32" or "bf16"
+    weight_dtype: str        # "f32", "bf16", or a weight band "q8" / "q4" (bf16 tables)
     kv_dtype: str            # "f32" or "bf16"
     batch: int = 1
     frames: int = 32

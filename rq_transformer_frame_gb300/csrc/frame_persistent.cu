@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
               mbar_arrive_expect_tx(&full[s], 2u * bytes);
               bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
               bulk_g2s(dst + (size_t)opt * row_bytes,
-                       W + (size_t)op.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes,
+                       W + (size_t)op.w_half + (size_t)r0 * row_bytes, bytes,
                        &full[s], pol);
             } else {
               const uint32_t bytes = (uint32_t)nv * row_bytes;

@@ -1,5 +1,5 @@
 // gemv.cu -- host side of the streaming GEMV: tile plan and dispatch to the kernel
-// instantiations compiled in gemv_bf16.cu / gemv_f32.cu.
+// instantiations compiled in gemv_bf16.cu / gemv_f32.cu / gemv_band.cu.
 #include "kernels.h"
 
 #ifndef RQ_GEMV_STAGE_BUDGET
@@ -31,19 +31,24 @@ static int nch_bucket(int n) {
   return 0;  // unsupported
 }
 
-GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int num_sms) {
+GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int num_sms,
+                   int band) {
   GemvPlan pl{};
   pl.n_out = n_out;
   pl.K = K;
-  const int V = 16 / es;
+  // values per 16-byte chunk: 4 f32, 8 bf16, 16 q8 codes, 32 q4 codes
+  const int V = band == BAND_Q8 ? 16 : (band == BAND_Q4 ? 32 : 16 / es);
   const int CC = K / V;
   int tpr = kGemvConsumers;
   while (tpr > 32 && tpr > CC) tpr >>= 1;
   const int ng = kGemvConsumers / tpr;
   pl.nch = nch_bucket((CC + tpr - 1) / tpr);
-  pl.rg = pl.nch <= 2 ? 2 : 1;
+  // rows per thread group and tile: two while a thread's x fits in 32 values (bands) or
+  // 2 chunks (f32 / bf16)
+  pl.rg = band == BAND_NONE ? (pl.nch <= 2 ? 2 : 1) : (V * pl.nch <= 32 ? 2 : 1);
+  if (band != BAND_NONE && pl.nch > 3) pl.nch = 0;      // x in registers: <= 96 values
   if ((paired || even_rows) && ((ng * pl.rg) & 1)) pl.nch = 0;
-  const int row_bytes = K * es;
+  const int row_bytes = (int)band_row_bytes(band, es, K);
   pl.tpr = tpr;
   pl.tile_rows = ng * pl.rg;
   const int out_per_tile = paired ? pl.tile_rows / 2 : pl.tile_rows;
@@ -72,16 +77,23 @@ int gemv_chunks_per_thread(const GemvPlan& pl, int) {
 // Raise the dynamic shared-memory limit of every instantiation once per device,
 // before any launch is captured into a graph.
 cudaError_t gemv_configure_all() {
-  cudaError_t e = gemv_configure<uint16_t>(kMaxDynSmem);
-  cudaError_t f = gemv_configure<float>(kMaxDynSmem);
-  return e != cudaSuccess ? e : f;
+  cudaError_t e[4] = {gemv_configure<uint16_t>(kMaxDynSmem), gemv_configure<float>(kMaxDynSmem),
+                      gemv_configure<q8_t>(kMaxDynSmem), gemv_configure<q4_t>(kMaxDynSmem)};
+  for (cudaError_t x : e)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
 }
 
-cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
+cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, int wtype, int batch,
                         cudaStream_t s, bool pdl) {
   if (p.pl.smem > kMaxDynSmem || p.pl.nch == 0) return cudaErrorInvalidValue;
-  return bf16 ? gemv_dispatch<uint16_t>(p, pro, epi, batch, s, pdl)
-              : gemv_dispatch<float>(p, pro, epi, batch, s, pdl);
+  switch (wtype) {
+    case 0: return gemv_dispatch<float>(p, pro, epi, batch, s, pdl);
+    case 1: return gemv_dispatch<uint16_t>(p, pro, epi, batch, s, pdl);
+    case BAND_Q8: return gemv_dispatch<q8_t>(p, pro, epi, batch, s, pdl);
+    case BAND_Q4: return gemv_dispatch<q4_t>(p, pro, epi, batch, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace rqk

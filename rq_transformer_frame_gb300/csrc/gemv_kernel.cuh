@@ -36,6 +36,9 @@ struct Chunk;
 template <>
 struct Chunk<uint16_t> {  // bf16 bit patterns
   static constexpr int V = 8;
+  static constexpr bool kBand = false;
+  using Table = uint16_t;
+  static __host__ __device__ size_t row_bytes(int K) { return (size_t)K * 2; }
   static __device__ __forceinline__ float dot(const uint4 w, const float (&x)[8], float acc) {
     acc = fmaf(bf16lo(w.x), x[0], acc);
     acc = fmaf(bf16hi(w.x), x[1], acc);
@@ -66,6 +69,9 @@ struct Chunk<uint16_t> {  // bf16 bit patterns
 template <>
 struct Chunk<float> {
   static constexpr int V = 4;
+  static constexpr bool kBand = false;
+  using Table = float;
+  static __host__ __device__ size_t row_bytes(int K) { return (size_t)K * 4; }
   static __device__ __forceinline__ float dot(const uint4 w, const float (&x)[4], float acc) {
     acc = fmaf(__uint_as_float(w.x), x[0], acc);
     acc = fmaf(__uint_as_float(w.y), x[1], acc);
@@ -82,6 +88,58 @@ struct Chunk<float> {
   }
   static __device__ __forceinline__ float elem(const void* base, size_t i) {
     return static_cast<const float*>(base)[i];
+  }
+};
+
+// Weight bands (kernels.h: codes, then one f32 scale per 32 values of the row).  Value i
+// is (float)q_i * d, multiplied with x_i as the dequantized weight would be; the tables
+// of a band model stay bf16.
+template <>
+struct Chunk<q8_t> {
+  static constexpr int V = 16;  // 16 one-byte codes per 16-byte chunk: half a group
+  static constexpr bool kBand = true;
+  using Table = uint16_t;
+  static __host__ __device__ size_t row_bytes(int K) { return band_row_bytes(BAND_Q8, 1, K); }
+  static __device__ __forceinline__ size_t scale_off(int K, int c) {
+    return (size_t)K + (size_t)(c >> 1) * 4;
+  }
+  static __device__ __forceinline__ void dot2s(const uint4 w, float d, const float (&x)[16],
+                                               float& a, float& b) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float q = (float)((int32_t)(u[k] << (24 - 8 * j)) >> 24);
+        if (j & 1)
+          b = fmaf(q * d, x[4 * k + j], b);
+        else
+          a = fmaf(q * d, x[4 * k + j], a);
+      }
+  }
+};
+
+template <>
+struct Chunk<q4_t> {
+  static constexpr int V = 32;  // one group: byte i holds values i and i + 16
+  static constexpr bool kBand = true;
+  using Table = uint16_t;
+  static __host__ __device__ size_t row_bytes(int K) { return band_row_bytes(BAND_Q4, 1, K); }
+  static __device__ __forceinline__ size_t scale_off(int K, int c) {
+    return (size_t)K / 2 + (size_t)c * 4;
+  }
+  static __device__ __forceinline__ void dot2s(const uint4 w, float d, const float (&x)[32],
+                                               float& a, float& b) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (u[k] >> (8 * j)) & 0xffu;
+        const int i = 4 * k + j;
+        a = fmaf((float)((int)(byte & 15u) - 8) * d, x[i], a);
+        b = fmaf((float)((int)(byte >> 4) - 8) * d, x[i + 16], b);
+      }
   }
 };
 
@@ -102,10 +160,10 @@ struct GemvShape {
 };
 
 template <typename WT, int PRO, int EPI, int NCH>
-__global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, Chunk<WT>::kBand ? 2 : GemvShape<NCH>::MIN_BLOCKS)
     gemv_kernel(const GemvParams p) {
   constexpr int V = Chunk<WT>::V;
-  constexpr int RG = GemvShape<NCH>::RG;
+  constexpr int RG = Chunk<WT>::kBand ? (V * NCH <= 32 ? 2 : 1) : GemvShape<NCH>::RG;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_red[kConsumers / 32];
   __shared__ float s_att[kMaxAttPairs];
@@ -121,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
   const int t1 = (int)(((long long)pl.tiles * (blockIdx.x + 1)) / G);
   const int nt = t1 - t0;
   const int K = pl.K;
-  const uint32_t row_bytes = (uint32_t)K * (uint32_t)sizeof(WT);
+  const uint32_t row_bytes = (uint32_t)Chunk<WT>::row_bytes(K);
   const uint32_t tile_bytes = row_bytes * (uint32_t)pl.tile_rows;
   const int NS = pl.n_stages;
   const int wpg = pl.tpr >> 5;
@@ -169,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
           mbar_arrive_expect_tx(&full[s], 2u * bytes);
           bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
           bulk_g2s(dst + (size_t)out_per_tile * row_bytes,
-                   W + (size_t)p.w_half * sizeof(WT) + (size_t)r0 * row_bytes, bytes, &full[s],
+                   W + (size_t)p.w_half + (size_t)r0 * row_bytes, bytes, &full[s],
                    pol);
         } else {
           mbar_arrive_expect_tx(&full[s], bytes);
@@ -327,7 +385,17 @@ __global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
 #pragma unroll
       for (int j = 0; j < NCH; ++j)
 #pragma unroll
-        for (int r = 0; r < RG; ++r) Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
+        for (int r = 0; r < RG; ++r) {
+          if constexpr (Chunk<WT>::kBand) {
+            const int c = tig + j * pl.tpr;
+            const float d = (c < CC) ? *reinterpret_cast<const float*>(
+                                           row0 + (size_t)r * row_bytes + Chunk<WT>::scale_off(K, c))
+                                     : 0.f;
+            Chunk<WT>::dot2s(w[j][r], d, xr[j], acc[r][0], acc[r][1]);
+          } else {
+            Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
+          }
+        }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
       float* pp = part + (size_t)(i * pl.tile_rows + g * RG) * wpg + (warp % wpg);
@@ -392,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, GemvShape<NCH>::MIN_BLOCKS)
       if (EPI == EPI_DEPIN) {
         // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
         if (prev != -1)
-          out[row] = y + Chunk<WT>::elem(p.emb, (size_t)max(prev, 0) * pl.n_out + row);
+          out[row] = y + Chunk<typename Chunk<WT>::Table>::elem(
+                             p.emb, (size_t)max(prev, 0) * pl.n_out + row);
         else
           out[row] = y;
       }

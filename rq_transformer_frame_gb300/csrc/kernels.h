@@ -16,6 +16,25 @@ namespace rqk {
 constexpr int kOpndParts = RQ_OPND_PARTS;
 static_assert(kOpndParts == 2 || kOpndParts == 3, "two or three bf16 parts");
 
+// ---------------------------------------------------------------- weight bands
+// "moshi_lm.rs", `qn_roundtrip` (Q4_0: d = max / -8): every 32 consecutive values of a
+// matrix row share one f32 scale d; value i is q_i * d with q_i an integer in
+// [-2^(bits-1), 2^(bits-1) - 1].  A row of K values is stored as its codes followed by
+// its K/32 scales: q8 one two's-complement byte per value (K bytes); q4 16 bytes per
+// group, byte i = (q_i + 8) | (q_(i+16) + 8) << 4 (the Q4_0 layout, K/2 bytes).
+struct q8_t {};
+struct q4_t {};
+enum WeightBand : int { BAND_NONE = 0, BAND_Q8 = 8, BAND_Q4 = 4 };
+// bytes of one stored row of K values (K a multiple of 32); es: 4 f32, 2 bf16
+__host__ __device__ inline size_t band_row_bytes(int band, int es, long long K) {
+  if (band == BAND_Q8) return (size_t)K + (size_t)K / 8;
+  if (band == BAND_Q4) return (size_t)K / 2 + (size_t)K / 8;
+  return (size_t)K * es;
+}
+// quantize f32 or bf16 rows [rows][cols] (cols a multiple of 32) into the band layout
+cudaError_t launch_quantize_band(int band, const void* src, bool src_bf16, long long rows,
+                                 int cols, void* dst, cudaStream_t s);
+
 // ---------------------------------------------------------------- token picks
 // "moshi_lm.rs", `Sampling` / `pick`: greedy argmax, top-k temperature sampling or
 // full-vocabulary Gumbel-max, driven by one xorshift64 state per session.  Within a
@@ -82,7 +101,7 @@ struct GemvPlan {
 
 struct GemvParams {
   const void* W;
-  long long w_half;  // SWIGLU: element offset of the multiplier half
+  long long w_half;  // SWIGLU: byte offset of the multiplier half
   GemvPlan pl;
   // prologue
   const float* in;
@@ -120,12 +139,13 @@ struct GemvParams {
 };
 
 GemvPlan plan_gemv(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
-                   int num_sms);
+                   int num_sms, int band = BAND_NONE);
 int gemv_chunks_per_thread(const GemvPlan& pl, int elem_bytes);
 cudaError_t gemv_configure_all();
 constexpr int kGemvMaxChunks = 6;  // 16-byte chunks of x per thread
 constexpr int kGemvConsumers = 256;  // consumer threads of a GEMV CTA (+1 producer warp)
-cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, bool bf16, int batch,
+// wtype: 0 f32, 1 bf16, BAND_Q8, BAND_Q4 (matrix storage)
+cudaError_t launch_gemv(const GemvParams& p, int pro, int epi, int wtype, int batch,
                         cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- decode attention
@@ -233,7 +253,7 @@ struct PersOp {
   int pro, epi;   // GEMV prologue / epilogue (GemvPro / GemvEpi)
   int plan;       // index into PersParams::plans
   const void* W;  // weights of this op
-  long long w_half;
+  long long w_half;  // SWIGLU: byte offset of the multiplier half
   const float* in;      // prologue input (PRO_DATTN: the query)
   const float* alpha;
   float* side_out;

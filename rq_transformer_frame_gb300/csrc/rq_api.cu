@@ -28,7 +28,9 @@ struct rq_handle {
   cudaStream_t cap = nullptr;     // private stream used for graph capture
   int device = 0, num_sms = 0;
   bool wbf = false, kvbf = false;
-  int wes = 4, kves = 4;
+  int wes = 4, kves = 4;  // element bytes of the tables (and of f32 / bf16 matrices), of K/V
+  int band = BAND_NONE;   // matrices in a weight band (their tables are then bf16)
+  int wtype = 0;          // matrix storage for launch_gemv: 0 f32, 1 bf16, BAND_Q8, BAND_Q4
   IoLayout io{1};
   // device state
   int32_t* ring = nullptr;
@@ -114,6 +116,11 @@ rq_status cuda_fail(rq_handle* h, cudaError_t e, const char* where) {
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // elements -> byte offset into a weight array
+// the matrix that follows `rows_before` rows of K values in a stacked weight array
+const void* mat(const rq_handle* h, const void* base, size_t rows_before, long long K) {
+  return static_cast<const char*>(base) + rows_before * band_row_bytes(h->band, h->wes, K);
+}
+
 const void* woff(const void* base, size_t elems, int es) {
   return static_cast<const char*>(base) + elems * (size_t)es;
 }
@@ -131,9 +138,13 @@ rq_status validate_config(const rq_config* c, std::string* why) {
   if (c->dheads * c->dhead_dim != c->ddim) return bad("ddim != dheads * dhead_dim");
   if (!hd_ok(c->head_dim) || !hd_ok(c->dhead_dim)) return uns("head dims must be 32, 64 or 128");
   if (c->dheads > 32) return uns("at most 32 depformer heads");
-  if ((c->weight_dtype != RQ_F32 && c->weight_dtype != RQ_BF16) ||
+  if ((c->weight_dtype != RQ_F32 && c->weight_dtype != RQ_BF16 && c->weight_dtype != RQ_Q8 &&
+       c->weight_dtype != RQ_Q4) ||
       (c->kv_dtype != RQ_F32 && c->kv_dtype != RQ_BF16))
-    return bad("dtype must be RQ_F32 or RQ_BF16");
+    return bad("weight_dtype must be RQ_F32, RQ_BF16, RQ_Q8 or RQ_Q4; kv_dtype RQ_F32 or RQ_BF16");
+  if ((c->weight_dtype == RQ_Q8 || c->weight_dtype == RQ_Q4) &&
+      (c->dim % 128 || c->hidden % 128 || c->ddim % 128 || c->dhidden % 128))
+    return uns("weight bands need dim, hidden, ddim and dhidden multiples of 128");
   if (c->dim % 8 || c->hidden % 8 || c->ddim % 8 || c->dhidden % 8)
     return uns("dim, hidden, ddim and dhidden must be multiples of 8");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
@@ -168,7 +179,7 @@ GemvParams base_params(const rq_handle* h, const GemvPlan& pl, const void* W) {
 cudaError_t op_qkv(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const rq_config& c = h->cfg;
   const size_t D = c.dim, C = c.context, L = c.layers;
-  GemvParams p = base_params(h, h->p_qkv, woff(h->w.in_proj, (size_t)l * 3 * D * D, h->wes));
+  GemvParams p = base_params(h, h->p_qkv, mat(h, h->w.in_proj, (size_t)l * 3 * D, D));
   p.in = h->x;
   p.in_bs = D;
   p.alpha = h->w.norm1 + (size_t)l * D;
@@ -177,7 +188,7 @@ cudaError_t op_qkv(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   p.kcache = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
   p.vcache = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
   p.kv_bs = (long long)(L * C * D);
-  return launch_gemv(p, PRO_RMS, EPI_QKV, h->wbf, c.batch, s, pdl);
+  return launch_gemv(p, PRO_RMS, EPI_QKV, h->wtype, c.batch, s, pdl);
 }
 
 cudaError_t op_attn(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
@@ -207,34 +218,34 @@ cudaError_t op_attn(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
 
 cudaError_t op_out(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const size_t D = h->cfg.dim;
-  GemvParams p = base_params(h, h->p_out, woff(h->w.out_proj, (size_t)l * D * D, h->wes));
+  GemvParams p = base_params(h, h->p_out, mat(h, h->w.out_proj, (size_t)l * D, D));
   p.in = h->attn;
   p.in_bs = D;
   p.out = h->x;
   p.out_bs = D;
-  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, h->cfg.batch, s, pdl);
+  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wtype, h->cfg.batch, s, pdl);
 }
 
 cudaError_t op_gate_in(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const size_t D = h->cfg.dim, F = h->cfg.hidden;
-  GemvParams p = base_params(h, h->p_gin, woff(h->w.gate_in, (size_t)l * 2 * F * D, h->wes));
-  p.w_half = (long long)(F * D);
+  GemvParams p = base_params(h, h->p_gin, mat(h, h->w.gate_in, (size_t)l * 2 * F, D));
+  p.w_half = (long long)(F * band_row_bytes(h->band, h->wes, D));
   p.in = h->x;
   p.in_bs = D;
   p.alpha = h->w.norm2 + (size_t)l * D;
   p.out = h->u;
   p.out_bs = F;
-  return launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wbf, h->cfg.batch, s, pdl);
+  return launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wtype, h->cfg.batch, s, pdl);
 }
 
 cudaError_t op_gate_out(const rq_handle* h, int l, cudaStream_t s, bool pdl) {
   const size_t D = h->cfg.dim, F = h->cfg.hidden;
-  GemvParams p = base_params(h, h->p_gout, woff(h->w.gate_out, (size_t)l * D * F, h->wes));
+  GemvParams p = base_params(h, h->p_gout, mat(h, h->w.gate_out, (size_t)l * D, F));
   p.in = h->u;
   p.in_bs = F;
   p.out = h->x;
   p.out_bs = D;
-  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, h->cfg.batch, s, pdl);
+  return launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wtype, h->cfg.batch, s, pdl);
 }
 
 // out_norm + text head + first-wins argmax ("moshi_lm.rs", `step_ext` steps 4-5)
@@ -249,7 +260,7 @@ cudaError_t op_head(const rq_handle* h, cudaStream_t s, bool pdl) {
   p.out = h->text_logits;
   p.out_bs = V;
   p.key_index = 0;
-  return launch_gemv(p, PRO_RMS, EPI_ARGMAX, h->wbf, h->cfg.batch, s, pdl);
+  return launch_gemv(p, PRO_RMS, EPI_ARGMAX, h->wtype, h->cfg.batch, s, pdl);
 }
 
 // ---- depformer step cb ("moshi_lm.rs", `depformer_cycle`)
@@ -262,14 +273,14 @@ size_t dkv_off(const rq_handle* h, int l, int kv, int j) {
 cudaError_t op_dep_in(const rq_handle* h, int cb, cudaStream_t s, bool pdl) {
   const rq_config& c = h->cfg;
   const size_t D = c.dim, DD = c.ddim, A = c.audio_card;
-  GemvParams p = base_params(h, h->p_depin, woff(h->w.dep_in, (size_t)cb * DD * D, h->wes));
+  GemvParams p = base_params(h, h->p_depin, mat(h, h->w.dep_in, (size_t)cb * DD, D));
   p.in = h->tout;
   p.in_bs = D;
   p.out = h->dx;
   p.out_bs = DD;
   p.emb = cb == 0 ? h->w.dep_text_emb : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, h->wes);
   p.key_index = cb;  // text token for cb 0, else audio cb-1 (key 1 + (cb-1))
-  return launch_gemv(p, PRO_PLAIN, EPI_DEPIN, h->wbf, c.batch, s, pdl);
+  return launch_gemv(p, PRO_PLAIN, EPI_DEPIN, h->wtype, c.batch, s, pdl);
 }
 
 cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pdl) {
@@ -279,7 +290,7 @@ cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pd
   const long long dkv_bs = (long long)c.dlayers * 2 * 8 * DD;
   cudaError_t e;
   {  // rms_norm + in_projs[cb] -> q, per-frame K/V entry cb
-    GemvParams p = base_params(h, h->p_dqkv, woff(h->w.d_in_proj, ls * 3 * DD * DD, h->wes));
+    GemvParams p = base_params(h, h->p_dqkv, mat(h, h->w.d_in_proj, ls * 3 * DD, DD));
     p.in = h->dx;
     p.in_bs = DD;
     p.alpha = h->w.dnorm1 + (size_t)l * DD;
@@ -288,10 +299,10 @@ cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pd
     p.dk_out = h->dkv + dkv_off(h, l, 0, cb);
     p.dv_out = h->dkv + dkv_off(h, l, 1, cb);
     p.dkv_bs = dkv_bs;
-    if ((e = launch_gemv(p, PRO_RMS, EPI_DQKV, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+    if ((e = launch_gemv(p, PRO_RMS, EPI_DQKV, h->wtype, c.batch, s, pdl)) != cudaSuccess) return e;
   }
   {  // attention over entries 0..cb fused as the prologue of out_projs[cb] + residual
-    GemvParams p = base_params(h, h->p_dout, woff(h->w.d_out_proj, ls * DD * DD, h->wes));
+    GemvParams p = base_params(h, h->p_dout, mat(h, h->w.d_out_proj, ls * DD, DD));
     p.dq = h->dq;
     p.dq_bs = DD;
     p.dk = h->dkv + dkv_off(h, l, 0, 0);
@@ -303,25 +314,25 @@ cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pd
     p.in = h->dq;  // unused by this prologue
     p.out = h->dx;
     p.out_bs = DD;
-    if ((e = launch_gemv(p, PRO_DATTN, EPI_RESID, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+    if ((e = launch_gemv(p, PRO_DATTN, EPI_RESID, h->wtype, c.batch, s, pdl)) != cudaSuccess) return e;
   }
   {  // rms_norm + gating[cb].linear_in + silu gate
-    GemvParams p = base_params(h, h->p_dgin, woff(h->w.d_gate_in, ls * 2 * DF * DD, h->wes));
-    p.w_half = (long long)(DF * DD);
+    GemvParams p = base_params(h, h->p_dgin, mat(h, h->w.d_gate_in, ls * 2 * DF, DD));
+    p.w_half = (long long)(DF * band_row_bytes(h->band, h->wes, DD));
     p.in = h->dx;
     p.in_bs = DD;
     p.alpha = h->w.dnorm2 + (size_t)l * DD;
     p.out = h->du;
     p.out_bs = DF;
-    if ((e = launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+    if ((e = launch_gemv(p, PRO_RMS, EPI_SWIGLU, h->wtype, c.batch, s, pdl)) != cudaSuccess) return e;
   }
   {  // gating[cb].linear_out + residual
-    GemvParams p = base_params(h, h->p_dgout, woff(h->w.d_gate_out, ls * DD * DF, h->wes));
+    GemvParams p = base_params(h, h->p_dgout, mat(h, h->w.d_gate_out, ls * DD, DF));
     p.in = h->du;
     p.in_bs = DF;
     p.out = h->dx;
     p.out_bs = DD;
-    if ((e = launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wbf, c.batch, s, pdl)) != cudaSuccess) return e;
+    if ((e = launch_gemv(p, PRO_PLAIN, EPI_RESID, h->wtype, c.batch, s, pdl)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -329,13 +340,13 @@ cudaError_t op_dlayer(const rq_handle* h, int cb, int l, cudaStream_t s, bool pd
 cudaError_t op_linear(const rq_handle* h, int cb, cudaStream_t s, bool pdl) {
   const rq_config& c = h->cfg;
   const size_t DD = c.ddim, A = c.audio_card;
-  GemvParams p = base_params(h, h->p_lin, woff(h->w.linears, (size_t)cb * A * DD, h->wes));
+  GemvParams p = base_params(h, h->p_lin, mat(h, h->w.linears, (size_t)cb * A, DD));
   p.in = h->dx;
   p.in_bs = DD;
   p.out = h->audio_logits + (size_t)cb * A;
   p.out_bs = 8 * A;
   p.key_index = 1 + cb;
-  return launch_gemv(p, PRO_PLAIN, EPI_ARGMAX, h->wbf, c.batch, s, pdl);
+  return launch_gemv(p, PRO_PLAIN, EPI_ARGMAX, h->wtype, c.batch, s, pdl);
 }
 
 FrameParams frame_params(const rq_handle* h) {
@@ -366,7 +377,7 @@ FrameParams frame_params(const rq_handle* h) {
 cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
   cudaError_t e;
   const FrameParams f = frame_params(h);
-  if ((e = launch_frame_begin(f, h->wbf, s)) != cudaSuccess) return e;
+  if ((e = launch_frame_begin(f, h->wes == 2, s)) != cudaSuccess) return e;
   if (h->schedule == RQ_SCHEDULE_PERSISTENT) {
     if ((e = launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
         cudaSuccess)
@@ -436,18 +447,18 @@ cudaError_t dalloc(T** p, size_t bytes) {
 
 rq_status plan_all(rq_handle* h, std::string* why) {
   const rq_config& c = h->cfg;
-  const int es = h->wes, sms = h->num_sms;
-  h->p_qkv = plan_gemv(3 * c.dim, c.dim, es, false, true, sms);
-  h->p_out = plan_gemv(c.dim, c.dim, es, false, false, sms);
-  h->p_gin = plan_gemv(c.hidden, c.dim, es, true, false, sms);
-  h->p_gout = plan_gemv(c.dim, c.hidden, es, false, false, sms);
-  h->p_head = plan_gemv(c.text_card, c.dim, es, false, false, sms);
-  h->p_depin = plan_gemv(c.ddim, c.dim, es, false, false, sms);
-  h->p_dqkv = plan_gemv(3 * c.ddim, c.ddim, es, false, false, sms);
-  h->p_dout = plan_gemv(c.ddim, c.ddim, es, false, false, sms);
-  h->p_dgin = plan_gemv(c.dhidden, c.ddim, es, true, false, sms);
-  h->p_dgout = plan_gemv(c.ddim, c.dhidden, es, false, false, sms);
-  h->p_lin = plan_gemv(c.audio_card, c.ddim, es, false, false, sms);
+  const int es = h->wes, sms = h->num_sms, bd = h->band;
+  h->p_qkv = plan_gemv(3 * c.dim, c.dim, es, false, true, sms, bd);
+  h->p_out = plan_gemv(c.dim, c.dim, es, false, false, sms, bd);
+  h->p_gin = plan_gemv(c.hidden, c.dim, es, true, false, sms, bd);
+  h->p_gout = plan_gemv(c.dim, c.hidden, es, false, false, sms, bd);
+  h->p_head = plan_gemv(c.text_card, c.dim, es, false, false, sms, bd);
+  h->p_depin = plan_gemv(c.ddim, c.dim, es, false, false, sms, bd);
+  h->p_dqkv = plan_gemv(3 * c.ddim, c.ddim, es, false, false, sms, bd);
+  h->p_dout = plan_gemv(c.ddim, c.ddim, es, false, false, sms, bd);
+  h->p_dgin = plan_gemv(c.dhidden, c.ddim, es, true, false, sms, bd);
+  h->p_dgout = plan_gemv(c.ddim, c.dhidden, es, false, false, sms, bd);
+  h->p_lin = plan_gemv(c.audio_card, c.ddim, es, false, false, sms, bd);
   const GemvPlan* all[] = {&h->p_qkv, &h->p_out, &h->p_gin, &h->p_gout, &h->p_head, &h->p_depin,
                            &h->p_dqkv, &h->p_dout, &h->p_dgin, &h->p_dgout, &h->p_lin};
   for (const GemvPlan* p : all) {
@@ -524,7 +535,7 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
     o.out = h->x;
     ops.push_back(o);
     o = gemv(PRO_RMS, EPI_SWIGLU, 2, woff(h->w.gate_in, (size_t)l * 2 * F * D, es));
-    o.w_half = (long long)(F * D);
+    o.w_half = (long long)(F * D * es);
     o.in = h->x;
     o.alpha = h->w.norm2 + (size_t)l * D;
     o.out = h->u;
@@ -574,7 +585,7 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
       o.out = h->dx;
       ops.push_back(o);
       o = gemv(PRO_RMS, EPI_SWIGLU, 8, woff(h->w.d_gate_in, ls * 2 * DF * DD, es));
-      o.w_half = (long long)(DF * DD);
+      o.w_half = (long long)(DF * DD * es);
       o.in = h->dx;
       o.alpha = h->w.dnorm2 + (size_t)l * DD;
       o.out = h->du;
@@ -898,14 +909,14 @@ rq_status setup_schedule(rq_handle* h) {
                   "dhidden multiples of 64");
     return setup_tensor(h);
   }
-  const bool can = c.batch == 1 && h->wbf == h->kvbf;
+  const bool can = c.batch == 1 && h->wbf == h->kvbf && h->band == BAND_NONE;
   if (c.schedule == RQ_SCHEDULE_GRAPH || (c.schedule == RQ_SCHEDULE_AUTO && !can)) {
     h->schedule = RQ_SCHEDULE_GRAPH;
     return RQ_OK;
   }
   if (!can)
     return fail(h, RQ_ERR_UNSUPPORTED,
-                "the persistent schedule needs batch 1 and one dtype for weights and K/V");
+                "the persistent schedule needs batch 1 and f32 or bf16 weights of the K/V dtype");
   GemvPlan pl[kPersMaxPlans];
   int G = 2 * h->num_sms, slot = 0, part = 0, ns = 0, smem = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
@@ -1123,7 +1134,9 @@ rq_status rq_create(const rq_config* cfg, const rq_weights* w, void* cuda_stream
   h->stream = static_cast<cudaStream_t>(cuda_stream);
   h->wbf = cfg->weight_dtype == RQ_BF16;
   h->kvbf = cfg->kv_dtype == RQ_BF16;
-  h->wes = h->wbf ? 2 : 4;
+  h->band = cfg->weight_dtype == RQ_Q8 ? BAND_Q8 : (cfg->weight_dtype == RQ_Q4 ? BAND_Q4 : BAND_NONE);
+  h->wtype = h->band != BAND_NONE ? h->band : (h->wbf ? 1 : 0);
+  h->wes = (h->wbf || h->band != BAND_NONE) ? 2 : 4;
   h->kves = h->kvbf ? 2 : 4;
   h->io = IoLayout{cfg->batch};
   st = create_impl(h);
@@ -1443,6 +1456,30 @@ rq_status rq_get_rng(rq_handle* h, uint64_t* states) {
   if (!states) return fail(h, RQ_ERR_ARG, "null states");
   RQ_CUDA(h, cudaStreamSynchronize(h->stream));
   RQ_CUDA(h, cudaMemcpy(states, h->rng, (size_t)h->cfg.batch * 8, cudaMemcpyDeviceToHost));
+  return RQ_OK;
+}
+
+size_t rq_band_row_bytes(int32_t dtype, int32_t cols) {
+  if (cols <= 0 || cols % 32 != 0) return 0;
+  if (dtype == RQ_Q8) return band_row_bytes(BAND_Q8, 1, cols);
+  if (dtype == RQ_Q4) return band_row_bytes(BAND_Q4, 1, cols);
+  if (dtype == RQ_BF16) return (size_t)cols * 2;
+  if (dtype == RQ_F32) return (size_t)cols * 4;
+  return 0;
+}
+
+rq_status rq_quantize(int32_t dtype, const void* src, int32_t src_dtype, int64_t rows,
+                      int32_t cols, void* dst, void* cuda_stream) {
+  if ((dtype != RQ_Q8 && dtype != RQ_Q4) || (src_dtype != RQ_F32 && src_dtype != RQ_BF16) ||
+      rows < 0 || cols <= 0 || cols % 32 != 0 || (rows > 0 && (!src || !dst)))
+    return RQ_ERR_ARG;
+  const cudaError_t e =
+      launch_quantize_band(dtype == RQ_Q8 ? BAND_Q8 : BAND_Q4, src, src_dtype == RQ_BF16, rows,
+                           cols, dst, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RQ_ERR_CUDA;
+  }
   return RQ_OK;
 }
 

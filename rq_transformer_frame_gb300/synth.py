@@ -91,8 +91,9 @@ def _draw_block(out: torch.Tensor, kind: str, bf16: bool, seed: int) -> None:
 def make_weights(c: RQConfig, seed: int = 0, threads: int | None = None) -> dict:
     """All weights as contiguous CPU tensors in the C-ABI layout.
 
-    Matrices and tables are bfloat16 (bf16 models) or float32; alphas float32."""
-    bf16 = c.weight_dtype == "bf16"
+    Matrices and tables are bfloat16 (bf16 models and the bands, which quantize the bf16
+    matrices) or float32; alphas float32."""
+    bf16 = c.weight_dtype in ("bf16", "q8", "q4")  # the bands start from bf16 weights
     mdt = torch.bfloat16 if bf16 else torch.float32
     out, jobs = {}, []
     for name, kind, lead, block in weight_layout(c):
