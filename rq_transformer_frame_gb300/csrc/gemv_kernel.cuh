@@ -103,19 +103,26 @@ struct Chunk<q8_t> {
   static __device__ __forceinline__ size_t scale_off(int K, int c) {
     return (size_t)K + (size_t)(c >> 1) * 4;
   }
+  // sum_i q_i x_i, then times d: each code becomes a float with one byte permute and one
+  // add (2^23 + 128 + q has the bits 0x4B0000nn, nn = q + 128), no int-to-float convert
   static __device__ __forceinline__ void dot2s(const uint4 w, float d, const float (&x)[16],
                                                float& a, float& b) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t u[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
+                           w.w ^ 0x80808080u};
+    float sa = 0.f, sb = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float q = (float)((int32_t)(u[k] << (24 - 8 * j)) >> 24);
+        const float q = __uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7640u + j)) -
+                        8388736.0f;
         if (j & 1)
-          b = fmaf(q * d, x[4 * k + j], b);
+          sb = fmaf(q, x[4 * k + j], sb);
         else
-          a = fmaf(q * d, x[4 * k + j], a);
+          sa = fmaf(q, x[4 * k + j], sa);
       }
+    a = fmaf(sa, d, a);
+    b = fmaf(sb, d, b);
   }
 };
 
@@ -128,18 +135,24 @@ struct Chunk<q4_t> {
   static __device__ __forceinline__ size_t scale_off(int K, int c) {
     return (size_t)K / 2 + (size_t)c * 4;
   }
+  // sum_i (q_i - 8) x_i, then times d: a nibble n becomes n - 8 with one mask-and-or
+  // (the bits 0x4B00000n are 2^23 + n) and one add
   static __device__ __forceinline__ void dot2s(const uint4 w, float d, const float (&x)[32],
                                                float& a, float& b) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    float sa = 0.f, sb = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = (u[k] >> (8 * j)) & 0xffu;
         const int i = 4 * k + j;
-        a = fmaf((float)((int)(byte & 15u) - 8) * d, x[i], a);
-        b = fmaf((float)((int)(byte >> 4) - 8) * d, x[i + 16], b);
+        const float lo = __uint_as_float(((u[k] >> (8 * j)) & 0xfu) | 0x4B000000u) - 8388616.0f;
+        const float hi = __uint_as_float(((u[k] >> (8 * j + 4)) & 0xfu) | 0x4B000000u) - 8388616.0f;
+        sa = fmaf(lo, x[i], sa);
+        sb = fmaf(hi, x[i + 16], sb);
       }
+    a = fmaf(sa, d, a);
+    b = fmaf(sb, d, b);
   }
 };
 
