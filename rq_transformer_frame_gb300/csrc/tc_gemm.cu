@@ -329,6 +329,9 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   int splits = (2 * num_sms) / pl.tiles_m;
   const int max_splits = pl.ksteps / 4 > 0 ? pl.ksteps / 4 : 1;
   if (splits > max_splits) splits = max_splits;
+  // at 64 columns a split's partial tile is 32 KB and beyond four splits merging them
+  // costs more than the extra CTAs return (measured on out_proj / gate_out)
+  if (NB >= 64 && splits > 4) splits = 4;
   if (splits < 1) splits = 1;
   pl.ksteps_split = (pl.ksteps + splits - 1) / splits;
   pl.splits = (pl.ksteps + pl.ksteps_split - 1) / pl.ksteps_split;
