@@ -85,3 +85,34 @@ def test_calls_on_null_handle_are_errors(lib):
     assert lib.rq_step(None, None, None, None) == binding.RQ_ERR_ARG
     assert lib.rq_frame_kernel_count(None) == 0
     lib.rq_destroy(None)
+
+
+def test_band_row_bytes_and_quantizer_arguments_on_host(lib):
+    # codes, then one f32 scale per 32 values
+    assert lib.rq_band_row_bytes(binding.RQ_Q8, 4096) == 4096 + 512
+    assert lib.rq_band_row_bytes(binding.RQ_Q4, 4096) == 2048 + 512
+    assert lib.rq_band_row_bytes(binding.RQ_BF16, 64) == 128
+    assert lib.rq_band_row_bytes(binding.RQ_Q4, 48) == 0  # not a multiple of 32
+    bad = [(binding.RQ_Q4, binding.RQ_BF16, 2, 48), (binding.RQ_BF16, binding.RQ_BF16, 2, 64),
+           (binding.RQ_Q8, 9, 2, 64), (binding.RQ_Q8, binding.RQ_F32, -1, 64)]
+    for dt, sdt, rows, cols in bad:
+        assert lib.rq_quantize(dt, 16, sdt, rows, cols, 32, None) == binding.RQ_ERR_ARG
+    assert set(binding.MATRIX_FIELDS) <= set(binding.WEIGHT_FIELDS)
+
+
+def test_create_rejects_bands_with_short_rows_on_host(lib):
+    c = binding.make_config(configs.TINY.with_(weight_dtype="q4"))  # hidden 704, not /128
+    h = C.c_void_p()
+    assert lib.rq_create(C.byref(c), C.byref(_null_weights()), None, C.byref(h)) == \
+        binding.RQ_ERR_UNSUPPORTED
+    assert not h.value
+
+
+def test_new_entry_points_on_null_handle_are_errors(lib):
+    assert lib.rq_set_sampling(None, 1, 0.8, 0.7, 25, 25, None) == binding.RQ_ERR_ARG
+    assert lib.rq_get_rng(None, None) == binding.RQ_ERR_ARG
+    assert lib.rq_prime(None, 0, 1, None, None) == binding.RQ_ERR_ARG
+    assert lib.rq_replay(None, 0, 1, None) == binding.RQ_ERR_ARG
+    assert lib.rq_snapshot_size(None, 0) == 0
+    assert lib.rq_snapshot(None, 0, None, 0) == binding.RQ_ERR_ARG
+    assert lib.rq_restore(None, 0, None, 0) == binding.RQ_ERR_ARG
