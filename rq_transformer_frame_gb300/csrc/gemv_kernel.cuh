@@ -126,6 +126,25 @@ struct Chunk<q8_t> {
   }
 };
 
+// two f32 lanes in one 64-bit register pair, with the packed add and FMA of sm_100+
+typedef unsigned long long gv_f32x2;
+__device__ __forceinline__ gv_f32x2 gv_pack2(float a, float b) {
+  gv_f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void gv_unpack2(gv_f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ gv_f32x2 gv_add2(gv_f32x2 a, gv_f32x2 b) {
+  gv_f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ void gv_fma2(gv_f32x2& d, gv_f32x2 a, gv_f32x2 b) {  // d += a * b
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 template <>
 struct Chunk<q4_t> {
   static constexpr int V = 32;  // one group: byte i holds values i and i + 16
@@ -135,24 +154,35 @@ struct Chunk<q4_t> {
   static __device__ __forceinline__ size_t scale_off(int K, int c) {
     return (size_t)K / 2 + (size_t)c * 4;
   }
-  // sum_i (q_i - 8) x_i, then times d: a nibble n becomes n - 8 with one mask-and-or
-  // (the bits 0x4B00000n are 2^23 + n) and one add
+  // sum_i (q_i - 8) x_i, then times d: one mask per word of codes, one byte permute per
+  // code (the bits 0x4B00000n are 2^23 + n) and, two at a time, one packed add
   static __device__ __forceinline__ void dot2s(const uint4 w, float d, const float (&x)[32],
                                                float& a, float& b) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    float sa = 0.f, sb = 0.f;
+    const gv_f32x2 off = gv_pack2(-8388616.0f, -8388616.0f);
+    gv_f32x2 sl = gv_pack2(0.f, 0.f), sh = gv_pack2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = u[k] & 0x0F0F0F0Fu, hi = (u[k] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = 4 * k + j;
-        const float lo = __uint_as_float(((u[k] >> (8 * j)) & 0xfu) | 0x4B000000u) - 8388616.0f;
-        const float hi = __uint_as_float(((u[k] >> (8 * j + 4)) & 0xfu) | 0x4B000000u) - 8388616.0f;
-        sa = fmaf(lo, x[i], sa);
-        sb = fmaf(hi, x[i + 16], sb);
+      for (int j = 0; j < 4; j += 2) {
+        const gv_f32x2 l =
+            gv_add2(gv_pack2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7640u + j)),
+                             __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7641u + j))),
+                    off);
+        const gv_f32x2 h =
+            gv_add2(gv_pack2(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7640u + j)),
+                             __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7641u + j))),
+                    off);
+        gv_fma2(sl, l, gv_pack2(x[4 * k + j], x[4 * k + j + 1]));       // values 4k + j, +1
+        gv_fma2(sh, h, gv_pack2(x[4 * k + j + 16], x[4 * k + j + 17]));  // the same + 16
       }
-    a = fmaf(sa, d, a);
-    b = fmaf(sb, d, b);
+    }
+    float p0, p1, p2, p3;
+    gv_unpack2(sl, p0, p1);
+    gv_unpack2(sh, p2, p3);
+    a = fmaf(p0 + p1, d, a);
+    b = fmaf(p2 + p3, d, b);
   }
 };
 
