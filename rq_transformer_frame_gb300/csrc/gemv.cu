@@ -8,6 +8,14 @@
 #ifndef RQ_GEMV_MAX_STAGES
 #define RQ_GEMV_MAX_STAGES 8
 #endif
+#ifndef RQ_BAND_STAGE_BYTES
+#define RQ_BAND_STAGE_BYTES (24 * 1024)  // largest band stage (tile) built from rounds
+#endif
+#ifndef RQ_BAND_STAGE_BUDGET
+#define RQ_BAND_STAGE_BUDGET (64 * 1024)  // band CTAs: two per SM
+#endif
+constexpr int kBandStageBytes = RQ_BAND_STAGE_BYTES;
+constexpr int kBandStageBudget = RQ_BAND_STAGE_BUDGET;
 #ifndef RQ_GEMV_CTAS_PER_SM
 #define RQ_GEMV_CTAS_PER_SM 2
 #endif
@@ -51,13 +59,24 @@ GemvPlan plan_gemv(int n_out, int K, int es, bool paired, bool even_rows, int nu
   const int row_bytes = (int)band_row_bytes(band, es, K);
   pl.tpr = tpr;
   pl.tile_rows = ng * pl.rg;
+  const int max_grid = num_sms * RQ_GEMV_CTAS_PER_SM;
+  if (band != BAND_NONE) {
+    // band rows are short: a tile takes several rounds of the row groups, so each bulk
+    // copy stays large (a producer thread keeps only a few copies in flight), as long
+    // as every CTA of the grid still gets a tile
+    const int per = paired ? pl.tile_rows / 2 : pl.tile_rows;
+    int rounds = 1;
+    while (rounds < 4 && 2 * rounds * pl.tile_rows * row_bytes <= kBandStageBytes &&
+           (n_out + 2 * rounds * per - 1) / (2 * rounds * per) >= max_grid)
+      rounds *= 2;
+    pl.tile_rows *= rounds;
+  }
   const int out_per_tile = paired ? pl.tile_rows / 2 : pl.tile_rows;
   pl.tiles = (n_out + out_per_tile - 1) / out_per_tile;
-  const int max_grid = num_sms * RQ_GEMV_CTAS_PER_SM;
   pl.grid = pl.tiles < max_grid ? pl.tiles : max_grid;
   pl.max_tiles = (pl.tiles + pl.grid - 1) / pl.grid;
   const int tile_bytes = pl.tile_rows * row_bytes;
-  int ns = (RQ_GEMV_STAGE_BUDGET) / tile_bytes;
+  int ns = (band != BAND_NONE ? kBandStageBudget : RQ_GEMV_STAGE_BUDGET) / tile_bytes;
   ns = ns < 2 ? 2 : (ns > RQ_GEMV_MAX_STAGES ? RQ_GEMV_MAX_STAGES : ns);
   if (ns > pl.max_tiles) ns = pl.max_tiles < 1 ? 1 : pl.max_tiles;
   pl.n_stages = ns;

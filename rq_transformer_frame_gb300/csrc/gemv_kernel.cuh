@@ -304,18 +304,19 @@ __global__ void __launch_bounds__(kThreads, Chunk<WT>::kBand ? 2 : GemvShape<NCH
       }
     }
     if (PRO == PRO_RMS) {
-      // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n))
+      // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).
+      // Every row group holds the whole vector: group 0's warps sum the squares from
+      // registers.
       float ss = 0.f;
-      for (int k = tid; k < K; k += kConsumers) {
-        const float v = in[k];
-        ss = fmaf(v, v, ss);
-      }
+#pragma unroll
+      for (int j = 0; j < NCH; ++j)
+#pragma unroll
+        for (int v = 0; v < V; ++v) ss = fmaf(xr[j][v], xr[j][v], ss);
       ss = warp_sum(ss);
       if (lane == 0) s_red[warp] = ss;
       bar_sync(1, kConsumers);
       float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumers / 32; ++w) tot += s_red[w];
+      for (int w = 0; w < pl.tpr / 32; ++w) tot += s_red[w];
       const float inv = 1.0f / sqrtf(p.eps + tot / (float)K);
       const bool side = p.side_out != nullptr && blockIdx.x == 0 && g == 0;
 #pragma unroll
@@ -323,7 +324,13 @@ __global__ void __launch_bounds__(kThreads, Chunk<WT>::kBand ? 2 : GemvShape<NCH
         const int c = tig + j * pl.tpr;
         if (c < CC) {
 #pragma unroll
-          for (int v = 0; v < V; ++v) xr[j][v] = xr[j][v] * p.alpha[c * V + v] * inv;
+          for (int v = 0; v < V; v += 4) {  // alpha rows are 16-byte aligned (dims % 8)
+            const float4 a = *reinterpret_cast<const float4*>(p.alpha + c * V + v);
+            xr[j][v] = xr[j][v] * a.x * inv;
+            xr[j][v + 1] = xr[j][v + 1] * a.y * inv;
+            xr[j][v + 2] = xr[j][v + 2] * a.z * inv;
+            xr[j][v + 3] = xr[j][v + 3] * a.w * inv;
+          }
           if (side) {
 #pragma unroll
             for (int v = 0; v < V; ++v) p.side_out[(size_t)b * p.side_bs + c * V + v] = xr[j][v];
@@ -402,6 +409,10 @@ __global__ void __launch_bounds__(kThreads, Chunk<WT>::kBand ? 2 : GemvShape<NCH
       }
     }
 
+    // a tile is `rounds` rounds of the row groups (one round for bf16 / f32; band tiles
+    // take several so that each bulk copy stays large)
+    const int rstride = (kConsumers / pl.tpr) * RG;  // rows of one round
+    const int rounds = Chunk<WT>::kBand ? pl.tile_rows / rstride : 1;
     for (int i = 0; i < nt; ++i) {
       if (s_abort) break;
       const int s = i % NS;
@@ -410,55 +421,61 @@ __global__ void __launch_bounds__(kThreads, Chunk<WT>::kBand ? 2 : GemvShape<NCH
         s_abort = 1;
         break;
       }
-      const uint8_t* row0 = stages + (size_t)s * tile_bytes + (size_t)(g * RG) * row_bytes;
-      // two accumulators per row (even / odd elements) halve the FMA dependency chain
-      float acc[RG][2];
+      for (int rd = 0; rd < rounds; ++rd) {
+        const int lr0 = rd * rstride + g * RG;  // this group's first row in the tile
+        const uint8_t* row0 = stages + (size_t)s * tile_bytes + (size_t)lr0 * row_bytes;
+        // two accumulators per row (even / odd elements) halve the FMA dependency chain
+        float acc[RG][2];
 #pragma unroll
-      for (int r = 0; r < RG; ++r) acc[r][0] = acc[r][1] = 0.f;
-      uint4 w[NCH][RG];
+        for (int r = 0; r < RG; ++r) acc[r][0] = acc[r][1] = 0.f;
+        uint4 w[NCH][RG];
 #pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const int c = tig + j * pl.tpr;
+        for (int j = 0; j < NCH; ++j) {
+          const int c = tig + j * pl.tpr;
 #pragma unroll
-        for (int r = 0; r < RG; ++r)
-          w[j][r] = (c < CC) ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
-                                                               (size_t)c * 16)
-                             : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int j = 0; j < NCH; ++j)
-#pragma unroll
-        for (int r = 0; r < RG; ++r) {
-          if constexpr (Chunk<WT>::kBand) {
-            const int c = tig + j * pl.tpr;
-            const float d = (c < CC) ? *reinterpret_cast<const float*>(
-                                           row0 + (size_t)r * row_bytes + Chunk<WT>::scale_off(K, c))
-                                     : 0.f;
-            Chunk<WT>::dot2s(w[j][r], d, xr[j], acc[r][0], acc[r][1]);
-          } else {
-            Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
-          }
+          for (int r = 0; r < RG; ++r)
+            w[j][r] = (c < CC) ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
+                                                                 (size_t)c * 16)
+                               : make_uint4(0u, 0u, 0u, 0u);
         }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
-      float* pp = part + (size_t)(i * pl.tile_rows + g * RG) * wpg + (warp % wpg);
-      if (RG == 2) {
-        // reduce two rows with five shuffles: lanes 0-15 end with row 0, 16-31 row 1
-        const bool up = (lane & 16) != 0;
-        const float r0 = acc[0][0] + acc[0][1];
-        const float r1 = acc[RG - 1][0] + acc[RG - 1][1];
-        float keep = up ? r1 : r0;
-        const float send = up ? r0 : r1;
-        keep += __shfl_xor_sync(0xffffffffu, send, 16);
-        keep += __shfl_xor_sync(0xffffffffu, keep, 8);
-        keep += __shfl_xor_sync(0xffffffffu, keep, 4);
-        keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-        keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-        if (lane == 0) pp[0] = keep;
-        if (lane == 16) pp[wpg] = keep;
-      } else {
-        const float r0 = warp_sum(acc[0][0] + acc[0][1]);
-        if (lane == 0) pp[0] = r0;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int r = 0; r < RG; ++r) {
+            if constexpr (Chunk<WT>::kBand) {
+              const int c = tig + j * pl.tpr;
+              const float d =
+                  (c < CC) ? *reinterpret_cast<const float*>(row0 + (size_t)r * row_bytes +
+                                                             Chunk<WT>::scale_off(K, c))
+                           : 0.f;
+              Chunk<WT>::dot2s(w[j][r], d, xr[j], acc[r][0], acc[r][1]);
+            } else {
+              Chunk<WT>::dot2(w[j][r], xr[j], acc[r][0], acc[r][1]);
+            }
+          }
+        if (rd == rounds - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+        }
+        float* pp = part + (size_t)(i * pl.tile_rows + lr0) * wpg + (warp % wpg);
+        if (RG == 2) {
+          // reduce two rows with five shuffles: lanes 0-15 end with row 0, 16-31 row 1
+          const bool up = (lane & 16) != 0;
+          const float r0 = acc[0][0] + acc[0][1];
+          const float r1 = acc[RG - 1][0] + acc[RG - 1][1];
+          float keep = up ? r1 : r0;
+          const float send = up ? r0 : r1;
+          keep += __shfl_xor_sync(0xffffffffu, send, 16);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 8);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+          if (lane == 0) pp[0] = keep;
+          if (lane == 16) pp[wpg] = keep;
+        } else {
+          const float r0 = warp_sum(acc[0][0] + acc[0][1]);
+          if (lane == 0) pp[0] = r0;
+        }
       }
     }
   }

@@ -1,12 +1,13 @@
 """Time single operations of the decode step through the C ABI (rq_launch_op).
 
   python -m rq_transformer_frame_gb300.op_probe --workload moshi7b_2layer \
-      --ops gate_in,qkv --reps 3 [--frames 4] [--batch 16] [--prefill 2900]
+      --ops gate_in,qkv --reps 3 [--frames 4] [--batch 16] [--prefill 2900] [--band q4]
 
 Builds the decoder for the workload (seeded synthetic weights; `--batch` overrides the
 session count, `--prefill n` fills every session's temporal K/V with the workload's
 synthetic positions 0..n-1; `--context` shrinks the K/V window, e.g. to profile a
-linear on a small device footprint), runs `--frames` whole frames, then for each op launches it
+linear on a small device footprint; `--band q8|q4` quantizes the matrices into that weight
+band, which runs under the graph schedule), runs `--frames` whole frames, then for each op launches it
 once per temporal layer `--reps` times, timed with CUDA events on the decoder's stream,
 and prints one JSON line per op.  Used as the command under the profiler for the kernel
 summaries in profiles/.
@@ -32,6 +33,7 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--prefill", type=int, default=-1)
     ap.add_argument("--context", type=int, default=0)
+    ap.add_argument("--band", default="", choices=["", "q8", "q4"])
     a = ap.parse_args(argv)
     cfg = configs.CONFIGS[a.workload]
     if a.batch > 0:
@@ -42,6 +44,9 @@ def main(argv=None):
         cfg = cfg.with_(context=a.context)
     torch.cuda.set_device(0)
     w = binding.upload_weights(synth.make_weights(cfg, seed=0))
+    if a.band:
+        w = binding.quantize_weights(w, binding.RQ_Q8 if a.band == "q8" else binding.RQ_Q4)
+        cfg = cfg.with_(weight_dtype=a.band)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dec = binding.Decoder(cfg, w, stream=stream)
