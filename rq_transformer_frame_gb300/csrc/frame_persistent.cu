@@ -369,36 +369,47 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
 }
 
 // ---------------------------------------------------------------- attention items
-template <typename KT, int EPL>
-__device__ __forceinline__ void load_row(const KT* p, float (&o)[EPL]);
-template <>
-__device__ __forceinline__ void load_row<float, 4>(const float* p, float (&o)[4]) {
-  const float4 f = __ldcg(reinterpret_cast<const float4*>(p));
-  o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
-}
-template <>
-__device__ __forceinline__ void load_row<float, 2>(const float* p, float (&o)[2]) {
-  const float2 f = __ldcg(reinterpret_cast<const float2*>(p));
-  o[0] = f.x; o[1] = f.y;
-}
-template <>
-__device__ __forceinline__ void load_row<float, 1>(const float* p, float (&o)[1]) {
-  o[0] = __ldcg(p);
-}
-template <>
-__device__ __forceinline__ void load_row<uint16_t, 4>(const uint16_t* p, float (&o)[4]) {
-  const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
-  o[0] = bf16lo(u.x); o[1] = bf16hi(u.x); o[2] = bf16lo(u.y); o[3] = bf16hi(u.y);
-}
-template <>
-__device__ __forceinline__ void load_row<uint16_t, 2>(const uint16_t* p, float (&o)[2]) {
-  const unsigned u = __ldcg(reinterpret_cast<const unsigned*>(p));
-  o[0] = bf16lo(u); o[1] = bf16hi(u);
-}
-template <>
-__device__ __forceinline__ void load_row<uint16_t, 1>(const uint16_t* p, float (&o)[1]) {
-  o[0] = __uint_as_float(((unsigned)__ldcg(reinterpret_cast<const unsigned short*>(p))) << 16);
-}
+// one lane's EPL elements of a K/V row as loaded (no conversion): the next key's row is
+// fetched while the current one is used
+template <typename KT, int EPL> struct KvRaw;
+template <> struct KvRaw<uint16_t, 4> {
+  uint2 u;
+  __device__ __forceinline__ void load(const uint16_t* p) { u = __ldcg(reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ void get(float (&o)[4]) const {
+    o[0] = bf16lo(u.x); o[1] = bf16hi(u.x); o[2] = bf16lo(u.y); o[3] = bf16hi(u.y);
+  }
+};
+template <> struct KvRaw<uint16_t, 2> {
+  unsigned u;
+  __device__ __forceinline__ void load(const uint16_t* p) { u = __ldcg(reinterpret_cast<const unsigned*>(p)); }
+  __device__ __forceinline__ void get(float (&o)[2]) const { o[0] = bf16lo(u); o[1] = bf16hi(u); }
+};
+template <> struct KvRaw<uint16_t, 1> {
+  unsigned u;
+  __device__ __forceinline__ void load(const uint16_t* p) {
+    u = (unsigned)__ldcg(reinterpret_cast<const unsigned short*>(p));
+  }
+  __device__ __forceinline__ void get(float (&o)[1]) const { o[0] = __uint_as_float(u << 16); }
+};
+template <int EPL> struct KvRawF;
+template <> struct KvRawF<4> {
+  float4 f;
+  __device__ __forceinline__ void load(const float* p) { f = __ldcg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ void get(float (&o)[4]) const { o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w; }
+};
+template <> struct KvRawF<2> {
+  float2 f;
+  __device__ __forceinline__ void load(const float* p) { f = __ldcg(reinterpret_cast<const float2*>(p)); }
+  __device__ __forceinline__ void get(float (&o)[2]) const { o[0] = f.x; o[1] = f.y; }
+};
+template <> struct KvRawF<1> {
+  float f;
+  __device__ __forceinline__ void load(const float* p) { f = __ldcg(p); }
+  __device__ __forceinline__ void get(float (&o)[1]) const { o[0] = f; }
+};
+template <> struct KvRaw<float, 4> : KvRawF<4> {};
+template <> struct KvRaw<float, 2> : KvRawF<2> {};
+template <> struct KvRaw<float, 1> : KvRawF<1> {};
 
 // "moshi_lm.rs", `attend` for one session: work item (head, split of kps positions)
 // per group of 4 warps; the last group to finish a head merges its splits in order.
@@ -427,20 +438,45 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
     const int h = it % P.H, split = it / P.H;
     const int j0 = first + split * kps;
     const int j1 = min(j0 + kps, pos + 1);
-    float q[EPL];
-    const float* qp = P.attn_q + (size_t)h * HD + lane * EPL;
+    const KT* kb = static_cast<const KT*>(op.kcache) + (size_t)h * HD + lane * EPL;
+    const KT* vb = static_cast<const KT*>(op.vcache) + (size_t)h * HD + lane * EPL;
+    // keys of this warp in flight: one; two to four (a register ring) spill at this
+    // kernel's 96-register cap and slow every op down more than they save here
+    constexpr int KPF = 1;
+    KvRaw<KT, EPL> kr[KPF], vr[KPF];  // this warp's first keys, issued before q
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) q[e] = ldcg(qp + e) * scale;
+    for (int pf = 0; pf < KPF; ++pf) {
+      const int j = j0 + wig + 4 * pf;
+      if (j < j1) {
+        const size_t off = (size_t)(j % P.context) * P.D;
+        kr[pf].load(kb + off);
+        vr[pf].load(vb + off);
+      }
+    }
+    float q[EPL];
+    {
+      KvRawF<EPL> qr;
+      qr.load(P.attn_q + (size_t)h * HD + lane * EPL);
+      qr.get(q);
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) q[e] *= scale;
     float m = ninf, l = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    const KT* kb = static_cast<const KT*>(op.kcache) + (size_t)h * HD + lane * EPL;
-    const KT* vb = static_cast<const KT*>(op.vcache) + (size_t)h * HD + lane * EPL;
-    for (int j = j0 + wig; j < j1; j += 4) {
-      const size_t off = (size_t)(j % P.context) * P.D;
+    for (int jb = j0 + wig; jb < j1; jb += 4 * KPF)
+#pragma unroll
+    for (int pf = 0; pf < KPF; ++pf) {
+      const int j = jb + 4 * pf;
+      if (j >= j1) break;
       float k[EPL], v[EPL];
-      load_row<KT, EPL>(kb + off, k);
-      load_row<KT, EPL>(vb + off, v);
+      kr[pf].get(k);
+      vr[pf].get(v);
+      if (j + 4 * KPF < j1) {  // this slot's next key, in flight during the others
+        const size_t off = (size_t)((j + 4 * KPF) % P.context) * P.D;
+        kr[pf].load(kb + off);
+        vr[pf].load(vb + off);
+      }
       float sc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) sc = fmaf(q[e], k[e], sc);
@@ -488,13 +524,18 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
       __threadfence();
       const float* pb = P.part + (size_t)h * P.nsplit * pstride;
       if (gt < HD) {
-        float M = ninf;
-        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ldcg(pb + s * pstride));
-        float L = 0.f, A = 0.f;
+        // splits in order, one pass: the running max rescales what was summed so far
+        // (the loads of later splits do not wait on earlier ones)
+        float M = ninf, L = 0.f, A = 0.f;
+#pragma unroll 4
         for (int s = 0; s < nsplit; ++s) {
-          const float c = expf(ldcg(pb + s * pstride) - M);
-          L += ldcg(pb + s * pstride + 1) * c;
-          A += ldcg(pb + s * pstride + 2 + gt) * c;
+          const float ms = ldcg(pb + s * pstride), ls = ldcg(pb + s * pstride + 1);
+          const float as = ldcg(pb + s * pstride + 2 + gt);
+          const float mn = fmaxf(M, ms);
+          const float co = expf(M - mn), cs = expf(ms - mn);
+          L = L * co + ls * cs;
+          A = A * co + as * cs;
+          M = mn;
         }
         P.attn_out[(size_t)h * HD + gt] = A / L;
       }
