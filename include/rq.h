@@ -93,11 +93,12 @@ typedef struct {
 /* Frame schedules.  PERSISTENT runs all linears and attentions of a frame as one
  * cooperative kernel with grid barriers between dependent ops (batch 1, same weight and
  * K/V dtype); GRAPH launches one streaming-GEMV kernel per op inside a CUDA graph;
- * TENSOR (batch 16..64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
- * runs every linear as one tcgen05 tensor-core GEMM over all sessions, the normalised
- * f32 activations split into two bf16 operand parts (16 significant bits), inside a
- * CUDA graph.  AUTO
- * picks PERSISTENT when it applies, TENSOR at batch >= 16 when it applies, else GRAPH.
+ * TENSOR (batch <= 64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
+ * runs every linear as one tcgen05 tensor-core GEMM over all sessions (padded to a
+ * multiple of 16), the normalised f32 activations split into two bf16 operand parts
+ * (16 significant bits), inside a CUDA graph.  AUTO picks PERSISTENT when it applies
+ * (batch 1), TENSOR at batch >= 2 when it applies (it streams every weight once per
+ * frame, where GRAPH streams it once per session), else GRAPH.
  * Results agree within the parity tolerance. */
 enum {
   RQ_SCHEDULE_AUTO = 0,

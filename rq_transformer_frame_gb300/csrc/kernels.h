@@ -174,7 +174,7 @@ cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* 
                                  cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- tensor-core GEMM
-// Y[b][n] = X[b][:] . W[n][:] for all sessions b at once (batch >= 16): a CTA computes a
+// Y[b][n] = X[b][:] . W[n][:] for all sessions b at once (batch 2..64): a CTA computes a
 // 128-row tile of W against NB (padded) sessions on the tcgen05 tensor cores, operands
 // fed by TMA, accumulator in tensor memory; optional split-K merged in split order.
 struct TcPlan {

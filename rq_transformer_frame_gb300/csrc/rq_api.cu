@@ -902,7 +902,7 @@ rq_status upload_pers_ops(rq_handle* h) {
 rq_status setup_schedule(rq_handle* h) {
   const rq_config& c = h->cfg;
   if (c.schedule == RQ_SCHEDULE_TENSOR ||
-      (c.schedule == RQ_SCHEDULE_AUTO && c.batch >= 16 && tensor_eligible(h))) {
+      (c.schedule == RQ_SCHEDULE_AUTO && c.batch >= 2 && tensor_eligible(h))) {
     if (!tensor_eligible(h))
       return fail(h, RQ_ERR_UNSUPPORTED,
                   "the tensor schedule needs batch <= 64, bf16 weights and dim, hidden, ddim, "

@@ -1,4 +1,4 @@
-// tc_frame.cu -- a whole frame at batch >= 16 on the tensor cores: per linear, one
+// tc_frame.cu -- a whole frame at batch 2..64 on the tensor cores: per linear, one
 // tcgen05 GEMM over all sessions (weights read once per frame), bf16 operands prepared
 // by a small normalisation kernel, the fused epilogues of the streaming path.
 //

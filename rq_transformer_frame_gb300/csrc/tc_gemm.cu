@@ -1,4 +1,5 @@
-// tc_gemm.cu -- weights x batch on the tcgen05 tensor cores (batch >= 16).
+// tc_gemm.cu -- weights x batch on the tcgen05 tensor cores (batch 2..64, padded to a
+// multiple of 16).
 //
 // At batch B the linears of a frame become Y[b][n] = sum_k X[b][k] W[n][k], a real dense
 // contraction (B flops per weight byte... still below the tensor ridge, so the kernel

@@ -73,9 +73,10 @@ def test_small_batch16_all_sessions_forced():
     run_batch_forced(configs.SMALL.with_(batch=16), 6, range(16))
 
 
-@pytest.mark.parametrize("batch", [20, 64])
+@pytest.mark.parametrize("batch", [3, 20, 64])
 def test_small_padded_and_full_tiles(batch):
-    """batch 20 pads the session tile to 32 (rows 20..31 stay zero); 64 fills it."""
+    """batch 3 pads the session tile to 16 and 20 to 32 (the padding rows stay zero); 64
+    fills it."""
     run_batch_forced(configs.SMALL.with_(batch=batch), 4, [0, batch // 2, batch - 1])
 
 
@@ -113,11 +114,15 @@ def test_small_batch16_free_run():
     dec.close()
 
 
-def test_auto_picks_tensor_at_batch16():
+def test_auto_picks_tensor_from_batch2():
     c = configs.SMALL.with_(batch=16)
     w = binding.upload_weights(weights_of(c))
-    d = binding.Decoder(c, w)
-    assert d.schedule == binding.RQ_SCHEDULE_TENSOR
+    for b in (2, 4, 16):
+        d = binding.Decoder(c.with_(batch=b), w)
+        assert d.schedule == binding.RQ_SCHEDULE_TENSOR, b
+        d.close()
+    d = binding.Decoder(c.with_(batch=1), w)
+    assert d.schedule == binding.RQ_SCHEDULE_PERSISTENT
     d.close()
     t = configs.TINY.with_(batch=16)  # f32 weights: the tensor schedule does not apply
     wt = binding.upload_weights(weights_of(t))
