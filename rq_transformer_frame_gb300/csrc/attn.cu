@@ -134,6 +134,27 @@ __device__ __forceinline__ bool attn_decode_item(const AttnParams& p, int it, At
   return true;
 }
 
+// The same items numbered densely: session b owns H * ns_b consecutive indices from
+// pref[b] (pref = prefix sums over sessions, pref[0] = 0), split-major, head fastest.
+// Every index is a real item, so the persistent grid never walks the empty splits
+// beyond short windows (at position 50 of a 3000-slot cache, 46 of 47 splits).
+constexpr int kAttnDenseMaxB = 256;  // sessions whose prefix sums fit the CTA's table
+
+// item i of the dense numbering; `b` is a session at or before the item's (a CTA's items
+// only move forward, so the walk from its previous item's session is short)
+__device__ __forceinline__ void attn_dense_item(const AttnParams& p, const int* pref, int i,
+                                                int& b, AttnItem& x) {
+  while (b + 1 < p.batch && pref[b + 1] <= i) ++b;
+  x.b = b;
+  const int r = i - pref[b];
+  x.h = r % p.H;
+  x.split = r / p.H;
+  const int lim = min(p.offsets[x.b] + 1, p.C);
+  x.ns = (lim + p.kps - 1) / p.kps;
+  x.j0 = x.split * p.kps;
+  x.j1 = min(x.j0 + p.kps, lim);
+}
+
 #ifndef RQ_ATTN_STAGES
 #define RQ_ATTN_STAGES 2
 #endif
@@ -162,38 +183,64 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t s_full[NS];
   __shared__ int s_item[NS];
+  __shared__ AttnItem s_info[NS];  // the item of each stage, decoded once by thread 0
   __shared__ float s_m[NW], s_l[NW];
   __shared__ float s_acc[NW][HD];
+  __shared__ int s_pref[kAttnDenseMaxB + 1];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kps = p.kps;
   KT* const stage0 = reinterpret_cast<KT*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const size_t stage_elems = (size_t)2 * kps * HD;  // K rows then V rows
   const uint32_t stage_bytes = (uint32_t)(stage_elems * sizeof(KT));
-  const int total = p.batch * p.H * p.nsplit;
+  const bool dense = p.batch <= kAttnDenseMaxB;
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&s_full[i], 1);
     fence_barrier_init();
     tc::prefetch_tmap(&kmap);
     tc::prefetch_tmap(&vmap);
   }
-  __syncthreads();
   pdl_wait();
+  if (dense && warp == 0) {
+    // prefix sums of H * ns_b over the sessions, 32 sessions per warp scan step
+    int run = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < p.batch) n = p.H * ((min(p.offsets[b] + 1, p.C) + kps - 1) / kps);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, n, o);
+        if (lane >= o) n += t;
+      }
+      if (b < p.batch) s_pref[b + 1] = run + n;
+      run += __shfl_sync(0xffffffffu, n, 31);
+    }
+    if (lane == 0) s_pref[0] = 0;
+  }
+  __syncthreads();
+  const int total = dense ? s_pref[p.batch] : p.batch * p.H * p.nsplit;
   const uint64_t pol = l2_policy_evict_first();
   // thread 0 only: the next valid item at or after `it` (stride gridDim.x), then its load
   int last = blockIdx.x - (int)gridDim.x;  // last item index issued by this CTA
+  int walk_b = 0;                          // dense numbering: session of that item
   auto issue_next = [&](int s) {
     AttnItem x;
     int it = last + (int)gridDim.x;
     const int G = (int)gridDim.x, per_b = p.nsplit * p.H;
-    while (it < total && !attn_decode_item(p, it, x)) {
-      // past session b's window: every later split of b is empty too, so go to the first
-      // item of session b + 1 in this CTA's stride class (it mod G fixed)
-      const int base = (x.b + 1) * per_b;
-      it = base + (((it - base) % G) + G) % G;
+    if (dense) {
+      if (it < total) attn_dense_item(p, s_pref, it, walk_b, x);
+    } else {
+      while (it < total && !attn_decode_item(p, it, x)) {
+        // past session b's window: every later split of b is empty too, so go to the
+        // first item of session b + 1 in this CTA's stride class (it mod G fixed)
+        const int base = (x.b + 1) * per_b;
+        it = base + (((it - base) % G) + G) % G;
+      }
     }
     s_item[s] = it;
     if (it >= total) return;
+    s_info[s] = x;
     last = it;
     KT* const st = stage0 + (size_t)s * stage_elems;
     const int row = (int)(p.row_bs * x.b + p.row0 + x.j0);
@@ -221,8 +268,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       }
       return;
     }
-    AttnItem cur;
-    attn_decode_item(p, item, cur);
+    const AttnItem cur = s_info[s];
     const int b = cur.b, h = cur.h, n = cur.j1 - cur.j0;
     // G lanes share one key, 16 dimensions each; a warp covers KPI keys per step
     constexpr int G = HD / 16, KPI = 32 / G;

@@ -52,6 +52,31 @@ def test_attention_matches_oracle(B, H, hd, C, positions, dtype):
             np.testing.assert_allclose(out[b], want, rtol=1e-4, atol=2e-5)
 
 
+@pytest.mark.parametrize("B", [256, 257])
+def test_attention_many_sessions(B):
+    """Up to 256 sessions the kernel numbers only the splits inside each window; past that
+    it walks every (session, split, head) and skips the empty ones.  Both must agree with
+    the oracle on windows of every length class (one key, a ragged split, full, wrapped)."""
+    H, hd, C = 2, 32, 96
+    g = torch.Generator().manual_seed(4242 + B)
+    D = H * hd
+    positions = [int(x) for x in torch.randint(0, 3 * C, (B,), generator=g)]
+    positions[:4] = [0, 37, C - 1, 2 * C + 5]
+    q = torch.randn(B, D, generator=g)
+    k = torch.randn(B, C, D, generator=g)
+    v = torch.randn(B, C, D, generator=g)
+    pos = torch.tensor(positions, dtype=torch.int32)
+    out = binding.attention(q.cuda(), k.cuda(), v.cuda(), pos.cuda(), H, hd).cpu().numpy()
+    for b in list(range(8)) + list(range(B - 8, B)):
+        ks = window_rows(k[b].numpy(), positions[b], C)
+        vs = window_rows(v[b].numpy(), positions[b], C)
+        want = oracle.attend(q[b].numpy(), ks, vs, H, hd)
+        if len(ks) == 1:
+            np.testing.assert_array_equal(out[b], want)
+        else:
+            np.testing.assert_allclose(out[b], want, rtol=1e-4, atol=2e-5)
+
+
 def test_attention_rejects_bad_arguments():
     L = binding.load()
     assert L.rq_attention(1, 4, 48, 64, 0, 1, 1, 1, 1, 1, 1, 1 << 20, None) == binding.RQ_ERR_UNSUPPORTED
