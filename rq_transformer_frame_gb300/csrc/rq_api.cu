@@ -52,6 +52,10 @@ struct rq_handle {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   int n_kernels = 0;
+  // persistent schedule only: the same frame as one kernel per op, replayed once the
+  // window is longer than kLongWindow (see frame_exec)
+  cudaGraph_t graph_long = nullptr;
+  cudaGraphExec_t exec_long = nullptr;
   // plans
   GemvPlan p_qkv{}, p_out{}, p_gin{}, p_gout{}, p_head{};
   GemvPlan p_depin{}, p_dqkv{}, p_dout{}, p_dgin{}, p_dgout{}, p_lin{};
@@ -374,17 +378,17 @@ FrameParams frame_params(const rq_handle* h) {
 }
 
 // One whole frame, in the page's order ("moshi_lm.rs", `step_ext` steps 1-8).
-cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s) {
+cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s, int sched) {
   cudaError_t e;
   const FrameParams f = frame_params(h);
   if ((e = launch_frame_begin(f, h->wes == 2, s)) != cudaSuccess) return e;
-  if (h->schedule == RQ_SCHEDULE_PERSISTENT) {
+  if (sched == RQ_SCHEDULE_PERSISTENT) {
     if ((e = launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
         cudaSuccess)
       return e;
     return launch_frame_end(f, s, true);
   }
-  if (h->schedule == RQ_SCHEDULE_TENSOR) {
+  if (sched == RQ_SCHEDULE_TENSOR) {
     if ((e = tc_frame_enqueue(h->tcf, s)) != cudaSuccess) return e;
     return launch_frame_end(f, s, true);
   }
@@ -420,6 +424,8 @@ namespace {
 void free_all(rq_handle* h) {
   if (h->exec) cudaGraphExecDestroy(h->exec);
   if (h->graph) cudaGraphDestroy(h->graph);
+  if (h->exec_long) cudaGraphExecDestroy(h->exec_long);
+  if (h->graph_long) cudaGraphDestroy(h->graph_long);
   void* dev[] = {h->ring, h->offsets, h->kcache, h->vcache, h->d_in, h->d_outb, h->x,
                  h->emb_sum, h->q, h->attn, h->u, h->tout, h->text_logits, h->audio_logits,
                  h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters, h->rng,
@@ -482,6 +488,8 @@ rq_status plan_all(rq_handle* h, std::string* why) {
 #define RQ_PERS_SLOT_BUDGET (96 * 1024)
 #endif
 constexpr int kPersSlotBudget = RQ_PERS_SLOT_BUDGET;
+// batch 1: windows longer than this run the one-kernel-per-op frame (see frame_exec)
+constexpr int kLongWindow = 1350;
 
 void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
   const rq_config& c = h->cfg;
@@ -1068,17 +1076,18 @@ rq_status create_impl(rq_handle* h) {
 
 // capture one frame as a graph (programmatic edges between consecutive kernels),
 // replacing the previous one
-rq_status capture_frame(rq_handle* h) {
-  if (h->exec) {
-    cudaGraphExecDestroy(h->exec);
-    h->exec = nullptr;
+// Capture one frame of schedule `sched` into (graph, exec), replacing what was there.
+rq_status capture_one(rq_handle* h, int sched, cudaGraph_t* graph, cudaGraphExec_t* exec) {
+  if (*exec) {
+    cudaGraphExecDestroy(*exec);
+    *exec = nullptr;
   }
-  if (h->graph) {
-    cudaGraphDestroy(h->graph);
-    h->graph = nullptr;
+  if (*graph) {
+    cudaGraphDestroy(*graph);
+    *graph = nullptr;
   }
   RQ_CUDA(h, cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
-  cudaError_t e = enqueue_frame(h, h->cap);
+  cudaError_t e = enqueue_frame(h, h->cap, sched);
   cudaGraph_t g = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(h->cap, &g);
   if (e != cudaSuccess) {
@@ -1086,8 +1095,15 @@ rq_status capture_frame(rq_handle* h) {
     return cuda_fail(h, e, "frame capture");
   }
   if (e2 != cudaSuccess) return cuda_fail(h, e2, "cudaStreamEndCapture");
-  h->graph = g;
-  RQ_CUDA(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
+  *graph = g;
+  RQ_CUDA(h, cudaGraphInstantiate(exec, *graph, 0));
+  RQ_CUDA(h, cudaGraphUpload(*exec, h->stream));
+  return RQ_OK;
+}
+
+rq_status capture_frame(rq_handle* h) {
+  rq_status st = capture_one(h, h->schedule, &h->graph, &h->exec);
+  if (st != RQ_OK) return st;
   size_t n = 0;
   RQ_CUDA(h, cudaGraphGetNodes(h->graph, nullptr, &n));
   std::vector<cudaGraphNode_t> nodes(n);
@@ -1099,8 +1115,23 @@ rq_status capture_frame(rq_handle* h) {
     if (t == cudaGraphNodeTypeKernel) ++k;
   }
   h->n_kernels = k;
-  RQ_CUDA(h, cudaGraphUpload(h->exec, h->stream));
+  if (h->schedule == RQ_SCHEDULE_PERSISTENT && h->cfg.context > kLongWindow)
+    return capture_one(h, RQ_SCHEDULE_GRAPH, &h->graph_long, &h->exec_long);
   return RQ_OK;
+}
+
+// The graph of the next frame.  At batch 1 the persistent kernel's attention keeps one
+// key per warp in flight, so its cost grows with the window faster than the split-K
+// attention kernel of the one-kernel-per-op frame, which streams K/V at the HBM rate.
+// Measured at the Moshi-7B shape: 4.39 / 4.61 ms per frame (persistent / per op) at a
+// 1000-position window, 4.78 / 4.69 ms at 1500, 5.26 / 4.99 ms at 2900.  Both frames
+// compute the same step on the same buffers.
+cudaGraphExec_t frame_exec(const rq_handle* h) {
+  if (h->exec_long) {
+    const int len = std::min(h->host_off[0] + 1, h->cfg.context);
+    if (len > kLongWindow) return h->exec_long;
+  }
+  return h->exec;
 }
 
 }  // namespace
@@ -1208,7 +1239,7 @@ rq_status run_frame_host(rq_handle* h, const int32_t* user, const int32_t* force
   }
   RQ_CUDA(h, cudaMemcpyAsync(h->d_in, h->h_in, io.in_words() * 4, cudaMemcpyHostToDevice, h->stream));
   h->forcing_dirty = forced != nullptr;
-  RQ_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  RQ_CUDA(h, cudaGraphLaunch(frame_exec(h), h->stream));
   RQ_CUDA(h, cudaMemcpyAsync(h->h_out, h->d_outb, io.out_bytes(), cudaMemcpyDeviceToHost, h->stream));
   RQ_CUDA(h, cudaStreamSynchronize(h->stream));
   for (int b = 0; b < B; ++b) h->host_off[b] += 1;
@@ -1250,7 +1281,7 @@ rq_status rq_step_device(rq_handle* h, const int32_t* d_user, int32_t* d_out_tok
     RQ_CUDA(h, cudaMemsetAsync(h->d_in + io.flag_off(), 0, (size_t)B * 4, h->stream));
     h->forcing_dirty = false;
   }
-  RQ_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  RQ_CUDA(h, cudaGraphLaunch(frame_exec(h), h->stream));
   if (d_out_tokens)
     RQ_CUDA(h, cudaMemcpyAsync(d_out_tokens, h->d_out_words() + io.out_off(), (size_t)B * 9 * 4,
                                cudaMemcpyDeviceToDevice, h->stream));

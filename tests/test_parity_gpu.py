@@ -105,6 +105,18 @@ def test_tiny_prefilled_start_and_eviction(schedule):
     run_free(c, 8, prefill=(k, v), schedule=schedule)
 
 
+def test_batch1_window_crosses_to_the_per_op_frame():
+    """At batch 1, windows longer than 1350 positions replay the one-kernel-per-op frame
+    instead of the persistent kernel: a session pre-filled to 1345 positions crosses the
+    switch in the middle of the run, and every frame must still match the oracle."""
+    c = configs.TINY.with_(context=1500)
+    g = torch.Generator().manual_seed(5)
+    n = 1345
+    k = torch.randn(c.layers, n, c.dim, generator=g)
+    v = torch.randn(c.layers, n, c.dim, generator=g)
+    run_free(c, 10, prefill=(k, v), schedule=binding.RQ_SCHEDULE_PERSISTENT)
+
+
 @pytest.mark.parametrize("schedule", SCHEDULES, ids=SCHED_IDS)
 def test_tiny_bf16_forced(schedule):
     run_forced(configs.TINY.with_(name="tiny_bf16", weight_dtype="bf16", kv_dtype="bf16"), 20,
