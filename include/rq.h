@@ -96,8 +96,9 @@ typedef struct {
  * TENSOR (batch <= 64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
  * runs every linear as one tcgen05 tensor-core GEMM over all sessions (padded to a
  * multiple of 16), the normalised f32 activations split into two bf16 operand parts
- * (16 significant bits), inside a CUDA graph.  AUTO picks PERSISTENT when it applies
- * (batch 1), TENSOR at batch >= 2 when it applies (it streams every weight once per
+ * (16 significant bits), inside a CUDA graph.  A PERSISTENT handle replays the GRAPH
+ * frame instead while the window is longer than 1350 positions (its attention kernel
+ * then streams K/V faster).  AUTO picks PERSISTENT when it applies (batch 1), TENSOR at batch >= 2 when it applies (it streams every weight once per
  * frame, where GRAPH streams it once per session), else GRAPH.
  * Results agree within the parity tolerance. */
 enum {
