@@ -343,10 +343,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     }
     __syncthreads();  // every warp is done with this stage and has published its state
     if (tid == 0) issue_next(s);  // refill the stage just consumed
-    // merge the warps in a fixed order into this split's partial (m, l, acc)
+    // merge the warps in a fixed order into this split's partial (m, l, acc); a window
+    // of one split is the whole result (the merge kernel skips it)
     if (tid < HD) {
       const size_t pstride = (size_t)HD + 2;
-      float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + cur.split) * pstride;
       float M = ninf;
 #pragma unroll
       for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
@@ -359,10 +359,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
           A += s_acc[w][tid] * c;
         }
       }
-      part[2 + tid] = A;
-      if (tid == 0) {
-        part[0] = M;
-        part[1] = L;
+      if (cur.ns == 1) {
+        const float o = A / L;
+        const size_t i = (size_t)b * p.D + (size_t)h * HD + tid;
+        p.out[i] = o;
+        if (p.out_bf16) store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, i, o);
+      } else {
+        float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + cur.split) * pstride;
+        part[2 + tid] = A;
+        if (tid == 0) {
+          part[0] = M;
+          part[1] = L;
+        }
       }
     }
     __syncthreads();  // s_m / s_acc / s_item are reused by the next item
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
   pdl_trigger();
   if (tid >= p.hd) return;
   const int ns = (min(p.offsets[b] + 1, p.C) + p.kps - 1) / p.kps;
+  if (ns == 1) return;  // the attention kernel wrote this (session, head) itself
   const size_t pstride = (size_t)p.hd + 2;
   const float* pb = p.part + ((size_t)b * p.H + h) * p.nsplit * pstride;
   float M = -__int_as_float(0x7f800000);
