@@ -341,13 +341,15 @@ size_t rq_band_row_bytes(int32_t dtype, int32_t cols);
 rq_status rq_quantize(int32_t dtype, const void *src, int32_t src_dtype, int64_t rows,
                       int32_t cols, void *dst, void *cuda_stream);
 
-/* Number of kernel launches in one frame (the captured graph's kernel nodes). */
+/* Number of kernel launches in one frame (the captured graph's kernel nodes; for a
+ * persistent handle, the frame that runs while the window is at most 1350 positions). */
 int32_t rq_frame_kernel_count(const rq_handle *h);
 
 /* The schedule the handle runs: RQ_SCHEDULE_GRAPH, _PERSISTENT or _TENSOR. */
 int32_t rq_schedule(const rq_handle *h);
 
-/* Per-op timeline of the last frame under the persistent schedule: us[i] = time from the
+/* Per-op timeline of the last frame the persistent kernel ran (frames past the long-window
+ * switch do not run it and leave the timeline as it was): us[i] = time from the
  * start of op i to the start of op i+1 (the last: to the end of all ops), in
  * microseconds, stamped on the device with %globaltimer (synchronizes the stream).  Ops
  * in frame order: per temporal layer [qkv, attention, out_proj, gate_in, gate_out], the
