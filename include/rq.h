@@ -353,8 +353,9 @@ int32_t rq_schedule(const rq_handle *h);
  * start of op i to the start of op i+1 (the last: to the end of all ops), in
  * microseconds, stamped on the device with %globaltimer (synchronizes the stream).  Ops
  * in frame order: per temporal layer [qkv, attention, out_proj, gate_in, gate_out], the
- * text head, then per depformer step [input, per layer (qkv, attention+out_proj,
- * gate_in, gate_out), head].  us == NULL returns the op count; returns the number
+ * text head, the input projections of all 8 depformer steps (one op), then per depformer
+ * step [per layer (qkv — the first adding the step's embedding row —,
+ * attention+out_proj, gate_in, gate_out), head].  us == NULL returns the op count; returns the number
  * written, 0 under the graph schedule.  -1 marks an op that was not stamped. */
 int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
 

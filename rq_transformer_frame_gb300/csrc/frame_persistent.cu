@@ -154,7 +154,31 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
       }
     }
   }
-  if (op.pro == PRO_RMS) {
+  if (op.pro == PRO_RMS_EMB) {
+    // a depformer step's input: dep_in[cb] . t (computed beside the text head) plus
+    // "moshi_lm.rs", `embed` of the step's conditioning token (-1 adds nothing, else row
+    // max(tok, 0)); CTA 0 keeps this x for the residuals
+    const IoLayout io{1};
+    const int prev = P.d_in[io.flag_off()] ? P.d_in[io.forced_off() + op.key_index]
+                                           : argmax_key_index(__ldcg(P.keys + op.key_index));
+    const bool keep = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
+#pragma unroll
+    for (int j = 0; j < kMaxNch; ++j) {
+      const int c = tig + j * pl.tpr;
+      if (j < nch && c < CC) {
+        if (prev != -1) {
+#pragma unroll
+          for (int v = 0; v < V; ++v)
+            xr[j][v] += Chunk<WT>::elem(op.emb, (size_t)max(prev, 0) * K + c * V + v);
+        }
+        if (keep) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) op.side_out[c * V + v] = xr[j][v];
+        }
+      }
+    }
+  }
+  if (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB) {
     // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).
     // Every row group holds the whole vector: group 0's warps sum the squares from
     // registers; alpha (a constant) was loaded before the grid barrier.
@@ -170,7 +194,8 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     for (int w = 0; w < pl.tpr / 32; ++w) tot += s_red[w];
     bar_sync(1, kCons);  // s_red is reused by the next op
     const float inv = 1.0f / sqrtf(P.eps + tot / (float)K);
-    const bool side = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
+    const bool side =
+        op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0;
 #pragma unroll
     for (int j = 0; j < kMaxNch; ++j) {
       const int c = tig + j * pl.tpr;
@@ -654,7 +679,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
     for (int k = 0; k < P.n_ops; ++k) {
       {  // constant alpha of an RMSNorm prologue: load it before waiting
         const PersOp& op = P.ops[k];
-        if (op.type == OPT_GEMV && op.pro == PRO_RMS) {
+        if (op.type == OPT_GEMV && (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB)) {
           const GemvPlan& pl = P.plans[op.plan];
           const int tig = tid % pl.tpr, CC = pl.K / V;
 #pragma unroll
@@ -665,7 +690,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           }
         }
       }
-      if (k > 0) {
+      if (k > 0 && !P.ops[k].nobar) {
         if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * gridDim.x)) {
           atomicOr(P.status, kDevTimeout);
           s_abort = 1;

@@ -70,7 +70,9 @@ long long frame_draws(const SampleParams& sp);
 enum GemvPro : int {
   PRO_PLAIN = 0,  // x = in[b]
   PRO_RMS = 1,    // x = in[b] * alpha * 1/sqrt(eps + mean(in[b]^2))
-  PRO_DATTN = 2   // x = depformer attention of dq[b] over keys 0..n_keys-1
+  PRO_DATTN = 2,  // x = depformer attention of dq[b] over keys 0..n_keys-1
+  PRO_RMS_EMB = 3  // persistent schedule: x = in + E[prev] (CTA 0 also stores this x to
+                   // side_out), then as PRO_RMS; prev is pick key_index (or the forced token)
 };
 enum GemvEpi : int {
   EPI_STORE = 0,   // out[b][r] = y
@@ -266,7 +268,9 @@ struct PersOp {
   float* dk_out;        // EPI_DQKV
   float* dv_out;
   int key_index;
-  const void* emb;      // EPI_DEPIN
+  const void* emb;      // EPI_DEPIN / PRO_RMS_EMB: table [rows][n_out or K]
+  int nobar;            // 1: no grid barrier before this op (it reads nothing the previous
+                        // op writes)
 };
 
 constexpr int kPersMaxPlans = 12;

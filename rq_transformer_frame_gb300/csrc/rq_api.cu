@@ -43,6 +43,7 @@ struct rq_handle {
   float *tout = nullptr, *text_logits = nullptr, *audio_logits = nullptr;
   unsigned long long* keys = nullptr;
   float *dx = nullptr, *dq = nullptr, *dkv = nullptr, *du = nullptr;
+  float* dep_pre = nullptr;  // persistent schedule: dep_in[cb] . t of the 8 steps [8][DD]
   float* part = nullptr;
   int* counters = nullptr;
   // pinned host staging
@@ -429,6 +430,7 @@ void free_all(rq_handle* h) {
   void* dev[] = {h->ring, h->offsets, h->kcache, h->vcache, h->d_in, h->d_outb, h->x,
                  h->emb_sum, h->q, h->attn, h->u, h->tout, h->text_logits, h->audio_logits,
                  h->keys, h->dx, h->dq, h->dkv, h->du, h->part, h->counters, h->rng,
+                 h->dep_pre,
                  h->xs_jump};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -505,8 +507,9 @@ void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
   pl[8] = plan_persistent(c.dhidden, c.ddim, es, true, false, G);
   pl[9] = plan_persistent(c.ddim, c.dhidden, es, false, false, G);
   pl[10] = plan_persistent(c.audio_card, c.ddim, es, false, false, G);
+  pl[11] = plan_persistent(8 * c.ddim, c.dim, es, false, false, G);
 }
-constexpr int kPersPlans = 11;
+constexpr int kPersPlans = 12;
 
 std::vector<PersOp> pers_ops(const rq_handle* h) {
   const rq_config& c = h->cfg;
@@ -560,6 +563,15 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
   hd.out = h->text_logits;
   hd.key_index = 0;
   ops.push_back(hd);
+  // the 8 steps' input projections dep_in[cb] . t at once, beside the text head: t is the
+  // same out_norm(x), so this op needs no barrier after the head; each step's first
+  // layer adds its embedding row E[prev] in its prologue
+  PersOp da = gemv(PRO_RMS, EPI_STORE, 11, h->w.dep_in);
+  da.in = h->x;
+  da.alpha = h->w.out_norm;
+  da.out = h->dep_pre;
+  da.nobar = 1;
+  ops.push_back(da);
   auto topk_op = [&](const float* logits, int p) {
     PersOp t{};
     t.type = OPT_TOPK;
@@ -570,16 +582,19 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
   const bool topk = h->samp.mode == SAMPLE_TOPK;
   if (topk) topk_op(h->text_logits, 0);
   for (int cb = 0; cb < 8; ++cb) {
-    PersOp o = gemv(PRO_PLAIN, EPI_DEPIN, 5, woff(h->w.dep_in, (size_t)cb * DD * D, es));
-    o.in = h->tout;
-    o.out = h->dx;
-    o.emb = cb == 0 ? h->w.dep_text_emb : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, es);
-    o.key_index = cb;
-    ops.push_back(o);
+    PersOp o{};
     for (int l = 0; l < c.dlayers; ++l) {
       const size_t ls = (size_t)l * 8 + cb;
-      o = gemv(PRO_RMS, EPI_DQKV, 6, woff(h->w.d_in_proj, ls * 3 * DD * DD, es));
+      o = gemv(l == 0 ? PRO_RMS_EMB : PRO_RMS, EPI_DQKV, 6,
+               woff(h->w.d_in_proj, ls * 3 * DD * DD, es));
       o.in = h->dx;
+      if (l == 0) {  // x = dep_in[cb] . t + E[prev], kept in dx for the residuals
+        o.in = h->dep_pre + (size_t)cb * DD;
+        o.side_out = h->dx;
+        o.emb = cb == 0 ? h->w.dep_text_emb
+                        : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, es);
+        o.key_index = cb;
+      }
       o.alpha = h->w.dnorm1 + (size_t)l * DD;
       o.out = h->dq;
       o.dk_out = h->dkv + dkv_off(h, l, 0, cb);
@@ -1047,6 +1062,7 @@ rq_status create_impl(rq_handle* h) {
     h->samp.jump = h->xs_jump;
   }
   RQ_ALLOC(h->dx, B * DD * 4);
+  RQ_ALLOC(h->dep_pre, B * 8 * DD * 4);
   RQ_ALLOC(h->dq, B * DD * 4);
   RQ_ALLOC(h->dkv, B * DL * 2 * 8 * DD * 4);
   RQ_ALLOC(h->du, B * DF * 4);
