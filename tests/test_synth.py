@@ -87,3 +87,23 @@ def test_kv_prefill_recipe():
     k3, _ = synth.kv_prefill(c, 3)
     assert not torch.equal(k, k3)
     assert abs(float(k.float().std()) - 1.0) < 0.05
+
+
+def test_moshi7b_shape_is_the_pages():
+    """The Moshi-7B workload has the page's decode shape (tests/golden/moshi7b_shape.json)."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "moshi7b_shape.json")))
+    c = configs.MOSHI7B
+    for k in ("dim", "layers", "heads", "head_dim", "context", "hidden", "ddim", "dlayers",
+              "dheads", "dhead_dim", "dhidden", "text_card", "audio_card"):
+        assert getattr(c, k) == g[k], k
+    assert c.eps == g["rms_eps"]
+    assert g["hidden"] == round(2 * 4.125 * g["dim"] / 3)
+    assert g["dhidden"] == round(2 * 4.125 * g["ddim"] / 3)
+    assert g["heads"] * g["head_dim"] == g["dim"] and g["dheads"] * g["dhead_dim"] == g["ddim"]
+    assert g["ring"] == g["max_delay"] + 2 and max(g["delays"]) == g["max_delay"]
+    assert len(g["delays"]) == 17
+    for name in ("moshi7b_b16", "moshi7b_b64"):
+        b = configs.CONFIGS[name]
+        assert (b.dim, b.layers, b.hidden, b.context) == (c.dim, c.layers, c.hidden, c.context)
