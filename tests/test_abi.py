@@ -116,3 +116,11 @@ def test_new_entry_points_on_null_handle_are_errors(lib):
     assert lib.rq_snapshot_size(None, 0) == 0
     assert lib.rq_snapshot(None, 0, None, 0) == binding.RQ_ERR_ARG
     assert lib.rq_restore(None, 0, None, 0) == binding.RQ_ERR_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """There is no CPU fallback: without the built CUDA library the binding raises."""
+    monkeypatch.setattr(binding, "LIBPATH", str(tmp_path / "librq.so"))
+    monkeypatch.setattr(binding, "_LIB", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load()
