@@ -147,7 +147,8 @@ typedef struct {
 typedef struct rq_handle rq_handle;
 
 /* Create a decoder for cfg->batch sessions on the current CUDA device, all sessions
- * fresh (ring UNGENERATED, offset 0, empty K/V).  `cuda_stream` is a cudaStream_t
+ * fresh (ring UNGENERATED, offset 0, empty K/V), as "moshi_lm.rs", `MoshiLm::state`
+ * makes one session.  `cuda_stream` is a cudaStream_t
  * (may be NULL).  Allocates every device buffer and captures the frame as a CUDA
  * graph.  On failure *out is NULL and nothing is leaked. */
 rq_status rq_create(const rq_config *cfg, const rq_weights *w, void *cuda_stream,
@@ -157,8 +158,9 @@ rq_status rq_create(const rq_config *cfg, const rq_weights *w, void *cuda_stream
  * no-op. */
 void rq_destroy(rq_handle *h);
 
-/* Return session `session` (or every session, -1) to the fresh state.  K/V memory is
- * not cleared: positions past the offset are never read.  rq_reset(h, -1) also
+/* Return session `session` (or every session, -1) to the fresh state of
+ * "moshi_lm.rs", `MoshiLm::state` (ring UNGENERATED, offset 0, empty K/V window).  K/V
+ * memory is not cleared: positions past the offset are never read.  rq_reset(h, -1) also
  * clears a poisoned handle. */
 rq_status rq_reset(rq_handle *h, int32_t session);
 
@@ -198,7 +200,8 @@ rq_status rq_step_device(rq_handle *h, const int32_t *d_user, int32_t *d_out_tok
 /* Synchronize the handle's stream and read the device status word. */
 rq_status rq_sync(rq_handle *h);
 
-/* Debug / parity reads of the last frame (synchronize the stream).
+/* Debug / parity reads of the last frame (synchronize the stream), the logits fields of
+ * "moshi_lm.rs", `StepTrace`:
  *   text  host [B][V] text-head logits;  audio host [B][8][A] depformer logits.
  * Either pointer may be NULL. */
 rq_status rq_get_logits(rq_handle *h, float *text, float *audio);
@@ -207,7 +210,9 @@ rq_status rq_get_logits(rq_handle *h, float *text, float *audio);
  * `StepTrace.emb_sum`, `.transformer_out`), host [B][D] each; either may be NULL. */
 rq_status rq_get_trace(rq_handle *h, float *emb_sum, float *transformer_out);
 
-/* The ring cache (host [B][17][3]) and offsets (host [B]); either may be NULL. */
+/* The delayed-token ring cache (host [B][17][3], stream-major, slot = step % 3) and the
+ * offsets (host [B]) of "moshi_lm.rs", `MoshiState` (`cache`, `offset`); either may be
+ * NULL. */
 rq_status rq_get_ring(rq_handle *h, int32_t *ring, int32_t *offsets);
 
 /* Pre-fill session `session`: temporal K/V positions 0..n_pos-1 of every layer take
@@ -268,8 +273,9 @@ rq_status rq_attention(int32_t batch, int32_t heads, int32_t head_dim, int32_t c
  *   rq_attention_workspace_size(batch, heads, head_dim, context), exceeds 4 MiB are
  *   refused with RQ_ERR_UNSUPPORTED before anything is enqueued.
  *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
- *   The first call on a device looks up the array's device address for that device;
- *   make that first call before any stream capture.
+ *   The first call on a device looks up the array's device address there (again after
+ *   the device's context changes, e.g. after cudaDeviceReset, so no stale address is
+ *   used); make that first call before any stream capture.
  *   Every call shares the one array and leaves its contents behind; the call clears
  *   what must start at zero itself.  Calls that overlap on the GPU (other streams or
  *   threads) race on the array: serialize them. */
@@ -358,6 +364,17 @@ int32_t rq_schedule(const rq_handle *h);
  * attention+out_proj, gate_in, gate_out), head].  us == NULL returns the op count; returns the number
  * written, 0 under the graph schedule.  -1 marks an op that was not stamped. */
 int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
+
+/* Test hook of the failure path: the limit, in nanoseconds, of the device-side waits of
+ * the batch-1 whole-frame kernel (its grid barrier and weight-ring waits); 0 restores the
+ * default of 2 s.  stall_op >= 0 makes the grid barrier in front of op `stall_op` of
+ * the frame's op table (the order of rq_get_op_times, op >= 1) wait for one CTA more than
+ * the grid holds, so every wait there runs out after limit_ns: the frame then returns
+ * RQ_ERR_TIMEOUT, later calls RQ_ERR_POISONED until rq_reset(h, -1).  -1 removes the
+ * stall.  Nothing traps and no wait is unbounded.  Applies to frames run by the
+ * persistent kernel (RQ_ERR_UNSUPPORTED under the other schedules); synchronizes the
+ * stream.  Survey of the failure handling: the timeout reports instead of hanging. */
+rq_status rq_set_wait_limit(rq_handle *h, uint64_t limit_ns, int32_t stall_op);
 
 const char *rq_last_error(const rq_handle *h);
 const char *rq_status_string(rq_status s);

@@ -98,6 +98,8 @@ def load() -> C.CDLL:
     L.rq_frame_kernel_count.restype = I32
     L.rq_schedule.argtypes = [P]
     L.rq_schedule.restype = I32
+    L.rq_set_wait_limit.argtypes = [P, C.c_uint64, I32]
+    L.rq_set_wait_limit.restype = C.c_int
     L.rq_get_op_times.argtypes = [P, P, I32]
     L.rq_get_op_times.restype = I32
     L.rq_last_error.argtypes = [P]
@@ -308,6 +310,11 @@ class Decoder:
         """k, v: [layers][n_pos][dim] tensors in the K/V dtype (host or device)."""
         k, v = k.contiguous(), v.contiguous()
         self._check(self.L.rq_set_kv(self.h, int(session), int(k.shape[1]), _p(k), _p(v)))
+
+    def set_wait_limit(self, limit_ns: int, stall_op: int = -1):
+        """Test hook (rq_set_wait_limit): device wait limit of the whole-frame kernel and
+        an op whose grid barrier is made unreachable (-1: none)."""
+        self._check(self.L.rq_set_wait_limit(self.h, int(limit_ns), int(stall_op)))
 
     def launch_op(self, op: int, layer: int, count: int) -> float:
         b = C.c_double(0)

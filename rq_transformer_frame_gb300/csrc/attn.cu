@@ -507,14 +507,10 @@ cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool 
 #include "../../include/rq.h"
 
 namespace {
-#ifndef RQ_ATTN_KPS
-#define RQ_ATTN_KPS 64
-#endif
-constexpr int kStandaloneKps = RQ_ATTN_KPS;  // positions per split, as in the frame
+constexpr int kStandaloneKps = rqk::kStandaloneAttnKps;  // positions per split, as in the frame
 
 size_t partial_bytes(int B, int H, int hd, int C) {
-  const size_t nsplit = (size_t)(C + kStandaloneKps - 1) / kStandaloneKps;
-  return ((size_t)B * H * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  return rqk::standalone_attn_partial_bytes(B, H, hd, C);
 }
 }  // namespace
 

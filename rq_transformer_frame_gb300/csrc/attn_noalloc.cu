@@ -9,9 +9,13 @@
 //
 // The array (kScratchBytes, 4 MiB) exists on every GPU that loads the library, until
 // the process exits.  Host code cannot use the array's name as a device address (on the
-// host it is only a stand-in), so the device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, and that pointer is what the
-// kernel receives.
+// host it is only a stand-in), so the device address is looked up with
+// cudaGetSymbolAddress while the device is current, and that pointer is what the
+// kernel receives.  The address belongs to the CUDA context the library's module was
+// loaded into: it is cached per device together with that context's unique id and
+// looked up again whenever the current context is another one (after cudaDeviceReset,
+// or under a caller's own driver-API context), so a stale address is never used.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,34 +26,74 @@
 namespace {
 
 constexpr size_t kScratchBytes = 4u << 20;  // 4 MiB: partials + tickets
-constexpr int kKps = 64;                     // positions per split, as in the frame
+constexpr int kKps = rqk::kStandaloneAttnKps;  // positions per split, as rq_attention
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_attn_scratch on the current device (looked up on first use).
+struct CachedAddr {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to
+  void* addr;
+};
+
+std::mutex g_mu;
+CachedAddr g_scratch[kMaxDevices] = {};
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+template <typename Fn>
+bool driver_fn(const char* name, int version, Fn* out) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !f)
+    return false;
+  *out = reinterpret_cast<Fn>(f);
+  return true;
+}
+
+// unique id of the calling thread's current context (0 if there is none yet)
+cudaError_t current_ctx_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (!ctx) return cudaSuccess;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Device address of g_attn_scratch for the current device and context: looked up with
+// cudaGetSymbolAddress on first use and whenever the current context has changed.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_ctx_current && (!driver_fn("cuCtxGetCurrent", 4000, &g_ctx_current) ||
+                         !driver_fn("cuCtxGetId", 12000, &g_ctx_id))) {
+    g_ctx_current = nullptr;
+    return cudaErrorNotSupported;
+  }
+  unsigned long long id = 0;
+  if ((e = current_ctx_id(&id)) != cudaSuccess) return e;
+  if (id == 0 || id != g_scratch[dev].ctx_id || !g_scratch[dev].addr) {
     void* p = nullptr;
+    // makes the device's primary context current if the thread has none yet
     e = cudaGetSymbolAddress(&p, g_attn_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    if ((e = current_ctx_id(&id)) != cudaSuccess) return e;
+    if (id == 0) return cudaErrorDeviceUninitialized;
+    g_scratch[dev] = CachedAddr{id, p};
   }
-  *out = g_scratch_addr[dev];
+  *out = g_scratch[dev].addr;
   return cudaSuccess;
 }
 
 size_t partial_bytes(int B, int H, int hd, int C) {
-  const size_t nsplit = (size_t)(C + kKps - 1) / kKps;
-  return ((size_t)B * H * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  return rqk::standalone_attn_partial_bytes(B, H, hd, C);
 }
 
 }  // namespace

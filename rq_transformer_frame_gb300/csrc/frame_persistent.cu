@@ -36,15 +36,16 @@ __device__ __forceinline__ void grid_arrive(unsigned* bar) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
 }
 
-// thread 0 of the consumers: wait until `target` CTAs have arrived (bounded)
-__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target) {
+// thread 0 of the consumers: wait until `target` CTAs have arrived (bounded by limit_ns)
+__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target,
+                                          uint64_t limit_ns) {
   if (ld_acquire(bar) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (ld_acquire(bar) >= target) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -59,14 +60,15 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
                                               uint8_t* ring, int slot_bytes, int NS,
                                               uint64_t* full, uint64_t* empty, float* part,
                                               const float (&xr)[kMaxNch][Chunk<WT>::V],
-                                              int g, int tig, int warp, int lane) {
+                                              int g, int tig, int warp, int lane,
+                                              uint64_t lim) {
   constexpr int RG = GemvShape<NCH>::RG;
   const uint32_t row_bytes = (uint32_t)Kw * (uint32_t)sizeof(WT);
   const int CC = Kw / Chunk<WT>::V;
   const int wpg = pl.tpr >> 5;
   for (int i = 0; i < nt; ++i, ++gi) {
     const int s = (int)(gi % (uint32_t)NS);
-    if (!mbar_wait(&full[s], (gi / (uint32_t)NS) & 1u)) return false;
+    if (!mbar_wait_for(&full[s], (gi / (uint32_t)NS) & 1u, lim)) return false;
     const uint8_t* row0 = ring + (size_t)s * slot_bytes + (size_t)(g * RG) * row_bytes;
     float acc[RG][2];
 #pragma unroll
@@ -586,6 +588,10 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
   __shared__ volatile int s_abort;
   __shared__ unsigned s_issued;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // wait limit of this launch (a test may shorten it), and the op whose barrier a test
+  // makes unreachable (-1: none)
+  const uint64_t lim = P.wait_ctl && P.wait_ctl[0] ? P.wait_ctl[0] : kWaitLimitNs;
+  const int stall_op = P.wait_ctl ? (int)P.wait_ctl[1] - 1 : -1;
   const int NS = P.n_slots;
   uint8_t* ring = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)NS * P.slot_bytes);
@@ -624,7 +630,8 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           const uint32_t seg = (uint32_t)Kw * (uint32_t)sizeof(WT);  // bytes of one row part
           for (int t = t0; t < t1; ++t) {
             const int s = (int)(gi % (uint32_t)NS);
-            if (gi >= (uint32_t)NS && !mbar_wait(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u)) {
+            if (gi >= (uint32_t)NS &&
+                !mbar_wait_for(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u, lim)) {
               atomicOr(P.status, kDevTimeout);
               s_abort = 1;
             }
@@ -691,7 +698,8 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         }
       }
       if (k > 0 && !P.ops[k].nobar) {
-        if (tid == 0 && !grid_wait(P.grid_bar, (unsigned)k * gridDim.x)) {
+        const unsigned target = (unsigned)k * gridDim.x + (k == stall_op ? 1u : 0u);
+        if (tid == 0 && !grid_wait(P.grid_bar, target, lim)) {
           atomicOr(P.status, kDevTimeout);
           s_abort = 1;
         }
@@ -737,10 +745,10 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
             form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, s_att);
             if (nch <= 1)
               ok = consume_tiles<WT, 1>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
-                                        empty, part, xr, g, tig, warp, lane);
+                                        empty, part, xr, g, tig, warp, lane, lim);
             else
               ok = consume_tiles<WT, 2>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
-                                        empty, part, xr, g, tig, warp, lane);
+                                        empty, part, xr, g, tig, warp, lane, lim);
           }
           if (!ok) {
             atomicOr(P.status, kDevTimeout);
@@ -754,13 +762,14 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
       bar_sync(1, kCons);
       if (tid == 0) grid_arrive(P.grid_bar);
     }
-    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x))
+    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x, lim))
       P.trace[P.n_ops] = global_timer_ns();
   }
   __syncthreads();
   pdl_trigger();
   if (s_abort) {
-    // wind down: wait (bounded) for this CTA's copies still in flight
+    // wind down: wait for this CTA's copies still in flight, bounded by the default
+    // limit (not a shortened one: the copies land on their own within microseconds)
     if (tid == 0) {
       const unsigned issued = s_issued;
       for (unsigned i = issued > (unsigned)NS ? issued - NS : 0u; i < issued; ++i)

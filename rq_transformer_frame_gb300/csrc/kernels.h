@@ -168,6 +168,17 @@ struct AttnParams {
   uint32_t* status;
 };
 cudaError_t launch_attn(const AttnParams& p, bool kv_bf16, cudaStream_t s, bool pdl);
+// Standalone decode attention (rq_attention and rq_attention_noalloc): positions per
+// split, and the bytes of the per-split partials that precede the merge tickets in the
+// scratch (B x H x nsplit rows of hd + 2 floats, rounded up to 256 bytes).
+#ifndef RQ_ATTN_KPS
+#define RQ_ATTN_KPS 64
+#endif
+constexpr int kStandaloneAttnKps = RQ_ATTN_KPS;
+inline size_t standalone_attn_partial_bytes(int B, int H, int hd, int C) {
+  const size_t nsplit = (size_t)(C + kStandaloneAttnKps - 1) / kStandaloneAttnKps;
+  return ((size_t)B * H * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+}
 // shared-memory attribute and occupancy of the attention kernel (call outside capture)
 cudaError_t attn_configure(int hd, bool kv_bf16, int kps);
 cudaError_t launch_dattn_batched(const float* dq, long long dq_bs, const float* dk,
@@ -296,6 +307,10 @@ struct PersParams {
   int* counters;
   int D, H, kps, nsplit;
   unsigned int* grid_bar;  // zero at launch
+  // wait control read once per launch: [0] limit of the grid-barrier and weight-ring
+  // waits in ns (0: kWaitLimitNs); [1] test stall: k + 1 makes the barrier before op k
+  // wait for one CTA more than the grid has, so every wait there runs out (0: none)
+  const unsigned long long* wait_ctl;
   uint32_t* status;
   unsigned long long* trace;  // [n_ops + 1] op start times (ns), CTA 0 (nullable)
   SampleParams samp;

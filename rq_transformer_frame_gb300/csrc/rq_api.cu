@@ -492,6 +492,9 @@ rq_status plan_all(rq_handle* h, std::string* why) {
 constexpr int kPersSlotBudget = RQ_PERS_SLOT_BUDGET;
 // batch 1: windows longer than this run the one-kernel-per-op frame (see frame_exec)
 constexpr int kLongWindow = 1350;
+// 64-bit word index, inside the grid barrier's 256-byte allocation, of the persistent
+// kernel's wait-control pair (see PersParams::wait_ctl)
+constexpr int kWaitCtlWord = 16;
 
 void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
   const rq_config& c = h->cfg;
@@ -999,6 +1002,8 @@ rq_status setup_schedule(rq_handle* h) {
   P.kps = 16;  // shortest split; the kernel sizes splits from the window (16..64)
   P.nsplit = (c.context + 15) / 16;
   P.grid_bar = h->grid_bar;
+  // the wait-control words live in the same 256-byte allocation, zero = defaults
+  P.wait_ctl = reinterpret_cast<const unsigned long long*>(h->grid_bar) + kWaitCtlWord;
   P.status = h->d_status();
   h->pers_grid = G;
   h->pers_smem = smem;
@@ -1671,6 +1676,20 @@ rq_status rq_restore(rq_handle* h, int32_t session, const void* src, size_t size
 int32_t rq_frame_kernel_count(const rq_handle* h) { return h ? h->n_kernels : 0; }
 
 int32_t rq_schedule(const rq_handle* h) { return h ? h->schedule : 0; }
+
+rq_status rq_set_wait_limit(rq_handle* h, uint64_t limit_ns, int32_t stall_op) {
+  if (!h) return RQ_ERR_ARG;
+  if (h->schedule != RQ_SCHEDULE_PERSISTENT || !h->grid_bar)
+    return fail(h, RQ_ERR_UNSUPPORTED, "the wait limit applies to the persistent schedule");
+  if (stall_op < -1 || stall_op == 0 || stall_op >= h->pers.n_ops)
+    return fail(h, RQ_ERR_ARG, "stall_op outside [1, ops) and not -1");
+  const unsigned long long ctl[2] = {(unsigned long long)limit_ns,
+                                     (unsigned long long)(stall_op + 1)};
+  RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  RQ_CUDA(h, cudaMemcpy(reinterpret_cast<unsigned long long*>(h->grid_bar) + kWaitCtlWord, ctl,
+                        sizeof(ctl), cudaMemcpyHostToDevice));
+  return RQ_OK;
+}
 
 int32_t rq_get_op_times(rq_handle* h, float* us, int32_t max_ops) {
   if (!h || h->schedule != RQ_SCHEDULE_PERSISTENT || !h->trace) return 0;

@@ -72,6 +72,23 @@ class Ref64:
                 "K": [[] for _ in range(self.c.layers)],
                 "V": [[] for _ in range(self.c.layers)]}
 
+    def prefilled_state(self, k, v):
+        """A session that resumes at offset n with the temporal window already holding
+        positions 0..n-1 of every layer: k, v [layers][n][dim] (any float dtype, taken
+        as already-rotated rows).  The clock moves without generating anything, as
+        `MoshiState::advance_clock` does, so the delayed-token ring stays all
+        UNGENERATED (-2)."""
+        st = self.new_state()
+        k = np.asarray(k, dtype=np.float64)
+        v = np.asarray(v, dtype=np.float64)
+        n = k.shape[1]
+        assert k.shape == v.shape == (self.c.layers, n, self.c.dim) and n <= self.c.context
+        for layer in range(self.c.layers):
+            st["K"][layer] = [k[layer, p].copy() for p in range(n)]
+            st["V"][layer] = [v[layer, p].copy() for p in range(n)]
+        st["off"] = n
+        return st
+
     def embed_row(self, table, tok):
         if tok == -1:
             return np.zeros(table.shape[1])

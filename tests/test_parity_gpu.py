@@ -62,14 +62,19 @@ def run_free(c, frames, w=None, prefill=None, schedule=binding.RQ_SCHEDULE_AUTO)
     dec.close()
 
 
-def run_forced(c, frames, w=None, schedule=binding.RQ_SCHEDULE_AUTO):
-    """The GPU is forced with the oracle's own tokens; compare own tokens + logits."""
+def run_forced(c, frames, w=None, schedule=binding.RQ_SCHEDULE_AUTO, prefill=None):
+    """The GPU is forced with the oracle's own tokens; compare own tokens + logits.
+    prefill: (K, V) CPU tensors [layers][n][dim] given to both sides before frame 0."""
     w = w if w is not None else weights_of(c)
     dec = binding.Decoder(c, binding.upload_weights(w), schedule=schedule)
     if schedule != binding.RQ_SCHEDULE_AUTO:
         assert dec.schedule == schedule
     orc = oracle.Oracle(c, w)
     st = orc.new_state()
+    if prefill is not None:
+        k, v = prefill
+        st.set_kv(k, v)
+        dec.set_kv(0, k.cuda(), v.cuda())
     users = synth.user_tokens(c, frames).numpy()
     for t in range(frames):
         r = orc.step(st, users[t], trace=True)
@@ -239,3 +244,15 @@ def test_moshi7b_full_size_forced_frames(schedule):
     """The Moshi-7B shape at batch 1 (the benchmark's workload; AUTO runs the
     persistent schedule) against the oracle on the first frames."""
     run_forced(configs.MOSHI7B, 4, schedule=schedule)
+
+
+@pytest.mark.parametrize("n_pos,frames", [(300, 4), (1345, 8)], ids=["window300", "window1345"])
+def test_moshi7b_prefilled_window_forced_frames(n_pos, frames):
+    """The Moshi-7B shape at batch 1 (AUTO: the persistent schedule) with the temporal
+    window pre-filled by N(0,1) bf16 rows, against the oracle.  At 300 positions the
+    whole-frame kernel's head_dim-128 attention runs many splits per head (16-position
+    splits) and merges them in order; from 1345 the window crosses 1350 positions at
+    frame 5, where the handle switches to its one-kernel-per-op frame."""
+    c = configs.MOSHI7B.with_(prefill=n_pos)
+    k, v = synth.kv_prefill(c, 0)
+    run_forced(c, frames, prefill=(k, v))

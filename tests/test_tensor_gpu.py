@@ -1,8 +1,9 @@
 """Parity of the batched tensor-core schedule (RQ_SCHEDULE_TENSOR: every linear one
 tcgen05 GEMM over all sessions, bf16 operands) with the CPU oracle, session by session.
 
-The GEMM operands are exact three-part bf16 expansions of the f32 activations, so the
-plain f32 oracle is the reference.  Same bar as the other parity tests: ring,
+The GEMM operands are two-part bf16 expansions hi + lo of the f32 activations (16
+significant bits, a relative representation error of at most 2^-17), so the plain
+f32 oracle is the reference.  Same bar as the other parity tests: ring,
 offsets and delayed outputs bit-exact; logits within 2e-2 * max|logit| (bf16 weights);
 a token may differ only where the oracle's top-2 margin is inside that tolerance.  Teacher-forced runs force every session with a
 seeded synthetic token stream on both sides, so a near-tie cannot fork a trajectory;
@@ -40,11 +41,22 @@ def forced_tokens(c, frames, seed=77):
 
 
 def run_batch_forced(c, frames, sessions):
+    """c.prefill > 0: every session starts as the batch-64 workload does -- K/V rows
+    0..prefill-1 of every layer from synth.kv_prefill (drawn on the GPU), offset
+    prefill, ring all UNGENERATED; the checked sessions' rows go to the oracle too."""
     w = weights_of(c)
     dec = binding.Decoder(c, binding.upload_weights(w), schedule=binding.RQ_SCHEDULE_TENSOR)
     assert dec.schedule == binding.RQ_SCHEDULE_TENSOR
     orc = oracle.Oracle(c, w)
     sts = {b: orc.new_state() for b in sessions}
+    if c.prefill > 0:
+        for b in range(c.batch):
+            k, v = synth.kv_prefill(c, b, device="cuda")
+            dec.set_kv(b, k, v)
+            if b in sts:
+                sts[b].set_kv(k.cpu(), v.cpu())
+            del k, v
+        torch.cuda.synchronize()
     users = synth.batch_user_tokens(c, frames).numpy()
     forced = forced_tokens(c, frames)
     worst = 0.0
@@ -140,3 +152,12 @@ def test_moshi7b_batch16_forced_frames():
 
 def test_moshi7b_batch64_forced_frames():
     run_batch_forced(configs.MOSHI7B.with_(batch=64), 2, [0, 63])
+
+
+def test_moshi7b_batch64_prefilled_workload():
+    """The batch-64 workload exactly as configured: 64 sessions whose temporal K/V hold
+    2900 pre-filled positions (offset 2900, ring all UNGENERATED, so frames 0-1 read
+    row 0 for -2), first frames on sessions 0 and 63 against the oracle."""
+    c = configs.MOSHI7B_B64
+    assert c.prefill == 2900 and c.batch == 64
+    run_batch_forced(c, 2, [0, 63])

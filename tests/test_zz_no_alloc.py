@@ -1,9 +1,11 @@
 """rq_attention_noalloc: decode attention for callers that cannot allocate device
 memory (a real-time audio thread that must not stall in cudaMalloc, a plug-in with a
 fixed memory budget).  Called through the C ABI, two calls in a row with different
-shapes (the second one runs on scratch the first one left behind), each compared with
-rq_attention -- the entry point that takes a caller workspace -- within the tolerance of
-the attention parity tests.  Oversized problems are refused before any launch.
+shapes, each compared with rq_attention -- the entry point that takes a caller
+workspace -- and with the CPU oracle's `attend`, within the tolerance of the attention
+parity tests.  The second call splits its windows into several 64-position parts but
+fewer than the first, so its merge reads partials written over the first call's
+leftovers.  Oversized problems are refused before any launch.
 
 This file is collected last so that a run stopping at the first failure has already
 run every other test."""
@@ -13,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from rq_transformer_frame_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -51,10 +54,24 @@ def _noalloc(L, q, k, v, pos, H, hd):
     return rc, out
 
 
+def _oracle_attend(q, k, v, positions, H, hd):
+    """The oracle's `attend` over each query's window: positions
+    max(0, pos - ctx + 1) .. pos, position j in cache slot j % ctx."""
+    ctx = k.shape[1]
+    kk, vv, qq = k.float().cpu().numpy(), v.float().cpu().numpy(), q.cpu().numpy()
+    out = []
+    for b, pos in enumerate(positions):
+        slots = [j % ctx for j in range(max(0, pos - ctx + 1), pos + 1)]
+        out.append(oracle.attend(qq[b], kk[b][slots], vv[b][slots], H, hd))
+    return np.stack(out)
+
+
 def test_noalloc_matches_workspace_entry_point_twice(lib):
     cases = [
-        (2, 32, 128, 3000, [2999, 17], torch.bfloat16, 1),  # Moshi temporal shape
-        (1, 4, 64, 64, [100], torch.float32, 2),             # smaller, on stale scratch
+        # Moshi temporal shape: 47 splits of the 3000-slot window for session 0
+        (2, 32, 128, 3000, [2999, 17], torch.bfloat16, 1),
+        # then 5 and 1 splits: the merge reads partials over the first call's leftovers
+        (2, 8, 64, 512, [300, 5], torch.float32, 2),
     ]
     for B, H, hd, ctx, positions, dtype, seed in cases:
         q, k, v, pos = _case(B, H, hd, ctx, positions, dtype, seed)
@@ -62,7 +79,10 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         assert rc == binding.RQ_OK
         want = binding.attention(q, k, v, pos, H, hd)
         torch.cuda.synchronize()
-        np.testing.assert_allclose(got.cpu().numpy(), want.cpu().numpy(), rtol=1e-4, atol=2e-5)
+        got = got.cpu().numpy()
+        np.testing.assert_allclose(got, want.cpu().numpy(), rtol=1e-4, atol=2e-5)
+        np.testing.assert_allclose(got, _oracle_attend(q, k, v, positions, H, hd),
+                                   rtol=1e-4, atol=2e-5)
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
