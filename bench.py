@@ -9,7 +9,10 @@ Prints ONE JSON line (rank 0).  `value` = session-frames/s with the user tokens
 already resident in HBM (rq_step_device), timed with CUDA events on the decode
 stream, max over ranks; `e2e` = the same through rq_step with host buffers (the
 host->device copy of the step's codes and the device->host read of its tokens inside
-the timed region).  N > 1 runs N independent replicas (sessions shard across GPUs;
+the timed region).  Unless --no-extra, the line also carries the other Moshi-7B
+workloads measured the same way (keys batch1_mean_window: batch 1 at the 375-frame
+workload's mean window; batch16; batch64: K/V pre-filled to 2900 positions), each
+with its own ms_per_step, clocks, roofline and dominant kernel.  N > 1 runs N independent replicas (sessions shard across GPUs;
 no collective on the data path), so scaling is weak.  The reference arm times the
 CPU oracle on the host cores on the same workload.
 """
@@ -228,40 +231,10 @@ def run_reference(args, cfg):
 
 
 # ---------------------------------------------------------------- native arm
-def run_native(args, cfg):
-    import numpy as np
+def time_frames(dec, d_users, d_out, d_has, first, K, stream, dev, ws, local):
+    """K device-resident frames after a barrier, CUDA events on the decode stream;
+    returns (seconds, max over ranks, clock samples)."""
     import torch
-
-    from rq_transformer_frame_gb300 import binding, synth
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    K, W, B = args.steps, args.warmup, cfg.batch
-    w_host = synth.make_weights(cfg, seed=0)
-    w_dev = binding.upload_weights(w_host, dev)
-    stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        sched = {"auto": binding.RQ_SCHEDULE_AUTO, "graph": binding.RQ_SCHEDULE_GRAPH,
-                 "persistent": binding.RQ_SCHEDULE_PERSISTENT,
-                 "tensor": binding.RQ_SCHEDULE_TENSOR}[args.schedule]
-        dec = binding.Decoder(cfg, w_dev, stream=stream, schedule=sched)
-        if cfg.prefill:
-            for b in range(B):
-                k, v = synth.kv_prefill(cfg, b, device=dev)
-                dec.set_kv(b, k, v)
-                del k, v
-    users = synth.batch_user_tokens(cfg, W + 2 * K)
-    d_users = users.to(dev)
-    d_out = torch.zeros((B, 9), dtype=torch.int32, device=dev)
-    d_has = torch.zeros(B, dtype=torch.uint8, device=dev)
-    start0 = cfg.prefill
-
-    # ---- warm-up, then K device-resident frames timed with events on the stream
-    for t in range(W):
-        dec.step_device(d_users[t], d_out, d_has)
     dec.sync()
     barrier(ws)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -269,32 +242,21 @@ def run_native(args, cfg):
         torch.cuda.synchronize(dev)
         ev0.record(stream)
         for t in range(K):
-            dec.step_device(d_users[W + t], d_out, d_has)
+            dec.step_device(d_users[first + t], d_out, d_has)
         ev1.record(stream)
         ev1.synchronize()
         torch.cuda.synchronize(dev)
     dec.sync()
     barrier(ws)
     sec = ev0.elapsed_time(ev1) / 1e3
-    sec_max = max_over_ranks(sec, ws, dev)
-    value = ws * B * K / sec_max
-    clocks = clk.summary()
-    offs = [[start0 + W + t] * B for t in range(K)]
-    fb = [frame_bytes(cfg, o) for o in offs]
-    bytes_frame = sum(f["total"] for f in fb) / K
+    return max_over_ranks(sec, ws, dev), clk.summary()
 
-    # ---- end to end through rq_step: host codes in, host tokens out, every step
-    users_h = users.numpy()
-    t0 = time.perf_counter()
-    for t in range(K):
-        dec.step(users_h[W + K + t])
-    e2e_sec = max_over_ranks(time.perf_counter() - t0, ws, dev)
-    e2e_value = ws * B * K / e2e_sec
-    h2d = B * 18 * 4
-    d2h = B * 18 * 4 + ((B + 3) // 4) * 4 + 4
 
-    # ---- per-kernel timing of the GEMVs (distinct layers, so nothing is L2-resident)
-    hbm_peak, peak_kind = peaks()
+def kernel_table(dec, cfg, stream, dev, hbm_peak):
+    """Each linear kind and the attention launched alone over distinct layers (nothing
+    L2-resident), CUDA events on the decode stream."""
+    import torch
+    from rq_transformer_frame_gb300 import binding
     kernels = {}
     names = {binding.RQ_OP_QKV: "qkv", binding.RQ_OP_ATTN: "attention",
              binding.RQ_OP_OUT: "out_proj", binding.RQ_OP_GATE_IN: "gate_in",
@@ -320,6 +282,164 @@ def run_native(args, cfg):
                          "frac_of_measured_hbm": round(nb / us / 1e3 / hbm_peak, 4),
                          "launches_per_frame": len(layers),
                          "ms_per_frame": round(us * len(layers) / 1e3, 3)}
+    return kernels
+
+
+def frame_kernel_roofline(dec, cfg, stream, dev, hbm_peak, peak_kind, traffic_name):
+    """The persistent whole-frame kernel at the handle's current window: launched alone
+    10 times with events on the decode stream; plus the stages of the last frame."""
+    import torch
+    from rq_transformer_frame_gb300 import binding
+    us_ops = dec.op_times()
+    nb = dec.launch_op(binding.RQ_OP_FRAME, 0, 0)
+    dec.launch_op(binding.RQ_OP_FRAME, 0, 2)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nrep = 10
+    e0.record(stream)
+    dec.launch_op(binding.RQ_OP_FRAME, 0, nrep)
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / nrep
+    roof = {"kernel": "frame_persistent_kernel (all linears and attentions of a frame)",
+            "bound": "hbm", "achieved": round(nb / us / 1e3, 1), "peak": hbm_peak,
+            "unit": "GB/s", "peak_kind": peak_kind,
+            "frac": round(nb / us / 1e3 / hbm_peak, 4), "us_per_launch": round(us, 1),
+            "bytes_per_launch": nb,
+            "traffic": profiled_traffic(traffic_name, "frame", nb) if traffic_name else None}
+    stages = None
+    if us_ops is not None:
+        L = cfg.layers
+        stages = {"temporal_ms": round(float(us_ops[:5 * L].sum()) / 1e3, 3),
+                  "text_head_ms": round(float(us_ops[5 * L]) / 1e3, 3),
+                  "depformer_ms": round(float(us_ops[5 * L + 1:].sum()) / 1e3, 3),
+                  "ops": int(len(us_ops))}
+    return roof, stages
+
+
+def dominant_roofline(dec, cfg, kernels, frame_s, hbm_peak, peak_kind):
+    """The kernel with the largest share of the frame (time per launch x launches)."""
+    from rq_transformer_frame_gb300 import binding
+    B = cfg.batch
+    name = max(kernels, key=lambda k: kernels[k]["ms_per_frame"])
+    dom = kernels[name]
+    tensor = dec.schedule == binding.RQ_SCHEDULE_TENSOR
+    if name == "attention":
+        label = "attn_decode_kernel (split-K decode attention over the K/V window, one layer)"
+        traffic = profiled_traffic("attn_%s.md" % cfg.name, "attn", dom["bytes_per_launch"])
+    elif tensor:
+        label = "tc_gemm_kernel<%d> (%s on the tcgen05 tensor cores, one layer)" % (
+            (B + 15) // 16 * 16, name)
+        traffic = profiled_traffic("tc_gemm_%s.md" % cfg.name, "tc", dom["bytes_per_launch"])
+    else:
+        label = "gemv_kernel<bf16> (%s, one layer)" % name
+        traffic = profiled_traffic("gemv_moshi7b_b1.md", "gemv")
+    return {"kernel": label, "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak,
+            "unit": "GB/s", "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
+            "us_per_launch": dom["us_per_launch"], "bytes_per_launch": dom["bytes_per_launch"],
+            "share_of_frame": round(dom["ms_per_frame"] / (1e3 * frame_s), 3),
+            "traffic": traffic}
+
+
+def make_decoder(cfg, w_dev, stream, sched, dev, prefill=0):
+    """A handle of cfg on the decode stream; prefill > 0 pre-fills every session's K/V
+    (synth.kv_prefill, drawn on the GPU) to that many positions."""
+    import torch
+    from rq_transformer_frame_gb300 import binding, synth
+    with torch.cuda.stream(stream):
+        dec = binding.Decoder(cfg, w_dev, stream=stream, schedule=sched)
+        if prefill:
+            c = cfg.with_(prefill=prefill)
+            for b in range(cfg.batch):
+                k, v = synth.kv_prefill(c, b, device=dev)
+                dec.set_kv(b, k, v)
+                del k, v
+    return dec
+
+
+def workload_line(cfg, w_dev, stream, dev, ws, local, K, W, prefill, hbm_peak, peak_kind):
+    """One more workload measured as the headline is (device-resident codes, events
+    around exactly K frames after W warm-up frames), with its own clocks and roofline."""
+    import torch
+    from rq_transformer_frame_gb300 import binding, synth
+    B = cfg.batch
+    dec = make_decoder(cfg, w_dev, stream, binding.RQ_SCHEDULE_AUTO, dev, prefill)
+    users = synth.batch_user_tokens(cfg, W + K).to(dev)
+    d_out = torch.zeros((B, 9), dtype=torch.int32, device=dev)
+    d_has = torch.zeros(B, dtype=torch.uint8, device=dev)
+    for t in range(W):
+        dec.step_device(users[t], d_out, d_has)
+    sec, clocks = time_frames(dec, users, d_out, d_has, W, K, stream, dev, ws, local)
+    fb = [frame_bytes(cfg, [prefill + W + t] * B) for t in range(K)]
+    bytes_frame = sum(f["total"] for f in fb) / K
+    frame_s = sec / K
+    line = {"workload": cfg.name, "batch": B, "start_offset": prefill + W,
+            "frames_timed": K, "ms_per_step": 1e3 * frame_s,
+            "value": ws * B / frame_s, "unit": "session-frames/s",
+            "tokens_per_s": 9 * ws * B / frame_s,
+            "schedule": {1: "graph", 2: "persistent", 3: "tensor"}.get(dec.schedule, "?"),
+            "hbm": {"bytes_per_frame": bytes_frame,
+                    "GB/s": round(bytes_frame / frame_s / 1e9, 1),
+                    "frac_of_measured": round(bytes_frame / frame_s / 1e9 / hbm_peak, 4)},
+            "clocks": clocks}
+    if dec.schedule == binding.RQ_SCHEDULE_PERSISTENT:
+        line["roofline"], line["stages"] = frame_kernel_roofline(
+            dec, cfg, stream, dev, hbm_peak, peak_kind, None)
+    else:
+        kernels = kernel_table(dec, cfg, stream, dev, hbm_peak)
+        line["roofline"] = dominant_roofline(dec, cfg, kernels, frame_s, hbm_peak, peak_kind)
+        line["kernels"] = kernels
+    dec.close()
+    return line
+
+
+def run_native(args, cfg):
+    import numpy as np
+    import torch
+
+    from rq_transformer_frame_gb300 import binding, configs, synth
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    K, W, B = args.steps, args.warmup, cfg.batch
+    w_host = synth.make_weights(cfg, seed=0)
+    w_dev = binding.upload_weights(w_host, dev)
+    stream = torch.cuda.Stream(device=dev)
+    sched = {"auto": binding.RQ_SCHEDULE_AUTO, "graph": binding.RQ_SCHEDULE_GRAPH,
+             "persistent": binding.RQ_SCHEDULE_PERSISTENT,
+             "tensor": binding.RQ_SCHEDULE_TENSOR}[args.schedule]
+    dec = make_decoder(cfg, w_dev, stream, sched, dev, cfg.prefill)
+    users = synth.batch_user_tokens(cfg, W + 2 * K)
+    d_users = users.to(dev)
+    d_out = torch.zeros((B, 9), dtype=torch.int32, device=dev)
+    d_has = torch.zeros(B, dtype=torch.uint8, device=dev)
+    start0 = cfg.prefill
+
+    # ---- warm-up, then K device-resident frames timed with events on the stream
+    for t in range(W):
+        dec.step_device(d_users[t], d_out, d_has)
+    sec_max, clocks = time_frames(dec, d_users, d_out, d_has, W, K, stream, dev, ws, local)
+    value = ws * B * K / sec_max
+    offs = [[start0 + W + t] * B for t in range(K)]
+    fb = [frame_bytes(cfg, o) for o in offs]
+    bytes_frame = sum(f["total"] for f in fb) / K
+
+    # ---- end to end through rq_step: host codes in, host tokens out, every step
+    users_h = users.numpy()
+    t0 = time.perf_counter()
+    for t in range(K):
+        dec.step(users_h[W + K + t])
+    e2e_sec = max_over_ranks(time.perf_counter() - t0, ws, dev)
+    e2e_value = ws * B * K / e2e_sec
+    h2d = B * 18 * 4
+    d2h = B * 18 * 4 + ((B + 3) // 4) * 4 + 4
+
+    # ---- per-kernel timing of the GEMVs (distinct layers, so nothing is L2-resident)
+    hbm_peak, peak_kind = peaks()
+    kernels = kernel_table(dec, cfg, stream, dev, hbm_peak)
     dec.reset(-1)
     stages = None
     if dec.schedule == binding.RQ_SCHEDULE_PERSISTENT:
@@ -327,50 +447,32 @@ def run_native(args, cfg):
         for t in range(W):
             dec.step_device(d_users[t], d_out, d_has)
         dec.sync()
-        us_ops = dec.op_times()
-        nb = dec.launch_op(binding.RQ_OP_FRAME, 0, 0)
-        dec.launch_op(binding.RQ_OP_FRAME, 0, 2)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        nrep = 10
-        e0.record(stream)
-        dec.launch_op(binding.RQ_OP_FRAME, 0, nrep)
-        e1.record(stream)
-        e1.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / nrep
-        roof = {"kernel": "frame_persistent_kernel (all linears and attentions of a frame)",
-                "bound": "hbm", "achieved": round(nb / us / 1e3, 1), "peak": hbm_peak,
-                "unit": "GB/s", "peak_kind": peak_kind,
-                "frac": round(nb / us / 1e3 / hbm_peak, 4), "us_per_launch": round(us, 1),
-                "bytes_per_launch": nb,
-                "traffic": profiled_traffic("frame_persistent_moshi7b.md", "frame", nb)}
-        if us_ops is not None:
-            L, DL = cfg.layers, cfg.dlayers
-            stages = {"temporal_ms": round(float(us_ops[:5 * L].sum()) / 1e3, 3),
-                      "text_head_ms": round(float(us_ops[5 * L]) / 1e3, 3),
-                      "depformer_ms": round(float(us_ops[5 * L + 1:].sum()) / 1e3, 3),
-                      "ops": int(len(us_ops))}
+        roof, stages = frame_kernel_roofline(dec, cfg, stream, dev, hbm_peak, peak_kind,
+                                             "frame_persistent_moshi7b.md")
         dec.reset(-1)
     else:
-        # the kernel with the largest share of the frame (time per launch x launches)
-        name = max(kernels, key=lambda k: kernels[k]["ms_per_frame"])
-        dom = kernels[name]
-        tensor = dec.schedule == binding.RQ_SCHEDULE_TENSOR
-        if name == "attention":
-            label = "attn_decode_kernel (split-K decode attention over the K/V window, one layer)"
-            traffic = profiled_traffic("attn_%s.md" % cfg.name, "attn", dom["bytes_per_launch"])
-        elif tensor:
-            label = "tc_gemm_kernel<%d> (%s on the tcgen05 tensor cores, one layer)" % (
-                (B + 15) // 16 * 16, name)
-            traffic = profiled_traffic("tc_gemm_%s.md" % cfg.name, "tc", dom["bytes_per_launch"])
-        else:
-            label = "gemv_kernel<bf16> (%s, one layer)" % name
-            traffic = profiled_traffic("gemv_moshi7b_b1.md", "gemv")
-        roof = {"kernel": label, "bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak,
-                "unit": "GB/s", "peak_kind": peak_kind, "frac": round(dom["GB/s"] / hbm_peak, 4),
-                "us_per_launch": dom["us_per_launch"], "bytes_per_launch": dom["bytes_per_launch"],
-                "share_of_frame": round(dom["ms_per_frame"] / (1e3 * sec_max / K), 3),
-                "traffic": traffic}
+        roof = dominant_roofline(dec, cfg, kernels, sec_max / K, hbm_peak, peak_kind)
+    n_launch = dec.kernels_per_frame
+    sched_name = {1: "graph", 2: "persistent", 3: "tensor"}.get(dec.schedule, "?")
+    dec.close()
+
+    # ---- the other Moshi-7B workloads, each measured the same way on this GPU
+    extra = {}
+    if not args.no_extra and args.workload is None and args.schedule == "auto":
+        KX = min(K, 20)
+        # batch 1 at the mean window of the 375-frame workload (positions 0..374: 188)
+        mean_pos = configs.MOSHI7B.frames // 2
+        pre = max(0, mean_pos - W - KX // 2)
+        todo = [("batch1_mean_window", configs.MOSHI7B, pre),
+                ("batch16", configs.MOSHI7B_B16, 0),
+                ("batch64", configs.MOSHI7B_B64, configs.MOSHI7B_B64.prefill)]
+        for key, c, pre in todo:
+            if c.name == cfg.name and pre == cfg.prefill:
+                continue
+            kx = min(KX, c.context - pre - W)
+            extra[key] = workload_line(c, w_dev, stream, dev, ws, local, kx, W, pre,
+                                       hbm_peak, peak_kind)
+            torch.cuda.empty_cache()
 
     # ---- the oracle on this machine's host cores, on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -393,20 +495,20 @@ def run_native(args, cfg):
                          % (fb[0]["weights"] / 1e9),
                    "arith": ("bf16 weights and K/V, f32 activations and accumulation" +
                              ("; tensor-core GEMMs on two-part bf16 activation operands (16 significant bits)"
-                              if dec.schedule == binding.RQ_SCHEDULE_TENSOR else ""))},
+                              if sched_name == "tensor" else ""))},
         "tokens_per_s": 9 * value,
         "hbm": {"bytes_per_frame": bytes_frame, "GB/s": round(bytes_frame / (sec_max / K) / 1e9, 1),
                 "frac_of_measured": round(bytes_frame / (sec_max / K) / 1e9 / hbm_peak, 4),
                 "frac_of_8TBs": round(bytes_frame / (sec_max / K) / 8e12, 4)},
         "roofline": roof, "kernels": kernels, "stages": stages,
-        "schedule": {1: "graph", 2: "persistent", 3: "tensor"}.get(dec.schedule, "?"),
+        "schedule": sched_name,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "session-frames/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": K * dec.kernels_per_frame,
+        "gpu_launches": K * n_launch,
         "clocks": clocks,
     }
-    dec.close()
+    line.update(extra)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -424,6 +526,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="only the headline workload (skip the other batch sizes)")
     ap.add_argument("--workload", default=None, help="override: a name from configs.CONFIGS")
     ap.add_argument("--schedule", default="auto",
                     choices=["auto", "graph", "persistent", "tensor"])

@@ -368,7 +368,8 @@ int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
 /* Test hook of the failure path: the limit, in nanoseconds, of the device-side waits of
  * the batch-1 whole-frame kernel (its grid barrier and weight-ring waits); 0 restores the
  * default of 2 s.  stall_op >= 0 makes the grid barrier in front of op `stall_op` of
- * the frame's op table (the order of rq_get_op_times, op >= 1) wait for one CTA more than
+ * the frame's op table (the order of rq_get_op_times; op >= 1 and not the depformer
+ * input projections beside the text head, which have no barrier) wait for one CTA more than
  * the grid holds, so every wait there runs out after limit_ns: the frame then returns
  * RQ_ERR_TIMEOUT, later calls RQ_ERR_POISONED until rq_reset(h, -1).  -1 removes the
  * stall.  Nothing traps and no wait is unbounded.  Applies to frames run by the

@@ -64,6 +64,7 @@ struct rq_handle {
   // persistent schedule
   int schedule = RQ_SCHEDULE_GRAPH;
   PersOp* d_ops = nullptr;
+  std::vector<char> pers_nobar;  // host copy: op k has no grid barrier in front of it
   unsigned int* grid_bar = nullptr;
   unsigned long long* trace = nullptr;
   PersParams pers{};
@@ -920,6 +921,8 @@ rq_status upload_pers_ops(rq_handle* h) {
   }
   h->pers.ops = h->d_ops;
   h->pers.n_ops = (int)ops.size();
+  h->pers_nobar.assign(ops.size(), 0);
+  for (size_t k = 0; k < ops.size(); ++k) h->pers_nobar[k] = ops[k].nobar ? 1 : 0;
   h->pers.trace = h->trace;
   h->pers.samp = h->samp;
   return RQ_OK;
@@ -1681,8 +1684,9 @@ rq_status rq_set_wait_limit(rq_handle* h, uint64_t limit_ns, int32_t stall_op) {
   if (!h) return RQ_ERR_ARG;
   if (h->schedule != RQ_SCHEDULE_PERSISTENT || !h->grid_bar)
     return fail(h, RQ_ERR_UNSUPPORTED, "the wait limit applies to the persistent schedule");
-  if (stall_op < -1 || stall_op == 0 || stall_op >= h->pers.n_ops)
-    return fail(h, RQ_ERR_ARG, "stall_op outside [1, ops) and not -1");
+  if (stall_op < -1 || stall_op == 0 || stall_op >= h->pers.n_ops ||
+      (stall_op > 0 && h->pers_nobar[stall_op]))
+    return fail(h, RQ_ERR_ARG, "stall_op is not an op with a grid barrier in front (or -1)");
   const unsigned long long ctl[2] = {(unsigned long long)limit_ns,
                                      (unsigned long long)(stall_op + 1)};
   RQ_CUDA(h, cudaStreamSynchronize(h->stream));

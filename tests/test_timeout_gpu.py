@@ -44,6 +44,8 @@ def test_wait_timeout_poisons_and_reset_recovers(stall_op):
         dec.set_wait_limit(20_000_000, 0)  # op 0 has no barrier in front of it
     with pytest.raises(binding.RQError):
         dec.set_wait_limit(20_000_000, n_ops)
+    with pytest.raises(binding.RQError):  # the input projections beside the text head
+        dec.set_wait_limit(20_000_000, 5 * c.layers + 1)
     dec.set_wait_limit(20_000_000, stall_op)
 
     with pytest.raises(binding.RQError) as ei:
