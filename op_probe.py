@@ -1,6 +1,6 @@
 """Time single operations of the decode step through the C ABI (rq_launch_op).
 
-  python -m rq_transformer_frame_gb300.op_probe --workload moshi7b_2layer \
+  python op_probe.py --workload moshi7b_2layer \
       --ops gate_in,qkv --reps 3 [--frames 4] [--batch 16] [--prefill 2900] [--band q4]
 
 Builds the decoder for the workload (seeded synthetic weights; `--batch` overrides the
@@ -14,10 +14,13 @@ summaries in profiles/.
 """
 import argparse
 import json
+import os
+import sys
 
 import torch
 
-from . import binding, configs, synth
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from rq_transformer_frame_gb300 import binding, configs, synth  # noqa: E402
 
 OPS = {"qkv": binding.RQ_OP_QKV, "attn": binding.RQ_OP_ATTN, "out_proj": binding.RQ_OP_OUT,
        "gate_in": binding.RQ_OP_GATE_IN, "gate_out": binding.RQ_OP_GATE_OUT,

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
         const float o = A / L;
         const size_t i = (size_t)b * p.D + (size_t)h * HD + tid;
         p.out[i] = o;
-        if (p.out_bf16) store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, i, o);
+        if (p.out_bf16) store_bf16_parts(p.out_bf16, (size_t)p.nb * p.D, i, o);
       } else {
         float* part = p.part + (((size_t)b * p.H + h) * p.nsplit + cur.split) * pstride;
         part[2 + tid] = A;
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
   const float o = A / L;
   const size_t i = (size_t)b * p.D + (size_t)h * p.hd + tid;
   p.out[i] = o;
-  if (p.out_bf16) store_bf16x3(p.out_bf16, (size_t)p.nb * p.D, i, o);
+  if (p.out_bf16) store_bf16_parts(p.out_bf16, (size_t)p.nb * p.D, i, o);
 }
 
 // Resident CTAs per SM of one instantiation at `smem` bytes (sets the shared-memory
@@ -566,7 +566,7 @@ namespace rqk {
 
 // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1, for every
 // session: one warp per (session, head), the head's dimensions spread over the lanes;
-// writes the bf16x3 operand of the next tensor-core GEMM (parts nb rows apart).
+// writes the bf16 operand parts of the next tensor-core GEMM (parts nb rows apart).
 // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1 (<= 8) for
 // session b, head h: one warp, dimension e = lane + 32 i on lane `lane`.  The query, every
 // key and then every value are loaded together (two round trips instead of one per key);
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(32) dattn_batched_kernel(const float* dq, long
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (j < n_keys) o += sc[j] / den * kk[j][i];
-    store_bf16x3(out, (size_t)nb * out_bs, (size_t)b * out_bs + (size_t)h * hd + e, o);
+    store_bf16_parts(out, (size_t)nb * out_bs, (size_t)b * out_bs + (size_t)h * hd + e, o);
   }
 }
 

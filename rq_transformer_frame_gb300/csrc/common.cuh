@@ -147,13 +147,13 @@ __device__ __forceinline__ void bar_sync(int id, int n) {
 }
 
 // ---------------------------------------------------------------- numerics
-// Three-term bf16 expansion of an f32: hi = bf16(x), mid = bf16(x - hi), lo = x - hi - mid.
-// Both differences are exact (Sterbenz) and lo needs at most 8 significant bits, so
-// hi + mid + lo == x for every normal-range x: a bf16 x bf16 tensor-core product over the
-// three parts, accumulated in f32, sees the f32 operand itself.  Parts go to
-// base[idx], base[ps + idx], base[2 ps + idx].
-// With kOpndParts == 2 only hi and mid = bf16(x - hi) are kept (16 significant bits).
-__device__ __forceinline__ void store_bf16x3(uint16_t* base, size_t ps, size_t idx, float x) {
+// bf16 expansion of an f32 for the tensor-core operand: hi = bf16(x), mid = bf16(x - hi)
+// (x - hi is exact), and with kOpndParts == 3 also lo = bf16(x - hi - mid).  Two parts keep
+// 16 significant bits (relative representation error <= 2^-17); three parts are exact
+// for every normal-range x (lo needs at most 8 significant bits).  A bf16 x bf16
+// tensor-core product over the parts, accumulated in f32, sees hi + mid (+ lo).  Parts
+// go to base[idx], base[ps + idx] (and base[2 ps + idx]).
+__device__ __forceinline__ void store_bf16_parts(uint16_t* base, size_t ps, size_t idx, float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   const float r1 = x - __bfloat162float(h);
   const __nv_bfloat16 m = __float2bfloat16_rn(r1);

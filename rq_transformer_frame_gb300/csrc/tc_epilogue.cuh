@@ -1,6 +1,6 @@
 // tc_epilogue.cuh -- pieces shared by the tensor-core GEMM kernels (one launch per linear,
 // and the persistent batched depformer): tile geometry, the fused epilogues of one
-// 16-session chunk of an accumulator tile, and the tensor-memory read of a bf16x3 tile.
+// 16-session chunk of an accumulator tile, and the tensor-memory read of a tile over the bf16 operand parts.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -41,7 +41,7 @@ __device__ __forceinline__ void feed_next(const TcParams& p, int row, bool valid
                                           float v) {
   const TcPlan& pl = p.pl;
   if (valid)
-    store_bf16x3(p.opnd, (size_t)pl.NB * pl.n_out, (size_t)b * pl.n_out + row,
+    store_bf16_parts(p.opnd, (size_t)pl.NB * pl.n_out, (size_t)b * pl.n_out + row,
                  b < p.B ? (p.alpha_next ? v * p.alpha_next[row] : v) : 0.f);
 }
 
@@ -107,7 +107,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float g = d[i], mu = ex[m][i];
-        store_bf16x3(p.out_bf16, (size_t)pl.NB * p.outb_bs, (size_t)(c0 + i) * p.outb_bs + j,
+        store_bf16_parts(p.out_bf16, (size_t)pl.NB * p.outb_bs, (size_t)(c0 + i) * p.outb_bs + j,
                      g / (1.0f + expf(-g)) * mu);
       }
     }

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 namespace rqk {
 namespace tcg {
 
-// one CTA per padded session row: xb[.][b] = bf16x3(in[b] (* alpha * 1/sqrt(eps +
+// one CTA per padded session row: xb[.][b] = bf16 parts of (in[b] (* alpha * 1/sqrt(eps +
 // mean(in^2)))) ("moshi_lm.rs", `rms_norm`), zero rows for b >= B; side[b] = the f32 result
 __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long long in_bs,
                                                         const float* alpha, float eps, int B,
@@ -273,9 +273,9 @@ __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long lo
   const int b = blockIdx.x, tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  const size_t ps = (size_t)gridDim.x * K;  // bf16x3 part stride
+  const size_t ps = (size_t)gridDim.x * K;  // operand part stride
   if (b >= B) {
-    for (int k = tid; k < K; k += 256) store_bf16x3(xb, ps, (size_t)b * K + k, 0.f);
+    for (int k = tid; k < K; k += 256) store_bf16_parts(xb, ps, (size_t)b * K + k, 0.f);
     return;
   }
   const float* x = in + (size_t)b * in_bs;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(256) prep_bf16_kernel(const float* in, long lo
   }
   for (int k = tid; k < K; k += 256) {
     const float v = alpha ? x[k] * alpha[k] * inv : x[k];
-    store_bf16x3(xb, ps, (size_t)b * K + k, v);
+    store_bf16_parts(xb, ps, (size_t)b * K + k, v);
     if (side) side[(size_t)b * side_bs + k] = v;
   }
 }
