@@ -22,6 +22,25 @@ constexpr int kCons = 256;    // consumer threads
 constexpr int kThr = 288;     // + 1 producer warp
 constexpr int kMaxNch = 2;  // long reductions are split into parts (GemvPlan::kparts)
 constexpr int kMaxStage = 1024;  // depformer attention output staged in shared memory (DD <= 1024)
+#ifndef RQ_PERS_BURST_T
+#define RQ_PERS_BURST_T 4
+#endif
+#ifndef RQ_PERS_STREAM_T
+#define RQ_PERS_STREAM_T 2
+#endif
+#ifndef RQ_PERS_STREAM_BURST
+#define RQ_PERS_STREAM_BURST 0
+#endif
+#ifndef RQ_PERS_STREAM_MIN
+#define RQ_PERS_STREAM_MIN 4
+#endif
+// tile groups: resident tiles (ops of a few tiles per CTA) in bursts of kBurstT; the
+// weight stream of long ops (more than kStreamMinTiles tiles per CTA) kStreamT at a time
+constexpr int kBurstT = RQ_PERS_BURST_T;
+constexpr int kStreamT = RQ_PERS_STREAM_T;
+constexpr bool kStreamBurst = RQ_PERS_STREAM_BURST != 0;
+constexpr int kStreamMinTiles = RQ_PERS_STREAM_MIN;
+
 
 // ---------------------------------------------------------------- grid barrier
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -52,68 +71,132 @@ __device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target,
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
 // ---------------------------------------------------------------- tile consumer
-// Consume this CTA's `nt` tiles of one GEMV op from the ring (slots advance with the
-// CTA-wide tile counter `gi`), leaving one partial per (row, warp) in `part`.
-template <typename WT, int NCH>
+// Sum each of R row values over the warp's 32 lanes with a transposing butterfly: at
+// every halving step a lane keeps half of its values and adds its partner's copy of
+// them, so R rows take R - 1 + (5 - log2 R) shuffles instead of 5 R.  Afterwards lanes
+// [q * 32/R, (q + 1) * 32/R) all hold the full sum of row q (returned).
+template <int R>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[R], int lane) {
+#pragma unroll
+  for (int n = R, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int m = 0; m < n / 2; ++m) {
+      const float keep = up ? v[m + n / 2] : v[m];
+      const float send = up ? v[m] : v[m + n / 2];
+      v[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 / R; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  return v[0];
+}
+
+// Consume this CTA's `nt` tiles of one GEMV op from the ring (slot `slot`, phase `ph`
+// advance tile by tile), leaving one partial per (row, warp) in `part`.  Tiles go in
+// groups of T with one butterfly over the group's 2T rows.  BURST (tiles already
+// resident, the latency-bound depformer ops): every wait of a group, then every
+// shared-memory load, the FMAs and the slots' release, so the chain of dependent
+// latencies is paid once per group.  Otherwise (the weight stream): each tile is loaded
+// and multiplied as soon as it lands and its slot goes back to the producer at once.
+template <typename WT, int NCH, int T, bool BURST>
 __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool accumulate,
-                                              int nt, uint32_t& gi,
+                                              int nt, int& slot, uint32_t& ph,
                                               uint8_t* ring, int slot_bytes, int NS,
                                               uint64_t* full, uint64_t* empty, float* part,
                                               const float (&xr)[kMaxNch][Chunk<WT>::V],
                                               int g, int tig, int warp, int lane,
                                               uint64_t lim) {
-  constexpr int RG = GemvShape<NCH>::RG;
+  constexpr int RG = 2;  // rows per thread group and tile (every persistent plan)
+  constexpr int R = T * RG;
   const uint32_t row_bytes = (uint32_t)Kw * (uint32_t)sizeof(WT);
   const int CC = Kw / Chunk<WT>::V;
   const int wpg = pl.tpr >> 5;
-  for (int i = 0; i < nt; ++i, ++gi) {
-    const int s = (int)(gi % (uint32_t)NS);
-    if (!mbar_wait_for(&full[s], (gi / (uint32_t)NS) & 1u, lim)) return false;
-    const uint8_t* row0 = ring + (size_t)s * slot_bytes + (size_t)(g * RG) * row_bytes;
-    float acc[RG][2];
+  for (int i0 = 0; i0 < nt; i0 += T) {
+    float acc[R][2];
 #pragma unroll
-    for (int r = 0; r < RG; ++r) acc[r][0] = acc[r][1] = 0.f;
-    // weights in batches of two chunks: loads of a batch issue together, and the
-    // register footprint stays small for long rows
+    for (int q = 0; q < R; ++q) acc[q][0] = acc[q][1] = 0.f;
+    if (BURST) {
+      int sl[T];
+      const uint8_t* row0[T];
 #pragma unroll
-    for (int jb = 0; jb < NCH; jb += 2) {
-      uint4 w[2][RG];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int c = tig + (jb + jj) * pl.tpr;
-#pragma unroll
-        for (int r = 0; r < RG; ++r)
-          w[jj][r] = (jb + jj < NCH && c < CC)
-                         ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
-                                                           (size_t)c * 16)
-                         : make_uint4(0u, 0u, 0u, 0u);
+      for (int t = 0; t < T; ++t) {
+        sl[t] = slot;
+        row0[t] = ring + (size_t)slot * slot_bytes + (size_t)(g * RG) * row_bytes;
+        if (i0 + t < nt) {
+          if (!mbar_wait_for(&full[slot], ph, lim)) return false;
+          if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
       }
+      uint4 w[T][NCH][RG];
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-        if (jb + jj < NCH)
+      for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c = tig + j * pl.tpr;
 #pragma unroll
           for (int r = 0; r < RG; ++r)
-            Chunk<WT>::dot2(w[jj][r], xr[jb + jj < NCH ? jb + jj : 0], acc[r][0], acc[r][1]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    float* pp = part + (size_t)(i * pl.tile_rows + g * RG) * wpg + (warp % wpg);
-    if (RG == 2) {
-      const bool up = (lane & 16) != 0;
-      const float r0 = acc[0][0] + acc[0][1];
-      const float r1 = acc[RG - 1][0] + acc[RG - 1][1];
-      float keep = up ? r1 : r0;
-      const float send = up ? r0 : r1;
-      keep += __shfl_xor_sync(0xffffffffu, send, 16);
-      keep += __shfl_xor_sync(0xffffffffu, keep, 8);
-      keep += __shfl_xor_sync(0xffffffffu, keep, 4);
-      keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-      keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-      if (lane == 0) pp[0] = accumulate ? pp[0] + keep : keep;
-      if (lane == 16) pp[wpg] = accumulate ? pp[wpg] + keep : keep;
+            w[t][j][r] = (i0 + t < nt && c < CC)
+                             ? *reinterpret_cast<const uint4*>(row0[t] + (size_t)r * row_bytes +
+                                                               (size_t)c * 16)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int r = 0; r < RG; ++r)
+            Chunk<WT>::dot2(w[t][j][r], xr[j], acc[t * RG + r][0], acc[t * RG + r][1]);
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+          if (i0 + t < nt) mbar_arrive(&empty[sl[t]]);
+      }
     } else {
-      const float r0 = warp_sum(acc[0][0] + acc[0][1]);
-      if (lane == 0) pp[0] = accumulate ? pp[0] + r0 : r0;
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        if (i0 + t < nt) {
+          if (!mbar_wait_for(&full[slot], ph, lim)) return false;
+          const uint8_t* row0 = ring + (size_t)slot * slot_bytes + (size_t)(g * RG) * row_bytes;
+          uint4 w[NCH][RG];
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            const int c = tig + j * pl.tpr;
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+              w[j][r] = c < CC ? *reinterpret_cast<const uint4*>(row0 + (size_t)r * row_bytes +
+                                                                 (size_t)c * 16)
+                               : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+              Chunk<WT>::dot2(w[j][r], xr[j], acc[t * RG + r][0], acc[t * RG + r][1]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+    float v[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) v[q] = acc[q][0] + acc[q][1];
+    const float sum = warp_sum_rows<R>(v, lane);
+    // row q = t * RG + r of the group: tile i0 + t, row g * RG + r of that tile
+    const int q = lane / (32 / R);
+    const int t = q / RG, r = q % RG;
+    if (lane % (32 / R) == 0 && i0 + t < nt) {
+      float* pp = part + (size_t)((i0 + t) * pl.tile_rows + g * RG + r) * wpg + (warp % wpg);
+      *pp = accumulate ? *pp + sum : sum;
     }
   }
   return true;
@@ -127,6 +210,75 @@ __device__ __forceinline__ void tile_range(const GemvPlan& pl, int& t0, int& t1)
   t1 = (int)((T * (blockIdx.x + 1) + G - 1) / G);
 }
 
+// ---------------------------------------------------------------- weight tile sequence
+// One position in this CTA's sequence of weight tiles: every GEMV op's tile range, every
+// reduction part of it, in op order -- the order the producer fills the ring in.
+struct TileCur {
+  int k, kp, t, t0, t1;
+};
+
+// from op c.k on, the first GEMV op with a tile for this CTA
+template <typename WT>
+__device__ __forceinline__ bool cur_seek(const PersParams& P, TileCur& c) {
+  for (; c.k < P.n_ops; ++c.k) {
+    const PersOp& op = P.ops[c.k];
+    if (op.type != OPT_GEMV) continue;
+    tile_range(P.plans[op.plan], c.t0, c.t1);
+    if (c.t0 < c.t1) {
+      c.kp = 0;
+      c.t = c.t0;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <typename WT>
+__device__ __forceinline__ bool cur_next(const PersParams& P, TileCur& c) {
+  if (++c.t < c.t1) return true;
+  if (++c.kp < P.plans[P.ops[c.k].plan].kparts) {
+    c.t = c.t0;
+    return true;
+  }
+  ++c.k;
+  return cur_seek<WT>(P, c);
+}
+
+// the source byte ranges of the tile at c, each with its offset in the ring slot:
+// f(src, bytes, slot_offset); all 16-byte aligned, sizes multiples of 16
+template <typename WT, typename F>
+__device__ __forceinline__ void cur_ranges(const PersParams& P, const TileCur& c, F&& f) {
+  const PersOp& op = P.ops[c.k];
+  const GemvPlan& pl = P.plans[op.plan];
+  const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
+  const bool paired = op.epi == EPI_SWIGLU;
+  const int opt = paired ? pl.tile_rows / 2 : pl.tile_rows;
+  const uint8_t* W = static_cast<const uint8_t*>(op.W);
+  const int r0 = c.t * opt;
+  const int nv = min(opt, pl.n_out - r0);
+  if (pl.kparts > 1) {
+    // one range per row: the part's columns are a strided window of W
+    const int k0 = c.kp * pl.kp_width;
+    const int Kw = c.kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
+    const uint32_t seg = (uint32_t)Kw * (uint32_t)sizeof(WT);
+    for (int r = 0; r < nv; ++r)
+      f(W + (size_t)(r0 + r) * row_bytes + (size_t)k0 * sizeof(WT), seg, (uint32_t)r * seg);
+  } else if (paired) {
+    const uint32_t bytes = (uint32_t)nv * row_bytes;
+    f(W + (size_t)r0 * row_bytes, bytes, 0u);
+    f(W + (size_t)op.w_half + (size_t)r0 * row_bytes, bytes, (uint32_t)opt * row_bytes);
+  } else {
+    f(W + (size_t)r0 * row_bytes, (uint32_t)nv * row_bytes, 0u);
+  }
+}
+
+template <typename WT>
+__device__ __forceinline__ uint32_t cur_bytes(const PersParams& P, const TileCur& c) {
+  uint32_t n = 0;
+  cur_ranges<WT>(P, c, [&](const uint8_t*, uint32_t bytes, uint32_t) { n += bytes; });
+  return n;
+}
+
 // ---------------------------------------------------------------- prologue
 // x for this op into registers: chunk j of thread (g, tig) covers columns
 // [(tig + j*tpr)*V, +V).  Returns nothing; uses consumer barrier 1.
@@ -136,10 +288,11 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                        float (&xr)[kMaxNch][Chunk<WT>::V],
                                        const float (&ar)[2][Chunk<WT>::V], int g, int tig,
                                        int tid, int warp, int lane, float* s_red,
-                                       float* s_att) {
+                                       int red_half, float* s_att, int forcing) {
   constexpr int V = Chunk<WT>::V;
   const int K = pl.K, CC = Kw / V;
   const float* in = op.in + k0;  // this part's columns [k0, k0 + Kw)
+  (void)tid;
 #pragma unroll
   for (int j = 0; j < kMaxNch; ++j) {
     const int c = tig + j * pl.tpr;
@@ -161,7 +314,7 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     // "moshi_lm.rs", `embed` of the step's conditioning token (-1 adds nothing, else row
     // max(tok, 0)); CTA 0 keeps this x for the residuals
     const IoLayout io{1};
-    const int prev = P.d_in[io.flag_off()] ? P.d_in[io.forced_off() + op.key_index]
+    const int prev = forcing ? P.d_in[io.forced_off() + op.key_index]
                                            : argmax_key_index(__ldcg(P.keys + op.key_index));
     const bool keep = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
 #pragma unroll
@@ -181,20 +334,27 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     }
   }
   if (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB) {
-    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).
+    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)); alpha (a
+    // constant) was loaded before the grid barrier.
     // Every row group holds the whole vector: group 0's warps sum the squares from
-    // registers; alpha (a constant) was loaded before the grid barrier.
+    // registers.  s_red alternates between two halves op by op, so one CTA barrier is
+    // enough (the next op writes the other half).
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxNch; ++j)
 #pragma unroll
       for (int v = 0; v < V; ++v) ss = fmaf(xr[j][v], xr[j][v], ss);
     ss = warp_sum(ss);
-    if (lane == 0) s_red[warp] = ss;
+    float* red = s_red + red_half * (kCons / 32);
+    if (lane == 0) red[warp] = ss;
     bar_sync(1, kCons);
+    float rv[kCons / 32];
+#pragma unroll
+    for (int w = 0; w < kCons / 32; ++w) rv[w] = red[w];
     float tot = 0.f;
-    for (int w = 0; w < pl.tpr / 32; ++w) tot += s_red[w];
-    bar_sync(1, kCons);  // s_red is reused by the next op
+#pragma unroll
+    for (int w = 0; w < kCons / 32; ++w)
+      if (w < pl.tpr / 32) tot += rv[w];
     const float inv = 1.0f / sqrtf(P.eps + tot / (float)K);
     const bool side =
         op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0;
@@ -217,8 +377,9 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1.
     // hd/4 threads per head, one float4 of dimensions each: q and every key in one
     // round trip, scores reduced with shuffles, the softmax in registers, then the
-    // values in one more round trip; the output is staged in shared memory and read
-    // back in the chunk layout of x.
+    // values in one more round trip (keys and values at once would need 64 registers
+    // more than the kernel's cap leaves); the output is staged in shared memory and
+    // read back in the chunk layout of x.
     const int nk = op.n_keys, dh = P.dheads, hd = P.dhead_dim;
     const float scale = 1.0f / sqrtf((float)hd);
     const int tph = hd / 4;
@@ -292,12 +453,16 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
                                          const GemvPlan& pl, int t0, int nt, const float* part,
                                          int tid, int warp, int lane,
                                          unsigned long long* s_key, const float2* s_rope,
-                                         float resid_old) {
+                                         float resid_old, int pos, int forcing) {
   const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
   const int nrows = nt * tr;
-  auto yrow = [&](int lr) {
+  auto yrow = [&](int lr) {  // wpg <= 8: the partials load together, then add in order
+    float pv[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) pv[w] = w < wpg ? part[(size_t)lr * wpg + w] : 0.f;
     float y = 0.f;
-    for (int w = 0; w < wpg; ++w) y += part[(size_t)lr * wpg + w];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) y += pv[w];
     return y;
   };
   auto grow = [&](int lr) { return (t0 + lr / tr) * tr + lr % tr; };
@@ -306,7 +471,6 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
     int prev = -1;
     if (epi == EPI_DEPIN) {
       const IoLayout io{1};
-      const int forcing = P.d_in[io.flag_off()];
       prev = forcing ? P.d_in[io.forced_off() + op.key_index]
                      : argmax_key_index(__ldcg(P.keys + op.key_index));
     }
@@ -335,7 +499,6 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
     }
   } else if (epi == EPI_QKV) {
     const int D = pl.n_out / 3;
-    const int pos = P.offsets[0];
     const int slot = pos % P.context;
     const int hd = P.head_dim;
     for (int lr = 2 * tid; lr < nrows; lr += 2 * kCons) {
@@ -447,10 +610,9 @@ template <typename KT, int EPL>
 __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op, int tid,
                                            int warp, int lane, float (*s_am)[4],
                                            float (*s_al)[4], float (*s_aacc)[4][EPL * 32],
-                                           int* s_last) {
+                                           int* s_last, int pos) {
   constexpr int HD = EPL * 32;
   const int group = warp >> 2, wig = warp & 3, gt = tid & 127;
-  const int pos = P.offsets[0];
   const int len = min(pos + 1, P.context);
   const int first = pos + 1 - len;
   const int groups = (int)gridDim.x * 2;
@@ -578,7 +740,7 @@ template <typename WT, typename KT, int EPL>
 __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersParams P) {
   constexpr int V = Chunk<WT>::V;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_red[kCons / 32];
+  __shared__ float s_red[2 * (kCons / 32)];
   __shared__ __align__(16) float s_att[kMaxStage];
   __shared__ unsigned long long s_key[kCons / 32];
   __shared__ float2 s_rope[64];  // (cos, sin) of each rotary pair at this frame's position
@@ -587,6 +749,12 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
   __shared__ int s_last[2];
   __shared__ volatile int s_abort;
   __shared__ unsigned s_issued;
+  // the consumers read op descriptors, plans and the launch's position from shared
+  // memory: op k+1's descriptor is fetched during op k and published by its last CTA
+  // barrier, so no op starts with a round trip to global memory for its own parameters
+  __shared__ __align__(16) PersOp s_op[2];
+  __shared__ __align__(16) GemvPlan s_plan[kPersMaxPlans];
+  __shared__ int s_pos, s_forcing;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // wait limit of this launch (a test may shorten it), and the op whose barrier a test
   // makes unreachable (-1: none)
@@ -612,65 +780,45 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
     // ------------------------------------------------ producer: every op's weight tiles
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
+      TileCur c{};
+      bool more = cur_seek<WT>(P, c);
       uint32_t gi = 0;
-      bool stop = false;
-      for (int k = 0; k < P.n_ops && !stop; ++k) {
-        const PersOp& op = P.ops[k];
-        if (op.type != OPT_GEMV) continue;
-        const GemvPlan& pl = P.plans[op.plan];
-        int t0, t1;
-        tile_range(pl, t0, t1);
-        const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
-        const bool paired = op.epi == EPI_SWIGLU;
-        const int opt = paired ? pl.tile_rows / 2 : pl.tile_rows;
-        const uint8_t* W = static_cast<const uint8_t*>(op.W);
-        for (int kp = 0; kp < pl.kparts && !stop; ++kp) {
-          const int k0 = kp * pl.kp_width;
-          const int Kw = kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
-          const uint32_t seg = (uint32_t)Kw * (uint32_t)sizeof(WT);  // bytes of one row part
-          for (int t = t0; t < t1; ++t) {
-            const int s = (int)(gi % (uint32_t)NS);
-            if (gi >= (uint32_t)NS &&
-                !mbar_wait_for(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u, lim)) {
-              atomicOr(P.status, kDevTimeout);
-              s_abort = 1;
-            }
-            if (s_abort) {
-              stop = true;
-              break;
-            }
-            const int r0 = t * opt;
-            const int nv = min(opt, pl.n_out - r0);
-            uint8_t* dst = ring + (size_t)s * P.slot_bytes;
-            if (pl.kparts > 1) {
-              // one copy per row: the part's columns are a strided window of W
-              mbar_arrive_expect_tx(&full[s], (uint32_t)nv * seg);
-              for (int r = 0; r < nv; ++r)
-                bulk_g2s(dst + (size_t)r * seg,
-                         W + (size_t)(r0 + r) * row_bytes + (size_t)k0 * sizeof(WT), seg,
-                         &full[s], pol);
-            } else if (paired) {
-              const uint32_t bytes = (uint32_t)nv * row_bytes;
-              mbar_arrive_expect_tx(&full[s], 2u * bytes);
-              bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-              bulk_g2s(dst + (size_t)opt * row_bytes,
-                       W + (size_t)op.w_half + (size_t)r0 * row_bytes, bytes,
-                       &full[s], pol);
-            } else {
-              const uint32_t bytes = (uint32_t)nv * row_bytes;
-              mbar_arrive_expect_tx(&full[s], bytes);
-              bulk_g2s(dst, W + (size_t)r0 * row_bytes, bytes, &full[s], pol);
-            }
-            ++gi;
-          }
+      while (more) {
+        const int s = (int)(gi % (uint32_t)NS);
+        if (gi >= (uint32_t)NS &&
+            !mbar_wait_for(&empty[s], ((gi / (uint32_t)NS) - 1u) & 1u, lim)) {
+          atomicOr(P.status, kDevTimeout);
+          s_abort = 1;
         }
+        if (s_abort) break;
+        uint8_t* dst = ring + (size_t)s * P.slot_bytes;
+        mbar_arrive_expect_tx(&full[s], cur_bytes<WT>(P, c));
+        cur_ranges<WT>(P, c, [&](const uint8_t* src, uint32_t bytes, uint32_t off) {
+          bulk_g2s(dst + off, src, bytes, &full[s], pol);
+        });
+        ++gi;
+        more = cur_next<WT>(P, c);
       }
       s_issued = gi;
     }
     __syncwarp();
   } else {
     // ------------------------------------------------ consumers: ops in order
+    constexpr int kOpWords = (int)(sizeof(PersOp) / 8);
+    constexpr int kPlanWords = (int)(sizeof(GemvPlan) * kPersMaxPlans / 4);
+    static_assert(sizeof(PersOp) % 8 == 0 && kOpWords <= kCons, "op descriptor words");
+    static_assert((sizeof(GemvPlan) * kPersMaxPlans) % 4 == 0 && kPlanWords <= kCons,
+                  "plan words");
+    const unsigned long long* ops64 = reinterpret_cast<const unsigned long long*>(P.ops);
+    unsigned long long* s_op64 = reinterpret_cast<unsigned long long*>(s_op);
+    if (tid < kPlanWords)
+      reinterpret_cast<int*>(s_plan)[tid] = reinterpret_cast<const int*>(P.plans)[tid];
+    if (tid < kOpWords) s_op64[tid] = ops64[tid];
     pdl_wait();
+    if (tid == 0) {
+      s_pos = P.offsets[0];
+      s_forcing = P.d_in[IoLayout{1}.flag_off()];
+    }
     if (tid < P.head_dim / 2) {
       // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos;
       // every layer rotates at the same position, so the pairs are computed once
@@ -679,15 +827,20 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
       s_rope[tid] = make_float2(cosf(ang), sinf(ang));
     }
     bar_sync(1, kCons);
-    uint32_t gi = 0;
+    const int pos = s_pos, forcing = s_forcing;
+    int cslot = 0;       // ring slot of the next tile to consume
+    uint32_t cph = 0u;   // and the phase its "full" barrier completes
     float xr[kMaxNch][V];
     const bool stamp = P.trace != nullptr && blockIdx.x == 0 && tid == 0;
     float ar[2][V];
     for (int k = 0; k < P.n_ops; ++k) {
+      // op k+1's descriptor, loaded now, stored to shared memory at the end of op k
+      const unsigned long long nxt =
+          (tid < kOpWords && k + 1 < P.n_ops) ? ops64[(size_t)(k + 1) * kOpWords + tid] : 0ull;
       {  // constant alpha of an RMSNorm prologue: load it before waiting
-        const PersOp& op = P.ops[k];
+        const PersOp& op = s_op[k & 1];
         if (op.type == OPT_GEMV && (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB)) {
-          const GemvPlan& pl = P.plans[op.plan];
+          const GemvPlan& pl = s_plan[op.plan];
           const int tig = tid % pl.tpr, CC = pl.K / V;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -697,7 +850,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           }
         }
       }
-      if (k > 0 && !P.ops[k].nobar) {
+      if (k > 0 && !s_op[k & 1].nobar) {
         const unsigned target = (unsigned)k * gridDim.x + (k == stall_op ? 1u : 0u);
         if (tid == 0 && !grid_wait(P.grid_bar, target, lim)) {
           atomicOr(P.status, kDevTimeout);
@@ -707,9 +860,9 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         if (s_abort) break;
       }
       if (stamp) P.trace[k] = global_timer_ns();
-      const PersOp& op = P.ops[k];
+      const PersOp& op = s_op[k & 1];
       if (op.type == OPT_ATTN) {
-        attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last);
+        attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last, pos);
       } else if (op.type == OPT_TOPK) {
         // "moshi_lm.rs", `topk_sample` for pick key_index over the logits the previous op
         // wrote, by CTA 0 (its partial-sum buffer holds the selection's scratch)
@@ -725,7 +878,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           if (tid == 0) P.keys[pk] = argmax_key(__ldcg(op.in + tok), (uint32_t)tok);
         }
       } else {
-        const GemvPlan& pl = P.plans[op.plan];
+        const GemvPlan& pl = s_plan[op.plan];
         int t0, t1;
         tile_range(pl, t0, t1);
         const int nt = t1 - t0;
@@ -742,13 +895,25 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
             const int k0 = kp * pl.kp_width;
             const int Kw = kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
             const int nch = (Kw / V + pl.tpr - 1) / pl.tpr;
-            form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, s_att);
-            if (nch <= 1)
-              ok = consume_tiles<WT, 1>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
-                                        empty, part, xr, g, tig, warp, lane, lim);
+            form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, k & 1,
+                       s_att, forcing);
+            if (nch <= 1 && nt > 2)
+              ok = consume_tiles<WT, 1, kBurstT, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                                                       P.slot_bytes, NS, full, empty, part, xr,
+                                                       g, tig, warp, lane, lim);
+            else if (nch <= 1)
+              ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                                                 P.slot_bytes, NS, full, empty, part, xr, g,
+                                                 tig, warp, lane, lim);
+            else if (nt > kStreamMinTiles)
+              ok = consume_tiles<WT, 2, kStreamT, kStreamBurst>(pl, Kw, kp > 0, nt, cslot, cph,
+                                                                ring, P.slot_bytes, NS, full,
+                                                                empty, part, xr, g, tig, warp,
+                                                                lane, lim);
             else
-              ok = consume_tiles<WT, 2>(pl, Kw, kp > 0, nt, gi, ring, P.slot_bytes, NS, full,
-                                        empty, part, xr, g, tig, warp, lane, lim);
+              ok = consume_tiles<WT, 2, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                                                 P.slot_bytes, NS, full, empty, part, xr, g,
+                                                 tig, warp, lane, lim);
           }
           if (!ok) {
             atomicOr(P.status, kDevTimeout);
@@ -756,9 +921,11 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           }
           bar_sync(1, kCons);
           if (s_abort) break;
-          epilogue<WT>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope, resid_old);
+          epilogue<WT>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope, resid_old, pos,
+                       forcing);
         }
       }
+      if (tid < kOpWords && k + 1 < P.n_ops) s_op64[((k + 1) & 1) * kOpWords + tid] = nxt;
       bar_sync(1, kCons);
       if (tid == 0) grid_arrive(P.grid_bar);
     }
