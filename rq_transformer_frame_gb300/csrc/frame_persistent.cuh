@@ -339,30 +339,21 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     }
   }
   if (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB) {
-    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)); alpha (a
-    // constant) was loaded before the grid barrier.
-    // Every row group holds the whole vector: group 0's warps sum the squares from
-    // registers.  s_red alternates between two halves op by op, so one CTA barrier is
-    // enough (the next op writes the other half).
+    // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).  The factor
+    // 1 / sqrt(...) is one scalar for the whole vector, so W (x * alpha * r) = r W (x *
+    // alpha): the tiles run on x * alpha (alpha, a constant, was loaded before the grid
+    // barrier) and the epilogue multiplies by r (rms_scale), after the CTA barrier that
+    // follows the tiles -- the reduction is off the path from x to the first tile.  Here
+    // each warp leaves its partial sum of squares in s_red: every row group holds the
+    // whole vector, group 0's warps' partials cover it once.  s_red alternates between
+    // two halves op by op (the next op writes the other half).
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxNch; ++j)
 #pragma unroll
       for (int v = 0; v < V; ++v) ss = fmaf(xr[j][v], xr[j][v], ss);
     ss = warp_sum(ss);
-    float* red = s_red + red_half * (kCons / 32);
-    if (lane == 0) red[warp] = ss;
-    bar_sync(1, kCons);
-    float rv[kCons / 32];
-#pragma unroll
-    for (int w = 0; w < kCons / 32; ++w) rv[w] = red[w];
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCons / 32; ++w)
-      if (w < pl.tpr / 32) tot += rv[w];
-    const float inv = 1.0f / sqrtf(P.eps + tot / (float)K);
-    const bool side =
-        op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0;
+    if (lane == 0) s_red[red_half * (kCons / 32) + warp] = ss;
 #pragma unroll
     for (int j = 0; j < kMaxNch; ++j) {
       const int c = tig + j * pl.tpr;
@@ -370,11 +361,7 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
 #pragma unroll
         for (int v = 0; v < V; ++v) {
           const float a = j < 2 ? ar[j < 2 ? j : 0][v] : op.alpha[c * V + v];
-          xr[j][v] = xr[j][v] * a * inv;
-        }
-        if (side) {
-#pragma unroll
-          for (int v = 0; v < V; ++v) op.side_out[c * V + v] = xr[j][v];
+          xr[j][v] = xr[j][v] * a;
         }
       }
     }
@@ -451,6 +438,21 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
   }
 }
 
+// The RMSNorm factor 1 / sqrt(eps + sum(x^2) / K) of an RMS op, from the per-warp sums
+// form_x left (call after a CTA barrier that follows form_x); every thread sums them in
+// the same order, so every thread gets the same value.
+__device__ __forceinline__ float rms_scale(const PersParams& P, const GemvPlan& pl,
+                                           const float* s_red, int red_half) {
+  float rv[kCons / 32];
+#pragma unroll
+  for (int w = 0; w < kCons / 32; ++w) rv[w] = s_red[red_half * (kCons / 32) + w];
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCons / 32; ++w)
+    if (w < pl.tpr / 32) tot += rv[w];
+  return 1.0f / sqrtf(P.eps + tot / (float)pl.K);
+}
+
 // ---------------------------------------------------------------- epilogue
 // Finish rows [t0*tr, (t0+nt)*tr) of one GEMV op from the per-warp partials (batch 1).
 template <typename WT, bool PICKS>
@@ -458,17 +460,20 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
                                          const GemvPlan& pl, int t0, int nt, const float* part,
                                          int tid, int warp, int lane,
                                          unsigned long long* s_key, const float2* s_rope,
-                                         float resid_old, int pos, int forcing) {
+                                         float resid_old, int pos, int forcing,
+                                         float scale) {
   const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
   const int nrows = nt * tr;
-  auto yrow = [&](int lr) {  // wpg <= 8: the partials load together, then add in order
+  // the row's value: the partials (wpg <= 8, loaded together, added in order), times the
+  // RMSNorm factor of an RMS op (1 otherwise)
+  auto yrow = [&](int lr) {
     float pv[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) pv[w] = w < wpg ? part[(size_t)lr * wpg + w] : 0.f;
     float y = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) y += pv[w];
-    return y;
+    return y * scale;
   };
   auto grow = [&](int lr) { return (t0 + lr / tr) * tr + lr % tr; };
   const int epi = op.epi;
@@ -930,8 +935,22 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
           }
           bar_sync(1, kCons);
           if (s_abort) break;
+          const bool rms = op.pro == PRO_RMS || op.pro == PRO_RMS_EMB;
+          const float scale = rms ? rms_scale(P, pl, s_red, k & 1) : 1.0f;
+          if (op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0) {
+            // CTA 0 keeps the normalised vector (the head's transformer_out)
+            constexpr int V2 = Chunk<WT>::V;
+#pragma unroll
+            for (int j = 0; j < kMaxNch; ++j) {
+              const int c = tig + j * pl.tpr;
+              if (c < pl.K / V2 && j * pl.tpr < pl.K / V2) {
+#pragma unroll
+                for (int v = 0; v < V2; ++v) op.side_out[c * V2 + v] = xr[j][v] * scale;
+              }
+            }
+          }
           epilogue<WT, PICKS>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope, resid_old,
-                              pos, forcing);
+                              pos, forcing, scale);
         }
       }
       if (tid < kOpWords && k + 1 < P.n_ops) s_op64[((k + 1) & 1) * kOpWords + tid] = nxt;
