@@ -40,7 +40,10 @@ __global__ void __launch_bounds__(256) frame_begin_kernel(const FrameParams p) {
       ring[s * kRing + (off + stream_delay(s)) % kRing] = user[tid];
     }
     if (tid < 9) p.keys[(size_t)b * 9 + tid] = 0ull;
-    if (tid == 0 && b == 0 && p.grid_bar) *p.grid_bar = 0u;
+    if (tid == 0 && b == 0 && p.grid_bar) {
+      p.grid_bar[0] = 0u;                // the temporal launch's grid barrier
+      p.grid_bar[kPersDepBarWord] = 0u;  // the depformer launch's
+    }
     if (p.rope && tid < p.head_dim / 2) {
       // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos
       const float freq = expf(-logf(p.rope_theta) * 2.0f * (float)tid / (float)p.head_dim);

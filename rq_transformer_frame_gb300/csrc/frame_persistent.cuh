@@ -23,6 +23,12 @@ namespace pers {
 constexpr int kCons = 256;    // consumer threads
 constexpr int kThr = 288;     // + 1 producer warp
 constexpr int kMaxNch = 2;  // long reductions are split into parts (GemvPlan::kparts)
+// chunks of x a consumer thread holds: two for f32 / bf16 rows (4 or 8 values each), one
+// for weight bands (16 q8 or 32 q4 values)
+template <typename WT>
+struct Nx {
+  static constexpr int N = Chunk<WT>::kBand ? 1 : kMaxNch;
+};
 constexpr int kMaxStage = 1024;  // depformer attention output staged in shared memory (DD <= 1024)
 #ifndef RQ_PERS_BURST_T
 #define RQ_PERS_BURST_T 4
@@ -97,6 +103,22 @@ __device__ __forceinline__ float warp_sum_rows(float (&v)[R], int lane) {
   return v[0];
 }
 
+// one 16-byte chunk of a staged weight row times the thread's chunk of x: f32 / bf16
+// values, or a weight band's codes times the scale of their group (read from the row)
+template <typename WT>
+__device__ __forceinline__ void tile_dot(const uint8_t* row, int Kw, int c, const uint4 w,
+                                         const float (&x)[Chunk<WT>::V], float& a, float& b) {
+  if constexpr (Chunk<WT>::kBand) {
+    const float d = *reinterpret_cast<const float*>(row + Chunk<WT>::scale_off(Kw, c));
+    Chunk<WT>::dot2s(w, d, x, a, b);
+  } else {
+    (void)row;
+    (void)Kw;
+    (void)c;
+    Chunk<WT>::dot2(w, x, a, b);
+  }
+}
+
 // Consume this CTA's `nt` tiles of one GEMV op from the ring (slot `slot`, phase `ph`
 // advance tile by tile), leaving one partial per (row, warp) in `part`.  Tiles go in
 // groups of T with one butterfly over the group's 2T rows.  BURST (tiles already
@@ -109,12 +131,13 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
                                               int nt, int& slot, uint32_t& ph,
                                               uint8_t* ring, int slot_bytes, int NS,
                                               uint64_t* full, uint64_t* empty, float* part,
-                                              const float (&xr)[kMaxNch][Chunk<WT>::V],
+                                              const float (&xr)[Nx<WT>::N][Chunk<WT>::V],
                                               int g, int tig, int warp, int lane,
                                               uint64_t lim) {
   constexpr int RG = 2;  // rows per thread group and tile (every persistent plan)
   constexpr int R = T * RG;
-  const uint32_t row_bytes = (uint32_t)Kw * (uint32_t)sizeof(WT);
+  static_assert(NCH <= Nx<WT>::N, "x chunks held per thread");
+  const uint32_t row_bytes = (uint32_t)Chunk<WT>::row_bytes(Kw);
   const int CC = Kw / Chunk<WT>::V;
   const int wpg = pl.tpr >> 5;
   for (int i0 = 0; i0 < nt; i0 += T) {
@@ -152,10 +175,15 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
 #pragma unroll
       for (int t = 0; t < T; ++t)
 #pragma unroll
-        for (int j = 0; j < NCH; ++j)
+        for (int j = 0; j < NCH; ++j) {
+          const int c = tig + j * pl.tpr;
+          // past the row: zero weights for f32 / bf16; a band code 0 stands for -8, skip
+          if (Chunk<WT>::kBand && c >= CC) continue;
 #pragma unroll
           for (int r = 0; r < RG; ++r)
-            Chunk<WT>::dot2(w[t][j][r], xr[j], acc[t * RG + r][0], acc[t * RG + r][1]);
+            tile_dot<WT>(row0[t] + (size_t)r * row_bytes, Kw, c, w[t][j][r], xr[j],
+                         acc[t * RG + r][0], acc[t * RG + r][1]);
+        }
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
@@ -179,10 +207,14 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
                                : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
-          for (int j = 0; j < NCH; ++j)
+          for (int j = 0; j < NCH; ++j) {
+            const int c = tig + j * pl.tpr;
+            if (Chunk<WT>::kBand && c >= CC) continue;  // see the burst path
 #pragma unroll
             for (int r = 0; r < RG; ++r)
-              Chunk<WT>::dot2(w[j][r], xr[j], acc[t * RG + r][0], acc[t * RG + r][1]);
+              tile_dot<WT>(row0 + (size_t)r * row_bytes, Kw, c, w[j][r], xr[j],
+                           acc[t * RG + r][0], acc[t * RG + r][1]);
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot]);
           if (++slot == NS) {
@@ -255,19 +287,31 @@ template <typename WT, typename F>
 __device__ __forceinline__ void cur_ranges(const PersParams& P, const TileCur& c, F&& f) {
   const PersOp& op = P.ops[c.k];
   const GemvPlan& pl = P.plans[op.plan];
-  const uint32_t row_bytes = (uint32_t)pl.K * (uint32_t)sizeof(WT);
+  const uint32_t row_bytes = (uint32_t)Chunk<WT>::row_bytes(pl.K);
   const bool paired = op.epi == EPI_SWIGLU;
   const int opt = paired ? pl.tile_rows / 2 : pl.tile_rows;
   const uint8_t* W = static_cast<const uint8_t*>(op.W);
   const int r0 = c.t * opt;
   const int nv = min(opt, pl.n_out - r0);
   if (pl.kparts > 1) {
-    // one range per row: the part's columns are a strided window of W
+    // per row, the part's columns are a strided window of W; a weight band's row part is
+    // its codes, then its groups' scales (the layout of a Kw-column band row)
     const int k0 = c.kp * pl.kp_width;
     const int Kw = c.kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
-    const uint32_t seg = (uint32_t)Kw * (uint32_t)sizeof(WT);
-    for (int r = 0; r < nv; ++r)
-      f(W + (size_t)(r0 + r) * row_bytes + (size_t)k0 * sizeof(WT), seg, (uint32_t)r * seg);
+    const uint32_t seg = (uint32_t)Chunk<WT>::row_bytes(Kw);
+    for (int r = 0; r < nv; ++r) {
+      const uint8_t* row = W + (size_t)(r0 + r) * row_bytes;
+      if constexpr (Chunk<WT>::kBand) {
+        const uint32_t sc = (uint32_t)Kw / 8u;          // f32 scale per 32 values
+        const uint32_t cd = seg - sc;                   // code bytes of the part
+        const uint32_t cd0 = (uint32_t)Chunk<WT>::row_bytes(k0) - (uint32_t)k0 / 8u;
+        const uint32_t codes_row = row_bytes - (uint32_t)pl.K / 8u;
+        f(row + cd0, cd, (uint32_t)r * seg);
+        f(row + codes_row + (uint32_t)k0 / 8u, sc, (uint32_t)r * seg + cd);
+      } else {
+        f(row + (size_t)k0 * sizeof(WT), seg, (uint32_t)r * seg);
+      }
+    }
   } else if (paired) {
     const uint32_t bytes = (uint32_t)nv * row_bytes;
     f(W + (size_t)r0 * row_bytes, bytes, 0u);
@@ -290,16 +334,18 @@ __device__ __forceinline__ uint32_t cur_bytes(const PersParams& P, const TileCur
 template <typename WT>
 __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                        const GemvPlan& pl, int nch, int k0, int Kw,
-                                       float (&xr)[kMaxNch][Chunk<WT>::V],
-                                       const float (&ar)[2][Chunk<WT>::V], int g, int tig,
-                                       int tid, int warp, int lane, float* s_red,
+                                       float (&xr)[Nx<WT>::N][Chunk<WT>::V],
+                                       const float (&ar)[Nx<WT>::N][Chunk<WT>::V], int g,
+                                       int tig, int tid, int warp, int lane, float* s_red,
                                        int red_half, float* s_att, int forcing) {
   constexpr int V = Chunk<WT>::V;
+  constexpr int NX = Nx<WT>::N;
+  using TT = typename Chunk<WT>::Table;  // embedding tables: bf16 for weight bands
   const int K = pl.K, CC = Kw / V;
   const float* in = op.in + k0;  // this part's columns [k0, k0 + Kw)
   (void)tid;
 #pragma unroll
-  for (int j = 0; j < kMaxNch; ++j) {
+  for (int j = 0; j < NX; ++j) {
     const int c = tig + j * pl.tpr;
 #pragma unroll
     for (int v = 0; v < V; ++v) xr[j][v] = 0.f;
@@ -323,13 +369,13 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                            : argmax_key_index(__ldcg(P.keys + op.key_index));
     const bool keep = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
 #pragma unroll
-    for (int j = 0; j < kMaxNch; ++j) {
+    for (int j = 0; j < NX; ++j) {
       const int c = tig + j * pl.tpr;
       if (j < nch && c < CC) {
         if (prev != -1) {
 #pragma unroll
           for (int v = 0; v < V; ++v)
-            xr[j][v] += Chunk<WT>::elem(op.emb, (size_t)max(prev, 0) * K + c * V + v);
+            xr[j][v] += Chunk<TT>::elem(op.emb, (size_t)max(prev, 0) * K + c * V + v);
         }
         if (keep) {
 #pragma unroll
@@ -341,27 +387,36 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
   if (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB) {
     // "moshi_lm.rs", `rms_norm`: x * alpha * (1 / sqrt(eps + sum(x^2) / n)).  The factor
     // 1 / sqrt(...) is one scalar for the whole vector, so W (x * alpha * r) = r W (x *
-    // alpha): the tiles run on x * alpha (alpha, a constant, was loaded before the grid
-    // barrier) and the epilogue multiplies by r (rms_scale), after the CTA barrier that
-    // follows the tiles -- the reduction is off the path from x to the first tile.  Here
-    // each warp leaves its partial sum of squares in s_red: every row group holds the
-    // whole vector, group 0's warps' partials cover it once.  s_red alternates between
-    // two halves op by op (the next op writes the other half).
+    // alpha): the tiles run on x * alpha and the epilogue multiplies by r (rms_scale),
+    // after the CTA barrier that follows the tiles -- the reduction is off the path from
+    // x to the first tile.  Here each warp leaves its partial sum of squares in s_red:
+    // every row group holds the whole vector, group 0's warps' partials cover it once.
+    // s_red alternates between two halves op by op (the next op writes the other half).
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxNch; ++j)
+    for (int j = 0; j < NX; ++j)
 #pragma unroll
       for (int v = 0; v < V; ++v) ss = fmaf(xr[j][v], xr[j][v], ss);
     ss = warp_sum(ss);
     if (lane == 0) s_red[red_half * (kCons / 32) + warp] = ss;
 #pragma unroll
-    for (int j = 0; j < kMaxNch; ++j) {
+    for (int j = 0; j < NX; ++j) {
       const int c = tig + j * pl.tpr;
       if (j < nch && c < CC) {
+        if constexpr (Chunk<WT>::kBand) {
+          // weight bands: x is one chunk of 16 / 32 values, too many registers to keep
+          // alpha from before the grid barrier; it loads here (16-byte aligned rows)
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const float a = j < 2 ? ar[j < 2 ? j : 0][v] : op.alpha[c * V + v];
-          xr[j][v] = xr[j][v] * a;
+          for (int v = 0; v < V; v += 4) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(op.alpha + c * V + v));
+            xr[j][v] *= a.x;
+            xr[j][v + 1] *= a.y;
+            xr[j][v + 2] *= a.z;
+            xr[j][v + 3] *= a.w;
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < V; ++v) xr[j][v] *= ar[j][v];  // loaded before the barrier
         }
       }
     }
@@ -427,7 +482,7 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     }
     bar_sync(1, kCons);
 #pragma unroll
-    for (int j = 0; j < kMaxNch; ++j) {
+    for (int j = 0; j < NX; ++j) {
       const int c = tig + j * pl.tpr;
       if (j < nch && c < CC) {
 #pragma unroll
@@ -493,7 +548,8 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       if (epi == EPI_DEPIN) {
         // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
         op.out[row] = (prev != -1)
-                          ? y + Chunk<WT>::elem(op.emb, (size_t)max(prev, 0) * pl.n_out + row)
+                          ? y + Chunk<typename Chunk<WT>::Table>::elem(
+                                    op.emb, (size_t)max(prev, 0) * pl.n_out + row)
                           : y;
       }
     }
@@ -749,9 +805,11 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
 // PICKS: with the token-pick ops (top-k, Gumbel scores); without them (greedy frames) the
 // kernel is about a quarter smaller, which leaves more of its hot code in the SM's
 // instruction caches (measured: 18 us less per Moshi-7B frame)
-template <typename WT, typename KT, int EPL, bool PICKS>
-// two CTAs per SM: the register cap follows from 2 x 288 threads
-__global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersParams P) {
+// MINB: CTAs per SM.  Two for the temporal stack's weight stream (16 consumer warps per
+// SM keep up with HBM; the register cap follows from 2 x 288 threads: 96), one for the
+// depformer's latency-bound small ops (a 152-CTA grid barrier, 163 registers, no spills).
+template <typename WT, typename KT, int EPL, bool PICKS, int MINB>
+__global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const PersParams P) {
   constexpr int V = Chunk<WT>::V;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_red[2 * (kCons / 32)];
@@ -773,7 +831,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
   // wait limit of this launch (a test may shorten it), and the op whose barrier a test
   // makes unreachable (-1: none)
   const uint64_t lim = P.wait_ctl && P.wait_ctl[0] ? P.wait_ctl[0] : kWaitLimitNs;
-  const int stall_op = P.wait_ctl ? (int)P.wait_ctl[1] - 1 : -1;
+  const int stall_op = P.wait_ctl ? (int)P.wait_ctl[1] - 1 - P.op_base : -1;
   const int NS = P.n_slots;
   uint8_t* ring = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)NS * P.slot_bytes);
@@ -844,20 +902,20 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
     const int pos = s_pos, forcing = s_forcing;
     int cslot = 0;       // ring slot of the next tile to consume
     uint32_t cph = 0u;   // and the phase its "full" barrier completes
-    float xr[kMaxNch][V];
+    float xr[Nx<WT>::N][V];
     const bool stamp = P.trace != nullptr && blockIdx.x == 0 && tid == 0;
-    float ar[2][V];
+    float ar[Nx<WT>::N][V];  // an RMSNorm op's alpha, loaded before its grid barrier
     for (int k = 0; k < P.n_ops; ++k) {
       // op k+1's descriptor, loaded now, stored to shared memory at the end of op k
       const unsigned long long nxt =
           (tid < kOpWords && k + 1 < P.n_ops) ? ops64[(size_t)(k + 1) * kOpWords + tid] : 0ull;
-      {  // constant alpha of an RMSNorm prologue: load it before waiting
+      if constexpr (!Chunk<WT>::kBand) {  // constant alpha of an RMSNorm prologue
         const PersOp& op = s_op[k & 1];
         if (op.type == OPT_GEMV && (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB)) {
           const GemvPlan& pl = s_plan[op.plan];
           const int tig = tid % pl.tpr, CC = pl.K / V;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
+          for (int j = 0; j < Nx<WT>::N; ++j) {
             const int c = tig + j * pl.tpr;
 #pragma unroll
             for (int v = 0; v < V; ++v) ar[j][v] = (c < CC) ? op.alpha[c * V + v] : 0.f;
@@ -873,7 +931,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
         bar_sync(1, kCons);
         if (s_abort) break;
       }
-      if (stamp) P.trace[k] = global_timer_ns();
+      if (stamp) P.trace[P.op_base + k] = global_timer_ns();
       const PersOp& op = s_op[k & 1];
       if (op.type == OPT_ATTN) {
         attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last, pos);
@@ -919,15 +977,17 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
               ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
                                                  P.slot_bytes, NS, full, empty, part, xr, g,
                                                  tig, warp, lane, lim);
-            else if (nt > kStreamMinTiles)
-              ok = consume_tiles<WT, 2, kStreamT, kStreamBurst>(pl, Kw, kp > 0, nt, cslot, cph,
-                                                                ring, P.slot_bytes, NS, full,
-                                                                empty, part, xr, g, tig, warp,
-                                                                lane, lim);
-            else
-              ok = consume_tiles<WT, 2, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
-                                                 P.slot_bytes, NS, full, empty, part, xr, g,
-                                                 tig, warp, lane, lim);
+            else if constexpr (Nx<WT>::N >= 2) {  // two x chunks (weight bands hold one)
+              if (nt > kStreamMinTiles)
+                ok = consume_tiles<WT, 2, kStreamT, kStreamBurst>(pl, Kw, kp > 0, nt, cslot,
+                                                                  cph, ring, P.slot_bytes, NS,
+                                                                  full, empty, part, xr, g, tig,
+                                                                  warp, lane, lim);
+              else
+                ok = consume_tiles<WT, 2, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                                                   P.slot_bytes, NS, full, empty, part, xr, g,
+                                                   tig, warp, lane, lim);
+            }
           }
           if (!ok) {
             atomicOr(P.status, kDevTimeout);
@@ -941,9 +1001,9 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
             // CTA 0 keeps the normalised vector (the head's transformer_out)
             constexpr int V2 = Chunk<WT>::V;
 #pragma unroll
-            for (int j = 0; j < kMaxNch; ++j) {
+            for (int j = 0; j < Nx<WT>::N; ++j) {
               const int c = tig + j * pl.tpr;
-              if (c < pl.K / V2 && j * pl.tpr < pl.K / V2) {
+              if (c < pl.K / V2) {
 #pragma unroll
                 for (int v = 0; v < V2; ++v) op.side_out[c * V2 + v] = xr[j][v] * scale;
               }
@@ -958,7 +1018,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
       if (tid == 0) grid_arrive(P.grid_bar);
     }
     if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x, lim))
-      P.trace[P.n_ops] = global_timer_ns();
+      P.trace[P.op_base + P.n_ops] = global_timer_ns();
   }
   __syncthreads();
   pdl_trigger();
@@ -974,7 +1034,7 @@ __global__ void __launch_bounds__(kThr, 2) frame_persistent_kernel(const PersPar
   }
 }
 
-template <typename WT, typename KT, int EPL, bool PICKS>
+template <typename WT, typename KT, int EPL, bool PICKS, int MINB>
 cudaError_t launch_t(const PersParams& p, int grid, int smem, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -988,14 +1048,14 @@ cudaError_t launch_t(const PersParams& p, int grid, int smem, cudaStream_t s, bo
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, frame_persistent_kernel<WT, KT, EPL, PICKS>, p);
+  return cudaLaunchKernelEx(&cfg, frame_persistent_kernel<WT, KT, EPL, PICKS, MINB>, p);
 }
 
-template <typename WT, typename KT, int EPL, bool PICKS>
+template <typename WT, typename KT, int EPL, bool PICKS, int MINB>
 int max_grid_t(int smem) {
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
-                                                    frame_persistent_kernel<WT, KT, EPL, PICKS>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, frame_persistent_kernel<WT, KT, EPL, PICKS, MINB>,
                                                     kThr, (size_t)smem) != cudaSuccess)
     return 0;
   cudaGetDevice(&dev);
@@ -1003,26 +1063,37 @@ int max_grid_t(int smem) {
   return per_sm * sms;
 }
 
-template <typename WT, typename KT, int EPL, bool PICKS>
+template <typename WT, typename KT, int EPL, bool PICKS, int MINB>
 cudaError_t configure_t(int smem) {
-  return cudaFuncSetAttribute(frame_persistent_kernel<WT, KT, EPL, PICKS>,
+  return cudaFuncSetAttribute(frame_persistent_kernel<WT, KT, EPL, PICKS, MINB>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-// the greedy-only instantiations live in frame_persistent_greedy.cu (compiled in parallel)
-#define RQ_PERS_EXTERN(W, K, E, PK)                                                        \
-  extern template cudaError_t launch_t<W, K, E, PK>(const PersParams&, int, int,            \
-                                                    cudaStream_t, bool);                    \
-  extern template int max_grid_t<W, K, E, PK>(int);                                        \
-  extern template cudaError_t configure_t<W, K, E, PK>(int);
-#define RQ_PERS_INSTANTIATE(W, K, E, PK)                                                   \
-  template cudaError_t launch_t<W, K, E, PK>(const PersParams&, int, int, cudaStream_t,     \
-                                             bool);                                         \
-  template int max_grid_t<W, K, E, PK>(int);                                               \
-  template cudaError_t configure_t<W, K, E, PK>(int);
+// Instantiation sets.  Two CTAs per SM (the temporal launch): frame_persistent.cu (with
+// token picks), frame_persistent_greedy.cu, frame_persistent_band.cu.  One CTA per SM
+// (the depformer launch, which runs no temporal attention, so one head-size variant):
+// frame_persistent_dep.cu.
+#define RQ_PERS_EXTERN(W, K, E, PK, MB)                                                    \
+  extern template cudaError_t launch_t<W, K, E, PK, MB>(const PersParams&, int, int,        \
+                                                        cudaStream_t, bool);                \
+  extern template int max_grid_t<W, K, E, PK, MB>(int);                                    \
+  extern template cudaError_t configure_t<W, K, E, PK, MB>(int);
+#define RQ_PERS_INSTANTIATE(W, K, E, PK, MB)                                               \
+  template cudaError_t launch_t<W, K, E, PK, MB>(const PersParams&, int, int, cudaStream_t, \
+                                                 bool);                                     \
+  template int max_grid_t<W, K, E, PK, MB>(int);                                           \
+  template cudaError_t configure_t<W, K, E, PK, MB>(int);
 #define RQ_PERS_ALL(M, PK)                                                                 \
-  M(float, float, 1, PK) M(float, float, 2, PK) M(float, float, 4, PK)                     \
-  M(uint16_t, uint16_t, 1, PK) M(uint16_t, uint16_t, 2, PK) M(uint16_t, uint16_t, 4, PK)
+  M(float, float, 1, PK, 2) M(float, float, 2, PK, 2) M(float, float, 4, PK, 2)            \
+  M(uint16_t, uint16_t, 1, PK, 2) M(uint16_t, uint16_t, 2, PK, 2)                          \
+  M(uint16_t, uint16_t, 4, PK, 2)
+// weight bands (bf16 K/V), head_dim 64 and 128: frame_persistent_band.cu
+#define RQ_PERS_BANDS(M, PK)                                                               \
+  M(q8_t, uint16_t, 2, PK, 2) M(q8_t, uint16_t, 4, PK, 2) M(q4_t, uint16_t, 2, PK, 2)      \
+  M(q4_t, uint16_t, 4, PK, 2)
+#define RQ_PERS_DEP(M, PK)                                                                 \
+  M(float, float, 1, PK, 1) M(uint16_t, uint16_t, 1, PK, 1) M(q8_t, uint16_t, 1, PK, 1)    \
+  M(q4_t, uint16_t, 1, PK, 1)
 
 }  // namespace pers
 

@@ -287,8 +287,9 @@ struct PersOp {
 constexpr int kPersMaxPlans = 12;
 
 struct PersParams {
-  const PersOp* ops;
+  const PersOp* ops;    // this launch's ops (the frame's op table from op_base on)
   int n_ops;
+  int op_base;          // frame op index of ops[0]: the trace and the test stall use frame indices
   GemvPlan plans[kPersMaxPlans];
   int slot_bytes;   // bytes of one ring slot (>= every op's tile)
   int n_slots;
@@ -317,7 +318,7 @@ struct PersParams {
 };
 
 GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
-                         int grid);
+                         int grid, int band = BAND_NONE);
 // ---------------------------------------------------------------- tensor-core frame
 // Everything a batched frame needs between frame_begin and frame_end: the per-op plans,
 // the bf16 operand buffers [kOpndParts][NB][K] (hi, mid[, lo] parts; rows >= B stay zero) and one
@@ -388,10 +389,14 @@ cudaError_t launch_prefill_begin(const PrefillParams& p, bool bf16, cudaStream_t
 // 5 text head): the GEMM on the operands left by the last frame
 cudaError_t tc_frame_launch_op(const TcFrame& f, int op, int layer, cudaStream_t s);
 
-cudaError_t launch_persistent(const PersParams& p, bool bf16, bool kv_bf16, int grid,
-                              int smem, cudaStream_t s, bool pdl);
-cudaError_t persistent_configure(bool bf16, bool kv_bf16, int smem, int head_dim);
-int persistent_max_grid(bool bf16, bool kv_bf16, int smem, int head_dim);
+// minb: CTAs per SM of the launch (2: the temporal stack; 1: the depformer)
+cudaError_t launch_persistent(const PersParams& p, int wtype, bool kv_bf16, int grid,
+                              int smem, cudaStream_t s, bool pdl, int minb = 2);
+// uint32 index, in the persistent schedule's barrier allocation, of the depformer launch's
+// grid-barrier counter (its own 128-byte line); frame_begin zeroes it with the first one
+constexpr int kPersDepBarWord = 64;
+cudaError_t persistent_configure(int wtype, bool kv_bf16, int smem, int head_dim, int minb);
+int persistent_max_grid(int wtype, bool kv_bf16, int smem, int head_dim, int minb);
 
 // ---------------------------------------------------------------- frame begin / end
 struct FrameParams {

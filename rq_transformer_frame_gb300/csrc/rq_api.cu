@@ -69,6 +69,10 @@ struct rq_handle {
   unsigned long long* trace = nullptr;
   PersParams pers{};
   int pers_grid = 0, pers_smem = 0;
+  // the depformer's ops run as a second cooperative launch at one CTA per SM (pers_split:
+  // frame op index of its first op; == the op count when everything runs in the first)
+  PersParams pers_dep{};
+  int pers_dep_grid = 0, pers_dep_smem = 0, pers_split = 0;
   // prompt prefill: up to kPrefillCols positions of one session per tensor-core pass
   TcFrame pf{};
   bool pf_ready = false;
@@ -385,8 +389,12 @@ cudaError_t enqueue_frame(const rq_handle* h, cudaStream_t s, int sched) {
   const FrameParams f = frame_params(h);
   if ((e = launch_frame_begin(f, h->wes == 2, s)) != cudaSuccess) return e;
   if (sched == RQ_SCHEDULE_PERSISTENT) {
-    if ((e = launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
+    if ((e = launch_persistent(h->pers, h->wtype, h->kvbf, h->pers_grid, h->pers_smem, s, true)) !=
         cudaSuccess)
+      return e;
+    if (h->pers_dep_grid > 0 && h->pers_dep.n_ops > 0 &&
+        (e = launch_persistent(h->pers_dep, h->wtype, h->kvbf, h->pers_dep_grid,
+                               h->pers_dep_smem, s, true, 1)) != cudaSuccess)
       return e;
     return launch_frame_end(f, s, true);
   }
@@ -491,31 +499,35 @@ rq_status plan_all(rq_handle* h, std::string* why) {
 #define RQ_PERS_SLOT_BUDGET (96 * 1024)
 #endif
 constexpr int kPersSlotBudget = RQ_PERS_SLOT_BUDGET;
+#ifndef RQ_PERS_DEP_SLOT_BUDGET
+#define RQ_PERS_DEP_SLOT_BUDGET (192 * 1024)  // the depformer launch: one CTA per SM
+#endif
+constexpr int kPersDepSlotBudget = RQ_PERS_DEP_SLOT_BUDGET;
 // batch 1: windows longer than this run the one-kernel-per-op frame (see frame_exec)
 constexpr int kLongWindow = 1350;
-// 64-bit word index, inside the grid barrier's 256-byte allocation, of the persistent
+// 64-bit word index, inside the grid barriers' 512-byte allocation, of the persistent
 // kernel's wait-control pair (see PersParams::wait_ctl)
 constexpr int kWaitCtlWord = 16;
 
 void pers_plans(const rq_handle* h, int G, GemvPlan* pl) {
   const rq_config& c = h->cfg;
-  const int es = h->wes;
-  pl[0] = plan_persistent(3 * c.dim, c.dim, es, false, true, G);
-  pl[1] = plan_persistent(c.dim, c.dim, es, false, false, G);
-  pl[2] = plan_persistent(c.hidden, c.dim, es, true, false, G);
-  pl[3] = plan_persistent(c.dim, c.hidden, es, false, false, G);
-  pl[4] = plan_persistent(c.text_card, c.dim, es, false, false, G);
-  pl[5] = plan_persistent(c.ddim, c.dim, es, false, false, G);
-  pl[6] = plan_persistent(3 * c.ddim, c.ddim, es, false, false, G);
-  pl[7] = plan_persistent(c.ddim, c.ddim, es, false, false, G);
-  pl[8] = plan_persistent(c.dhidden, c.ddim, es, true, false, G);
-  pl[9] = plan_persistent(c.ddim, c.dhidden, es, false, false, G);
-  pl[10] = plan_persistent(c.audio_card, c.ddim, es, false, false, G);
-  pl[11] = plan_persistent(8 * c.ddim, c.dim, es, false, false, G);
+  const int es = h->wes, bd = h->band;
+  pl[0] = plan_persistent(3 * c.dim, c.dim, es, false, true, G, bd);
+  pl[1] = plan_persistent(c.dim, c.dim, es, false, false, G, bd);
+  pl[2] = plan_persistent(c.hidden, c.dim, es, true, false, G, bd);
+  pl[3] = plan_persistent(c.dim, c.hidden, es, false, false, G, bd);
+  pl[4] = plan_persistent(c.text_card, c.dim, es, false, false, G, bd);
+  pl[5] = plan_persistent(c.ddim, c.dim, es, false, false, G, bd);
+  pl[6] = plan_persistent(3 * c.ddim, c.ddim, es, false, false, G, bd);
+  pl[7] = plan_persistent(c.ddim, c.ddim, es, false, false, G, bd);
+  pl[8] = plan_persistent(c.dhidden, c.ddim, es, true, false, G, bd);
+  pl[9] = plan_persistent(c.ddim, c.dhidden, es, false, false, G, bd);
+  pl[10] = plan_persistent(c.audio_card, c.ddim, es, false, false, G, bd);
+  pl[11] = plan_persistent(8 * c.ddim, c.dim, es, false, false, G, bd);
 }
 constexpr int kPersPlans = 12;
 
-std::vector<PersOp> pers_ops(const rq_handle* h) {
+std::vector<PersOp> pers_ops(const rq_handle* h, int* dep_first) {
   const rq_config& c = h->cfg;
   const size_t D = c.dim, C = c.context, F = c.hidden, A = c.audio_card;
   const size_t DD = c.ddim, DF = c.dhidden;
@@ -533,7 +545,7 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
   for (int l = 0; l < c.layers; ++l) {
     void* kc = static_cast<char*>(h->kcache) + (size_t)l * C * D * h->kves;
     void* vc = static_cast<char*>(h->vcache) + (size_t)l * C * D * h->kves;
-    PersOp o = gemv(PRO_RMS, EPI_QKV, 0, woff(h->w.in_proj, (size_t)l * 3 * D * D, es));
+    PersOp o = gemv(PRO_RMS, EPI_QKV, 0, mat(h, h->w.in_proj, (size_t)l * 3 * D, D));
     o.in = h->x;
     o.alpha = h->w.norm1 + (size_t)l * D;
     o.out = h->q;
@@ -545,17 +557,17 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
     a.kcache = kc;
     a.vcache = vc;
     ops.push_back(a);
-    o = gemv(PRO_PLAIN, EPI_RESID, 1, woff(h->w.out_proj, (size_t)l * D * D, es));
+    o = gemv(PRO_PLAIN, EPI_RESID, 1, mat(h, h->w.out_proj, (size_t)l * D, D));
     o.in = h->attn;
     o.out = h->x;
     ops.push_back(o);
-    o = gemv(PRO_RMS, EPI_SWIGLU, 2, woff(h->w.gate_in, (size_t)l * 2 * F * D, es));
-    o.w_half = (long long)(F * D * es);
+    o = gemv(PRO_RMS, EPI_SWIGLU, 2, mat(h, h->w.gate_in, (size_t)l * 2 * F, D));
+    o.w_half = (long long)(F * band_row_bytes(h->band, es, D));
     o.in = h->x;
     o.alpha = h->w.norm2 + (size_t)l * D;
     o.out = h->u;
     ops.push_back(o);
-    o = gemv(PRO_PLAIN, EPI_RESID, 3, woff(h->w.gate_out, (size_t)l * D * F, es));
+    o = gemv(PRO_PLAIN, EPI_RESID, 3, mat(h, h->w.gate_out, (size_t)l * D, F));
     o.in = h->u;
     o.out = h->x;
     ops.push_back(o);
@@ -585,12 +597,13 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
   };
   const bool topk = h->samp.mode == SAMPLE_TOPK;
   if (topk) topk_op(h->text_logits, 0);
+  if (dep_first) *dep_first = (int)ops.size();
   for (int cb = 0; cb < 8; ++cb) {
     PersOp o{};
     for (int l = 0; l < c.dlayers; ++l) {
       const size_t ls = (size_t)l * 8 + cb;
       o = gemv(l == 0 ? PRO_RMS_EMB : PRO_RMS, EPI_DQKV, 6,
-               woff(h->w.d_in_proj, ls * 3 * DD * DD, es));
+               mat(h, h->w.d_in_proj, ls * 3 * DD, DD));
       o.in = h->dx;
       if (l == 0) {  // x = dep_in[cb] . t + E[prev], kept in dx for the residuals
         o.in = h->dep_pre + (size_t)cb * DD;
@@ -604,25 +617,25 @@ std::vector<PersOp> pers_ops(const rq_handle* h) {
       o.dk_out = h->dkv + dkv_off(h, l, 0, cb);
       o.dv_out = h->dkv + dkv_off(h, l, 1, cb);
       ops.push_back(o);
-      o = gemv(PRO_DATTN, EPI_RESID, 7, woff(h->w.d_out_proj, ls * DD * DD, es));
+      o = gemv(PRO_DATTN, EPI_RESID, 7, mat(h, h->w.d_out_proj, ls * DD, DD));
       o.in = h->dq;
       o.dk = h->dkv + dkv_off(h, l, 0, 0);
       o.dv = h->dkv + dkv_off(h, l, 1, 0);
       o.n_keys = cb + 1;
       o.out = h->dx;
       ops.push_back(o);
-      o = gemv(PRO_RMS, EPI_SWIGLU, 8, woff(h->w.d_gate_in, ls * 2 * DF * DD, es));
-      o.w_half = (long long)(DF * DD * es);
+      o = gemv(PRO_RMS, EPI_SWIGLU, 8, mat(h, h->w.d_gate_in, ls * 2 * DF, DD));
+      o.w_half = (long long)(DF * band_row_bytes(h->band, es, DD));
       o.in = h->dx;
       o.alpha = h->w.dnorm2 + (size_t)l * DD;
       o.out = h->du;
       ops.push_back(o);
-      o = gemv(PRO_PLAIN, EPI_RESID, 9, woff(h->w.d_gate_out, ls * DD * DF, es));
+      o = gemv(PRO_PLAIN, EPI_RESID, 9, mat(h, h->w.d_gate_out, ls * DD, DF));
       o.in = h->du;
       o.out = h->dx;
       ops.push_back(o);
     }
-    o = gemv(PRO_PLAIN, EPI_ARGMAX, 10, woff(h->w.linears, (size_t)cb * A * DD, es));
+    o = gemv(PRO_PLAIN, EPI_ARGMAX, 10, mat(h, h->w.linears, (size_t)cb * A, DD));
     o.in = h->dx;
     o.out = h->audio_logits + (size_t)cb * A;
     o.key_index = 1 + cb;
@@ -907,7 +920,8 @@ int prefill_chunk(const rq_handle* h, int session, int left) {
 // the persistent kernel's op table for the current sampler (top-k adds a pick after the
 // text head and after each linears[cb]); the op timeline has room for both tables
 rq_status upload_pers_ops(rq_handle* h) {
-  std::vector<PersOp> ops = pers_ops(h);
+  int dep_first = 0;
+  std::vector<PersOp> ops = pers_ops(h, &dep_first);
   if (h->d_ops) {
     cudaFree(h->d_ops);
     h->d_ops = nullptr;
@@ -919,8 +933,16 @@ rq_status upload_pers_ops(rq_handle* h) {
     RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->trace), n * 8));
     RQ_CUDA(h, cudaMemset(h->trace, 0, n * 8));
   }
+  const int n = (int)ops.size();
+  h->pers_split = h->pers_dep_grid > 0 ? dep_first : n;
   h->pers.ops = h->d_ops;
-  h->pers.n_ops = (int)ops.size();
+  h->pers.n_ops = h->pers_split;
+  h->pers.op_base = 0;
+  h->pers_dep.ops = h->d_ops + h->pers_split;
+  h->pers_dep.n_ops = n - h->pers_split;
+  h->pers_dep.op_base = h->pers_split;
+  h->pers_dep.trace = h->trace;
+  h->pers_dep.samp = h->samp;
   h->pers_nobar.assign(ops.size(), 0);
   for (size_t k = 0; k < ops.size(); ++k) h->pers_nobar[k] = ops[k].nobar ? 1 : 0;
   h->pers.trace = h->trace;
@@ -938,37 +960,55 @@ rq_status setup_schedule(rq_handle* h) {
                   "dhidden multiples of 64");
     return setup_tensor(h);
   }
-  const bool can = c.batch == 1 && h->wbf == h->kvbf && h->band == BAND_NONE;
+  // batch 1; f32 or bf16 weights with K/V of the same type, or a weight band (bf16 K/V,
+  // head_dim 64 or 128)
+  const bool can = c.batch == 1 &&
+                   (h->band == BAND_NONE ? h->wbf == h->kvbf
+                                         : h->kvbf && (c.head_dim == 64 || c.head_dim == 128));
+  // weight bands run on the persistent kernel only when asked for: on Moshi-7B at batch 1
+  // its band tiles take 4.85 (q8) / 7.16 ms (q4) per frame, the graph schedule 4.08 / 4.07
+  if (c.schedule == RQ_SCHEDULE_AUTO && h->band != BAND_NONE) {
+    h->schedule = RQ_SCHEDULE_GRAPH;
+    return RQ_OK;
+  }
   if (c.schedule == RQ_SCHEDULE_GRAPH || (c.schedule == RQ_SCHEDULE_AUTO && !can)) {
     h->schedule = RQ_SCHEDULE_GRAPH;
     return RQ_OK;
   }
   if (!can)
     return fail(h, RQ_ERR_UNSUPPORTED,
-                "the persistent schedule needs batch 1 and f32 or bf16 weights of the K/V dtype");
+                "the persistent schedule needs batch 1 and f32 or bf16 weights of the K/V "
+                "dtype, or a weight band with bf16 K/V and head_dim 64 or 128");
   GemvPlan pl[kPersMaxPlans];
   int G = 2 * h->num_sms, slot = 0, part = 0, ns = 0, smem = 0;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    pers_plans(h, G, pl);
-    slot = 0;
-    part = 0;
+  // plans for a grid of G CTAs and the ring geometry of a shared-memory budget
+  auto geometry = [&](int grid, int budget, GemvPlan* p, int& sl, int& pa, int& n,
+                      int& sm) -> bool {
+    pers_plans(h, grid, p);
+    sl = 0;
+    pa = 0;
     for (int i = 0; i < kPersPlans; ++i) {
-      if (pl[i].nch == 0) return fail(h, RQ_ERR_UNSUPPORTED, "GEMV shape unsupported");
-      const int tb = pl[i].tile_rows * pl[i].kp_width * h->wes;
-      slot = tb > slot ? tb : slot;
-      const int pf = (pl[i].max_tiles * pl[i].tile_rows * (pl[i].tpr / 32) + 3) & ~3;
-      part = pf > part ? pf : part;
+      if (p[i].nch == 0) return false;
+      const int tb = p[i].tile_rows * (int)band_row_bytes(h->band, h->wes, p[i].kp_width);
+      sl = tb > sl ? tb : sl;
+      const int pf = (p[i].max_tiles * p[i].tile_rows * (p[i].tpr / 32) + 3) & ~3;
+      pa = pf > pa ? pf : pa;
     }
     // the partial-sum buffer also holds a top-k pick's scratch
     const int topk_floats = (int)((sizeof(TopkShared) + 15) / 16 * 4);
-    part = part > topk_floats ? part : topk_floats;
-    slot = (slot + 127) & ~127;
-    ns = kPersSlotBudget / slot;
-    if (ns < 2) ns = 2;
-    smem = ns * slot + part * 4 + 2 * ns * 8;
-    cudaError_t e = persistent_configure(h->wbf, h->kvbf, smem, c.head_dim);
+    pa = pa > topk_floats ? pa : topk_floats;
+    sl = (sl + 127) & ~127;
+    n = budget / sl;
+    if (n < 2) n = 2;
+    sm = n * sl + pa * 4 + 2 * n * 8;
+    return true;
+  };
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (!geometry(G, kPersSlotBudget, pl, slot, part, ns, smem))
+      return fail(h, RQ_ERR_UNSUPPORTED, "GEMV shape unsupported");
+    cudaError_t e = persistent_configure(h->wtype, h->kvbf, smem, c.head_dim, 2);
     if (e != cudaSuccess) return cuda_fail(h, e, "persistent_configure");
-    const int maxg = persistent_max_grid(h->wbf, h->kvbf, smem, c.head_dim);
+    const int maxg = persistent_max_grid(h->wtype, h->kvbf, smem, c.head_dim, 2);
     if (maxg >= G) break;
     if (attempt == 1 || maxg < h->num_sms) {
       if (c.schedule == RQ_SCHEDULE_PERSISTENT)
@@ -978,8 +1018,8 @@ rq_status setup_schedule(rq_handle* h) {
     }
     G = h->num_sms;
   }
-  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->grid_bar), 256));
-  RQ_CUDA(h, cudaMemset(h->grid_bar, 0, 256));
+  RQ_CUDA(h, cudaMalloc(reinterpret_cast<void**>(&h->grid_bar), 512));
+  RQ_CUDA(h, cudaMemset(h->grid_bar, 0, 512));
   PersParams& P = h->pers;
   P = PersParams{};
   for (int i = 0; i < kPersPlans; ++i) P.plans[i] = pl[i];
@@ -1005,11 +1045,36 @@ rq_status setup_schedule(rq_handle* h) {
   P.kps = 16;  // shortest split; the kernel sizes splits from the window (16..64)
   P.nsplit = (c.context + 15) / 16;
   P.grid_bar = h->grid_bar;
-  // the wait-control words live in the same 256-byte allocation, zero = defaults
+  // the wait-control words live in the same 512-byte allocation, zero = defaults
   P.wait_ctl = reinterpret_cast<const unsigned long long*>(h->grid_bar) + kWaitCtlWord;
   P.status = h->d_status();
   h->pers_grid = G;
   h->pers_smem = smem;
+  // The depformer's ops as a second cooperative launch at one CTA per SM: its small ops
+  // are latency-bound, and a 152-CTA grid barrier, a register budget without spills and a
+  // ring twice as deep run them faster (Moshi-7B: 1.29 -> 1.12 ms per frame), while the
+  // temporal stack keeps two CTAs per SM to stream its weights.  If that launch does not
+  // fit, the first one runs every op.
+  h->pers_dep_grid = 0;
+  {
+    GemvPlan pl2[kPersMaxPlans];
+    int slot2 = 0, part2 = 0, ns2 = 0, smem2 = 0;
+    const int G2 = h->num_sms;
+    if (G == 2 * h->num_sms && geometry(G2, kPersDepSlotBudget, pl2, slot2, part2, ns2, smem2) &&
+        persistent_configure(h->wtype, h->kvbf, smem2, c.head_dim, 1) == cudaSuccess &&
+        persistent_max_grid(h->wtype, h->kvbf, smem2, c.head_dim, 1) >= G2) {
+      PersParams& Q = h->pers_dep;
+      Q = P;
+      for (int i = 0; i < kPersPlans; ++i) Q.plans[i] = pl2[i];
+      Q.slot_bytes = slot2;
+      Q.n_slots = ns2;
+      Q.part_floats = part2;
+      Q.grid_bar = h->grid_bar + kPersDepBarWord;
+      h->pers_dep_grid = G2;
+      h->pers_dep_smem = smem2;
+    }
+    cudaGetLastError();  // a refused configuration leaves no sticky error
+  }
   h->schedule = RQ_SCHEDULE_PERSISTENT;
   return upload_pers_ops(h);
 }
@@ -1415,17 +1480,24 @@ rq_status rq_launch_op(rq_handle* h, int32_t op, int32_t layer, int32_t count,
   if (op == RQ_OP_FRAME) {
     if (h->schedule != RQ_SCHEDULE_PERSISTENT)
       return fail(h, RQ_ERR_UNSUPPORTED, "RQ_OP_FRAME needs the persistent schedule");
-    const double es = h->wes, D = c.dim, F = c.hidden, DD = c.ddim, DF = c.dhidden;
-    bytes = es * (c.layers * (3 * D * D + D * D + 2 * F * D + D * F) + (double)c.text_card * D +
-                  8.0 * c.dlayers * (3 * DD * DD + DD * DD + 2 * DF * DD + DD * DF) +
-                  8.0 * DD * D + 8.0 * c.audio_card * DD);
+    const double D = c.dim, F = c.hidden, DD = c.ddim, DF = c.dhidden;
+    // bytes of one stored row of K values (weight bands: codes and scales)
+    auto rb = [&](long long K) { return (double)band_row_bytes(h->band, h->wes, K); };
+    bytes = c.layers * ((3 * D + D + 2 * F) * rb(c.dim) + D * rb(c.hidden)) +
+            (double)c.text_card * rb(c.dim) +
+            8.0 * c.dlayers * ((3 * DD + DD + 2 * DF) * rb(c.ddim) + DD * rb(c.dhidden)) +
+            8.0 * DD * rb(c.dim) + 8.0 * c.audio_card * rb(c.ddim);
     const int len = h->host_off[0] + 1 < c.context ? h->host_off[0] + 1 : c.context;
     bytes += 2.0 * len * c.dim * h->kves * c.layers;
     if (bytes_per_launch) *bytes_per_launch = bytes;
     for (int i = 0; i < count; ++i) {
       RQ_CUDA(h, cudaMemsetAsync(h->grid_bar, 0, 4, h->stream));
-      RQ_CUDA(h, launch_persistent(h->pers, h->wbf, h->kvbf, h->pers_grid, h->pers_smem,
+      RQ_CUDA(h, cudaMemsetAsync(h->grid_bar + kPersDepBarWord, 0, 4, h->stream));
+      RQ_CUDA(h, launch_persistent(h->pers, h->wtype, h->kvbf, h->pers_grid, h->pers_smem,
                                    h->stream, false));
+      if (h->pers_dep_grid > 0 && h->pers_dep.n_ops > 0)
+        RQ_CUDA(h, launch_persistent(h->pers_dep, h->wtype, h->kvbf, h->pers_dep_grid,
+                                     h->pers_dep_smem, h->stream, false, 1));
     }
     return RQ_OK;
   }
@@ -1684,7 +1756,7 @@ rq_status rq_set_wait_limit(rq_handle* h, uint64_t limit_ns, int32_t stall_op) {
   if (!h) return RQ_ERR_ARG;
   if (h->schedule != RQ_SCHEDULE_PERSISTENT || !h->grid_bar)
     return fail(h, RQ_ERR_UNSUPPORTED, "the wait limit applies to the persistent schedule");
-  if (stall_op < -1 || stall_op == 0 || stall_op >= h->pers.n_ops ||
+  if (stall_op < -1 || stall_op == 0 || stall_op >= h->pers.n_ops + h->pers_dep.n_ops ||
       (stall_op > 0 && h->pers_nobar[stall_op]))
     return fail(h, RQ_ERR_ARG, "stall_op is not an op with a grid barrier in front (or -1)");
   const unsigned long long ctl[2] = {(unsigned long long)limit_ns,
@@ -1697,7 +1769,7 @@ rq_status rq_set_wait_limit(rq_handle* h, uint64_t limit_ns, int32_t stall_op) {
 
 int32_t rq_get_op_times(rq_handle* h, float* us, int32_t max_ops) {
   if (!h || h->schedule != RQ_SCHEDULE_PERSISTENT || !h->trace) return 0;
-  const int n = h->pers.n_ops;
+  const int n = h->pers.n_ops + h->pers_dep.n_ops;
   if (!us) return n;
   if (cudaStreamSynchronize(h->stream) != cudaSuccess) return 0;
   std::vector<unsigned long long> t((size_t)n + 1);

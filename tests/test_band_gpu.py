@@ -73,13 +73,17 @@ def band_weights_for_oracle(w_bf16: dict, bits: int) -> dict:
     return out
 
 
+SCHEDULES = [binding.RQ_SCHEDULE_GRAPH, binding.RQ_SCHEDULE_PERSISTENT]
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES, ids=["graph", "persistent"])
 @pytest.mark.parametrize("dtype,bits,name", BANDS, ids=[b[2] for b in BANDS])
-def test_band_frames_match_roundtrip_oracle(dtype, bits, name):
+def test_band_frames_match_roundtrip_oracle(dtype, bits, name, schedule):
     c = configs.SMALL.with_(weight_dtype=name)
     w = weights_of(configs.SMALL)  # the bf16 weights the band quantizes
     dev = binding.quantize_weights(binding.upload_weights(w), dtype)
-    dec = binding.Decoder(c, dev)
-    assert dec.schedule == binding.RQ_SCHEDULE_GRAPH
+    dec = binding.Decoder(c, dev, schedule=schedule)
+    assert dec.schedule == schedule
     orc = oracle.Oracle(c.with_(weight_dtype="f32"), band_weights_for_oracle(w, bits))
     st = orc.new_state()
     users = synth.user_tokens(c, 8).numpy()
@@ -105,8 +109,39 @@ def test_band_models_refuse_the_bf16_only_schedules():
     c = configs.SMALL.with_(weight_dtype="q4")
     dev = binding.quantize_weights(binding.upload_weights(weights_of(configs.SMALL)),
                                    binding.RQ_Q4)
-    for sched in (binding.RQ_SCHEDULE_PERSISTENT, binding.RQ_SCHEDULE_TENSOR):
-        with pytest.raises(binding.RQError):
-            binding.Decoder(c, dev, schedule=sched)
+    with pytest.raises(binding.RQError):
+        binding.Decoder(c, dev, schedule=binding.RQ_SCHEDULE_TENSOR)
+    d = binding.Decoder(c, dev)  # AUTO keeps bands on one GEMV kernel per op (faster)
+    assert d.schedule == binding.RQ_SCHEDULE_GRAPH
+    d.close()
+    d = binding.Decoder(c, dev, schedule=binding.RQ_SCHEDULE_PERSISTENT)
+    assert d.schedule == binding.RQ_SCHEDULE_PERSISTENT
+    d.close()
+    d = binding.Decoder(c.with_(batch=2), dev)  # batch > 1: one GEMV kernel per op
+    assert d.schedule == binding.RQ_SCHEDULE_GRAPH
+    d.close()
     with pytest.raises(ValueError):
         binding.quantize(torch.zeros(4, 48, device="cuda"), binding.RQ_Q4)
+
+
+@pytest.mark.parametrize("dtype,bits,name", BANDS, ids=[b[2] for b in BANDS])
+def test_band_moshi7b_layer_shapes_persistent(dtype, bits, name):
+    """The Moshi-7B layer shapes (2 temporal layers, the whole depformer and heads) as a
+    weight band on the persistent kernel: gate_out's 11264-column rows run as reduction
+    parts whose codes and scales are copied separately; the depformer's 1024-column rows
+    give one warp per row.  Two forced frames against the roundtrip oracle."""
+    base = configs.MOSHI7B_2L
+    c = base.with_(weight_dtype=name)
+    w = weights_of(base)
+    dev = binding.quantize_weights(binding.upload_weights(w), dtype)
+    dec = binding.Decoder(c, dev, schedule=binding.RQ_SCHEDULE_PERSISTENT)
+    assert dec.schedule == binding.RQ_SCHEDULE_PERSISTENT
+    orc = oracle.Oracle(c.with_(weight_dtype="f32"), band_weights_for_oracle(w, bits))
+    st = orc.new_state()
+    users = synth.user_tokens(c, 2).numpy()
+    for t in range(2):
+        r = orc.step(st, users[t], trace=True)
+        own, out, has = dec.step_forced(users[t][None], r["own"][None])
+        text, audio = dec.logits()
+        check_logits_and_tokens(c, own[0], r, text[0], audio[0], t)
+    dec.close()
