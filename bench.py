@@ -301,7 +301,9 @@ def frame_kernel_roofline(dec, cfg, stream, dev, hbm_peak, peak_kind, traffic_na
     e1.record(stream)
     e1.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / nrep
-    roof = {"kernel": "frame_persistent_kernel (all linears and attentions of a frame)",
+    roof = {"kernel": "frame_persistent_kernel: the frame's two cooperative launches (temporal "
+                      "stack, text head and input projections at 2 CTAs/SM; depformer at 1 "
+                      "CTA/SM) -- every linear and attention of a frame",
             "bound": "hbm", "achieved": round(nb / us / 1e3, 1), "peak": hbm_peak,
             "unit": "GB/s", "peak_kind": peak_kind,
             "frac": round(nb / us / 1e3 / hbm_peak, 4), "us_per_launch": round(us, 1),

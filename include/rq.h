@@ -90,17 +90,23 @@ typedef struct {
   int32_t schedule;     /* RQ_SCHEDULE_*: how a frame is launched [RQ_SCHEDULE_AUTO] */
 } rq_config;
 
-/* Frame schedules.  PERSISTENT runs all linears and attentions of a frame as one
- * cooperative kernel with grid barriers between dependent ops (batch 1, same weight and
- * K/V dtype); GRAPH launches one streaming-GEMV kernel per op inside a CUDA graph;
- * TENSOR (batch <= 64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64)
- * runs every linear as one tcgen05 tensor-core GEMM over all sessions (padded to a
- * multiple of 16), the normalised f32 activations split into two bf16 operand parts
- * (16 significant bits), inside a CUDA graph.  A PERSISTENT handle replays the GRAPH
- * frame instead while the window is longer than 1350 positions (its attention kernel
- * then streams K/V faster).  AUTO picks PERSISTENT when it applies (batch 1), TENSOR at batch >= 2 when it applies (it streams every weight once per
- * frame, where GRAPH streams it once per session), else GRAPH.
- * Results agree within the parity tolerance. */
+/* Frame schedules.
+ *   PERSISTENT  batch 1; f32 or bf16 weights with K/V of the same type, or a weight band
+ *               with bf16 K/V.  All linears and attentions of a frame run as cooperative
+ *               kernels with grid barriers between dependent ops: two launches per frame,
+ *               the temporal stack, text head and depformer input projections at two CTAs
+ *               per SM, then the depformer at one CTA per SM.  While the window is longer
+ *               than 1350 positions the handle replays the GRAPH frame instead (its
+ *               attention kernel then streams K/V faster).
+ *   GRAPH       one streaming-GEMV kernel per op inside a CUDA graph.
+ *   TENSOR      batch <= 64, bf16 weights, dim, hidden, ddim and dhidden multiples of 64:
+ *               every linear as one tcgen05 tensor-core GEMM over all sessions (padded to
+ *               a multiple of 16), the normalised f32 activations split into two bf16
+ *               operand parts (16 significant bits), inside a CUDA graph.
+ * AUTO picks PERSISTENT at batch 1 when it applies (not for weight bands: GRAPH runs them
+ * faster), TENSOR at batch >= 2 when it applies (it streams every weight once per frame,
+ * where GRAPH streams it once per session), else GRAPH.  Results agree within the parity
+ * tolerance. */
 enum {
   RQ_SCHEDULE_AUTO = 0,
   RQ_SCHEDULE_GRAPH = 1,
@@ -238,7 +244,9 @@ enum {
   RQ_OP_GATE_IN = 3,  /* RMSNorm + gate_in GEMV + SiLU gate */
   RQ_OP_GATE_OUT = 4, /* gate_out GEMV + residual */
   RQ_OP_HEAD = 5,     /* out_norm + text head GEMV + argmax */
-  RQ_OP_FRAME = 6     /* the persistent schedule's whole-frame kernel (layer ignored);
+  RQ_OP_FRAME = 6     /* the persistent schedule's whole-frame kernel: its two cooperative
+                         launches (the temporal stack, text head and depformer input
+                         projections; then the depformer), layer ignored;
                          *bytes_per_launch = every weight once + the live K/V window */
 };
 rq_status rq_launch_op(rq_handle *h, int32_t op, int32_t layer, int32_t count,

@@ -45,6 +45,11 @@ constexpr int kMaxStage = 1024;  // depformer attention output staged in shared 
 // tile groups: resident tiles (ops of a few tiles per CTA) in bursts of kBurstT; the
 // weight stream of long ops (more than kStreamMinTiles tiles per CTA) kStreamT at a time
 constexpr int kBurstT = RQ_PERS_BURST_T;
+#ifndef RQ_PERS_BURST_T_WIDE
+#define RQ_PERS_BURST_T_WIDE 8
+#endif
+// the one-CTA-per-SM launch (the depformer) has the registers for bigger groups
+constexpr int kBurstTWide = RQ_PERS_BURST_T_WIDE;
 constexpr int kStreamT = RQ_PERS_STREAM_T;
 constexpr bool kStreamBurst = RQ_PERS_STREAM_BURST != 0;
 constexpr int kStreamMinTiles = RQ_PERS_STREAM_MIN;
@@ -423,10 +428,10 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
   } else if (op.pro == PRO_DATTN) {
     // "moshi_lm.rs", `attend` over the depformer's per-frame keys 0..n_keys-1.
     // hd/4 threads per head, one float4 of dimensions each: q and every key in one
-    // round trip, scores reduced with shuffles, the softmax in registers, then the
-    // values in one more round trip (keys and values at once would need 64 registers
-    // more than the kernel's cap leaves); the output is staged in shared memory and
-    // read back in the chunk layout of x.
+    // round trip, scores reduced with shuffles, the softmax in registers, then the values
+    // in one more round trip (loading them with the keys measured 10 us per frame slower
+    // in the one-CTA-per-SM launch); the output is staged in shared memory and read back
+    // in the chunk layout of x.
     const int nk = op.n_keys, dh = P.dheads, hd = P.dhead_dim;
     const float scale = 1.0f / sqrtf((float)hd);
     const int tph = hd / 4;
@@ -969,10 +974,11 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
             const int nch = (Kw / V + pl.tpr - 1) / pl.tpr;
             form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, k & 1,
                        s_att, forcing);
+            constexpr int BT = MINB == 1 ? kBurstTWide : kBurstT;
             if (nch <= 1 && nt > 2)
-              ok = consume_tiles<WT, 1, kBurstT, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
-                                                       P.slot_bytes, NS, full, empty, part, xr,
-                                                       g, tig, warp, lane, lim);
+              ok = consume_tiles<WT, 1, BT, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                                                  P.slot_bytes, NS, full, empty, part, xr, g,
+                                                  tig, warp, lane, lim);
             else if (nch <= 1)
               ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
                                                  P.slot_bytes, NS, full, empty, part, xr, g,

@@ -503,6 +503,10 @@ constexpr int kPersSlotBudget = RQ_PERS_SLOT_BUDGET;
 #define RQ_PERS_DEP_SLOT_BUDGET (192 * 1024)  // the depformer launch: one CTA per SM
 #endif
 constexpr int kPersDepSlotBudget = RQ_PERS_DEP_SLOT_BUDGET;
+#ifndef RQ_PERS_DEP_FIT
+#define RQ_PERS_DEP_FIT 1
+#endif
+constexpr bool kPersDepFit = RQ_PERS_DEP_FIT != 0;
 // batch 1: windows longer than this run the one-kernel-per-op frame (see frame_exec)
 constexpr int kLongWindow = 1350;
 // 64-bit word index, inside the grid barriers' 512-byte allocation, of the persistent
@@ -982,13 +986,16 @@ rq_status setup_schedule(rq_handle* h) {
   GemvPlan pl[kPersMaxPlans];
   int G = 2 * h->num_sms, slot = 0, part = 0, ns = 0, smem = 0;
   // plans for a grid of G CTAs and the ring geometry of a shared-memory budget
-  auto geometry = [&](int grid, int budget, GemvPlan* p, int& sl, int& pa, int& n,
-                      int& sm) -> bool {
+  // (dep: the depformer launch, whose ops use plans 6..10 -- its slots are sized by its
+  // own tiles, not the temporal ones)
+  auto geometry = [&](int grid, int budget, GemvPlan* p, int& sl, int& pa, int& n, int& sm,
+                      bool dep) -> bool {
     pers_plans(h, grid, p);
     sl = 0;
     pa = 0;
     for (int i = 0; i < kPersPlans; ++i) {
       if (p[i].nch == 0) return false;
+      if (kPersDepFit && dep && (i < 6 || i > 10)) continue;
       const int tb = p[i].tile_rows * (int)band_row_bytes(h->band, h->wes, p[i].kp_width);
       sl = tb > sl ? tb : sl;
       const int pf = (p[i].max_tiles * p[i].tile_rows * (p[i].tpr / 32) + 3) & ~3;
@@ -1004,7 +1011,7 @@ rq_status setup_schedule(rq_handle* h) {
     return true;
   };
   for (int attempt = 0; attempt < 2; ++attempt) {
-    if (!geometry(G, kPersSlotBudget, pl, slot, part, ns, smem))
+    if (!geometry(G, kPersSlotBudget, pl, slot, part, ns, smem, false))
       return fail(h, RQ_ERR_UNSUPPORTED, "GEMV shape unsupported");
     cudaError_t e = persistent_configure(h->wtype, h->kvbf, smem, c.head_dim, 2);
     if (e != cudaSuccess) return cuda_fail(h, e, "persistent_configure");
@@ -1060,7 +1067,7 @@ rq_status setup_schedule(rq_handle* h) {
     GemvPlan pl2[kPersMaxPlans];
     int slot2 = 0, part2 = 0, ns2 = 0, smem2 = 0;
     const int G2 = h->num_sms;
-    if (G == 2 * h->num_sms && geometry(G2, kPersDepSlotBudget, pl2, slot2, part2, ns2, smem2) &&
+    if (G == 2 * h->num_sms && geometry(G2, kPersDepSlotBudget, pl2, slot2, part2, ns2, smem2, true) &&
         persistent_configure(h->wtype, h->kvbf, smem2, c.head_dim, 1) == cudaSuccess &&
         persistent_max_grid(h->wtype, h->kvbf, smem2, c.head_dim, 1) >= G2) {
       PersParams& Q = h->pers_dep;
