@@ -67,7 +67,8 @@ KERNEL_SOURCES = {
     "gemv": ("gemv_kernel.cuh", "gemv_launch.cuh", "gemv.cu", "sampling.cuh", "common.cuh",
              "kernels.h"),
     "frame": ("frame_persistent.cuh", "frame_persistent.cu", "frame_persistent_greedy.cu",
-              "gemv_kernel.cuh", "sampling.cuh", "common.cuh", "kernels.h"),
+              "frame_persistent_dep.cu", "frame_persistent_band.cu", "gemv_kernel.cuh",
+              "sampling.cuh", "common.cuh", "kernels.h"),
     "tc": ("tc_gemm.cu", "tc_epilogue.cuh", "tc_common.cuh", "sampling.cuh", "common.cuh",
            "kernels.h"),
     "attn": ("attn.cu", "common.cuh", "kernels.h"),
