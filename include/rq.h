@@ -93,9 +93,11 @@ typedef struct {
 /* Frame schedules.
  *   PERSISTENT  batch 1; f32 or bf16 weights with K/V of the same type, or a weight band
  *               with bf16 K/V.  All linears and attentions of a frame run as cooperative
- *               kernels with grid barriers between dependent ops: two launches per frame,
- *               the temporal stack, text head and depformer input projections at two CTAs
- *               per SM, then the depformer at one CTA per SM.  While the window is longer
+ *               kernels: two launches per frame, the temporal stack, text head and
+ *               depformer input projections at two CTAs per SM with grid barriers between
+ *               dependent ops, then the depformer at one CTA per SM, whose ops exchange
+ *               tagged 64-bit words (value and producing op) instead of meeting at
+ *               barriers.  While the window is longer
  *               than 1350 positions the handle replays the GRAPH frame instead (its
  *               attention kernel then streams K/V faster).
  *   GRAPH       one streaming-GEMV kernel per op inside a CUDA graph.
@@ -374,11 +376,13 @@ int32_t rq_schedule(const rq_handle *h);
 int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
 
 /* Test hook of the failure path: the limit, in nanoseconds, of the device-side waits of
- * the batch-1 whole-frame kernel (its grid barrier and weight-ring waits); 0 restores the
- * default of 2 s.  stall_op >= 0 makes the grid barrier in front of op `stall_op` of
- * the frame's op table (the order of rq_get_op_times; op >= 1 and not the depformer
- * input projections beside the text head, which have no barrier) wait for one CTA more than
- * the grid holds, so every wait there runs out after limit_ns: the frame then returns
+ * the batch-1 whole-frame kernel (its grid-barrier, tagged-word and weight-ring waits); 0
+ * restores the default of 2 s.  stall_op >= 0 makes the waits in front of op `stall_op` of
+ * the frame's op table (the order of rq_get_op_times; op >= 1, not the depformer input
+ * projections beside the text head and not the first op of the depformer launch, which
+ * wait for nothing) unsatisfiable: its grid barrier waits for one CTA more than the grid
+ * holds, or its tagged words for a tag nothing writes, so every wait there runs out after
+ * limit_ns: the frame then returns
  * RQ_ERR_TIMEOUT, later calls RQ_ERR_POISONED until rq_reset(h, -1).  -1 removes the
  * stall.  Nothing traps and no wait is unbounded.  Applies to frames run by the
  * persistent kernel (RQ_ERR_UNSUPPORTED under the other schedules); synchronizes the

@@ -159,6 +159,20 @@ __device__ __forceinline__ void bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// bar.sync of n threads that also returns whether any of them passed `pred` true: the
+// same answer in every thread, so a decision taken on it (leave a loop) stays uniform
+// even while another warp may still change the flag behind `pred`
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+  unsigned r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((unsigned)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0u;
+}
+
 // ---------------------------------------------------------------- numerics
 // bf16 expansion of an f32 for the tensor-core operand: hi = bf16(x), mid = bf16(x - hi)
 // (x - hi is exact), and with kOpndParts == 3 also lo = bf16(x - hi - mid).  Two parts keep

@@ -3,15 +3,17 @@
 // frame_persistent_greedy.cu (greedy frames).
 //
 // Every CTA walks the same op table (temporal layers, text head, the 8 depformer
-// steps).  Between dependent ops the CTAs meet at a grid barrier (one atomic counter,
-// bounded spin).  The weights of every op are known before the frame starts, so each
+// steps).  Between dependent ops the CTAs of the two-CTAs-per-SM launch meet at a grid
+// barrier (one atomic counter, bounded spin); the one-CTA-per-SM launch (the depformer)
+// instead polls tagged words, each value carrying the op that wrote it.  The weights of every op are known before the frame starts, so each
 // CTA's producer warp streams the weight tiles it owns for ALL ops, in order, into one
 // shared-memory ring with cp.async.bulk, running ahead of the consumers across op
 // boundaries: HBM keeps streaming the next ops' weights while the consumers wait on a
 // barrier, which removes the per-kernel drain and fill of a launch-per-op schedule.
 // Consumers run the prologues / epilogues of the streaming GEMV (gemv_kernel.cuh)
 // selected per op at run time, and the split-K decode attention as work items.
-// Activations written by other CTAs are read with L2-only loads (ld.global.cg).
+// Activations written by other CTAs are read with L2-only loads (ld.global.cg), or as
+// tagged words with relaxed gpu-scope loads.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -85,6 +87,89 @@ __device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target,
 }
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------- tagged words
+// The depformer launch (one CTA per SM) runs without grid barriers.  Every value that one
+// CTA writes and another reads is one 64-bit word, (tag << 32) | f32 bits, stored by a
+// single relaxed store; a reader polls the word until it carries the tag of the op that
+// produces it.  An aligned 64-bit access is single-copy atomic, so a word is seen either
+// old or new, never half of each, and a value needs no ordering against any other: the
+// wait for the producer and the load of its output are one round trip instead of a
+// barrier's arrival, its polling and then the load.  Tags are (frame epoch << 10) | the
+// frame index of the producing op: words of earlier frames, and of earlier ops writing
+// the same buffer, never match.  Buffers are reused safely because every op waits for
+// the whole output of the op before it, so no CTA can be more than one op ahead of any
+// CTA that still has to read what it would overwrite.
+__device__ __forceinline__ void ll_st(float* base, size_t i, uint32_t tag, float v) {
+  const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(
+                   reinterpret_cast<unsigned long long*>(base) + i),
+               "l"(w)
+               : "memory");
+}
+// two consecutive words (16-byte aligned)
+__device__ __forceinline__ void ll_ld2(const float* base, size_t i, unsigned long long& a,
+                                       unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(a), "=l"(b)
+               : "l"(reinterpret_cast<const unsigned long long*>(base) + i)
+               : "memory");
+}
+__device__ __forceinline__ unsigned long long ll_ld1(const float* base, size_t i) {
+  unsigned long long a;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+               : "=l"(a)
+               : "l"(reinterpret_cast<const unsigned long long*>(base) + i)
+               : "memory");
+  return a;
+}
+__device__ __forceinline__ float ll_val(unsigned long long w) {
+  return __uint_as_float((uint32_t)w);
+}
+__device__ __forceinline__ bool ll_is(unsigned long long w, uint32_t tag) {
+  return (uint32_t)(w >> 32) == tag;
+}
+
+// the CTA's abort flag: raised by a wait that ran out (or by the producer), it ends every
+// other wait of the CTA and, read at a CTA barrier, the op loop
+__shared__ volatile int s_abort;
+
+// The launch's view of the tags: the epoch base and `flip` (all ones for the op a test
+// stalls: it turns every tag that op waits for into one that nothing writes).
+struct LLCtx {
+  uint32_t ebase, flip;
+  const PersParams& P;
+  __device__ __forceinline__ uint32_t want(int op_index) const {
+    return (ebase | (uint32_t)op_index) ^ flip;
+  }
+  // After an attempt that found a word without its tag: whether to try again.  The first
+  // miss starts the clock (t0); on the wait limit it records a timeout and raises the
+  // CTA's abort flag (the op's results are then garbage and the launch winds down).
+  // Written as a loop in the caller, not a callback, so that the words polled stay in
+  // registers.
+  __device__ __forceinline__ bool again(uint64_t& t0) const {
+    if (t0 == 0ull) {
+      t0 = global_timer_ns();
+      return true;
+    }
+    if (s_abort) return false;
+    const uint64_t lim = P.wait_ctl && P.wait_ctl[0] ? P.wait_ctl[0] : kWaitLimitNs;
+    if (global_timer_ns() - t0 > lim) {
+      atomicOr(P.status, kDevTimeout);
+      s_abort = 1;
+      return false;
+    }
+    return true;
+  }
+  __device__ __forceinline__ float wait1(const float* base, size_t i, uint32_t tag) const {
+    unsigned long long w;
+    uint64_t t0 = 0ull;
+    do {
+      w = ll_ld1(base, i);
+    } while (!ll_is(w, tag) && again(t0));
+    return ll_val(w);
+  }
+};
 
 // ---------------------------------------------------------------- tile consumer
 // Sum each of R row values over the warp's 32 lanes with a transposing butterfly: at
@@ -335,26 +420,36 @@ __device__ __forceinline__ uint32_t cur_bytes(const PersParams& P, const TileCur
 
 // ---------------------------------------------------------------- prologue
 // x for this op into registers: chunk j of thread (g, tig) covers columns
-// [(tig + j*tpr)*V, +V).  Returns nothing; uses consumer barrier 1.
-template <typename WT>
+// [(tig + j*tpr)*V, +V).  Returns nothing; uses consumer barrier 1.  LL: the launch
+// exchanges tagged words (wtag: this op's tag; lc: the tags it waits for).
+template <typename WT, bool LL, bool PICKS>
 __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                        const GemvPlan& pl, int nch, int k0, int Kw,
                                        float (&xr)[Nx<WT>::N][Chunk<WT>::V],
                                        const float (&ar)[Nx<WT>::N][Chunk<WT>::V], int g,
                                        int tig, int tid, int warp, int lane, float* s_red,
-                                       int red_half, float* s_att, int forcing) {
+                                       int red_half, float* s_att, int forcing,
+                                       const LLCtx& lc, uint32_t wtag,
+                                       unsigned long long* s_key) {
   constexpr int V = Chunk<WT>::V;
   constexpr int NX = Nx<WT>::N;
+  constexpr int VG = PICKS ? 4 : 8;  // tagged values polled per round trip
   using TT = typename Chunk<WT>::Table;  // embedding tables: bf16 for weight bands
   const int K = pl.K, CC = Kw / V;
   const float* in = op.in + k0;  // this part's columns [k0, k0 + Kw)
   (void)tid;
+  (void)wtag;
+  (void)s_key;
+  // tagged input: every chunk polled until all its words carry the producer's tag
+  const bool tagged = LL && (op.pro == PRO_PLAIN || op.pro == PRO_RMS);
 #pragma unroll
   for (int j = 0; j < NX; ++j) {
     const int c = tig + j * pl.tpr;
+    if (op.pro != PRO_DATTN) {  // (the attention sets x at its end: fewer live registers)
 #pragma unroll
-    for (int v = 0; v < V; ++v) xr[j][v] = 0.f;
-    if (op.pro != PRO_DATTN && j < nch && c < CC) {
+      for (int v = 0; v < V; ++v) xr[j][v] = 0.f;
+    }
+    if (!tagged && op.pro != PRO_DATTN && j < nch && c < CC) {
 #pragma unroll
       for (int v = 0; v < V; v += 4) {
         const float4 f = __ldcg(reinterpret_cast<const float4*>(in + (size_t)c * V + v));
@@ -365,13 +460,86 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
       }
     }
   }
+  // the tagged launch loads an RMSNorm's alpha here, in flight with the poll of x (the
+  // other launches load it before their grid barrier)
+  float al[NX][V];
+  if constexpr (LL && !Chunk<WT>::kBand) {
+    if (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB) {
+#pragma unroll
+      for (int j = 0; j < NX; ++j) {
+        const int c = tig + j * pl.tpr;
+#pragma unroll
+        for (int v = 0; v < V; v += 4) {
+          const float4 a = (j < nch && c < CC)
+                               ? __ldg(reinterpret_cast<const float4*>(op.alpha + (size_t)c * V + v))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          al[j][v] = a.x;
+          al[j][v + 1] = a.y;
+          al[j][v + 2] = a.z;
+          al[j][v + 3] = a.w;
+        }
+      }
+    }
+  } else {
+    (void)al;
+  }
+  if constexpr (LL) {
+    if (tagged) {
+      const uint32_t t = lc.want(op.tag_in);
+      uint64_t t0 = 0ull;
+      bool ok;
+      do {
+        ok = true;
+#pragma unroll
+        for (int j = 0; j < NX; ++j) {
+          const int c = tig + j * pl.tpr;
+          if (j < nch && c < CC) {
+#pragma unroll
+            for (int v = 0; v < V; v += 2) {
+              unsigned long long a, b;
+              ll_ld2(op.in, (size_t)k0 + (size_t)c * V + v, a, b);
+              xr[j][v] = ll_val(a);
+              xr[j][v + 1] = ll_val(b);
+              ok &= ll_is(a, t) & ll_is(b, t);
+            }
+          }
+        }
+      } while (!ok && lc.again(t0));
+    }
+  }
   if (op.pro == PRO_RMS_EMB) {
     // a depformer step's input: dep_in[cb] . t (computed beside the text head) plus
     // "moshi_lm.rs", `embed` of the step's conditioning token (-1 adds nothing, else row
     // max(tok, 0)); CTA 0 keeps this x for the residuals
     const IoLayout io{1};
-    const int prev = forcing ? P.d_in[io.forced_off() + op.key_index]
-                                           : argmax_key_index(__ldcg(P.keys + op.key_index));
+    int prev;
+    if (LL && op.tag_key >= 0) {
+      // the pick's key: the largest of the CTAs' tagged best keys (or the one slot a top-k
+      // pick wrote).  Polled even when the token is forced: this op must not start before
+      // every CTA is done with the op before it (the chain that keeps buffers safe).
+      unsigned long long best = 0ull;
+      if (tid < op.key_slots) {
+        const float* sp = reinterpret_cast<const float*>(P.key_ll) +
+                          ((size_t)op.key_index * gridDim.x + tid) * 4;
+        const uint32_t t = lc.want(op.tag_key);
+        unsigned long long a, b;
+        uint64_t t0 = 0ull;
+        do {
+          ll_ld2(sp, 0, a, b);
+        } while (!(ll_is(a, t) & ll_is(b, t)) && lc.again(t0));
+        best = ((unsigned long long)(uint32_t)b << 32) | (uint32_t)a;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) s_key[warp] = best;
+      bar_sync(1, kCons);
+      unsigned long long m = 0ull;
+#pragma unroll
+      for (int w = 0; w < kCons / 32; ++w) m = s_key[w] > m ? s_key[w] : m;
+      prev = forcing ? P.d_in[io.forced_off() + op.key_index] : argmax_key_index(m);
+    } else {
+      prev = forcing ? P.d_in[io.forced_off() + op.key_index]
+                     : argmax_key_index(__ldcg(P.keys + op.key_index));
+    }
     const bool keep = op.side_out != nullptr && blockIdx.x == 0 && g == 0;
 #pragma unroll
     for (int j = 0; j < NX; ++j) {
@@ -384,7 +552,12 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
         }
         if (keep) {
 #pragma unroll
-          for (int v = 0; v < V; ++v) op.side_out[c * V + v] = xr[j][v];
+          for (int v = 0; v < V; ++v) {
+            if constexpr (LL)
+              ll_st(op.side_out, (size_t)c * V + v, wtag, xr[j][v]);
+            else
+              op.side_out[c * V + v] = xr[j][v];
+          }
         }
       }
     }
@@ -419,6 +592,9 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
             xr[j][v + 2] *= a.z;
             xr[j][v + 3] *= a.w;
           }
+        } else if constexpr (LL) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) xr[j][v] *= al[j][v];
         } else {
 #pragma unroll
           for (int v = 0; v < V; ++v) xr[j][v] *= ar[j][v];  // loaded before the barrier
@@ -436,17 +612,51 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
     const float scale = 1.0f / sqrtf((float)hd);
     const int tph = hd / 4;
     const int hpp = kCons / tph;
+    // a float4 of tagged words at element i of base, ok &= all four carry tag t
+    auto ld4 = [&](const float* base, size_t i, uint32_t t, float4& f, bool& ok) {
+      unsigned long long a, b, c, d;
+      ll_ld2(base, i, a, b);
+      ll_ld2(base, i + 2, c, d);
+      f = make_float4(ll_val(a), ll_val(b), ll_val(c), ll_val(d));
+      ok &= ll_is(a, t) & ll_is(b, t) & ll_is(c, t) & ll_is(d, t);
+    };
+    (void)ld4;
     for (int h0 = 0; h0 < dh; h0 += hpp) {
       const int h = h0 + tid / tph, sub = tid % tph;
       const bool act = h < dh;
       const size_t col = (size_t)h * hd + 4 * sub;
       float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 kk[8];
-      if (act) q4 = __ldcg(reinterpret_cast<const float4*>(in + col));
+      if constexpr (LL) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        kk[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dk + (size_t)j * K + col))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 8; ++j) kk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (act) {
+          const uint32_t tq = lc.want(op.tag_in);
+          // q and the keys in groups of four (all eight tagged keys in flight take more
+          // registers than the launch has; windows of up to four keys take one round trip)
+#pragma unroll
+          for (int j0 = 0; j0 < 8; j0 += 4) {
+            if (j0 > 0 && j0 >= nk) break;
+            uint64_t t0 = 0ull;
+            bool ok;
+            do {
+              ok = true;
+              if (j0 == 0) ld4(op.in, col, tq, q4, ok);  // (k0 is 0: x is one part)
+#pragma unroll
+              for (int j = j0; j < j0 + 4; ++j)
+                if (j < nk)
+                  ld4(op.dk, (size_t)j * K + col, lc.want(op.tag_kv + j * op.tag_kv_step), kk[j],
+                      ok);
+            } while (!ok && lc.again(t0));
+          }
+        }
+      } else {
+        if (act) q4 = __ldcg(reinterpret_cast<const float4*>(in + col));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          kk[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dk + (size_t)j * K + col))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       float sc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -468,10 +678,33 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
         den += sc[j];
       }
       float4 vv[8];
+      if constexpr (LL) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        vv[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)j * K + col))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 8; ++j) vv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (act) {
+          // the values in groups of VG (four with the token-pick code, which needs the
+          // registers)
+#pragma unroll
+          for (int j0 = 0; j0 < 8; j0 += VG) {
+            if (j0 > 0 && j0 >= nk) break;
+            uint64_t t0 = 0ull;
+            bool ok;
+            do {
+              ok = true;
+#pragma unroll
+              for (int j = j0; j < j0 + VG; ++j)
+                if (j < nk)
+                  ld4(op.dv, (size_t)j * K + col, lc.want(op.tag_kv + j * op.tag_kv_step), vv[j],
+                      ok);
+            } while (!ok && lc.again(t0));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          vv[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)j * K + col))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -489,10 +722,8 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
 #pragma unroll
     for (int j = 0; j < NX; ++j) {
       const int c = tig + j * pl.tpr;
-      if (j < nch && c < CC) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) xr[j][v] = s_att[c * V + v];
-      }
+      for (int v = 0; v < V; ++v) xr[j][v] = (j < nch && c < CC) ? s_att[c * V + v] : 0.f;
     }
     bar_sync(1, kCons);  // the staging buffer is reused by the next op
   }
@@ -514,16 +745,36 @@ __device__ __forceinline__ float rms_scale(const PersParams& P, const GemvPlan& 
 }
 
 // ---------------------------------------------------------------- epilogue
+// slot `cta` of pick `pick`'s tagged key halves (the readers take the largest key)
+__device__ __forceinline__ void put_key_slot(const PersParams& P, int pick, int cta,
+                                             uint32_t tag, unsigned long long key) {
+  float* sp = reinterpret_cast<float*>(P.key_ll) + ((size_t)pick * gridDim.x + cta) * 4;
+  const unsigned long long lo = ((unsigned long long)tag << 32) | (uint32_t)key;
+  const unsigned long long hi = ((unsigned long long)tag << 32) | (uint32_t)(key >> 32);
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(sp), "l"(lo), "l"(hi)
+               : "memory");
+}
+
 // Finish rows [t0*tr, (t0+nt)*tr) of one GEMV op from the per-warp partials (batch 1).
-template <typename WT, bool PICKS>
+// LL: outputs other CTAs read are tagged words (wtag), the residual's other rows are
+// polled (lc).
+template <typename WT, bool PICKS, bool LL>
 __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
                                          const GemvPlan& pl, int t0, int nt, const float* part,
                                          int tid, int warp, int lane,
                                          unsigned long long* s_key, const float2* s_rope,
                                          float resid_old, int pos, int forcing,
-                                         float scale) {
+                                         float scale, const LLCtx& lc, uint32_t wtag) {
   const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
   const int nrows = nt * tr;
+  (void)lc;
+  (void)wtag;
+  auto put = [&](float* base, size_t i, float v) {
+    if constexpr (LL)
+      ll_st(base, i, wtag, v);
+    else
+      base[i] = v;
+  };
   // the row's value: the partials (wpg <= 8, loaded together, added in order), times the
   // RMSNorm factor of an RMS op (1 otherwise)
   auto yrow = [&](int lr) {
@@ -548,8 +799,12 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       const int row = grow(lr);
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
-      if (epi == EPI_STORE) op.out[row] = y;
-      if (epi == EPI_RESID) op.out[row] = (lr == tid ? resid_old : ldcg(op.out + row)) + y;
+      if (epi == EPI_STORE) put(op.out, row, y);
+      if (epi == EPI_RESID) {
+        float old = resid_old;
+        if (lr != tid) old = LL ? lc.wait1(op.out, row, lc.want(op.tag_res)) : ldcg(op.out + row);
+        put(op.out, row, old + y);
+      }
       if (epi == EPI_DEPIN) {
         // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
         op.out[row] = (prev != -1)
@@ -566,7 +821,7 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       const int j = (t0 + lr / tr) * half + r;
       if (j >= pl.n_out) continue;
       const float gt = yrow(lr), mu = yrow(lr + half);
-      op.out[j] = gt / (1.0f + expf(-gt)) * mu;
+      put(op.out, j, gt / (1.0f + expf(-gt)) * mu);
     }
   } else if (epi == EPI_QKV) {
     const int D = pl.n_out / 3;
@@ -602,11 +857,11 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
       if (row < DD)
-        op.out[row] = y;
+        put(op.out, row, y);
       else if (row < 2 * DD)
-        op.dk_out[row - DD] = y;
+        put(op.dk_out, row - DD, y);
       else
-        op.dv_out[row - 2 * DD] = y;
+        put(op.dv_out, row - 2 * DD, y);
     }
   } else if (epi == EPI_ARGMAX) {
     unsigned long long best = 0ull;
@@ -615,6 +870,7 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       if (row >= pl.n_out) continue;
       const float y = yrow(lr);
       op.out[row] = y;
+      if (LL && op.side_out) ll_st(op.side_out, row, wtag, y);  // for the top-k pick
       const unsigned long long k = PICKS ? pick_key(P.samp, 0, op.key_index, y, (uint32_t)row)
                                          : argmax_key(y, (uint32_t)row);
       best = k > best ? k : best;
@@ -625,7 +881,8 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
     if (tid == 0) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kCons / 32; ++w) m = s_key[w] > m ? s_key[w] : m;
-      atomicMax(P.keys + op.key_index, m);
+      if (!LL || !op.no_keymax) atomicMax(P.keys + op.key_index, m);
+      if (LL && !op.no_keymax) put_key_slot(P, op.key_index, blockIdx.x, wtag, m);
     }
   }
 }
@@ -812,10 +1069,12 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
 // instruction caches (measured: 18 us less per Moshi-7B frame)
 // MINB: CTAs per SM.  Two for the temporal stack's weight stream (16 consumer warps per
 // SM keep up with HBM; the register cap follows from 2 x 288 threads: 96), one for the
-// depformer's latency-bound small ops (a 152-CTA grid barrier, 163 registers, no spills).
+// depformer's latency-bound small ops, which exchange tagged words instead of meeting at
+// grid barriers.
 template <typename WT, typename KT, int EPL, bool PICKS, int MINB>
 __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const PersParams P) {
   constexpr int V = Chunk<WT>::V;
+  constexpr bool LL = MINB == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_red[2 * (kCons / 32)];
   __shared__ __align__(16) float s_att[kMaxStage];
@@ -824,7 +1083,6 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
   __shared__ float s_am[2][4], s_al[2][4];
   __shared__ float s_aacc[2][4][EPL * 32];
   __shared__ int s_last[2];
-  __shared__ volatile int s_abort;
   __shared__ unsigned s_issued;
   // the consumers read op descriptors, plans and the launch's position from shared
   // memory: op k+1's descriptor is fetched during op k and published by its last CTA
@@ -832,6 +1090,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
   __shared__ __align__(16) PersOp s_op[2];
   __shared__ __align__(16) GemvPlan s_plan[kPersMaxPlans];
   __shared__ int s_pos, s_forcing;
+  __shared__ uint32_t s_ebase;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // wait limit of this launch (a test may shorten it), and the op whose barrier a test
   // makes unreachable (-1: none)
@@ -895,6 +1154,10 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
     if (tid == 0) {
       s_pos = P.offsets[0];
       s_forcing = P.d_in[IoLayout{1}.flag_off()];
+      // the frame's first launch advances the epoch; the tagged launch reads it (after
+      // the first launch has finished)
+      if (P.epoch_bump && blockIdx.x == 0) atomicAdd(P.epoch, 1u);
+      s_ebase = LL ? ld_acquire(P.epoch) << 10 : 0u;
     }
     if (tid < P.head_dim / 2) {
       // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos;
@@ -905,6 +1168,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
     }
     bar_sync(1, kCons);
     const int pos = s_pos, forcing = s_forcing;
+    LLCtx lc{s_ebase, 0u, P};
     int cslot = 0;       // ring slot of the next tile to consume
     uint32_t cph = 0u;   // and the phase its "full" barrier completes
     float xr[Nx<WT>::N][V];
@@ -914,7 +1178,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
       // op k+1's descriptor, loaded now, stored to shared memory at the end of op k
       const unsigned long long nxt =
           (tid < kOpWords && k + 1 < P.n_ops) ? ops64[(size_t)(k + 1) * kOpWords + tid] : 0ull;
-      if constexpr (!Chunk<WT>::kBand) {  // constant alpha of an RMSNorm prologue
+      if constexpr (!Chunk<WT>::kBand && !LL) {  // constant alpha of an RMSNorm prologue
         const PersOp& op = s_op[k & 1];
         if (op.type == OPT_GEMV && (op.pro == PRO_RMS || op.pro == PRO_RMS_EMB)) {
           const GemvPlan& pl = s_plan[op.plan];
@@ -927,14 +1191,15 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
           }
         }
       }
-      if (k > 0 && !s_op[k & 1].nobar) {
+      lc.flip = (LL && k == stall_op) ? 0xffffffffu : 0u;
+      const uint32_t wtag = s_ebase | (uint32_t)(P.op_base + k);
+      if (!LL && k > 0 && !s_op[k & 1].nobar) {
         const unsigned target = (unsigned)k * gridDim.x + (k == stall_op ? 1u : 0u);
         if (tid == 0 && !grid_wait(P.grid_bar, target, lim)) {
           atomicOr(P.status, kDevTimeout);
           s_abort = 1;
         }
-        bar_sync(1, kCons);
-        if (s_abort) break;
+        if (bar_or(1, kCons, s_abort != 0)) break;
       }
       if (stamp) P.trace[P.op_base + k] = global_timer_ns();
       const PersOp& op = s_op[k & 1];
@@ -945,14 +1210,43 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
         // wrote, by CTA 0 (its partial-sum buffer holds the selection's scratch)
         if (blockIdx.x == 0) {
           const int pk = op.key_index;
+          const float* lg = op.in;
+          if constexpr (LL) {
+            // gather the logits from their tagged copy (8 words per thread and round trip)
+            const int n = pk == 0 ? P.samp.V : P.samp.A;
+            const uint32_t t = lc.want(op.tag_in);
+            for (int i0 = 0; i0 < n; i0 += 8 * kCons) {
+              // (a value is stored as it loads; a retry stores it again)
+              uint64_t t0 = 0ull;
+              bool ok;
+              do {
+                ok = true;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int i = i0 + e * kCons + tid;
+                  if (i < n) {
+                    const unsigned long long w = ll_ld1(op.in, i);
+                    P.topk_scratch[i] = ll_val(w);
+                    ok &= ll_is(w, t);
+                  }
+                }
+              } while (!ok && lc.again(t0));
+            }
+            bar_sync(1, kCons);
+            lg = P.topk_scratch;
+          }
           const double u = xs_u01(xs_advance(P.samp.rng[0], draws_before(P.samp, pk) + 1u,
                                              P.samp.jump));
           TopkShared& S = *reinterpret_cast<TopkShared*>(part);
-          const int tok = topk_pick_block(op.in, pk == 0 ? P.samp.V : P.samp.A,
+          const int tok = topk_pick_block(lg, pk == 0 ? P.samp.V : P.samp.A,
                                           pk == 0 ? P.samp.top_k_text : P.samp.top_k,
                                           pk == 0 ? P.samp.temp_text : P.samp.temp, u, tid,
                                           kCons, S, SyncNamed<kCons>{});
-          if (tid == 0) P.keys[pk] = argmax_key(__ldcg(op.in + tok), (uint32_t)tok);
+          if (tid == 0) {
+            const unsigned long long key = argmax_key(__ldcg(lg + tok), (uint32_t)tok);
+            P.keys[pk] = key;
+            if (LL) put_key_slot(P, pk, 0, wtag, key);
+          }
         }
       } else {
         const GemvPlan& pl = s_plan[op.plan];
@@ -964,7 +1258,8 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
           float resid_old = 0.f;  // the residual's old value, fetched before the tiles
           if (op.epi == EPI_RESID && tid < nt * pl.tile_rows) {
             const int row = (t0 + tid / pl.tile_rows) * pl.tile_rows + tid % pl.tile_rows;
-            if (row < pl.n_out) resid_old = ldcg(op.out + row);
+            if (row < pl.n_out)
+              resid_old = LL ? lc.wait1(op.out, row, lc.want(op.tag_res)) : ldcg(op.out + row);
           }
           bool ok = true;
           for (int kp = 0; kp < pl.kparts && ok; ++kp) {
@@ -972,8 +1267,8 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
             const int k0 = kp * pl.kp_width;
             const int Kw = kp == pl.kparts - 1 ? pl.K - k0 : pl.kp_width;
             const int nch = (Kw / V + pl.tpr - 1) / pl.tpr;
-            form_x<WT>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red, k & 1,
-                       s_att, forcing);
+            form_x<WT, LL, PICKS>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red,
+                           k & 1, s_att, forcing, lc, wtag, s_key);
             constexpr int BT = MINB == 1 ? kBurstTWide : kBurstT;
             if (nch <= 1 && nt > 2)
               ok = consume_tiles<WT, 1, BT, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
@@ -999,8 +1294,8 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
             atomicOr(P.status, kDevTimeout);
             s_abort = 1;
           }
-          bar_sync(1, kCons);
-          if (s_abort) break;
+          // the producer may raise s_abort at any time: decide on one uniform answer
+          if (bar_or(1, kCons, s_abort != 0)) break;
           const bool rms = op.pro == PRO_RMS || op.pro == PRO_RMS_EMB;
           const float scale = rms ? rms_scale(P, pl, s_red, k & 1) : 1.0f;
           if (op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0) {
@@ -1015,15 +1310,18 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
               }
             }
           }
-          epilogue<WT, PICKS>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope, resid_old,
-                              pos, forcing, scale);
+          epilogue<WT, PICKS, LL>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope,
+                                  resid_old, pos, forcing, scale, lc, wtag);
+        } else if (LL && op.epi == EPI_ARGMAX && !op.no_keymax && tid == 0) {
+          put_key_slot(P, op.key_index, blockIdx.x, wtag, 0ull);  // no rows here
         }
       }
       if (tid < kOpWords && k + 1 < P.n_ops) s_op64[((k + 1) & 1) * kOpWords + tid] = nxt;
       bar_sync(1, kCons);
-      if (tid == 0) grid_arrive(P.grid_bar);
+      if (!LL && tid == 0) grid_arrive(P.grid_bar);
     }
-    if (stamp && !s_abort && grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x, lim))
+    // end of the launch (tagged: when CTA 0 is done)
+    if (stamp && !s_abort && (LL || grid_wait(P.grid_bar, (unsigned)P.n_ops * gridDim.x, lim)))
       P.trace[P.op_base + P.n_ops] = global_timer_ns();
   }
   __syncthreads();

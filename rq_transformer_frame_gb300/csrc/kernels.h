@@ -282,6 +282,20 @@ struct PersOp {
   const void* emb;      // EPI_DEPIN / PRO_RMS_EMB: table [rows][n_out or K]
   int nobar;            // 1: no grid barrier before this op (it reads nothing the previous
                         // op writes)
+  // The one-CTA-per-SM launch (the depformer) has no grid barriers: every activation one
+  // CTA writes and another reads is a tagged word (see frame_persistent.cuh), and these
+  // are the frame op indices whose tags the op waits for (-1: a plain read of what an
+  // earlier launch wrote).  Its `in`, `out`, `side_out`, `dk`, `dv`, `dk_out`, `dv_out`
+  // then point at tagged-word arrays (uint64, same element indexing), except the logits
+  // (`out` of EPI_ARGMAX, plain f32 for the host; `side_out` there: their tagged copy for
+  // a top-k pick, or null) and `in` of PRO_RMS_EMB (the first launch's f32 dep_pre).
+  int tag_in;           // writer of `in` (PRO_DATTN: of the query; OPT_TOPK: of the logits)
+  int tag_res;          // EPI_RESID: last writer of the residual rows `out`
+  int tag_kv;           // PRO_DATTN: writer of key / value 0; key j's is tag_kv + j * tag_kv_step
+  int tag_kv_step;
+  int tag_key;          // PRO_RMS_EMB: the op that chose pick key_index (-1: the first launch)
+  int key_slots;        // PRO_RMS_EMB: that op's key slots (the grid's CTAs, or 1: a top-k pick)
+  int no_keymax;        // EPI_ARGMAX: a top-k pick follows; it alone writes keys[key_index]
 };
 
 constexpr int kPersMaxPlans = 12;
@@ -315,6 +329,12 @@ struct PersParams {
   uint32_t* status;
   unsigned long long* trace;  // [n_ops + 1] op start times (ns), CTA 0 (nullable)
   SampleParams samp;
+  // tagged-word exchange (the one-CTA-per-SM launch): tags are (*epoch << 10) | frame op
+  // index; a launch with epoch_bump set advances *epoch once (the frame's first launch)
+  unsigned int* epoch;
+  int epoch_bump;
+  unsigned long long* key_ll;  // [9][grid][2] tagged halves of each CTA's best key per pick
+  float* topk_scratch;         // [A] a top-k pick's logits, gathered from their tagged copy
 };
 
 GemvPlan plan_persistent(int n_out, int K, int elem_bytes, bool paired, bool even_rows,
@@ -395,6 +415,12 @@ cudaError_t launch_persistent(const PersParams& p, int wtype, bool kv_bf16, int 
 // uint32 index, in the persistent schedule's barrier allocation, of the depformer launch's
 // grid-barrier counter (its own 128-byte line); frame_begin zeroes it with the first one
 constexpr int kPersDepBarWord = 64;
+// uint32 index there of the frame epoch (never zeroed: tags of earlier frames must differ)
+constexpr int kPersEpochWord = 96;
+// frame op indices fit the low 10 bits of a tag
+constexpr int kPersMaxTaggedOps = 1024;
+// key slots a tagged reader polls, one consumer thread each
+constexpr int kPersMaxKeySlots = 256;
 cudaError_t persistent_configure(int wtype, bool kv_bf16, int smem, int head_dim, int minb);
 int persistent_max_grid(int wtype, bool kv_bf16, int smem, int head_dim, int minb);
 

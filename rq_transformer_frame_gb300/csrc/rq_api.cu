@@ -44,6 +44,11 @@ struct rq_handle {
   unsigned long long* keys = nullptr;
   float *dx = nullptr, *dq = nullptr, *dkv = nullptr, *du = nullptr;
   float* dep_pre = nullptr;  // persistent schedule: dep_in[cb] . t of the 8 steps [8][DD]
+  // the depformer launch's tagged-word copies (64-bit words, element indexing of dx, dq,
+  // du, dkv and the audio logits) and its key slots / top-k scratch
+  float *dx_ll = nullptr, *dq_ll = nullptr, *du_ll = nullptr, *dkv_ll = nullptr;
+  float *alog_ll = nullptr, *topk_scratch = nullptr;
+  unsigned long long* key_ll = nullptr;
   float* part = nullptr;
   int* counters = nullptr;
   // pinned host staging
@@ -444,7 +449,8 @@ void free_all(rq_handle* h) {
   for (void* p : dev)
     if (p) cudaFree(p);
   void* tcb[] = {h->rope, h->xb, h->attn_b, h->u_b, h->tout_b, h->dxb, h->do_b, h->du_b,
-                 h->tc_part, h->tc_tickets, h->ss_x, h->ss_dx};
+                 h->tc_part, h->tc_tickets, h->ss_x, h->ss_dx, h->dx_ll, h->dq_ll, h->du_ll,
+                 h->dkv_ll, h->alog_ll, h->topk_scratch, h->key_ll};
   for (void* p : tcb)
     if (p) cudaFree(p);
   for (void* p : h->pf_bufs)
@@ -602,49 +608,91 @@ std::vector<PersOp> pers_ops(const rq_handle* h, int* dep_first) {
   const bool topk = h->samp.mode == SAMPLE_TOPK;
   if (topk) topk_op(h->text_logits, 0);
   if (dep_first) *dep_first = (int)ops.size();
+  // The depformer launch exchanges tagged words (ll): its buffers are the tagged copies
+  // and every op names the frame op indices whose tags it waits for.  Otherwise (one launch
+  // for the whole frame) the plain buffers and grid barriers.
+  const bool ll = h->pers_dep_grid > 0;
+  auto L = [&](float* plain, float* tagged, size_t elem) -> float* {
+    return ll ? reinterpret_cast<float*>(reinterpret_cast<unsigned long long*>(tagged) + elem)
+              : plain + elem;
+  };
+  const int step_ops = 4 * c.dlayers + 1 + (topk ? 1 : 0);  // ops of one depformer step
+  std::vector<int> dqkv0(c.dlayers, -1);  // frame op index of step 0's qkv, per layer
+  int last_dx = -1, last_du = -1;        // last writer of dx / du
+  int key_tag = -1, key_slots = 0;       // the op that chose the previous step's token
   for (int cb = 0; cb < 8; ++cb) {
     PersOp o{};
     for (int l = 0; l < c.dlayers; ++l) {
       const size_t ls = (size_t)l * 8 + cb;
+      const int iq = (int)ops.size();
+      if (cb == 0) dqkv0[l] = iq;
       o = gemv(l == 0 ? PRO_RMS_EMB : PRO_RMS, EPI_DQKV, 6,
                mat(h, h->w.d_in_proj, ls * 3 * DD, DD));
-      o.in = h->dx;
+      o.in = L(h->dx, h->dx_ll, 0);
+      o.tag_in = last_dx;
       if (l == 0) {  // x = dep_in[cb] . t + E[prev], kept in dx for the residuals
         o.in = h->dep_pre + (size_t)cb * DD;
-        o.side_out = h->dx;
+        o.tag_in = -1;
+        o.side_out = L(h->dx, h->dx_ll, 0);
         o.emb = cb == 0 ? h->w.dep_text_emb
                         : woff(h->w.dep_emb, (size_t)(cb - 1) * (A + 1) * DD, es);
         o.key_index = cb;
+        o.tag_key = key_tag;
+        o.key_slots = key_slots;
+        last_dx = iq;
       }
       o.alpha = h->w.dnorm1 + (size_t)l * DD;
-      o.out = h->dq;
-      o.dk_out = h->dkv + dkv_off(h, l, 0, cb);
-      o.dv_out = h->dkv + dkv_off(h, l, 1, cb);
+      o.out = L(h->dq, h->dq_ll, 0);
+      o.dk_out = L(h->dkv, h->dkv_ll, dkv_off(h, l, 0, cb));
+      o.dv_out = L(h->dkv, h->dkv_ll, dkv_off(h, l, 1, cb));
       ops.push_back(o);
       o = gemv(PRO_DATTN, EPI_RESID, 7, mat(h, h->w.d_out_proj, ls * DD, DD));
-      o.in = h->dq;
-      o.dk = h->dkv + dkv_off(h, l, 0, 0);
-      o.dv = h->dkv + dkv_off(h, l, 1, 0);
+      o.in = L(h->dq, h->dq_ll, 0);
+      o.tag_in = iq;
+      o.dk = L(h->dkv, h->dkv_ll, dkv_off(h, l, 0, 0));
+      o.dv = L(h->dkv, h->dkv_ll, dkv_off(h, l, 1, 0));
+      o.tag_kv = dqkv0[l];
+      o.tag_kv_step = step_ops;
       o.n_keys = cb + 1;
-      o.out = h->dx;
+      o.out = L(h->dx, h->dx_ll, 0);
+      o.tag_res = last_dx;
+      last_dx = (int)ops.size();
       ops.push_back(o);
       o = gemv(PRO_RMS, EPI_SWIGLU, 8, mat(h, h->w.d_gate_in, ls * 2 * DF, DD));
       o.w_half = (long long)(DF * band_row_bytes(h->band, es, DD));
-      o.in = h->dx;
+      o.in = L(h->dx, h->dx_ll, 0);
+      o.tag_in = last_dx;
       o.alpha = h->w.dnorm2 + (size_t)l * DD;
-      o.out = h->du;
+      o.out = L(h->du, h->du_ll, 0);
+      last_du = (int)ops.size();
       ops.push_back(o);
       o = gemv(PRO_PLAIN, EPI_RESID, 9, mat(h, h->w.d_gate_out, ls * DD, DF));
-      o.in = h->du;
-      o.out = h->dx;
+      o.in = L(h->du, h->du_ll, 0);
+      o.tag_in = last_du;
+      o.out = L(h->dx, h->dx_ll, 0);
+      o.tag_res = last_dx;
+      last_dx = (int)ops.size();
       ops.push_back(o);
     }
     o = gemv(PRO_PLAIN, EPI_ARGMAX, 10, mat(h, h->w.linears, (size_t)cb * A, DD));
-    o.in = h->dx;
+    o.in = L(h->dx, h->dx_ll, 0);
+    o.tag_in = last_dx;
     o.out = h->audio_logits + (size_t)cb * A;
     o.key_index = 1 + cb;
+    if (ll && topk) {  // the pick reads the tagged copy and alone writes the key
+      o.side_out = L(nullptr, h->alog_ll, (size_t)cb * A);
+      o.no_keymax = 1;
+    }
+    key_tag = (int)ops.size();
+    key_slots = h->pers_dep_grid;
     ops.push_back(o);
-    if (topk) topk_op(h->audio_logits + (size_t)cb * A, 1 + cb);
+    if (topk) {
+      topk_op(ll ? L(nullptr, h->alog_ll, (size_t)cb * A) : h->audio_logits + (size_t)cb * A,
+              1 + cb);
+      ops.back().tag_in = key_tag;
+      key_tag = (int)ops.size() - 1;
+      key_slots = 1;
+    }
   }
   return ops;
 }
@@ -949,6 +997,8 @@ rq_status upload_pers_ops(rq_handle* h) {
   h->pers_dep.samp = h->samp;
   h->pers_nobar.assign(ops.size(), 0);
   for (size_t k = 0; k < ops.size(); ++k) h->pers_nobar[k] = ops[k].nobar ? 1 : 0;
+  // the depformer launch's first op waits for nothing (the first launch has finished)
+  if (h->pers_split < n) h->pers_nobar[h->pers_split] = 1;
   h->pers.trace = h->trace;
   h->pers.samp = h->samp;
   return RQ_OK;
@@ -1060,14 +1110,17 @@ rq_status setup_schedule(rq_handle* h) {
   // The depformer's ops as a second cooperative launch at one CTA per SM: its small ops
   // are latency-bound, and a 152-CTA grid barrier, a register budget without spills and a
   // ring twice as deep run them faster (Moshi-7B: 1.29 -> 1.12 ms per frame), while the
-  // temporal stack keeps two CTAs per SM to stream its weights.  If that launch does not
-  // fit, the first one runs every op.
+  // temporal stack keeps two CTAs per SM to stream its weights.  Its ops wait for tagged
+  // words instead of grid barriers (frame op indices must fit a tag's 10 bits: at most
+  // 5 L + 3 + 8 (4 DL + 2) ops).  If that launch does not fit, the first one runs every op.
   h->pers_dep_grid = 0;
   {
     GemvPlan pl2[kPersMaxPlans];
     int slot2 = 0, part2 = 0, ns2 = 0, smem2 = 0;
     const int G2 = h->num_sms;
-    if (G == 2 * h->num_sms && geometry(G2, kPersDepSlotBudget, pl2, slot2, part2, ns2, smem2, true) &&
+    const int max_ops = 5 * c.layers + 3 + 8 * (4 * c.dlayers + 2);
+    if (G == 2 * h->num_sms && max_ops < kPersMaxTaggedOps && G2 <= kPersMaxKeySlots &&
+        geometry(G2, kPersDepSlotBudget, pl2, slot2, part2, ns2, smem2, true) &&
         persistent_configure(h->wtype, h->kvbf, smem2, c.head_dim, 1) == cudaSuccess &&
         persistent_max_grid(h->wtype, h->kvbf, smem2, c.head_dim, 1) >= G2) {
       PersParams& Q = h->pers_dep;
@@ -1081,6 +1134,30 @@ rq_status setup_schedule(rq_handle* h) {
       h->pers_dep_smem = smem2;
     }
     cudaGetLastError();  // a refused configuration leaves no sticky error
+  }
+  if (h->pers_dep_grid > 0) {
+    const size_t DD = c.ddim, DF = c.dhidden, A = c.audio_card, DL = c.dlayers;
+    RQ_CUDA(h, dalloc(&h->dx_ll, DD * 8));
+    RQ_CUDA(h, dalloc(&h->dq_ll, DD * 8));
+    RQ_CUDA(h, dalloc(&h->du_ll, DF * 8));
+    RQ_CUDA(h, dalloc(&h->dkv_ll, DL * 2 * 8 * DD * 8));
+    RQ_CUDA(h, dalloc(&h->alog_ll, 8 * A * 8));
+    RQ_CUDA(h, dalloc(&h->topk_scratch, A * 4));
+    RQ_CUDA(h, dalloc(&h->key_ll, (size_t)9 * h->pers_dep_grid * 16));
+    // zero tags: epoch 0 is never a frame's (the first frame advances it to 1)
+    RQ_CUDA(h, cudaMemset(h->dx_ll, 0, DD * 8));
+    RQ_CUDA(h, cudaMemset(h->dq_ll, 0, DD * 8));
+    RQ_CUDA(h, cudaMemset(h->du_ll, 0, DF * 8));
+    RQ_CUDA(h, cudaMemset(h->dkv_ll, 0, DL * 2 * 8 * DD * 8));
+    RQ_CUDA(h, cudaMemset(h->alog_ll, 0, 8 * A * 8));
+    RQ_CUDA(h, cudaMemset(h->key_ll, 0, (size_t)9 * h->pers_dep_grid * 16));
+    P.epoch = h->grid_bar + kPersEpochWord;
+    P.epoch_bump = 1;
+    PersParams& Q = h->pers_dep;
+    Q.epoch = P.epoch;
+    Q.epoch_bump = 0;
+    Q.key_ll = h->key_ll;
+    Q.topk_scratch = h->topk_scratch;
   }
   h->schedule = RQ_SCHEDULE_PERSISTENT;
   return upload_pers_ops(h);

@@ -3,8 +3,9 @@ whole-frame kernel): the frame reports RQ_ERR_TIMEOUT, the handle is poisoned un
 rq_reset(h, -1), and after that reset the handle decodes like a fresh one.
 
 The wait is made to run out without any fault: a test hook shortens the wait limit to
-20 ms and makes the grid barrier in front of one op wait for one CTA more than the grid
-holds (a count that nothing reaches).  Every CTA gives up at its own bounded wait,
+20 ms and makes the waits in front of one op unsatisfiable -- in the temporal launch its
+grid barrier waits for one CTA more than the grid holds, in the depformer launch its
+tagged words for a tag that nothing writes.  Every CTA gives up at its own bounded wait,
 records the timeout in the status word, waits for its own bulk copies in flight and
 returns; the context stays usable."""
 import numpy as np
@@ -46,6 +47,8 @@ def test_wait_timeout_poisons_and_reset_recovers(stall_op):
         dec.set_wait_limit(20_000_000, n_ops)
     with pytest.raises(binding.RQError):  # the input projections beside the text head
         dec.set_wait_limit(20_000_000, 5 * c.layers + 1)
+    with pytest.raises(binding.RQError):  # the depformer launch's first op waits for nothing
+        dec.set_wait_limit(20_000_000, 5 * c.layers + 2)
     dec.set_wait_limit(20_000_000, stall_op)
 
     with pytest.raises(binding.RQError) as ei:
