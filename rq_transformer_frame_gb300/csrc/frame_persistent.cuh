@@ -433,7 +433,6 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
                                        unsigned long long* s_key) {
   constexpr int V = Chunk<WT>::V;
   constexpr int NX = Nx<WT>::N;
-  constexpr int VG = PICKS ? 4 : 8;  // tagged values polled per round trip
   using TT = typename Chunk<WT>::Table;  // embedding tables: bf16 for weight bands
   const int K = pl.K, CC = Kw / V;
   const float* in = op.in + k0;  // this part's columns [k0, k0 + Kw)
@@ -625,95 +624,116 @@ __device__ __forceinline__ void form_x(const PersParams& P, const PersOp& op,
       const int h = h0 + tid / tph, sub = tid % tph;
       const bool act = h < dh;
       const size_t col = (size_t)h * hd + 4 * sub;
-      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 kk[8];
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
       if constexpr (LL) {
+        // tagged: keys and values in groups of four, each group one round trip (with q in
+        // the first), folded in with the running-max softmax (windows of up to four keys:
+        // one round trip; eight tagged keys and values in flight would take more
+        // registers than the launch has)
+        float m = -__int_as_float(0x7f800000), l = 0.f;
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t tq = lc.want(op.tag_in);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) kk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (act) {
-          const uint32_t tq = lc.want(op.tag_in);
-          // q and the keys in groups of four (all eight tagged keys in flight take more
-          // registers than the launch has; windows of up to four keys take one round trip)
+        for (int j0 = 0; j0 < 8; j0 += 4) {
+          if (j0 > 0 && j0 >= nk) break;
+          float4 kk[4], vv[4];
 #pragma unroll
-          for (int j0 = 0; j0 < 8; j0 += 4) {
-            if (j0 > 0 && j0 >= nk) break;
+          for (int i = 0; i < 4; ++i) kk[i] = vv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (act) {
             uint64_t t0 = 0ull;
             bool ok;
             do {
               ok = true;
               if (j0 == 0) ld4(op.in, col, tq, q4, ok);  // (k0 is 0: x is one part)
 #pragma unroll
-              for (int j = j0; j < j0 + 4; ++j)
-                if (j < nk)
-                  ld4(op.dk, (size_t)j * K + col, lc.want(op.tag_kv + j * op.tag_kv_step), kk[j],
-                      ok);
+              for (int i = 0; i < 4; ++i) {
+                const int j = j0 + i;
+                if (j < nk) {
+                  const uint32_t tj = lc.want(op.tag_kv + j * op.tag_kv_step);
+                  ld4(op.dk, (size_t)j * K + col, tj, kk[i], ok);
+                  ld4(op.dv, (size_t)j * K + col, tj, vv[i], ok);
+                }
+              }
             } while (!ok && lc.again(t0));
           }
+          float sc[4];
+          float mn = m;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float d = q4.x * kk[i].x;
+            d = fmaf(q4.y, kk[i].y, d);
+            d = fmaf(q4.z, kk[i].z, d);
+            d = fmaf(q4.w, kk[i].w, d);
+            for (int w = tph >> 1; w > 0; w >>= 1) d += __shfl_xor_sync(0xffffffffu, d, w);
+            sc[i] = d * scale;
+            if (j0 + i < nk) mn = fmaxf(mn, sc[i]);
+          }
+          const float corr = expf(m - mn);  // 0 for the first group (m = -inf)
+          l *= corr;
+          o.x *= corr;
+          o.y *= corr;
+          o.z *= corr;
+          o.w *= corr;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (j0 + i < nk) {
+              const float e = expf(sc[i] - mn);
+              l += e;
+              o.x = fmaf(e, vv[i].x, o.x);
+              o.y = fmaf(e, vv[i].y, o.y);
+              o.z = fmaf(e, vv[i].z, o.z);
+              o.w = fmaf(e, vv[i].w, o.w);
+            }
+          }
+          m = mn;
         }
+        const float inv = 1.0f / l;
+        o.x *= inv;
+        o.y *= inv;
+        o.z *= inv;
+        o.w *= inv;
       } else {
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 kk[8];
         if (act) q4 = __ldcg(reinterpret_cast<const float4*>(in + col));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           kk[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dk + (size_t)j * K + col))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float sc[8];
+        float sc[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float d = q4.x * kk[j].x;
-        d = fmaf(q4.y, kk[j].y, d);
-        d = fmaf(q4.z, kk[j].z, d);
-        d = fmaf(q4.w, kk[j].w, d);
-        for (int o = tph >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        sc[j] = d * scale;
-      }
-      float mx = -__int_as_float(0x7f800000);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < nk) mx = fmaxf(mx, sc[j]);
-      float den = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc[j] = (j < nk) ? expf(sc[j] - mx) : 0.f;
-        den += sc[j];
-      }
-      float4 vv[8];
-      if constexpr (LL) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) vv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (act) {
-          // the values in groups of VG (four with the token-pick code, which needs the
-          // registers)
-#pragma unroll
-          for (int j0 = 0; j0 < 8; j0 += VG) {
-            if (j0 > 0 && j0 >= nk) break;
-            uint64_t t0 = 0ull;
-            bool ok;
-            do {
-              ok = true;
-#pragma unroll
-              for (int j = j0; j < j0 + VG; ++j)
-                if (j < nk)
-                  ld4(op.dv, (size_t)j * K + col, lc.want(op.tag_kv + j * op.tag_kv_step), vv[j],
-                      ok);
-            } while (!ok && lc.again(t0));
-          }
+        for (int j = 0; j < 8; ++j) {
+          float d = q4.x * kk[j].x;
+          d = fmaf(q4.y, kk[j].y, d);
+          d = fmaf(q4.z, kk[j].z, d);
+          d = fmaf(q4.w, kk[j].w, d);
+          for (int w = tph >> 1; w > 0; w >>= 1) d += __shfl_xor_sync(0xffffffffu, d, w);
+          sc[j] = d * scale;
         }
-      } else {
+        float mx = -__int_as_float(0x7f800000);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < nk) mx = fmaxf(mx, sc[j]);
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sc[j] = (j < nk) ? expf(sc[j] - mx) : 0.f;
+          den += sc[j];
+        }
+        float4 vv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           vv[j] = (act && j < nk) ? __ldcg(reinterpret_cast<const float4*>(op.dv + (size_t)j * K + col))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < nk) {
-          const float w = sc[j] / den;
-          o.x += w * vv[j].x;
-          o.y += w * vv[j].y;
-          o.z += w * vv[j].z;
-          o.w += w * vv[j].w;
+        for (int j = 0; j < 8; ++j) {
+          if (j < nk) {
+            const float w = sc[j] / den;
+            o.x += w * vv[j].x;
+            o.y += w * vv[j].y;
+            o.z += w * vv[j].z;
+            o.w += w * vv[j].w;
+          }
         }
       }
       if (act) *reinterpret_cast<float4*>(s_att + col) = o;
