@@ -209,8 +209,8 @@ __device__ __forceinline__ void tile_dot(const uint8_t* row, int Kw, int c, cons
   }
 }
 
-// Consume this CTA's `nt` tiles of one GEMV op from the ring (slot `slot`, phase `ph`
-// advance tile by tile), leaving one partial per (row, warp) in `part`.  Tiles go in
+// Consume `nt` tiles of one GEMV op from the ring (slot `slot`, phase `ph` advance tile by
+// tile), the CTA's tiles tb.. of the op, leaving one partial per (row, warp) in `part`.  Tiles go in
 // groups of T with one butterfly over the group's 2T rows.  BURST (tiles already
 // resident, the latency-bound depformer ops): every wait of a group, then every
 // shared-memory load, the FMAs and the slots' release, so the chain of dependent
@@ -218,7 +218,7 @@ __device__ __forceinline__ void tile_dot(const uint8_t* row, int Kw, int c, cons
 // and multiplied as soon as it lands and its slot goes back to the producer at once.
 template <typename WT, int NCH, int T, bool BURST>
 __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool accumulate,
-                                              int nt, int& slot, uint32_t& ph,
+                                              int nt, int tb, int& slot, uint32_t& ph,
                                               uint8_t* ring, int slot_bytes, int NS,
                                               uint64_t* full, uint64_t* empty, float* part,
                                               const float (&xr)[Nx<WT>::N][Chunk<WT>::V],
@@ -263,7 +263,7 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
                              : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-      for (int t = 0; t < T; ++t)
+      for (int t = 0; t < T; ++t) {
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           const int c = tig + j * pl.tpr;
@@ -274,6 +274,7 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
             tile_dot<WT>(row0[t] + (size_t)r * row_bytes, Kw, c, w[t][j][r], xr[j],
                          acc[t * RG + r][0], acc[t * RG + r][1]);
         }
+      }
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
@@ -322,7 +323,7 @@ __device__ __forceinline__ bool consume_tiles(const GemvPlan& pl, int Kw, bool a
     const int q = lane / (32 / R);
     const int t = q / RG, r = q % RG;
     if (lane % (32 / R) == 0 && i0 + t < nt) {
-      float* pp = part + (size_t)((i0 + t) * pl.tile_rows + g * RG + r) * wpg + (warp % wpg);
+      float* pp = part + (size_t)((tb + i0 + t) * pl.tile_rows + g * RG + r) * wpg + (warp % wpg);
       *pp = accumulate ? *pp + sum : sum;
     }
   }
@@ -1290,22 +1291,31 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
             form_x<WT, LL, PICKS>(P, op, pl, nch, k0, Kw, xr, ar, g, tig, tid, warp, lane, s_red,
                            k & 1, s_att, forcing, lc, wtag, s_key);
             constexpr int BT = MINB == 1 ? kBurstTWide : kBurstT;
-            if (nch <= 1 && nt > 2)
-              ok = consume_tiles<WT, 1, BT, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
-                                                  P.slot_bytes, NS, full, empty, part, xr, g,
-                                                  tig, warp, lane, lim);
-            else if (nch <= 1)
-              ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+            if (nch <= 1 && nt > 2) {
+              // full groups of BT; a remainder of one or two tiles as its own small group
+              // (its butterfly and loads sized for two tiles, not BT)
+              const int rem = MINB == 1 && nt > BT && nt % BT <= 2 ? nt % BT : 0;
+              ok = consume_tiles<WT, 1, BT, true>(pl, Kw, kp > 0, nt - rem, 0, cslot, cph,
+                                                  ring, P.slot_bytes, NS, full, empty, part,
+                                                  xr, g, tig, warp, lane, lim);
+              if constexpr (MINB == 1) {  // (the other launch keeps its smaller code)
+                if (ok && rem > 0)
+                  ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, rem, nt - rem, cslot, cph,
+                                                     ring, P.slot_bytes, NS, full, empty, part,
+                                                     xr, g, tig, warp, lane, lim);
+              }
+            } else if (nch <= 1)
+              ok = consume_tiles<WT, 1, 2, true>(pl, Kw, kp > 0, nt, 0, cslot, cph, ring,
                                                  P.slot_bytes, NS, full, empty, part, xr, g,
                                                  tig, warp, lane, lim);
             else if constexpr (Nx<WT>::N >= 2) {  // two x chunks (weight bands hold one)
               if (nt > kStreamMinTiles)
-                ok = consume_tiles<WT, 2, kStreamT, kStreamBurst>(pl, Kw, kp > 0, nt, cslot,
+                ok = consume_tiles<WT, 2, kStreamT, kStreamBurst>(pl, Kw, kp > 0, nt, 0, cslot,
                                                                   cph, ring, P.slot_bytes, NS,
                                                                   full, empty, part, xr, g, tig,
                                                                   warp, lane, lim);
               else
-                ok = consume_tiles<WT, 2, 2, true>(pl, Kw, kp > 0, nt, cslot, cph, ring,
+                ok = consume_tiles<WT, 2, 2, true>(pl, Kw, kp > 0, nt, 0, cslot, cph, ring,
                                                    P.slot_bytes, NS, full, empty, part, xr, g,
                                                    tig, warp, lane, lim);
             }
