@@ -133,6 +133,8 @@ __device__ __forceinline__ bool ll_is(unsigned long long w, uint32_t tag) {
 // the CTA's abort flag: raised by a wait that ran out (or by the producer), it ends every
 // other wait of the CTA and, read at a CTA barrier, the op loop
 __shared__ volatile int s_abort;
+// the launch's wait limit (ns), set once by thread 0
+__shared__ unsigned long long s_wait_lim;
 
 // The launch's view of the tags: the epoch base and `flip` (all ones for the op a test
 // stalls: it turns every tag that op waits for into one that nothing writes).
@@ -153,8 +155,7 @@ struct LLCtx {
       return true;
     }
     if (s_abort) return false;
-    const uint64_t lim = P.wait_ctl && P.wait_ctl[0] ? P.wait_ctl[0] : kWaitLimitNs;
-    if (global_timer_ns() - t0 > lim) {
+    if (global_timer_ns() - t0 > s_wait_lim) {
       atomicOr(P.status, kDevTimeout);
       s_abort = 1;
       return false;
@@ -1130,6 +1131,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
     fence_barrier_init();
     s_abort = 0;
     s_issued = 0;
+    s_wait_lim = lim;
   }
   __syncthreads();
 
