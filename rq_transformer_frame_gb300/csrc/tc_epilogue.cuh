@@ -36,13 +36,13 @@ struct EpiShared {
 };
 
 // The next GEMM's operand for a new residual value v of row `row`, session b (fused
-// RMSNorm, see TcParams).
+// RMSNorm, see TcParams); `an` = alpha_next[row], loaded once by the caller (1 without).
 __device__ __forceinline__ void feed_next(const TcParams& p, int row, bool valid, int b,
-                                          float v) {
+                                          float v, float an) {
   const TcPlan& pl = p.pl;
   if (valid)
     store_bf16_parts(p.opnd, (size_t)pl.NB * pl.n_out, (size_t)b * pl.n_out + row,
-                 b < p.B ? (p.alpha_next ? v * p.alpha_next[row] : v) : 0.f);
+                     b < p.B ? v * an : 0.f);
 }
 
 // Sum over the warp's 32 rows of each of 16 per-lane values with 16 shuffles (a
@@ -87,6 +87,10 @@ __device__ __forceinline__ void tile_sumsq(float (&sq)[16], int lane, int q, int
   if ((lane & 1) == 0) es.ss[q][c0 + col] = w1;
 }
 
+// Every read of a chunk's epilogue (tables, positions, tokens) is issued before its first
+// store: the compiler may not move a load across a store to a possibly aliasing pointer,
+// and one round trip to L2 per session and chunk made the batch-64 qkv epilogue cost
+// three times the GEMM's main loop.
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&d)[16], int c0,
                                                int tile, int m, int lane, int q, EpiShared& es,
                                                const float (&old0)[16]) {
@@ -115,6 +119,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
   }
   const int row = tile * kBM + m;
   const bool valid = row < pl.n_out;
+  const float an = (p.opnd && p.alpha_next && valid) ? __ldg(p.alpha_next + row) : 1.0f;
   if (epi == EPI_RESID || epi == EPI_STORE) {
     float sq[16];
 #pragma unroll
@@ -126,7 +131,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
         *o = nv;
       }
       sq[i] = nv * nv;
-      if (p.opnd) feed_next(p, row, valid, c0 + i, nv);
+      if (p.opnd) feed_next(p, row, valid, c0 + i, nv, an);
     }
     if (p.ss_out) tile_sumsq(sq, lane, q, c0, es);
   } else if (epi == EPI_QKV) {
@@ -134,6 +139,18 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
     const int D = pl.n_out / 3;
     const int region = row / D, col = row % D;
     const bool odd = (lane & 1) != 0;
+    // each session's (cos, sin) of this pair and its cache slot, all loaded first
+    float2 rr[16];
+    int slot[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int b = c0 + i;
+      const bool ok = valid && b < B;
+      rr[i] = (ok && region < 2)
+                  ? __ldg(p.rope + (size_t)b * (p.head_dim / 2) + (col % p.head_dim) / 2)
+                  : make_float2(1.f, 0.f);
+      slot[i] = (ok && region > 0) ? __ldg(p.offsets + b) : 0;
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int b = c0 + i;
@@ -141,16 +158,16 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
       if (!valid || b >= B) continue;
       float v = d[i];
       if (region < 2) {
-        const float2 r = p.rope[(size_t)b * (p.head_dim / 2) + (col % p.head_dim) / 2];
+        const float2 r = rr[i];
         const float re = odd ? partner : v, im = odd ? v : partner;
         v = odd ? re * r.y + im * r.x : re * r.x - im * r.y;
       }
       if (region == 0) {
         p.out[(size_t)b * p.out_bs + col] = v;
       } else {
-        const int slot = p.offsets[b] % p.context;
         store_kv_tc(region == 1 ? p.kcache : p.vcache,
-                    (size_t)b * p.kv_bs + (size_t)slot * D + col, v, p.kv_bf16);
+                    (size_t)b * p.kv_bs + (size_t)(slot[i] % p.context) * D + col, v,
+                    p.kv_bf16);
       }
     }
   } else if (epi == EPI_DQKV) {
@@ -168,27 +185,37 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const float (&
           p.dv_out[(size_t)b * p.dkv_bs + row - 2 * DD] = d[i];
       }
   } else if (epi == EPI_DEPIN) {
-    // "moshi_lm.rs", `embed` of the previous step's token: -1 adds nothing
+    // "moshi_lm.rs", `embed` of the previous step's token: -1 adds nothing.  The tokens,
+    // then the embedding values, are loaded for the whole chunk before any store.
     const IoLayout io{p.B};
+    int tok[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int b = c0 + i;
+      tok[i] = -1;
+      if (valid && b < B)
+        tok[i] = p.d_in[io.flag_off() + b]
+                     ? p.d_in[io.forced_off() + (size_t)b * 9 + p.key_index]
+                     : argmax_key_index(p.keys[(size_t)b * 9 + p.key_index]);
+    }
+    float e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      e[i] = tok[i] != -1 ? __uint_as_float(((uint32_t)static_cast<const uint16_t*>(
+                                                 p.emb)[(size_t)max(tok[i], 0) * pl.n_out + row])
+                                             << 16)
+                          : 0.f;
     float sq[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int b = c0 + i;
       float nv = 0.f;
       if (valid && b < B) {
-        const int prev = p.d_in[io.flag_off() + b]
-                             ? p.d_in[io.forced_off() + (size_t)b * 9 + p.key_index]
-                             : argmax_key_index(p.keys[(size_t)b * 9 + p.key_index]);
-        float e = 0.f;
-        if (prev != -1)
-          e = __uint_as_float(((uint32_t)static_cast<const uint16_t*>(
-                                   p.emb)[(size_t)max(prev, 0) * pl.n_out + row])
-                              << 16);
-        nv = d[i] + e;
+        nv = d[i] + e[i];
         p.out[(size_t)b * p.out_bs + row] = nv;
       }
       sq[i] = nv * nv;
-      if (p.opnd) feed_next(p, row, valid, b, nv);
+      if (p.opnd) feed_next(p, row, valid, b, nv, an);
     }
     if (p.ss_out) tile_sumsq(sq, lane, q, c0, es);
   } else if (epi == EPI_ARGMAX) {

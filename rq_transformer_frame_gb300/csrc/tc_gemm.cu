@@ -192,26 +192,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         float v[16];
         if (pl.splits > 1) {
-          // splits added in split order (deterministic); two splits' loads are issued
-          // before their adds, so each round trip to L2 carries twice the data
+          // splits added in split order (deterministic); the loads of up to four splits
+          // are issued before their adds, one round trip to L2 for up to four partials
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = 0.f;
           const size_t sstride = (size_t)NB * kBM;  // floats between splits of a tile
           const float* src = p.partial + ((size_t)tile * pl.splits * NB + c0) * kBM + m;
-          int sp = 0;
-          for (; sp + 1 < pl.splits; sp += 2) {
-            float a[16], b[16];
+          for (int sp = 0; sp < pl.splits; sp += 4) {
+            float a[4][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              a[i] = __ldcg(src + (size_t)sp * sstride + (size_t)i * kBM);
-              b[i] = __ldcg(src + (size_t)(sp + 1) * sstride + (size_t)i * kBM);
-            }
+            for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = (v[i] + a[i]) + b[i];
-          }
-          if (sp < pl.splits) {
+              for (int i = 0; i < 16; ++i)
+                a[u][i] = sp + u < pl.splits
+                              ? __ldcg(src + (size_t)(sp + u) * sstride + (size_t)i * kBM)
+                              : 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] += __ldcg(src + (size_t)sp * sstride + (size_t)i * kBM);
+            for (int u = 0; u < 4; ++u)
+              if (sp + u < pl.splits) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += a[u][i];
+              }
           }
         } else {
           load_sum3<NB>(tmem + ((uint32_t)(q * 32) << 16), c0, v);
