@@ -195,6 +195,8 @@ struct TcPlan {
   int NB;             // padded batch: multiple of 16, <= 64 (operand rows: 3 NB)
   int paired;         // SiLU-gated: tile rows 0-63 gate, 64-127 multiplier
   int tiles_m, splits, ksteps, ksteps_split;
+  int cluster;        // 1: a tile's K splits form one thread-block cluster and merge
+                      // through its shared memory; 0: through L2 (partials + ticket)
   int n_stages, smem;
   double bytes;       // weight bytes one launch streams
 };

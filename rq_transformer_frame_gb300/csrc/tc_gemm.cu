@@ -12,8 +12,13 @@
 //                      each stage back to its "empty" barrier;
 //   warps 2-5          read the 128 x NB f32 accumulator from tensor memory
 //                      (tcgen05.ld, one lane = one W row) and run the fused epilogue.
-// With split-K each split stores its partial tile; the last split to finish (atomic
-// ticket) adds all splits in split order -- deterministic -- and runs the epilogue.
+// With split-K, from 32 sessions on, the splits of a tile run as one thread-block
+// cluster: each stores its partial tile in its own shared memory, and after a cluster
+// barrier split r adds every split's partial (distributed shared memory, in split order --
+// deterministic) for the 16-session chunks r, r + splits, ... and runs their epilogue, so
+// the merge needs no round trip to L2 and the epilogue is spread over the splits.  At 16
+// sessions (one chunk) each split stores its partial tile to L2 and the last one to finish
+// (atomic ticket) adds them in split order and runs the epilogue.
 #include "tc_epilogue.cuh"
 
 namespace rqk {
@@ -138,8 +143,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
     const int m = q * 32 + lane;
     const int et = tid - 64;  // 0..127 among the epilogue warps
+    // K splits: the CTAs of a tile form one cluster; split r (its rank) finishes the
+    // 16-session chunks r, r + splits, ... from every split's partial in the cluster's
+    // shared memory, in split order (deterministic)
+    const int S = pl.splits;
+    // (compile time: the 16-session instantiation keeps only the L2 merge, the others only
+    // the cluster one; the host plans the same split)
+    constexpr bool kClu = NB >= 32;
+    const bool clu = kClu && S > 1;
+    const int c0f = clu ? 16 * split : 0;  // this CTA's first chunk
+    const int cstep = clu ? 16 * S : 16;
     // while the MMAs run: the fused-RMSNorm scales, and the old residual values of the
-    // first 16 sessions
+    // first chunk
     if (p.ss_in && et < NB) {
       float ss = 0.f;
       for (int t = 0; t < p.ss_tiles; ++t) ss += p.ss_in[(size_t)t * NB + et];
@@ -150,19 +165,32 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int row = tile * kBM + m;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        old0[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && i < p.B)
-                      ? p.out[(size_t)i * p.out_bs + row]
+        old0[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && c0f + i < p.B)
+                      ? p.out[(size_t)(c0f + i) * p.out_bs + row]
                       : 0.f;
     }
     if (!mbar_wait(&s_done, 0u)) s_abort = 1;
     bar_sync(1, 128);
     const bool ok = !s_abort;  // the same for all epilogue threads
     tc::fence_after_sync();
-    bool run = ok;
     if (!ok) atomicOr(p.status, kDevTimeout);
-    if (ok && pl.splits > 1) {
+    // this split's accumulator into its shared memory as [NB][kBM] f32 (the stages are
+    // free: every MMA, hence every load into them, has completed)
+    float* part_s = reinterpret_cast<float*>(smem);
+    if (kClu && clu && ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        float v[16];
+        load_sum3<NB>(tmem + ((uint32_t)(q * 32) << 16), c0, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) part_s[(size_t)(c0 + i) * kBM + m] = v[i];
+      }
+    }
+    if (kClu && clu) tc::cluster_sync();  // every split's partial written
+    bool run = ok;
+    if (!kClu && S > 1 && ok) {
       // store this split's partial, then the last split of the tile merges in order
-      float* mine = p.partial + ((size_t)(tile * pl.splits + split) * NB) * kBM;
+      float* mine = p.partial + ((size_t)(tile * S + split) * NB) * kBM;
 #pragma unroll
       for (int c0 = 0; c0 < NB; c0 += 16) {
         float v[16];
@@ -172,44 +200,56 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __threadfence();
       bar_sync(1, 128);
-      if (et == 0) s_last = (atomicAdd(&p.tickets[tile], 1) == pl.splits - 1);
+      if (et == 0) s_last = (atomicAdd(&p.tickets[tile], 1) == S - 1);
       bar_sync(1, 128);
       run = s_last != 0;
       if (run) __threadfence();
     }
     if (run) {
+      const uint32_t part_a = smem_u32(part_s);
 #pragma unroll 1
-      for (int c0 = 0; c0 < NB; c0 += 16) {
-        // the residual's old values of the next chunk load while this one is processed
+      for (int c0 = c0f; c0 < NB; c0 += cstep) {
+        // the residual's old values of this CTA's next chunk load while this one runs
         float old1[16];
         {
           const int row = tile * kBM + m;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            old1[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && c0 + 16 + i < p.B)
-                          ? p.out[(size_t)(c0 + 16 + i) * p.out_bs + row]
+            old1[i] = (p.epi == EPI_RESID && !pl.paired && row < pl.n_out && c0 + cstep + i < p.B)
+                          ? p.out[(size_t)(c0 + cstep + i) * p.out_bs + row]
                           : 0.f;
         }
         float v[16];
-        if (pl.splits > 1) {
-          // splits added in split order (deterministic); the loads of up to four splits
-          // are issued before their adds, one round trip to L2 for up to four partials
+        if (kClu && clu) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int r = 0; r < S; ++r) {
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              a[i] = tc::ld_cluster(
+                  tc::mapa(part_a + (uint32_t)(((c0 + i) * kBM + m) * 4), (uint32_t)r));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += a[i];
+          }
+        } else if (!kClu && S > 1) {
+          // splits added in split order; the loads of up to four splits are issued before
+          // their adds, one round trip to L2 for up to four partials
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = 0.f;
           const size_t sstride = (size_t)NB * kBM;  // floats between splits of a tile
-          const float* src = p.partial + ((size_t)tile * pl.splits * NB + c0) * kBM + m;
-          for (int sp = 0; sp < pl.splits; sp += 4) {
+          const float* src = p.partial + ((size_t)tile * S * NB + c0) * kBM + m;
+          for (int sp = 0; sp < S; sp += 4) {
             float a[4][16];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                a[u][i] = sp + u < pl.splits
-                              ? __ldcg(src + (size_t)(sp + u) * sstride + (size_t)i * kBM)
-                              : 0.f;
+                a[u][i] = sp + u < S ? __ldcg(src + (size_t)(sp + u) * sstride + (size_t)i * kBM)
+                                     : 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              if (sp + u < pl.splits) {
+              if (sp + u < S) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] += a[u][i];
               }
@@ -235,15 +275,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (p.epi == EPI_ARGMAX) {
         bar_sync(1, 128);
-        if (et < NB && et < p.B) {
+        // the sessions of this CTA's chunks
+        if (et < NB && et < p.B && (!clu || ((et >> 4) % S) == split)) {
           unsigned long long k = s_epi.key[0][et];
           for (int w = 1; w < 4; ++w) k = s_epi.key[w][et] > k ? s_epi.key[w][et] : k;
           atomicMax(p.keys + (size_t)et * 9 + p.key_index, k);
         }
       }
-      if (pl.splits > 1 && et == 0) p.tickets[tile] = 0;
     }
+    if (!kClu && S > 1 && run && et == 0) p.tickets[tile] = 0;
     tc::fence_before_sync();
+    if (kClu && clu) tc::cluster_sync();  // this CTA's partial stays until every split read it
+  }
+  if (NB >= 32 && warp < 2 && pl.splits > 1) {
+    // the producer and MMA warps take part in the cluster's two barriers
+    tc::cluster_sync();
+    tc::cluster_sync();
   }
   __syncthreads();
   if (warp == 1) {
@@ -334,6 +381,10 @@ TcPlan plan_tc(int n_out, int K, int NB, bool paired, int num_sms) {
   // at 64 columns a split's partial tile is 32 KB and beyond four splits merging them
   // costs more than the extra CTAs return (measured on out_proj / gate_out)
   if (NB >= 64 && splits > 4) splits = 4;
+  // from 32 sessions (two or more 16-session chunks) the splits of a tile form one
+  // thread-block cluster (portable size: at most 8); at 16 the L2 merge measured faster
+  pl.cluster = NB >= 32 ? 1 : 0;
+  if (pl.cluster && splits > 8) splits = 8;
   if (splits < 1) splits = 1;
   pl.ksteps_split = (pl.ksteps + splits - 1) / splits;
   pl.splits = (pl.ksteps + pl.ksteps_split - 1) / pl.ksteps_split;
@@ -360,11 +411,22 @@ static cudaError_t launch_nb(const TcParams& p, const CUtensorMap& w, const CUte
   cfg.blockDim = dim3(tcg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)p.pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (p.pl.splits > 1 && p.pl.cluster) {  // the K splits of a tile form one cluster
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)p.pl.splits;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = (unsigned)n;
   return cudaLaunchKernelEx(&cfg, tcg::tc_gemm_kernel<NB>, p, w, x);
 }
 
