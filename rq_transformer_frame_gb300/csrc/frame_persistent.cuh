@@ -1050,11 +1050,21 @@ __device__ __forceinline__ void attn_items(const PersParams& P, const PersOp& op
           A += s_aacc[group][w][gt] * c;
         }
       }
-      part[2 + gt] = A;
-      if (gt == 0) {
-        part[0] = M;
-        part[1] = L;
+      if (nsplit == 1) {
+        // the whole window is this item's split: its merge is the output (what the ordered
+        // merge of one split gives, bit for bit), without the partial and the ticket
+        P.attn_out[(size_t)h * HD + gt] = A / L;
+      } else {
+        part[2 + gt] = A;
+        if (gt == 0) {
+          part[0] = M;
+          part[1] = L;
+        }
       }
+    }
+    if (nsplit == 1) {  // (uniform) the group's shared staging is reused by its next item
+      bar_sync(2 + group, 128);
+      continue;
     }
     __threadfence();
     bar_sync(2 + group, 128);
