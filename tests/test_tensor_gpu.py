@@ -85,10 +85,12 @@ def test_small_batch16_all_sessions_forced():
     run_batch_forced(configs.SMALL.with_(batch=16), 6, range(16))
 
 
-@pytest.mark.parametrize("batch", [3, 20, 64])
+@pytest.mark.parametrize("batch", [3, 20, 40, 64])
 def test_small_padded_and_full_tiles(batch):
-    """batch 3 pads the session tile to 16 and 20 to 32 (the padding rows stay zero); 64
-    fills it."""
+    """batch 3 pads the session tile to 16, 20 to 32 and 40 to 48 (the padding rows stay
+    zero); 64 fills it.  From 32 sessions the K splits of a tile merge through a
+    thread-block cluster's shared memory, each split finishing its own 16-session chunks
+    (20: two chunks, 40: three, 64: four), at 16 through L2."""
     run_batch_forced(configs.SMALL.with_(batch=batch), 4, [0, batch // 2, batch - 1])
 
 
