@@ -974,6 +974,21 @@ int prefill_chunk(const rq_handle* h, int session, int left) {
 rq_status upload_pers_ops(rq_handle* h) {
   int dep_first = 0;
   std::vector<PersOp> ops = pers_ops(h, &dep_first);
+  if (h->dx_ll) {
+    // a new op table renumbers the ops: clear every tagged word, so that no word written
+    // under the old numbering can carry a tag the new one waits for (words of the current
+    // numbering are rewritten every frame, and a tag's 22-bit epoch only repeats after
+    // 4 M frames)
+    const rq_config& c = h->cfg;
+    const size_t DD = c.ddim, DF = c.dhidden, A = c.audio_card, DL = c.dlayers;
+    RQ_CUDA(h, cudaMemsetAsync(h->dx_ll, 0, DD * 8, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->dq_ll, 0, DD * 8, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->du_ll, 0, DF * 8, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->dkv_ll, 0, DL * 2 * 8 * DD * 8, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->alog_ll, 0, 8 * A * 8, h->stream));
+    RQ_CUDA(h, cudaMemsetAsync(h->key_ll, 0, (size_t)9 * h->pers_dep_grid * 16, h->stream));
+    RQ_CUDA(h, cudaStreamSynchronize(h->stream));
+  }
   if (h->d_ops) {
     cudaFree(h->d_ops);
     h->d_ops = nullptr;
@@ -1144,13 +1159,8 @@ rq_status setup_schedule(rq_handle* h) {
     RQ_CUDA(h, dalloc(&h->alog_ll, 8 * A * 8));
     RQ_CUDA(h, dalloc(&h->topk_scratch, A * 4));
     RQ_CUDA(h, dalloc(&h->key_ll, (size_t)9 * h->pers_dep_grid * 16));
-    // zero tags: epoch 0 is never a frame's (the first frame advances it to 1)
-    RQ_CUDA(h, cudaMemset(h->dx_ll, 0, DD * 8));
-    RQ_CUDA(h, cudaMemset(h->dq_ll, 0, DD * 8));
-    RQ_CUDA(h, cudaMemset(h->du_ll, 0, DF * 8));
-    RQ_CUDA(h, cudaMemset(h->dkv_ll, 0, DL * 2 * 8 * DD * 8));
-    RQ_CUDA(h, cudaMemset(h->alog_ll, 0, 8 * A * 8));
-    RQ_CUDA(h, cudaMemset(h->key_ll, 0, (size_t)9 * h->pers_dep_grid * 16));
+    // (upload_pers_ops zeroes them: tag 0 is never a frame's, the first frame advances
+    // the epoch to 1)
     P.epoch = h->grid_bar + kPersEpochWord;
     P.epoch_bump = 1;
     PersParams& Q = h->pers_dep;
