@@ -1127,7 +1127,8 @@ rq_status setup_schedule(rq_handle* h) {
   // ring twice as deep run them faster (Moshi-7B: 1.29 -> 1.12 ms per frame), while the
   // temporal stack keeps two CTAs per SM to stream its weights.  Its ops wait for tagged
   // words instead of grid barriers (frame op indices must fit a tag's 10 bits: at most
-  // 5 L + 3 + 8 (4 DL + 2) ops).  If that launch does not fit, the first one runs every op.
+  // 5 L + 3 + 8 (4 DL + 2) ops).  If that launch does not fit, the frame runs on the graph
+  // schedule (the two-CTA kernel carries no depformer op).
   h->pers_dep_grid = 0;
   {
     GemvPlan pl2[kPersMaxPlans];
@@ -1150,7 +1151,15 @@ rq_status setup_schedule(rq_handle* h) {
     }
     cudaGetLastError();  // a refused configuration leaves no sticky error
   }
-  if (h->pers_dep_grid > 0) {
+  if (h->pers_dep_grid == 0) {
+    // the two-CTA launch runs no depformer op: without the depformer's launch the frame
+    // runs on the graph schedule
+    if (c.schedule == RQ_SCHEDULE_PERSISTENT)
+      return fail(h, RQ_ERR_UNSUPPORTED, "the persistent depformer launch does not fit on this device");
+    h->schedule = RQ_SCHEDULE_GRAPH;
+    return RQ_OK;
+  }
+  {
     const size_t DD = c.ddim, DF = c.dhidden, A = c.audio_card, DL = c.dlayers;
     RQ_CUDA(h, dalloc(&h->dx_ll, DD * 8));
     RQ_CUDA(h, dalloc(&h->dq_ll, DD * 8));
