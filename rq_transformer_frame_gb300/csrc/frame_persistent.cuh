@@ -788,8 +788,8 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
                                          const GemvPlan& pl, int t0, int nt, const float* part,
                                          int tid, int warp, int lane,
                                          unsigned long long* s_key, const float2* s_rope,
-                                         float resid_old, int pos, int forcing,
-                                         float scale, const LLCtx& lc, uint32_t wtag) {
+                                         float resid_old, int pos, float scale,
+                                         const LLCtx& lc, uint32_t wtag) {
   const int tr = pl.tile_rows, wpg = pl.tpr >> 5;
   const int nrows = nt * tr;
   (void)lc;
@@ -813,13 +813,9 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
   };
   auto grow = [&](int lr) { return (t0 + lr / tr) * tr + lr % tr; };
   const int epi = op.epi;
-  if (epi == EPI_STORE || epi == EPI_RESID || epi == EPI_DEPIN) {
-    int prev = -1;
-    if (epi == EPI_DEPIN) {
-      const IoLayout io{1};
-      prev = forcing ? P.d_in[io.forced_off() + op.key_index]
-                     : argmax_key_index(__ldcg(P.keys + op.key_index));
-    }
+  // (the op table adds a depformer step's embedding row in the first qkv's prologue,
+  // PRO_RMS_EMB, so this kernel has no EPI_DEPIN)
+  if (epi == EPI_STORE || epi == EPI_RESID) {
     for (int lr = tid; lr < nrows; lr += kCons) {
       const int row = grow(lr);
       if (row >= pl.n_out) continue;
@@ -829,13 +825,6 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
         float old = resid_old;
         if (lr != tid) old = LL ? lc.wait1(op.out, row, lc.want(op.tag_res)) : ldcg(op.out + row);
         put(op.out, row, old + y);
-      }
-      if (epi == EPI_DEPIN) {
-        // "moshi_lm.rs", `embed`: -1 adds nothing, else row max(tok, 0)
-        op.out[row] = (prev != -1)
-                          ? y + Chunk<typename Chunk<WT>::Table>::elem(
-                                    op.emb, (size_t)max(prev, 0) * pl.n_out + row)
-                          : y;
       }
     }
   } else if (epi == EPI_SWIGLU) {
@@ -848,7 +837,7 @@ __device__ __forceinline__ void epilogue(const PersParams& P, const PersOp& op,
       const float gt = yrow(lr), mu = yrow(lr + half);
       put(op.out, j, gt / (1.0f + expf(-gt)) * mu);
     }
-  } else if (epi == EPI_QKV) {
+  } else if (!LL && epi == EPI_QKV) {  // (the temporal stack's: not in the tagged kernel)
     const int D = pl.n_out / 3;
     const int slot = pos % P.context;
     const int hd = P.head_dim;
@@ -1195,7 +1184,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
       if (P.epoch_bump && blockIdx.x == 0) atomicAdd(P.epoch, 1u);
       s_ebase = LL ? ld_acquire(P.epoch) << 10 : 0u;
     }
-    if (tid < P.head_dim / 2) {
+    if (!LL && tid < P.head_dim / 2) {
       // "moshi_lm.rs", `rope_row`: freq_i = exp(-ln(theta) * 2i / hd), angle freq_i * pos;
       // every layer rotates at the same position, so the pairs are computed once
       const float freq = expf(-logf(P.rope_theta) * 2.0f * (float)tid / (float)P.head_dim);
@@ -1239,7 +1228,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
       }
       if (stamp) P.trace[P.op_base + k] = global_timer_ns();
       const PersOp& op = s_op[k & 1];
-      if (op.type == OPT_ATTN) {
+      if (!LL && op.type == OPT_ATTN) {  // (the temporal attention: not in the tagged kernel)
         attn_items<KT, EPL>(P, op, tid, warp, lane, s_am, s_al, s_aacc, s_last, pos);
       } else if (PICKS && op.type == OPT_TOPK) {
         // "moshi_lm.rs", `topk_sample` for pick key_index over the logits the previous op
@@ -1343,7 +1332,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
           if (bar_or(1, kCons, s_abort != 0)) break;
           const bool rms = op.pro == PRO_RMS || op.pro == PRO_RMS_EMB;
           const float scale = rms ? rms_scale(P, pl, s_red, k & 1) : 1.0f;
-          if (op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0) {
+          if (!LL && op.pro == PRO_RMS && op.side_out != nullptr && blockIdx.x == 0 && g == 0) {
             // CTA 0 keeps the normalised vector (the head's transformer_out)
             constexpr int V2 = Chunk<WT>::V;
 #pragma unroll
@@ -1356,7 +1345,7 @@ __global__ void __launch_bounds__(kThr, MINB) frame_persistent_kernel(const Pers
             }
           }
           epilogue<WT, PICKS, LL>(P, op, pl, t0, nt, part, tid, warp, lane, s_key, s_rope,
-                                  resid_old, pos, forcing, scale, lc, wtag);
+                                  resid_old, pos, scale, lc, wtag);
         } else if (LL && op.epi == EPI_ARGMAX && !op.no_keymax && tid == 0) {
           put_key_slot(P, op.key_index, blockIdx.x, wtag, 0ull);  // no rows here
         }
