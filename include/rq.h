@@ -57,7 +57,7 @@ typedef enum {
   RQ_ERR_CUDA = 3,        /* a CUDA runtime error (handle poisoned) */
   RQ_ERR_OOM = 4,         /* device or pinned-host allocation failed */
   RQ_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (handle poisoned) */
-  RQ_ERR_UNSUPPORTED = 6, /* shape or dtype this build does not implement */
+  RQ_ERR_UNSUPPORTED = 6, /* shape or dtype this library does not implement */
   RQ_ERR_POISONED = 7     /* an earlier CUDA error or timeout; rq_reset(h, -1) */
 } rq_status;
 
@@ -386,7 +386,7 @@ int32_t rq_get_op_times(rq_handle *h, float *us, int32_t max_ops);
  * RQ_ERR_TIMEOUT, later calls RQ_ERR_POISONED until rq_reset(h, -1).  -1 removes the
  * stall.  Nothing traps and no wait is unbounded.  Applies to frames run by the
  * persistent kernel (RQ_ERR_UNSUPPORTED under the other schedules); synchronizes the
- * stream.  Survey of the failure handling: the timeout reports instead of hanging. */
+ * stream.  A wait that runs out reports an error instead of hanging. */
 rq_status rq_set_wait_limit(rq_handle *h, uint64_t limit_ns, int32_t stall_op);
 
 const char *rq_last_error(const rq_handle *h);
