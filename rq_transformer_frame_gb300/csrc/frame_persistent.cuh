@@ -36,7 +36,7 @@ constexpr int kMaxStage = 1024;  // depformer attention output staged in shared 
 #define RQ_PERS_BURST_T 4
 #endif
 #ifndef RQ_PERS_STREAM_T
-#define RQ_PERS_STREAM_T 2
+#define RQ_PERS_STREAM_T 4
 #endif
 #ifndef RQ_PERS_STREAM_BURST
 #define RQ_PERS_STREAM_BURST 0
@@ -46,6 +46,8 @@ constexpr int kMaxStage = 1024;  // depformer attention output staged in shared 
 #endif
 // tile groups: resident tiles (ops of a few tiles per CTA) in bursts of kBurstT; the
 // weight stream of long ops (more than kStreamMinTiles tiles per CTA) kStreamT at a time
+// (4: once the two-CTA kernel ran without spills, groups of 4 measured 17 us per frame
+// faster than 2)
 constexpr int kBurstT = RQ_PERS_BURST_T;
 #ifndef RQ_PERS_BURST_T_WIDE
 #define RQ_PERS_BURST_T_WIDE 8
